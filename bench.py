@@ -1,0 +1,310 @@
+"""Benchmark of the dense prefill indexer on GB300.
+
+One step = one ``indexer_fused_topk`` call (fp8 MQA logits on tcgen05, ReLU +
+head-weighted sum + causal mask, key-blocked top-k with the exact merge) over
+one synthetic batch already resident in HBM.  Default workload: the cold
+chunk, T=2048 query rows ending a 65,536-token prefix, L=65,536 keys, H=32,
+D=128, top-2048.
+
+Prints one JSON line (rank 0).  ``value`` is scored pairs/s (sum of T_r*L_r
+per second, all GPUs); ``e2e`` repeats it with host inputs copied in and the
+indices copied out inside the timed region; ``roofline`` relates the logits
+kernel to the measured FP8 tensor peak; ``cpu_baseline`` times the CPU
+oracle on a bounded row sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("indexer scored pairs/s (T·L/s) & chunk latency at 1 GB300; % FP8 tensor peak; "
+          "peak transient")
+UNIT = "pairs/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_PER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate on GB300 (4.5 / 2.25 PFLOP/s)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="cold64k")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    return d
+
+
+def fp8_peak_tflops():
+    d = peaks()
+    if d:
+        for key in ("bf16_tflops", "bf16_tflops_burst", "bf16"):
+            v = d.get(key)
+            if isinstance(v, (int, float)) and v > 0:
+                return v * FP8_PER_BF16, "measured bf16 burst x2 (nominal FP8/BF16 ratio), of measured"
+    return FALLBACK_BF16_TFLOPS * FP8_PER_BF16, "fallback 1.9 PF bf16 x2, of fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.f.name)
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def oracle_sample(p, seconds: float, seed: int = 0):
+    """Time the CPU oracle (logits + top-k, as it stands) on a bounded row sample."""
+    from oracle import oracle as O
+    rng = np.random.default_rng(seed)
+    T = int(p.cu_seqlens_q[-1])
+    clen = p.compress_len.numpy()
+    threads = O.max_threads()
+    # calibrate on a few rows, then size the sample to about `seconds`
+    rows = np.sort(rng.choice(T, size=min(T, max(1, threads)), replace=False))
+    t0 = time.perf_counter()
+    O.problem_topk(p, rows)
+    dt = time.perf_counter() - t0
+    n = int(min(T, max(len(rows), len(rows) * seconds / max(dt, 1e-6))))
+    rows = np.sort(rng.choice(T, size=n, replace=False))
+    t0 = time.perf_counter()
+    O.problem_topk(p, rows)
+    dt = time.perf_counter() - t0
+    pairs = float(np.sum(np.minimum(clen[rows], p.k.shape[0])))
+    return {"value": pairs / dt, "unit": UNIT + " (causal-valid pairs)", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{n} of {T} rows against their full prefix (logits in fp64 + sort top-k), "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args, p, spec):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    steps = []
+    budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup + args.steps):
+        r = oracle_sample(p, budget, seed=i)
+        if i >= args.warmup:
+            steps.append(r)
+    value = statistics.median(s["value"] for s in steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": spec.dense_pairs / value * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": spec.name, "T": spec.total_rows, "L": spec.total_keys,
+                   "H": spec.H, "D": spec.D, "topk": spec.topk},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": steps[0]["cores"],
+                         "kind": "oracle", "sample": steps[0]["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    from sparse_attention_prefill_tcgen05_gb300 import workloads as W
+    spec = W.CONFIGS[args.config]
+    ws_n = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args, W.make_problem(spec), spec)
+        return
+
+    import torch
+    import sparse_attention_prefill_tcgen05_gb300 as K
+    ws_n, rank, local = dist_setup()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    p = W.make_problem(spec)
+    kd = K.IDX_K_FP8_E4M3 if spec.kdtype == "fp8" else K.IDX_K_FP4_E2M1_UE8M0
+    plan = K.indexer_plan(p.cu_seqlens_q, p.cu_seqlens_k, p.compress_len, p.H, p.D, p.topk,
+                          kdtype=kd, cand_block=spec.cand_block, cand_topk=spec.cand_topk,
+                          key_block=spec.key_block)
+    T = int(p.cu_seqlens_q[-1])
+    host = dict(q=p.q, s_q=p.s_q, w=p.w, k=p.k, k_scale=p.k_scale, compress_len=p.compress_len)
+    d = {n: t.to(dev) for n, t in host.items()}
+    idx = torch.empty((T, p.topk), dtype=torch.int32, device=dev)
+    val = torch.empty((T, p.topk), dtype=torch.float32, device=dev)
+    wsb = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        K.indexer_fused_topk(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"],
+                             d["compress_len"], None, idx, val, wsb)
+
+    clocks = ClockSampler(dev.index if ws_n == 1 else local)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert K.indexer_status(plan, wsb) == K.IDX_OK
+    mem0 = torch.cuda.memory_allocated()
+
+    def timed(fn, n):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for i in range(n):
+            flush.zero_()                     # evict L2 between iterations
+            starts[i].record(stream)
+            fn()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+    if ws_n > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    l0 = K.indexer_launch_count()
+    times = timed(step, args.steps)
+    launches = K.indexer_launch_count() - l0
+    torch.cuda.synchronize()
+    if ws_n > 1:
+        torch.distributed.barrier()
+    assert K.indexer_status(plan, wsb) == K.IDX_OK
+    total_ms = sum(times)
+    if ws_n > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    pairs = spec.dense_pairs
+    value = ws_n * pairs / (ms / 1e3)
+
+    # roofline: the logits kernel (tcgen05 contraction + fused epilogue) timed alone
+    ld = int(torch.diff(p.cu_seqlens_k).max())
+    logits = torch.empty((T, ld), dtype=torch.float32, device=dev)
+
+    def logits_only():
+        K.indexer_logits(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"],
+                         d["compress_len"], logits, wsb)
+
+    for _ in range(3):
+        logits_only()
+    ltimes = timed(logits_only, max(10, min(args.steps, 100)))
+    del logits
+    lms = statistics.mean(ltimes)
+    flops = 2.0 * pairs * spec.H * spec.D
+    peak, peak_note = fp8_peak_tflops()
+    achieved = flops / (lms / 1e3) / 1e12
+
+    # end to end through the C ABI with host buffers: H2D inputs, fused call, D2H indices
+    pinned = {n: t.pin_memory() for n, t in host.items()}
+    out_host = torch.empty((T, p.topk), dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for n, t in pinned.items():
+            d[n].copy_(t, non_blocking=True)
+        step()
+        out_host.copy_(idx, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    etimes = timed(e2e_step, max(10, min(args.steps, 100)))
+    ems = statistics.mean(etimes)
+    clk = clocks.stop()
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8", "data": "synthetic",
+        "config": {"workload": spec.name, "T": T, "L": ld, "H": spec.H, "D": spec.D,
+                   "topk": spec.topk, "dense_pairs_per_step": pairs,
+                   "causal_pairs_per_step": int(p.compress_len.long().sum()),
+                   "l2": "flushed between timed iterations (256 MiB write)",
+                   "parallelism": f"replicas{ws_n}", "plan": plan.info()},
+        "chunk_latency_ms": {"median": statistics.median(times), "mean": ms,
+                             "p10": float(np.percentile(times, 10)),
+                             "p90": float(np.percentile(times, 90))},
+        "pct_fp8_peak_step": 100.0 * flops / (ms / 1e3) / 1e12 / peak,
+        "peak_transient_bytes": plan.workspace_bytes,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "logits_tc_kernel<32,128,fp8> via indexer_logits",
+                     "kernel_ms": lms, "flops_per_launch": flops, "peak_source": peak_note},
+        "e2e": {"value": pairs / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": ems},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "memory_allocated_bytes": mem0,
+    }
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample(p, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws_n > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

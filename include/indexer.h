@@ -1,0 +1,221 @@
+/*
+ * indexer.h -- C ABI of the GB300 (sm_103a) dense prefill indexer.
+ *
+ * The indexer scores every query row t of a prefill chunk against every
+ * compressed prefix key j of the row's request,
+ *
+ *     logit[t,j] = sum_h w[t,h] * ReLU( s_q[t,h] * s_k[j] * <q[t,h,:], k[j,:]> ),
+ *
+ * for j < compress_len(t) (the row's causal length), and keeps each row's
+ * top-k keys.  Sources, by page and section:
+ *   - "chunked-prefill-memory.md", section 1: the low-ratio indexer scores the
+ *     chunk's T rows against the whole compressed prefix L and writes
+ *     [T, max_seqlen_k] fp32 logits; section 2.3: key blocks with a per-block
+ *     top-k and an exact top-k of the union; 8-key block pooling with the
+ *     top-2048 blocks as candidates; consumers mask non-candidates.
+ *   - SGLang PR #39187 "Bound the dense prefill indexer transient",
+ *     Motivation/Modifications: DeepGEMM fp8_fp4_mqa_logits scoring, ragged
+ *     requests, a caller-owned `selected` output, masks built straight into
+ *     one preallocated buffer, a bounded transient; a block-level mask as the
+ *     follow-up format.
+ *   - SGLang fork commit log, the ragged-plan commit: per-batch metadata is
+ *     built once and reused by every layer; host lengths avoid device syncs.
+ * The score formula itself is the problem statement's; the pages name the
+ * kernels but never print it.
+ *
+ * Conventions shared by every entry point:
+ *   - Layout.  Rows of all requests are packed: request r owns global rows
+ *     [cu_seqlens_q[r], cu_seqlens_q[r+1]) and packed keys
+ *     [cu_seqlens_k[r], cu_seqlens_k[r+1]).  Key indices in outputs are
+ *     request-local (0 = first key of the row's request).
+ *   - Eligibility.  Key j is eligible for row t iff j < compress_len[t]
+ *     (compress_len is clamped to the request's key count) and, when a
+ *     candidate mask is given, its block byte is non-zero.
+ *   - Ties.  Equal scores are ordered by the lower key index.
+ *   - Output order.  Kept indices are listed in ascending key order, then -1
+ *     padding; `out_val` (optional) holds each kept key's score, -inf for
+ *     padding.  Results are bitwise reproducible run to run and do not
+ *     depend on the workspace size or the key-block size.
+ *   - Ownership.  The caller owns every buffer (inputs, outputs, workspace).
+ *     The plan owns only host metadata; the library allocates no device
+ *     memory.  Device pointers are CUDA device addresses on the current
+ *     device; `stream` is a cudaStream_t (NULL = legacy default stream).
+ *   - Errors.  Return codes only (no exceptions, no exit, no printing).
+ *     Argument errors are caught on the host before any launch.  Calls are
+ *     asynchronous and never synchronize; a device-side failure (a wait that
+ *     timed out) sets a status word in the workspace that indexer_status()
+ *     reads.
+ *   - Preconditions the library does not check on the device: q/k codes are
+ *     finite (no e4m3 NaN codes 0x7F/0xFF, no ue8m0 255), scales s_q, s_k are
+ *     positive and finite (so ReLU(s*x) = s*ReLU(x)), w is finite.
+ */
+#ifndef GB300_PREFILL_INDEXER_H
+#define GB300_PREFILL_INDEXER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define IDX_OK 0
+#define IDX_ERR_INVALID_ARG (-1)   /* bad size, pointer, alignment or layout */
+#define IDX_ERR_UNSUPPORTED (-2)   /* shape/format this build has no kernel for, or not sm_103 */
+#define IDX_ERR_WORKSPACE (-3)     /* workspace too small, or budget impossible at plan time */
+#define IDX_ERR_CUDA (-4)          /* a CUDA runtime/driver call failed */
+#define IDX_ERR_TIMEOUT (-5)       /* a device-side wait ran out (reported by indexer_status) */
+#define IDX_ERR_DEVICE_CHECK (-6)  /* a device-side check failed (reported by indexer_status) */
+
+/* Key formats. */
+#define IDX_K_FP8_E4M3 0           /* k: e4m3 [keys, D]; k_scale: float s_k[keys] */
+#define IDX_K_FP4_E2M1_UE8M0 1     /* k: e2m1 [keys, D/2], element 2i in the low nibble;
+                                      k_scale: uint8 ue8m0 [keys, D/32]; s_k is 1 */
+
+/*
+ * Problem description, read only by indexer_plan (host memory, copied).
+ *   num_requests  R >= 1 (at most 256)
+ *   total_rows    T = cu_seqlens_q[R];  total_keys = cu_seqlens_k[R]
+ *   H, D          heads and head dim of q; k has D too.  Built shapes:
+ *                 (H, D) in {(32,128), (16,128), (64,128), (4,64)}
+ *   topk          keys kept per row, 1 <= topk <= 2048
+ *   cu_seqlens_q  [R+1] non-decreasing row offsets, starts at 0
+ *   cu_seqlens_k  [R+1] non-decreasing key offsets, starts at 0
+ *   compress_len  [T] causal length of every row, 0 <= compress_len[t] <= the
+ *                 keys of its request (e.g. floor((pos+1)/ratio))
+ *   kdtype        IDX_K_FP8_E4M3 or IDX_K_FP4_E2M1_UE8M0
+ *   cand_block    keys per candidate block (0 means 8)
+ *   cand_topk     candidate blocks kept per row by indexer_candidate_blocks,
+ *                 1..4096 (e.g. 2048); 0 = the plan makes no candidate-block
+ *                 calls and reserves no workspace for them
+ *   key_block     keys per key block of the streamed top-k (0 = planner's
+ *                 choice; else a multiple of 128)
+ *   transient_budget_bytes  cap on the workspace of the top-k and candidate
+ *                 calls (0 means 2 GiB); the planner shrinks key blocks and
+ *                 row chunks to fit and fails with IDX_ERR_WORKSPACE if it
+ *                 cannot.
+ */
+typedef struct indexer_problem {
+    int32_t num_requests;
+    int32_t total_rows;
+    int32_t total_keys;
+    int32_t H;
+    int32_t D;
+    int32_t topk;
+    const int32_t* cu_seqlens_q;
+    const int32_t* cu_seqlens_k;
+    const int32_t* compress_len;
+    int32_t kdtype;
+    int32_t cand_block;
+    int32_t cand_topk;
+    int32_t key_block;
+    uint64_t transient_budget_bytes;
+} indexer_problem;
+
+typedef struct indexer_plan_s* indexer_plan_t;
+
+/*
+ * Validate a problem and build its plan (host metadata only: ragged tables,
+ * key-block and row-chunk sizes, workspace layout).  Built once per batch and
+ * reused by every layer of that batch (SGLang fork commit log, ragged-plan
+ * commit).  *workspace_bytes receives the workspace every call on this plan
+ * needs.  Needs no GPU.  Returns IDX_OK, IDX_ERR_INVALID_ARG,
+ * IDX_ERR_UNSUPPORTED or IDX_ERR_WORKSPACE (budget impossible).
+ */
+int indexer_plan(const indexer_problem* problem, indexer_plan_t* out_plan,
+                 size_t* workspace_bytes);
+void indexer_plan_destroy(indexer_plan_t plan);
+
+/* Key-block size and row-chunk size the plan chose (for reporting). */
+int indexer_plan_info(indexer_plan_t plan, int32_t* key_block, int32_t* row_chunk,
+                      int32_t* max_splits);
+
+/*
+ * Dense logits ("chunked-prefill-memory.md" section 1: [T, max_seqlen_k] fp32).
+ *   q        e4m3 [T, H, D] (16-byte aligned)
+ *   s_q, w   float [T, H]
+ *   k        see kdtype (16-byte aligned); k_scale see kdtype
+ *   compress_len  int32 [T] on the device, same values as the plan's
+ *   logits   float [T, ld], ld >= the largest key count of the batch;
+ *            logits[t, j] for j < compress_len[t], -inf for the rest of the row
+ * ws/ws_bytes: the plan's workspace (256-byte aligned).
+ */
+int indexer_logits(indexer_plan_t plan, const void* q, const float* s_q, const float* w,
+                   const void* k, const void* k_scale, const int32_t* compress_len,
+                   float* logits, int64_t ld, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Ragged per-row top-k over given logits [T, ld] (the ragged top-k of
+ * "chunked-prefill-memory.md" section 2.3).  Entries j >= compress_len[t] and
+ * -inf entries are not eligible.  out_idx int32 [T, topk]; out_val float
+ * [T, topk] or NULL.
+ */
+int indexer_topk(indexer_plan_t plan, const float* logits, int64_t ld,
+                 const int32_t* compress_len, int32_t* out_idx, float* out_val, void* ws,
+                 size_t ws_bytes, void* stream);
+
+/*
+ * Fused logits + top-k with a bounded transient: keys are scored block by
+ * block and only per-block top-k candidates are kept, then merged exactly
+ * ("chunked-prefill-memory.md" section 2.3); the [T, L] logits are never
+ * materialised.  cand_mask (nullable) uint8 [T, ld_mask]: one byte per
+ * cand_block-key block, non-zero = candidate (the consumer layer's mask);
+ * ld_mask >= ceil(L/cand_block) for every request.
+ */
+int indexer_fused_topk(indexer_plan_t plan, const void* q, const float* s_q, const float* w,
+                       const void* k, const void* k_scale, const int32_t* compress_len,
+                       const uint8_t* cand_mask, int64_t ld_mask, int32_t* out_idx,
+                       float* out_val, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Candidate-source layer: pool each row's logits over cand_block-key blocks
+ * (maximum over eligible keys, blocks aligned at key 0), keep the cand_topk
+ * blocks with the largest pooled score (ties to the lower block) and write a
+ * block-level mask: cand_mask uint8 [T, ld_mask], 1 = kept, 0 otherwise
+ * (every byte of every row is written).  ld_mask >= ceil(L/cand_block).
+ */
+int indexer_candidate_blocks(indexer_plan_t plan, const void* q, const float* s_q,
+                             const float* w, const void* k, const void* k_scale,
+                             const int32_t* compress_len, uint8_t* cand_mask, int64_t ld_mask,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Expand a block-level mask to the key-level bool layout the pages' consumer
+ * format uses: key_mask uint8 [T, ld], key_mask[t,j] = cand_mask[t, j/cand_block]
+ * for j < compress_len[t], 0 otherwise.
+ */
+int indexer_expand_mask(indexer_plan_t plan, const uint8_t* cand_mask, int64_t ld_mask,
+                        const int32_t* compress_len, uint8_t* key_mask, int64_t ld,
+                        void* stream);
+
+/*
+ * Synchronizes `stream`, then reads the device status word in `ws`: IDX_OK,
+ * IDX_ERR_TIMEOUT or IDX_ERR_DEVICE_CHECK.  Every compute call clears the
+ * word when it starts.
+ */
+int indexer_status(indexer_plan_t plan, const void* ws, void* stream);
+
+/*
+ * Self-test of the bounded waits: launches one tiny kernel that waits on a
+ * barrier nothing arrives on, with a budget of `cycles` SM cycles; it must
+ * give up and set the timeout bit in the status word of `ws` (then
+ * indexer_status returns IDX_ERR_TIMEOUT).  Never hangs.
+ */
+int indexer_selftest_timeout(void* ws, long long cycles, void* stream);
+
+/* Budget, in SM clock cycles, of every device-side wait of later calls
+   (default about two seconds). */
+int indexer_set_wait_budget(indexer_plan_t plan, long long cycles);
+
+/* Number of kernels this library has launched in this process (a
+   diagnostic counter for benchmarks; never reset). */
+long long indexer_launch_count(void);
+
+const char* indexer_error_string(int status);
+int indexer_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,242 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Small cases are checked element by element; the full-size workloads are
+checked on sampled rows (the oracle computes rows independently, so a
+sampled row is checked exactly).  Also: the selector is bit-exact against
+the oracle's selector applied to the GPU's own fp32 logits, exact-arithmetic
+inputs give bitwise-equal logits and tie-exact selections, results do not
+depend on key-block size or run, and bounded waits report instead of hang.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from sparse_attention_prefill_tcgen05_gb300 import _lib as K
+from sparse_attention_prefill_tcgen05_gb300 import workloads as W
+
+from . import helpers as Hp
+
+pytestmark = pytest.mark.gpu
+
+
+def small(name, rows_div, keys_div, topk=None, **over):
+    spec = W.scaled(W.CONFIGS[name], rows_div, keys_div, **over)
+    if topk:
+        spec = dataclasses.replace(spec, topk=topk)
+    return W.make_problem(spec)
+
+
+def oracle_rows(p, rows, layer=1):
+    return O.problem_logits(p, rows, layer=layer)
+
+
+# ----------------------------------------------------------------- logits
+
+def check_all(p, key_block=0):
+    plan = Hp.make_plan(p, key_block=key_block)
+    d = Hp.device_inputs(p)
+    T = int(p.cu_seqlens_q[-1])
+    rows = np.arange(T)
+    ref = oracle_rows(p, rows)
+    g = Hp.gpu_logits(p, plan, d).cpu().numpy()
+    Hp.check_logits(g, ref)
+    cl = p.compress_len.numpy()
+    # selector isolation: oracle selector on the GPU's own logits == GPU top-k, ties included
+    sel_ref = O.topk_rows(g.astype(np.float64), cl, p.topk)
+    ti, tv = Hp.gpu_topk(p, plan, torch.from_numpy(g).cuda(), d)
+    fi, fv = Hp.gpu_fused(p, plan, d)
+    ti, fi = ti.cpu().numpy(), fi.cpu().numpy()
+    for t in range(T):
+        want = sorted(x for x in sel_ref[t].tolist() if x >= 0)
+        assert sorted(x for x in ti[t].tolist() if x >= 0) == want, t
+        assert np.array_equal(ti[t], fi[t]), t
+    assert torch.equal(tv.cpu(), fv.cpu())
+    # values are the GPU's own logits at the indices
+    gv = fv.cpu().numpy()
+    for t in range(T):
+        m = fi[t] >= 0
+        assert np.array_equal(gv[t][m], g[t][fi[t][m]])
+        assert np.all(np.isneginf(gv[t][~m]))
+    # against the fp64 oracle
+    exact = 0
+    for t in range(T):
+        exact += Hp.check_topk_row(fi[t], ref[t], int(cl[t]), p.topk)
+    return exact
+
+
+def test_tiny_full_parity():
+    p = W.make_problem(W.CONFIGS["tiny"])
+    exact = check_all(p)
+    assert exact >= 60
+
+
+@pytest.mark.parametrize("key_block", [0, 512])
+def test_cold_chunk_scaled_parity(key_block):
+    # 128 rows ending a 4096-key prefix, H=32, D=128, top-256: several tiles, ragged tail
+    p = small("cold64k", 16, 16, topk=256)
+    check_all(p, key_block=key_block)
+
+
+def test_long_context_scaled_parity_with_ties():
+    p = small("long488k", 128, 96, topk=96)
+    check_all(p, key_block=1024)
+
+
+def test_ragged_requests_parity():
+    spec = dataclasses.replace(W.CONFIGS["ragged_cand"], topk=64, cand_topk=48, requests=(
+        W.RequestSpec(100, 0, 1), W.RequestSpec(37, 0, 2), W.RequestSpec(0, 0, 1),
+        W.RequestSpec(129, 300, 1), W.RequestSpec(70, 5000, 1)))
+    p = W.make_problem(spec)
+    check_all(p, key_block=1024)
+
+
+def test_exact_arithmetic_inputs_are_bit_exact():
+    """Small integer codes and power-of-two scales: every fp32 step is exact, so GPU logits
+    equal the oracle's bitwise and selections match including ties."""
+    spec = dataclasses.replace(W.scaled(W.CONFIGS["cold64k"], 32, 32), topk=100, exact=True)
+    p = W.make_problem(spec)
+    plan = Hp.make_plan(p, key_block=512)
+    d = Hp.device_inputs(p)
+    T = int(p.cu_seqlens_q[-1])
+    ref = oracle_rows(p, np.arange(T))
+    g = Hp.gpu_logits(p, plan, d).cpu().numpy().astype(np.float64)
+    assert np.array_equal(g, ref)
+    fi, _ = Hp.gpu_fused(p, plan, d)
+    want = O.topk_rows(ref, p.compress_len.numpy(), p.topk)
+    fi = fi.cpu().numpy()
+    for t in range(T):
+        assert sorted(fi[t][fi[t] >= 0].tolist()) == sorted(want[t][want[t] >= 0].tolist())
+
+
+def test_runs_and_key_blocks_are_bitwise_identical():
+    p = small("cold64k", 16, 8, topk=300)
+    d = Hp.device_inputs(p)
+    outs = []
+    for kb in (0, 1024, 2048, 0):
+        i, v = Hp.gpu_fused(p, Hp.make_plan(p, key_block=kb), d)
+        outs.append((i.cpu(), v.cpu()))
+    for i, v in outs[1:]:
+        assert torch.equal(i, outs[0][0]) and torch.equal(v, outs[0][1])
+
+
+def test_row_chunking_is_bitwise_invariant():
+    """Scoring rows in one call or in pieces gives the same bits (SGLang PR #39187 Accuracy)."""
+    p = small("cold64k", 16, 16, topk=64)
+    d = Hp.device_inputs(p)
+    full = Hp.gpu_logits(p, Hp.make_plan(p), d)
+    T = int(p.cu_seqlens_q[-1])
+    for a, b in ((0, 8), (8, 9), (9, 77), (77, T)):
+        sub = dataclasses.replace(p, q=p.q[a:b], s_q=p.s_q[a:b], w=p.w[a:b],
+                                  compress_len=p.compress_len[a:b],
+                                  cu_seqlens_q=torch.tensor([0, b - a], dtype=torch.int32))
+        ds = Hp.device_inputs(sub)
+        part = Hp.gpu_logits(sub, Hp.make_plan(sub), ds)
+        assert torch.equal(part, full[a:b])
+
+
+# ------------------------------------------------------------- candidates
+
+def test_candidate_blocks_and_masked_consumer_scaled():
+    spec = dataclasses.replace(W.CONFIGS["ragged_cand"], topk=40, cand_topk=30, requests=(
+        W.RequestSpec(90, 0, 1), W.RequestSpec(90, 0, 2), W.RequestSpec(50, 2000, 1)))
+    p = W.make_problem(spec)
+    plan = Hp.make_plan(p, key_block=1024)
+    d = Hp.device_inputs(p)
+    T = int(p.cu_seqlens_q[-1])
+    rows = np.arange(T)
+    ref = oracle_rows(p, rows)
+    mask = Hp.gpu_candidates(p, plan, d).cpu().numpy()
+    cl = p.compress_len.numpy()
+    for t in rows:
+        Hp.check_mask_row(mask[t], ref[t], int(cl[t]), 8, 30)
+    # selector isolation at block level on the GPU's own logits
+    g = Hp.gpu_logits(p, plan, d).cpu().numpy().astype(np.float64)
+    want = O.candidates_rows(g, cl, 8, 30, mask.shape[1])
+    assert np.array_equal(want, mask)
+    # consumer: new queries, same keys, top-k within the candidate blocks
+    d2 = Hp.device_inputs(p, layer=2)
+    fi, _ = Hp.gpu_fused(p, plan, d2, mask=torch.from_numpy(mask).cuda())
+    fi = fi.cpu().numpy()
+    ref2 = oracle_rows(p, rows, layer=2)
+    for t in rows:
+        Hp.check_topk_row(fi[t], ref2[t], int(cl[t]), p.topk, mask_row=mask[t])
+    # key-level expansion of the block mask
+    km = torch.empty((T, Hp.max_keys(p)), dtype=torch.uint8, device="cuda")
+    K.indexer_expand_mask(plan, torch.from_numpy(mask).cuda(), d["compress_len"], km)
+    km = km.cpu().numpy()
+    j = np.arange(km.shape[1])
+    for t in rows:
+        assert np.array_equal(km[t], ((j < cl[t]) & (mask[t][j // 8] != 0)).astype(np.uint8))
+
+
+# ----------------------------------------------------------- full size
+
+def full_size_check(name, per_request, layer_mask=None):
+    p = W.make_problem(W.CONFIGS[name])
+    plan = Hp.make_plan(p, key_block=p.spec.key_block)
+    assert plan.workspace_bytes <= 2 << 30
+    d = Hp.device_inputs(p)
+    fi, fv = Hp.gpu_fused(p, plan, d)
+    rows = W.sample_rows(p, per_request)
+    ref = oracle_rows(p, rows)
+    fi = fi.cpu().numpy()
+    cl = p.compress_len.numpy()
+    exact = sum(Hp.check_topk_row(fi[t], ref[i], int(cl[t]), p.topk) for i, t in enumerate(rows))
+    return p, plan, d, exact, len(rows)
+
+
+def test_full_cold_chunk_t2048_l65536_top2048():
+    _, _, _, exact, n = full_size_check("cold64k", 48)
+    assert exact >= n // 2
+
+
+def test_full_long_context_t16384_l487936_top512():
+    _, _, _, exact, n = full_size_check("long488k", 16)
+    assert exact >= n // 2
+
+
+def test_full_ragged_candidates():
+    p = W.make_problem(W.CONFIGS["ragged_cand"])
+    plan = Hp.make_plan(p)
+    assert plan.workspace_bytes <= 2 << 30
+    d = Hp.device_inputs(p)
+    mask = Hp.gpu_candidates(p, plan, d)
+    rows = W.sample_rows(p, 12)
+    ref = oracle_rows(p, rows)
+    m = mask.cpu().numpy()
+    cl = p.compress_len.numpy()
+    for i, t in enumerate(rows):
+        Hp.check_mask_row(m[t], ref[i], int(cl[t]), 8, p.spec.cand_topk)
+    d2 = Hp.device_inputs(p, layer=2)
+    fi, _ = Hp.gpu_fused(p, plan, d2, mask=mask)
+    fi = fi.cpu().numpy()
+    ref2 = oracle_rows(p, rows, layer=2)
+    for i, t in enumerate(rows):
+        Hp.check_topk_row(fi[t], ref2[i], int(cl[t]), p.topk, mask_row=m[t])
+
+
+# ------------------------------------------------------------ failure paths
+
+def test_bounded_wait_reports_timeout_instead_of_hanging():
+    ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    K.indexer_selftest_timeout(ws, 200000)
+    assert K.indexer_status(None, ws) == K.IDX_ERR_TIMEOUT
+    # the context is still usable afterwards
+    p = W.make_problem(W.CONFIGS["tiny"])
+    plan = Hp.make_plan(p)
+    Hp.gpu_logits(p, plan, Hp.device_inputs(p))
+
+
+def test_workspace_too_small_is_rejected():
+    p = W.make_problem(W.CONFIGS["tiny"])
+    plan = Hp.make_plan(p)
+    d = Hp.device_inputs(p)
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    out = torch.empty((64, 1024), dtype=torch.float32, device="cuda")
+    with pytest.raises(K.IndexerError) as e:
+        K.indexer_logits(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"],
+                         d["compress_len"], out, ws)
+    assert e.value.code == K.IDX_ERR_WORKSPACE
