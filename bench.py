@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--config", default="cold64k")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["fused", "logits", "topk"], default=None,
+                    help="run just warmup+steps launches of one call (for profiler captures)")
     return ap.parse_args()
 
 
@@ -201,6 +203,29 @@ def main():
     def step():
         K.indexer_fused_topk(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"],
                              d["compress_len"], None, idx, val, wsb)
+
+    if args.only:
+        ld = int(torch.diff(p.cu_seqlens_k).max())
+        if args.only == "fused":
+            fn = step
+        else:
+            logits = torch.empty((T, ld), dtype=torch.float32, device=dev)
+
+            def fn_logits():
+                K.indexer_logits(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"],
+                                 d["compress_len"], logits, wsb)
+            fn = fn_logits
+            if args.only == "topk":
+                fn_logits()
+
+                def fn():
+                    K.indexer_topk(plan, logits, d["compress_len"], idx, val, wsb)
+        for _ in range(args.warmup + args.steps):
+            fn()
+        torch.cuda.synchronize()
+        assert K.indexer_status(plan, wsb) == K.IDX_OK
+        print(json.dumps({"only": args.only, "launches": args.warmup + args.steps}))
+        return
 
     clocks = ClockSampler(dev.index if ws_n == 1 else local)
     for _ in range(args.warmup):

@@ -47,8 +47,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool supported_shape(int H, int D, int kdtype)
 {
-    if (kdtype != IDX_K_FP8_E4M3)
-        return false;
+    if (kdtype == IDX_K_FP4_E2M1_UE8M0)
+        return H == 32 && D == 128;
     return (H == 32 && D == 128) || (H == 16 && D == 128) || (H == 64 && D == 128) ||
            (H == 4 && D == 64);
 }
@@ -130,6 +130,27 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t row_byte
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Map over packed e2m1 keys [rows, D/2 bytes] that unpacks each 16-element
+// group into a 16-byte shared-memory slot (8 data bytes, 8 bytes gap): the
+// 8-bit-container layout the f8f6f4 MMA kinds read 4-bit operands from.  A
+// box of 128 elements x box_rows lands as box_rows rows of 128 bytes,
+// 128-byte swizzled like the e4m3 tiles.
+bool make_map_fp4(CUtensorMap* m, const void* base, uint64_t rows, uint32_t D,
+                  uint32_t box_rows)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {D, rows};
+    const cuuint64_t strides[1] = {D / 2};
+    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 struct DeviceInfo {
     int sms = 0;
     bool ok = false;
@@ -167,7 +188,8 @@ int check_inputs(const indexer_plan_s* p, const void* q, const float* s_q, const
 {
     if (!q || !s_q || !w || !k || !k_scale || !clen)
         return IDX_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(s_q, 4) || !aligned(w, 4) ||
+    if (!aligned(q, 16) || !aligned(k, p->kdtype == IDX_K_FP8_E4M3 ? 16 : 32) ||
+        !aligned(s_q, 4) || !aligned(w, 4) ||
         !aligned(clen, 4) || (p->kdtype == IDX_K_FP8_E4M3 && !aligned(k_scale, 4)))
         return IDX_ERR_INVALID_ARG;
     return IDX_OK;
@@ -190,19 +212,21 @@ int fill_maps(Ctx& c, const void* q, const void* k)
 {
     const indexer_plan_s* p = c.p;
     std::memset(&c.lp, 0, sizeof(c.lp));
-    if (!make_map(&c.lp.tmap_q, q, (uint64_t)p->T * p->H, p->D, kTileN))
+    const int G = logits_rows_per_group(p->H, p->kdtype);
+    if (!make_map(&c.lp.tmap_q, q, (uint64_t)p->T * p->H, p->D, G * p->H))
         return IDX_ERR_CUDA;
-    const uint32_t krow = p->kdtype == IDX_K_FP8_E4M3 ? p->D : p->D / 2;
-    if (!make_map(&c.lp.tmap_k, k, (uint64_t)std::max(p->Lk, 1), krow, kTileKeys))
-        return IDX_ERR_CUDA;
-    return IDX_OK;
+    const uint64_t krows = (uint64_t)std::max(p->Lk, 1);
+    const bool ok = p->kdtype == IDX_K_FP8_E4M3
+                        ? make_map(&c.lp.tmap_k, k, krows, p->D, kTileKeys)
+                        : make_map_fp4(&c.lp.tmap_k, k, krows, p->D, kTileKeys);
+    return ok ? IDX_OK : IDX_ERR_CUDA;
 }
 
 // Launch the logits kernel over a list of segments (<= kMaxSegments).
 int run_logits(Ctx& c, const std::vector<Segment>& segs_in, float* out)
 {
     const indexer_plan_s* p = c.p;
-    const int G = kTileN / p->H;
+    const int G = logits_rows_per_group(p->H, p->kdtype);
     // choose key tiles per unit so that there are several units per SM
     int64_t work = 0;
     for (const Segment& s : segs_in)
@@ -463,7 +487,7 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
     // Key block: the caller's, else the candidate (whole prefix, 64K, 32K, ... 1K keys)
     // needing the fewest logits passes within the budget.
     const int round_L = std::max(kTileKeys, (p->max_L + kTileKeys - 1) / kTileKeys * kTileKeys);
-    const int G = kTileN / p->H;
+    const int G = logits_rows_per_group(p->H, p->kdtype);
     std::vector<int> cands;
     if (pr->key_block)
         cands.push_back(std::min(pr->key_block, round_L));

@@ -96,6 +96,7 @@ struct SelParams {
 cudaError_t launch_logits(const LogitsParams& p, int H, int D, int kfmt, int grid,
                           cudaStream_t stream);
 size_t logits_smem_bytes(int H, int D, int kfmt);
+int logits_rows_per_group(int H, int kfmt);   // query rows per MMA tile
 
 // Per-row top-k of dense rows into candidate slots (rows = total of segs).
 cudaError_t launch_select_dense(const SelParams& p, cudaStream_t stream);

@@ -30,21 +30,32 @@
 namespace idx {
 namespace {
 
-template <int H, int D>
+template <int H, int D, int KFMT>
 struct Cfg {
-    static constexpr int G = kTileN / H;              // query rows per tile
-    static constexpr int QBYTES = kTileN * D;         // Q tile: 256 rows of D bytes
-    static constexpr int KBYTES = kTileKeys * D;      // K tile: 128 keys of D bytes
+    // fp4 keys need TMEM columns for the block scales, so their tiles are
+    // 192 columns wide (two accumulators of 192 + scale columns <= 512).
+    static constexpr int NMAX = KFMT == kKeyFp8 ? kTileN : 192;
+    static constexpr int G = NMAX / H;                 // query rows per tile
+    static constexpr int N = G * H;                    // MMA N
+    static constexpr int QBYTES = N * D;               // Q tile: N rows of D bytes
+    static constexpr int KBYTES = kTileKeys * D;       // K tile in smem (fp4 unpacked to bytes)
     static constexpr int STAGES = (D >= 128) ? 6 : 8;
-    static constexpr int KSTEPS = D / 32;             // MMA K = 32 bytes of fp8
-    static constexpr int ROWS_PER_HALF = G / 2;       // rows one epilogue thread reduces
-    static constexpr int ACC_COLS = kTileN;           // TMEM columns per accumulator
+    static constexpr int KSTEPS = D / 32;              // MMA K = 32 elements
+    static constexpr int ROWS_PER_HALF = G / 2;        // rows one epilogue thread reduces
+    static constexpr int HALF_COLS = N / 2;
+    static constexpr int ACC_COLS = N;                 // TMEM columns per accumulator
+    static constexpr int SF_BYTES = KFMT == kKeyFp4 ? kTileKeys * 16 : 0;  // per stage
+    static constexpr int TMEM_SFA = 2 * ACC_COLS;      // 4 columns per stage
+    static constexpr int TMEM_SFB = TMEM_SFA + 4 * STAGES;
     static_assert(D == 32 || D == 64 || D == 128, "D must be 32, 64 or 128");
-    static_assert(kTileN % H == 0 && G >= 2, "H must divide 128");
+    static_assert(G >= 2 && G % 2 == 0 && N % 16 == 0, "H must leave an even row count");
+    static_assert(HALF_COLS % 32 == 0, "half tile must be whole 32-column loads");
+    static_assert(KFMT == kKeyFp8 || (D == 128 && TMEM_SFB + 4 <= 512), "fp4 needs D=128");
     // shared memory carve-up (offsets from a 1024-byte aligned base)
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + 2 * QBYTES;
-    static constexpr int OFF_C = OFF_K + STAGES * KBYTES;          // float c[2][256]
+    static constexpr int OFF_K = OFF_Q + ((2 * QBYTES + 1023) / 1024) * 1024;
+    static constexpr int OFF_SF = OFF_K + STAGES * KBYTES;
+    static constexpr int OFF_C = OFF_SF + STAGES * SF_BYTES;        // float c[2][N]
     static constexpr int OFF_BAR = OFF_C + 2 * kTileN * 4;
     static constexpr int NBARS = 2 + 2 + 2 * STAGES + 2 + 2 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
@@ -103,12 +114,13 @@ template <int H, int D, int KFMT>
 __global__ void __launch_bounds__(kThreads, 1)
     logits_tc_kernel(const __grid_constant__ LogitsParams p)
 {
-    using C = Cfg<H, D>;
+    using C = Cfg<H, D, KFMT>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* q_s = smem + C::OFF_Q;
     uint8_t* k_s = smem + C::OFF_K;
+    uint8_t* sf_s = smem + C::OFF_SF;
     float* c_s = reinterpret_cast<float*>(smem + C::OFF_C);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* q_full = bars;
@@ -132,7 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&a_empty[i], kEpiWarps);
         }
         for (int i = 0; i < C::STAGES; ++i) {
-            mbar_init(&k_full[i], 1);
+            // fp4: one arrival with the TMA bytes plus one after the scales are staged
+            mbar_init(&k_full[i], KFMT == kKeyFp4 ? 2 : 1);
             mbar_init(&k_empty[i], 1);
         }
         mbar_init(drain, 1);
@@ -152,6 +165,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const long long budget = p.timeout_cycles;
+    if (KFMT == kKeyFp4) {
+        // q carries no block scale: every B scale is 2^0 (ue8m0 127) in all bytes
+        if (warp >= 4 && warp < 8) {
+            const uint32_t one = 0x7F7F7F7Fu;
+            tmem_st_32x32b_x4(tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) +
+                                  C::TMEM_SFB,
+                              one, one, one, one);
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -175,23 +201,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(q_s + qb * C::QBYTES, &p.tmap_q, &q_full[qb], 0, ui.t0 * H);
                     ++q_issued[qb];
                 }
-                for (int i = 0; i < ui.ntiles_mma && ok; ++i) {
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            for (int i = 0; i < ui.ntiles_mma && ok; ++i) {
+                const int key0 = sg.key_base + ui.j0 + i * kTileKeys;
+                if (lane == 0) {
                     if (!mbar_wait(&k_empty[ks], kph ^ 1, budget, abort_flag)) {
                         report(p, abort_flag, kStatusTimeout);
                         ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&k_full[ks], C::KBYTES);
-                    tma_load_2d(k_s + ks * C::KBYTES, &p.tmap_k, &k_full[ks], 0,
-                                sg.key_base + ui.j0 + i * kTileKeys);
-                    ++issued[ks];
-                    if (++ks == C::STAGES) {
-                        ks = 0;
-                        kph ^= 1;
+                    } else {
+                        mbar_arrive_expect_tx(&k_full[ks], C::KBYTES);
+                        tma_load_2d(k_s + ks * C::KBYTES, &p.tmap_k, &k_full[ks], 0, key0);
+                        ++issued[ks];
                     }
                 }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok)
+                    break;
+                if (KFMT == kKeyFp4) {
+                    // stage the tile's ue8m0 scales, one 32-bit word (4 blocks of 32
+                    // elements) per key, at a 16-byte row pitch for tcgen05.cp
+                    uint8_t* sf = sf_s + ks * C::SF_BYTES;
+                    const uint32_t* src = reinterpret_cast<const uint32_t*>(p.k_sf);
+#pragma unroll
+                    for (int r = 0; r < kTileKeys / 32; ++r) {
+                        const int m = r * 32 + lane;
+                        const int key = key0 + m;
+                        const int local = ui.j0 + i * kTileKeys + m;
+                        const uint32_t word = local < sg.key_count ? __ldg(src + key) : 0x7F7F7F7Fu;
+                        *reinterpret_cast<uint32_t*>(sf + m * 16) = word;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&k_full[ks]);
+                }
+                if (++ks == C::STAGES) {
+                    ks = 0;
+                    kph ^= 1;
+                }
             }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (++qb == 2) {
                 qb = 0;
                 qph ^= 1;
@@ -209,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        constexpr uint32_t idesc = idesc_f8f6f4(kTileKeys, kTileN, 0, KFMT == kKeyFp8 ? 0 : 5);
+        constexpr uint32_t idesc = idesc_f8f6f4(kTileKeys, C::N, 0, 0);
         int ks = 0, kph = 0, qb = 0, qph = 0, ab = 0, aph = 0;
         bool ok = true;
         bool any = false;
@@ -233,11 +282,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t k_addr = smem_u32(k_s + ks * C::KBYTES);
                     const uint32_t d_tmem = tmem_base + ab * C::ACC_COLS;
+                    if (KFMT == kKeyFp8) {
 #pragma unroll
-                    for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                        const uint64_t adesc = smem_desc_kmajor(k_addr + kk * 32, D);
-                        const uint64_t bdesc = smem_desc_kmajor(q_addr + kk * 32, D);
-                        mma_f8f6f4(d_tmem, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                            const uint64_t adesc = smem_desc_kmajor(k_addr + kk * 32, D);
+                            const uint64_t bdesc = smem_desc_kmajor(q_addr + kk * 32, D);
+                            mma_f8f6f4(d_tmem, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+                        }
+                    } else {
+                        // key scales of this stage into TMEM, then one block-scaled MMA per
+                        // 32-element block (A = e2m1 keys, B = e4m3 queries)
+                        const uint32_t sfa = tmem_base + C::TMEM_SFA + 4 * ks;
+                        tmem_cp_128x128b(sfa, smem_desc_noswizzle(smem_u32(sf_s + ks * C::SF_BYTES), 128));
+#pragma unroll
+                        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                            const uint64_t adesc = smem_desc_kmajor(k_addr + kk * 32, D);
+                            const uint64_t bdesc = smem_desc_kmajor(q_addr + kk * 32, D);
+                            mma_mxf8f6f4(d_tmem, adesc, bdesc,
+                                         idesc_mxf8f6f4(kTileKeys, C::N, 5, 0, kk, kk), sfa,
+                                         tmem_base + C::TMEM_SFB, kk > 0 ? 1u : 0u);
+                        }
                     }
                     mma_commit(&k_empty[ks]);
                     mma_commit(&a_full[ab]);
@@ -281,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const UnitInfo ui = decode_unit<C::G>(p, u, lane);
             const Segment& sg = p.seg[ui.seg];
             float* cbuf = c_s + (it & 1) * kTileN;
-            {   // c[n] = w * s_q for column n = row * H + head (0 for rows past the group)
+            if (etid < C::N) {   // c[n] = w * s_q for column n = row * H + head
                 const int rl = etid / H;
                 const int t = ui.t0 + rl;
                 cbuf[etid] = rl < ui.nr ? p.w[(size_t)t * H + (etid % H)] *
@@ -318,11 +382,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int r = 0; r < C::ROWS_PER_HALF; ++r)
                         acc[r] = 0.0f;
                     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                           ab * C::ACC_COLS + half * (kTileN / 2);
+                                           ab * C::ACC_COLS + half * C::HALF_COLS;
                     const float4* cc4 =
-                        reinterpret_cast<const float4*>(cbuf + half * (kTileN / 2));
+                        reinterpret_cast<const float4*>(cbuf + half * C::HALF_COLS);
 #pragma unroll
-                    for (int ch = 0; ch < (kTileN / 2) / 32; ++ch) {
+                    for (int ch = 0; ch < C::HALF_COLS / 32; ++ch) {
                         float v[32];
                         tmem_ld_32x32b_x32(tbase + ch * 32, v);
                         tmem_wait_ld();
@@ -378,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int H, int D, int KFMT>
 cudaError_t launch_one(const LogitsParams& p, int grid, cudaStream_t stream)
 {
-    using C = Cfg<H, D>;
+    using C = Cfg<H, D, KFMT>;
     auto kern = logits_tc_kernel<H, D, KFMT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);
@@ -392,17 +456,20 @@ cudaError_t launch_one(const LogitsParams& p, int grid, cudaStream_t stream)
 
 size_t logits_smem_bytes(int H, int D, int kfmt)
 {
-    (void)kfmt;
+    if (kfmt == kKeyFp4)
+        return (H == 32 && D == 128) ? Cfg<32, 128, kKeyFp4>::SMEM : 0;
     if (H == 32 && D == 128)
-        return Cfg<32, 128>::SMEM;
+        return Cfg<32, 128, kKeyFp8>::SMEM;
     if (H == 4 && D == 64)
-        return Cfg<4, 64>::SMEM;
+        return Cfg<4, 64, kKeyFp8>::SMEM;
     if (H == 64 && D == 128)
-        return Cfg<64, 128>::SMEM;
+        return Cfg<64, 128, kKeyFp8>::SMEM;
     if (H == 16 && D == 128)
-        return Cfg<16, 128>::SMEM;
+        return Cfg<16, 128, kKeyFp8>::SMEM;
     return 0;
 }
+
+int logits_rows_per_group(int H, int kfmt) { return (kfmt == kKeyFp4 ? 192 : kTileN) / H; }
 
 cudaError_t launch_logits(const LogitsParams& p, int H, int D, int kfmt, int grid,
                           cudaStream_t stream)
@@ -416,6 +483,9 @@ cudaError_t launch_logits(const LogitsParams& p, int H, int D, int kfmt, int gri
             return launch_one<64, 128, kKeyFp8>(p, grid, stream);
         if (H == 16 && D == 128)
             return launch_one<16, 128, kKeyFp8>(p, grid, stream);
+    } else if (kfmt == kKeyFp4) {
+        if (H == 32 && D == 128)
+            return launch_one<32, 128, kKeyFp4>(p, grid, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -93,6 +93,23 @@ def test_ragged_requests_parity():
     check_all(p, key_block=1024)
 
 
+def test_fp4_keys_scaled_parity():
+    """fp8 queries x e2m1 keys with one ue8m0 scale per 32 elements (block-scaled MMA)."""
+    p = small("v4ratio2", 16, 32, topk=64)
+    check_all(p, key_block=1024)
+
+
+def test_fp4_exact_arithmetic_inputs_are_bit_exact():
+    spec = dataclasses.replace(W.scaled(W.CONFIGS["v4ratio2"], 32, 64), topk=50, exact=True)
+    p = W.make_problem(spec)
+    plan = Hp.make_plan(p, key_block=512)
+    d = Hp.device_inputs(p)
+    T = int(p.cu_seqlens_q[-1])
+    ref = oracle_rows(p, np.arange(T))
+    g = Hp.gpu_logits(p, plan, d).cpu().numpy().astype(np.float64)
+    assert np.array_equal(g, ref)
+
+
 def test_exact_arithmetic_inputs_are_bit_exact():
     """Small integer codes and power-of-two scales: every fp32 step is exact, so GPU logits
     equal the oracle's bitwise and selections match including ties."""
@@ -190,6 +207,11 @@ def full_size_check(name, per_request, layer_mask=None):
 
 def test_full_cold_chunk_t2048_l65536_top2048():
     _, _, _, exact, n = full_size_check("cold64k", 48)
+    assert exact >= n // 2
+
+
+def test_full_v4_low_ratio_fp4_t2048_l100000_top512():
+    _, _, _, exact, n = full_size_check("v4ratio2", 48)
     assert exact >= n // 2
 
 
