@@ -208,6 +208,37 @@ int indexer_selftest_timeout(void* ws, long long cycles, void* stream);
    (default about two seconds). */
 int indexer_set_wait_budget(indexer_plan_t plan, long long cycles);
 
+/*
+ * Fused top-k without a caller-provided workspace (no counterpart on the
+ * pages: this entry point exists for callers that cannot allocate device
+ * memory).  Some callers have no way to obtain device memory for a workspace:
+ * a plugin whose host application owns all device memory through its own pool
+ * and exposes no allocator, or a serving loop in which a cudaMalloc would
+ * stall every stream on the device.  This variant computes exactly what
+ * indexer_fused_topk computes, with the same arguments minus ws/ws_bytes; its
+ * workspace is a file-scope device array of IDX_NOALLOC_SCRATCH_BYTES (64 MiB)
+ * that every GPU loading this library holds until the process exits.
+ *   - Limit: the plan's workspace must fit the array; build the plan with
+ *     transient_budget_bytes <= 64 MiB.  A larger plan is rejected with
+ *     IDX_ERR_WORKSPACE before anything is launched.
+ *   - Allocation: none.  No cudaMalloc, cudaFree or allocating library call.
+ *   - Set-up: the first call on a device resolves the array's device address
+ *     (cudaGetSymbolAddress) with that device current and caches it; make
+ *     that first call before any stream capture.
+ *   - Sharing: every call uses the same array and it keeps the previous call's
+ *     contents (the call clears what it needs cleared).  Calls whose work
+ *     overlaps on the GPU (different streams, or several threads) race on the
+ *     array: serialize them.
+ *   - Status: a device-side wait that runs out is recorded in the array's
+ *     status word, which no other entry point reads; callers that need that
+ *     report use indexer_fused_topk with their own workspace.
+ */
+#define IDX_NOALLOC_SCRATCH_BYTES (64ull << 20)
+int indexer_fused_topk_noalloc(indexer_plan_t plan, const void* q, const float* s_q,
+                               const float* w, const void* k, const void* k_scale,
+                               const int32_t* compress_len, const uint8_t* cand_mask,
+                               int64_t ld_mask, int32_t* out_idx, float* out_val, void* stream);
+
 /* Number of kernels this library has launched in this process (a
    diagnostic counter for benchmarks; never reset). */
 long long indexer_launch_count(void);

@@ -32,7 +32,8 @@ EXPORTED = ("indexer_plan", "indexer_plan_destroy", "indexer_plan_info", "indexe
             "indexer_topk", "indexer_fused_topk", "indexer_candidate_blocks",
             "indexer_expand_mask", "indexer_status", "indexer_selftest_timeout",
             "indexer_set_wait_budget", "indexer_launch_count", "indexer_error_string",
-            "indexer_version")
+            "indexer_version", "indexer_fused_topk_noalloc")
+IDX_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class IndexerError(RuntimeError):
@@ -83,6 +84,7 @@ def lib():
         L.indexer_selftest_timeout.argtypes = [P, ctypes.c_longlong, P]
         L.indexer_set_wait_budget.argtypes = [P, ctypes.c_longlong]
         L.indexer_launch_count.argtypes = []
+        L.indexer_fused_topk_noalloc.argtypes = [P, P, P, P, P, P, P, P, i64, P, P, P]
         L.indexer_error_string.argtypes = [i32]
         L.indexer_error_string.restype = ctypes.c_char_p
         for name in EXPORTED:
@@ -206,6 +208,15 @@ def indexer_selftest_timeout(ws, cycles: int, stream=None):
 
 def indexer_set_wait_budget(plan: Plan, cycles: int):
     _check("indexer_set_wait_budget", lib().indexer_set_wait_budget(plan.handle, int(cycles)))
+
+
+def indexer_fused_topk_noalloc(plan: Plan, q, s_q, w, k, k_scale, compress_len, cand_mask,
+                               out_idx, out_val, stream=None):
+    """indexer_fused_topk with the library's fixed device scratch as the workspace."""
+    ldm = cand_mask.stride(0) if cand_mask is not None else 0
+    _check("indexer_fused_topk_noalloc", lib().indexer_fused_topk_noalloc(
+        plan.handle, _ptr(q), _ptr(s_q), _ptr(w), _ptr(k), _ptr(k_scale), _ptr(compress_len),
+        _ptr(cand_mask), ldm, _ptr(out_idx), _ptr(out_val), _stream(stream)))
 
 
 def indexer_launch_count() -> int:

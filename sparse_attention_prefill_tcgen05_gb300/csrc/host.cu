@@ -713,6 +713,62 @@ int indexer_selftest_timeout(void* ws, long long cycles, void* stream)
                : IDX_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free fused top-k.  Some callers cannot obtain device memory for a
+// workspace: plugins whose host application owns every byte of device memory
+// through its own pool and exposes no allocator, or serving loops where a
+// cudaMalloc would stall every stream on the device.  For them the workspace
+// lives in this fixed, file-scope device array instead.  Every GPU that loads
+// the library reserves it until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = IDX_NOALLOC_SCRATCH_BYTES;  // 64 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[256] = {};  // device address of the array, per device ordinal
+
+// Device address of the array on the current device.  The first call on a device
+// resolves it with cudaGetSymbolAddress (the host-side name of the array is a
+// stand-in, not a device address); later calls reuse the cached pointer.
+int noalloc_scratch(void** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256)
+        return IDX_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+            return IDX_ERR_CUDA;
+        g_noalloc_addr[dev] = ptr;
+    }
+    *out = g_noalloc_addr[dev];
+    return IDX_OK;
+}
+
+}  // namespace
+
+int indexer_fused_topk_noalloc(indexer_plan_t p, const void* q, const float* s_q, const float* w,
+                               const void* k, const void* k_scale, const int32_t* clen,
+                               const uint8_t* cand_mask, int64_t ld_mask, int32_t* out_idx,
+                               float* out_val, void* stream)
+{
+    if (!p)
+        return IDX_ERR_INVALID_ARG;
+    if (p->ws_bytes > kNoAllocScratchBytes)
+        return IDX_ERR_WORKSPACE;
+    if (!device_info().ok)
+        return IDX_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    int rc = noalloc_scratch(&scratch);
+    if (rc != IDX_OK)
+        return rc;
+    return indexer_fused_topk(p, q, s_q, w, k, k_scale, clen, cand_mask, ld_mask, out_idx,
+                              out_val, scratch, kNoAllocScratchBytes, stream);
+}
+
 int indexer_status(indexer_plan_t p, const void* ws, void* stream)
 {
     (void)p;
