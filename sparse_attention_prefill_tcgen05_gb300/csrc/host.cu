@@ -47,8 +47,10 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool supported_shape(int H, int D, int kdtype)
 {
+    // e2m1 keys: the block-scaled MMA kernel raised an illegal instruction on its
+    // first GB300 run and is not launched until that is understood.
     if (kdtype == IDX_K_FP4_E2M1_UE8M0)
-        return H == 32 && D == 128;
+        return false;
     return (H == 32 && D == 128) || (H == 16 && D == 128) || (H == 64 && D == 128) ||
            (H == 4 && D == 64);
 }
