@@ -19,7 +19,7 @@ ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libindexer.so")
 SOURCES = ["logits_tc.cu", "select.cu", "misc.cu", "host.cu"]
-HEADERS = ["internal.h", "ptx.cuh"]
+HEADERS = ["internal.h", "ptx.cuh", "groupsel.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]

@@ -8,31 +8,51 @@
 #include <new>
 #include <vector>
 
-#include "../../include/indexer.h"
+#include "indexer.h"
 #include "internal.h"
 #include "ptx.cuh"
 
 using namespace idx;
 
+namespace {
+
+// Rows [a, b) of request r whose lists live at list_off (entries) during one pass.
+struct PassPiece {
+    int r, a, b;
+    int64_t list_off;
+};
+
+// One pass of the streamed top-k: a logits launch that fills the pieces' lists
+// and the merge launch that selects from them.  Passes reuse the list area.
+struct Pass {
+    std::vector<PassPiece> pieces;
+};
+
+constexpr int kUpdateTiles = 4;          // tiles between threshold refreshes
+constexpr int64_t kTargetUnits = 1024;   // units per launch wanted for load balance
+
+}  // namespace
+
 struct indexer_plan_s {
     int R = 0, T = 0, Lk = 0, H = 0, D = 0, topk = 0, kdtype = 0;
     int cand_block = 8, cand_topk = 0;
+    int G = 8;                        // query rows per MMA tile
     std::vector<int32_t> row_begin;   // [R+1]
     std::vector<int32_t> key_begin;   // [R+1]
     std::vector<int32_t> L;           // [R]
     std::vector<int32_t> clen;        // [T]
     int max_L = 0;
     uint64_t budget = 0;
-    // blocked top-k
-    int key_block = 0;                // B_k (multiple of 128)
-    int row_chunk = 0;                // rows of scratch logits per pass
+    // streamed selection
+    int split_keys = 0;               // keys per split (multiple of 128)
     std::vector<int32_t> n_splits;    // per request
-    std::vector<int64_t> cand_off;    // per request, entries (topk per slot)
-    std::vector<int64_t> cblk_off;    // per request, entries (cand_topk per slot)
-    int64_t cand_entries = 0, cblk_entries = 0;
+    std::vector<int32_t> cap_k;       // sub-list capacity per (row, split, quadrant), keys
+    std::vector<int32_t> cap_b;       // sub-list capacity per (row, split, quadrant), blocks
+    std::vector<int64_t> cnt_base;    // counts index of the request's first row
+    std::vector<Pass> passes_k, passes_b;
+    int max_piece_rows = 0;
     // workspace layout (bytes)
-    size_t off_cand_val = 0, off_cand_idx = 0, off_cblk_val = 0, off_cblk_idx = 0;
-    size_t off_scratch = 0, scratch_bytes = 0, ws_bytes = 0;
+    size_t off_gtau = 0, off_counts = 0, off_lists = 0, ws_bytes = 0;
     long long wait_budget = 4000000000LL;
 };
 
@@ -55,41 +75,61 @@ bool supported_shape(int H, int D, int kdtype)
            (H == 4 && D == 64);
 }
 
-// Lay out the workspace for a key block and row chunk; returns total bytes.
-size_t layout(indexer_plan_s& p, int key_block, int row_chunk)
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Group the rows of every request into passes whose lists fit `entries`.
+// Returns false if even one row of some request does not fit.
+bool build_passes(const indexer_plan_s& p, const std::vector<int32_t>& cap, int64_t entries,
+                  std::vector<Pass>& passes, int& max_rows)
 {
-    p.key_block = key_block;
-    p.row_chunk = row_chunk;
-    p.n_splits.assign(p.R, 1);
-    p.cand_off.assign(p.R, 0);
-    p.cblk_off.assign(p.R, 0);
-    int64_t ce = 0, be = 0;
+    passes.clear();
+    Pass cur;
+    int64_t used = 0;
+    int segs = 0;
     for (int r = 0; r < p.R; ++r) {
-        const int ns = std::max(1, (p.L[r] + key_block - 1) / key_block);
-        p.n_splits[r] = ns;
-        p.cand_off[r] = ce;
-        p.cblk_off[r] = be;
-        const int64_t rows = p.row_begin[r + 1] - p.row_begin[r];
-        ce += rows * ns * p.topk;
-        be += rows * ns * p.cand_topk;
+        const int rb = p.row_begin[r], re = p.row_begin[r + 1];
+        if (re == rb)
+            continue;
+        const int64_t per_row = (int64_t)p.n_splits[r] * kListsPerSplit * cap[r];
+        int64_t fit = entries / per_row;
+        if (fit < 1)
+            return false;
+        if (fit >= p.G)
+            fit = fit / p.G * p.G;
+        for (int a = rb; a < re;) {
+            const int b = (int)std::min<int64_t>(re, a + fit);
+            const int64_t need = (int64_t)(b - a) * per_row;
+            if (!cur.pieces.empty() &&
+                (used + need > entries || segs + p.n_splits[r] > kMaxSegments ||
+                 (int)cur.pieces.size() == kMaxMergePieces)) {
+                passes.push_back(cur);
+                cur.pieces.clear();
+                used = 0;
+                segs = 0;
+            }
+            cur.pieces.push_back(PassPiece{r, a, b, used});
+            used += need;
+            segs += p.n_splits[r];
+            max_rows = std::max(max_rows, b - a);
+            a = b;
+        }
     }
-    if (p.cand_topk == 0)
-        be = 0;
-    p.cand_entries = ce;
-    p.cblk_entries = be;
-    // top-k candidates and candidate-block candidates are never live in the
-    // same call, so they share one area
-    const size_t area = (size_t)std::max(ce, be) * 4;
-    size_t off = kStatusBytes;
-    p.off_cand_val = p.off_cblk_val = off;
-    off = align_up(off + area, 256);
-    p.off_cand_idx = p.off_cblk_idx = off;
-    off = align_up(off + area, 256);
-    p.off_scratch = off;
-    p.scratch_bytes = (size_t)row_chunk * key_block * 4;
-    off = align_up(off + p.scratch_bytes, 256);
-    p.ws_bytes = off;
-    return off;
+    if (!cur.pieces.empty())
+        passes.push_back(cur);
+    return true;
+}
+
+int64_t pass_entries(const indexer_plan_s& p, const std::vector<Pass>& passes,
+                     const std::vector<int32_t>& cap)
+{
+    int64_t m = 0;
+    for (const Pass& ps : passes) {
+        int64_t u = 0;
+        for (const PassPiece& pc : ps.pieces)
+            u += (int64_t)(pc.b - pc.a) * p.n_splits[pc.r] * kListsPerSplit * cap[pc.r];
+        m = std::max(m, u);
+    }
+    return m;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -130,27 +170,6 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t row_byte
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Map over packed e2m1 keys [rows, D/2 bytes] that unpacks each 16-element
-// group into a 16-byte shared-memory slot (8 data bytes, 8 bytes gap): the
-// 8-bit-container layout the f8f6f4 MMA kinds read 4-bit operands from.  A
-// box of 128 elements x box_rows lands as box_rows rows of 128 bytes,
-// 128-byte swizzled like the e4m3 tiles.
-bool make_map_fp4(CUtensorMap* m, const void* base, uint64_t rows, uint32_t D,
-                  uint32_t box_rows)
-{
-    EncodeTiledFn enc = encode_fn();
-    if (!enc)
-        return false;
-    const cuuint64_t dims[2] = {D, rows};
-    const cuuint64_t strides[1] = {D / 2};
-    const cuuint32_t box[2] = {128, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
 }
 
 struct DeviceInfo {
@@ -197,12 +216,6 @@ int check_inputs(const indexer_plan_s* p, const void* q, const float* s_q, const
     return IDX_OK;
 }
 
-// One piece of blocked work: rows [a, b) of request r against key split s.
-struct Piece {
-    int r, a, b, s;
-    int width;  // keys of the split, rounded up to a tile (scratch row length)
-};
-
 struct Ctx {
     const indexer_plan_s* p;
     LogitsParams lp;
@@ -214,170 +227,127 @@ int fill_maps(Ctx& c, const void* q, const void* k)
 {
     const indexer_plan_s* p = c.p;
     std::memset(&c.lp, 0, sizeof(c.lp));
-    const int G = logits_rows_per_group(p->H, p->kdtype);
-    if (!make_map(&c.lp.tmap_q, q, (uint64_t)p->T * p->H, p->D, G * p->H))
+    if (!make_map(&c.lp.tmap_q, q, (uint64_t)p->T * p->H, p->D, p->G * p->H))
         return IDX_ERR_CUDA;
     const uint64_t krows = (uint64_t)std::max(p->Lk, 1);
-    const bool ok = p->kdtype == IDX_K_FP8_E4M3
-                        ? make_map(&c.lp.tmap_k, k, krows, p->D, kTileKeys)
-                        : make_map_fp4(&c.lp.tmap_k, k, krows, p->D, kTileKeys);
-    return ok ? IDX_OK : IDX_ERR_CUDA;
+    if (!make_map(&c.lp.tmap_k, k, krows, p->D, kTileKeys))
+        return IDX_ERR_CUDA;
+    return IDX_OK;
 }
 
-// Launch the logits kernel over a list of segments (<= kMaxSegments).
-int run_logits(Ctx& c, const std::vector<Segment>& segs_in, float* out)
+// Launch the logits kernel over a list of segments (<= kMaxSegments) whose
+// n_row_groups / n_chunks / unit_tiles are set; unit numbering is filled here.
+int run_logits(Ctx& c, std::vector<Segment>& segs, int sink)
 {
     const indexer_plan_s* p = c.p;
-    const int G = logits_rows_per_group(p->H, p->kdtype);
-    // choose key tiles per unit so that there are several units per SM
-    int64_t work = 0;
-    for (const Segment& s : segs_in)
-        work += (int64_t)((s.nrows + G - 1) / G) * ((s.j_end - s.j_begin + kTileKeys - 1) / kTileKeys);
-    int chunk = (int)std::min<int64_t>(64, std::max<int64_t>(4, work / (8LL * c.sms)));
     LogitsParams& lp = c.lp;
-    lp.chunk_tiles = chunk;
-    lp.num_segments = (int)segs_in.size();
+    lp.num_segments = (int)segs.size();
     int units = 0;
-    for (size_t i = 0; i < segs_in.size(); ++i) {
-        Segment s = segs_in[i];
-        s.n_row_groups = (s.nrows + G - 1) / G;
-        const int tiles = (s.j_end - s.j_begin + kTileKeys - 1) / kTileKeys;
-        s.n_chunks = (tiles + chunk - 1) / chunk;
-        s.unit_begin = units;
-        units += s.n_row_groups * s.n_chunks;
-        lp.seg[i] = s;
+    for (size_t i = 0; i < segs.size(); ++i) {
+        segs[i].unit_begin = units;
+        units += segs[i].n_row_groups * segs[i].n_chunks;
+        lp.seg[i] = segs[i];
     }
     lp.total_units = units;
-    lp.out = out;
     lp.timeout_cycles = p->wait_budget;
     if (units == 0)
         return IDX_OK;
     const int grid = std::min(units, c.sms);
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    return launch_logits(lp, p->H, p->D, p->kdtype, grid, c.st) == cudaSuccess ? IDX_OK
-                                                                              : IDX_ERR_CUDA;
+    return launch_logits(lp, p->H, p->D, p->kdtype, sink, grid, c.st) == cudaSuccess
+               ? IDX_OK
+               : IDX_ERR_CUDA;
 }
 
-// Blocked pass shared by fused top-k (pool = 0) and candidate blocks (pool = block):
-// score rows against key splits into scratch, keep per-split top-k candidates.
-int run_blocked(Ctx& c, uint8_t* ws, int pool)
+// Streamed top-k (pool = 0) or candidate blocks (pool > 0): every pass scores
+// its rows against every key split, appending threshold-passing entries to the
+// lists, then selects exactly from the lists.
+int run_streamed(Ctx& c, uint8_t* ws, int pool, int32_t* out_idx, float* out_val,
+                 uint8_t* mask, int64_t ld_mask)
 {
     const indexer_plan_s* p = c.p;
-    float* scratch = reinterpret_cast<float*>(ws + p->off_scratch);
-    const int kk = pool ? p->cand_topk : p->topk;
-    float* cval = reinterpret_cast<float*>(ws + (pool ? p->off_cblk_val : p->off_cand_val));
-    int32_t* cidx = reinterpret_cast<int32_t*>(ws + (pool ? p->off_cblk_idx : p->off_cand_idx));
-    const int64_t cap = (int64_t)p->row_chunk * p->key_block;  // scratch floats
-
-    std::vector<Piece> batch;
-    int64_t used = 0;
-    auto flush = [&]() -> int {
-        if (batch.empty())
-            return IDX_OK;
+    const std::vector<Pass>& passes = pool ? p->passes_b : p->passes_k;
+    const std::vector<int32_t>& cap = pool ? p->cap_b : p->cap_k;
+    const int keep = pool ? p->cand_topk : p->topk;
+    LogitsParams& lp = c.lp;
+    lp.lists = reinterpret_cast<uint2*>(ws + p->off_lists);
+    lp.counts = reinterpret_cast<uint32_t*>(ws + p->off_counts);
+    lp.gtau = reinterpret_cast<uint32_t*>(ws + p->off_gtau);
+    lp.keep = keep;
+    lp.pool = pool ? pool : 1;
+    lp.update_tiles = kUpdateTiles;
+    for (const Pass& ps : passes) {
+        // one launch per distinct capacity (capacity is a launch parameter)
         std::vector<Segment> segs;
-        SelParams sp;
-        std::memset(&sp, 0, sizeof(sp));
-        int64_t off = 0;
-        int rows = 0;
-        for (size_t i = 0; i < batch.size(); ++i) {
-            const Piece& pc = batch[i];
+        StreamMergeParams mp;
+        std::memset(&mp, 0, sizeof(mp));
+        int ctas = 0;
+        int launch_cap = -1;
+        auto flush = [&]() -> int {
+            if (segs.empty())
+                return IDX_OK;
+            lp.cap = launch_cap;
+            int rc = run_logits(c, segs, pool ? kSinkPool : kSinkStream);
+            segs.clear();
+            return rc;
+        };
+        for (const PassPiece& pc : ps.pieces) {
             const int r = pc.r;
-            const int j0 = pc.s * p->key_block;
-            const int j1 = std::min(p->L[r], j0 + p->key_block);
-            Segment s;
-            std::memset(&s, 0, sizeof(s));
-            s.row_begin = pc.a;
-            s.nrows = pc.b - pc.a;
-            s.key_base = p->key_begin[r];
-            s.key_count = p->L[r];
-            s.j_begin = j0;
-            s.j_end = j1;
-            s.out_offset = off;
-            s.out_ld = pc.width;
-            segs.push_back(s);
-            SelSegment& q = sp.seg[i];
-            q.row_begin = pc.a;
-            q.nrows = pc.b - pc.a;
-            q.j_begin = pool ? j0 / pool : j0;
-            q.n_entries = pool ? (j1 - j0 + pool - 1) / pool : (j1 - j0);
-            q.key_count = p->L[r];
-            q.cand_slot = pc.s;
-            q.n_slots = p->n_splits[r];
-            q.src_offset = off;
-            q.src_ld = pc.width;
-            q.cand_offset = (pool ? p->cblk_off[r] : p->cand_off[r]) +
-                            (int64_t)(pc.a - p->row_begin[r]) * p->n_splits[r] * kk;
-            q.row_block = rows;
-            rows += pc.b - pc.a;
-            off += (int64_t)(pc.b - pc.a) * pc.width;
+            const int ns = p->n_splits[r];
+            if (cap[r] != launch_cap || (int)segs.size() + ns > kMaxSegments) {
+                int rc = flush();
+                if (rc != IDX_OK)
+                    return rc;
+                launch_cap = cap[r];
+            }
+            for (int s = 0; s < ns; ++s) {
+                Segment sg;
+                std::memset(&sg, 0, sizeof(sg));
+                sg.row_begin = pc.a;
+                sg.nrows = pc.b - pc.a;
+                sg.key_base = p->key_begin[r];
+                sg.key_count = p->L[r];
+                sg.j_begin = s * p->split_keys;
+                sg.j_end = std::min(p->L[r], (s + 1) * p->split_keys);
+                sg.unit_tiles = (int)ceil_div(std::max(0, sg.j_end - sg.j_begin), kTileKeys);
+                sg.n_row_groups = (int)ceil_div(sg.nrows, p->G);
+                sg.n_chunks = 1;
+                // row-major [row][split][quadrant][cap]
+                sg.out_offset = pc.list_off + (int64_t)s * kListsPerSplit * cap[r];
+                sg.out_ld = (int64_t)ns * kListsPerSplit * cap[r];
+                sg.cnt_offset = p->cnt_base[r] +
+                                (int64_t)(pc.a - p->row_begin[r]) * ns * kListsPerSplit +
+                                (int64_t)s * kListsPerSplit;
+                sg.cnt_ld = ns * kListsPerSplit;
+                segs.push_back(sg);
+            }
+            MergePiece& mpc = mp.piece[mp.num_pieces++];
+            mpc.row_begin = pc.a;
+            mpc.nrows = pc.b - pc.a;
+            mpc.cta_begin = ctas;
+            mpc.slots = ns * kListsPerSplit;
+            mpc.cap = cap[r];
+            mpc.list_offset = pc.list_off;
+            mpc.count_offset = p->cnt_base[r] + (int64_t)(pc.a - p->row_begin[r]) * ns * kListsPerSplit;
+            ctas += pc.b - pc.a;
         }
-        int rc = run_logits(c, segs, scratch);
+        int rc = flush();
         if (rc != IDX_OK)
             return rc;
-        sp.src = scratch;
-        sp.compress_len = c.lp.compress_len;
-        sp.k = kk;
-        sp.pool = pool;
-        sp.num_segments = (int)batch.size();
-        sp.total_rows_launch = rows;
-        sp.cand_val = cval;
-        sp.cand_idx = cidx;
+        mp.lists = lp.lists;
+        mp.counts = lp.counts;
+        mp.gtau = lp.gtau;
+        mp.k = keep;
+        mp.total_ctas = ctas;
+        mp.out_idx = out_idx;
+        mp.out_val = out_val;
+        mp.mask = mask;
+        mp.ld_mask = ld_mask;
         g_launches.fetch_add(1, std::memory_order_relaxed);
-        if (launch_select_dense(sp, c.st) != cudaSuccess)
+        if (launch_stream_merge(mp, c.st) != cudaSuccess)
             return IDX_ERR_CUDA;
-        batch.clear();
-        used = 0;
-        return IDX_OK;
-    };
-
-    for (int r = 0; r < p->R; ++r) {
-        const int rb = p->row_begin[r], re = p->row_begin[r + 1];
-        if (re == rb)
-            continue;
-        for (int s = 0; s < p->n_splits[r]; ++s) {
-            const int j0 = s * p->key_block;
-            const int j1 = std::min(p->L[r], j0 + p->key_block);
-            const int width = std::max(kTileKeys, (j1 - j0 + kTileKeys - 1) / kTileKeys * kTileKeys);
-            const int rows_fit = (int)std::max<int64_t>(1, cap / width);
-            for (int a = rb; a < re; a += rows_fit) {
-                const int b = std::min(re, a + rows_fit);
-                const int64_t need = (int64_t)(b - a) * width;
-                if (used + need > cap || (int)batch.size() == kMaxSegments) {
-                    int rc = flush();
-                    if (rc != IDX_OK)
-                        return rc;
-                }
-                batch.push_back(Piece{r, a, b, s, width});
-                used += need;
-            }
-        }
     }
-    return flush();
-}
-
-int run_merge(Ctx& c, uint8_t* ws, int pool, int32_t* out_idx, float* out_val, uint8_t* mask,
-              int64_t ld_mask)
-{
-    const indexer_plan_s* p = c.p;
-    MergeParams mp;
-    std::memset(&mp, 0, sizeof(mp));
-    mp.cand_val = reinterpret_cast<const float*>(ws + (pool ? p->off_cblk_val : p->off_cand_val));
-    mp.cand_idx = reinterpret_cast<const int32_t*>(ws + (pool ? p->off_cblk_idx : p->off_cand_idx));
-    mp.k = pool ? p->cand_topk : p->topk;
-    mp.num_requests = p->R;
-    mp.total_rows = p->T;
-    mp.out_idx = out_idx;
-    mp.out_val = out_val;
-    mp.mask = mask;
-    mp.ld_mask = ld_mask;
-    for (int r = 0; r < p->R; ++r) {
-        mp.req_row_begin[r] = p->row_begin[r];
-        mp.req_slots[r] = p->n_splits[r];
-        mp.req_cand_offset[r] = pool ? p->cblk_off[r] : p->cand_off[r];
-    }
-    mp.req_row_begin[p->R] = p->row_begin[p->R];
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return launch_merge(mp, c.st) == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+    return IDX_OK;
 }
 
 int begin_call(Ctx& c, const indexer_plan_s* p, void* ws, void* stream)
@@ -409,7 +379,7 @@ void set_inputs(Ctx& c, const float* s_q, const float* w, const void* k_scale,
 
 extern "C" {
 
-int indexer_version(void) { return 1; }
+int indexer_version(void) { return 2; }
 
 long long indexer_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -442,7 +412,7 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
         return IDX_ERR_INVALID_ARG;
     const int cb = pr->cand_block ? pr->cand_block : 8;
     const int ct = pr->cand_topk;
-    if (cb < 1 || ct < 0 || ct > 4096 || (kTileKeys % cb) != 0)
+    if (cb < 1 || cb > 32 || (32 % cb) != 0 || ct < 0 || ct > 4096)
         return IDX_ERR_INVALID_ARG;
     if (pr->key_block < 0 || (pr->key_block % kTileKeys) != 0)
         return IDX_ERR_INVALID_ARG;
@@ -486,43 +456,68 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
         delete p;
         return IDX_ERR_UNSUPPORTED;
     }
-    // Key block: the caller's, else the candidate (whole prefix, 64K, 32K, ... 1K keys)
-    // needing the fewest logits passes within the budget.
-    const int round_L = std::max(kTileKeys, (p->max_L + kTileKeys - 1) / kTileKeys * kTileKeys);
-    const int G = logits_rows_per_group(p->H, p->kdtype);
-    std::vector<int> cands;
-    if (pr->key_block)
-        cands.push_back(std::min(pr->key_block, round_L));
-    else {
-        cands.push_back(round_L);
-        for (int kb = 65536; kb >= 1024; kb /= 2)
-            if (kb < round_L)
-                cands.push_back(kb);
-    }
-    int best_kb = 0, best_rc = 0;
-    int64_t best_passes = INT64_MAX;
-    for (int kb : cands) {
-        const size_t fixed = layout(*p, kb, 0);
-        if (fixed >= p->budget)
-            continue;
-        const int64_t rows = (int64_t)((p->budget - fixed) / ((size_t)kb * 4));
-        const int64_t rc = rows >= p->T ? std::max(p->T, 1) : rows / G * G;
-        if (rc < 1)
-            continue;
-        int64_t passes = 0;
+    p->G = logits_rows_per_group(p->H, p->kdtype);
+    const int G = p->G;
+
+    // Key splits: the caller's size, else the largest multiple of 128 that still
+    // gives about kTargetUnits (row group x split) units, but not below 8K keys.
+    const int round_L = (int)std::max<int64_t>(kTileKeys, ceil_div(p->max_L, kTileKeys) * kTileKeys);
+    auto units_for = [&](int S) {
+        int64_t u = 0;
         for (int r = 0; r < R; ++r)
-            passes += (p->row_begin[r + 1] - p->row_begin[r] + rc - 1) / rc * p->n_splits[r];
-        if (passes < best_passes || (passes == best_passes && kb <= 65536 && kb > best_kb)) {
-            best_passes = passes;
-            best_kb = kb;
-            best_rc = (int)rc;
+            u += ceil_div(p->row_begin[r + 1] - p->row_begin[r], G) *
+                 std::max<int64_t>(1, ceil_div(p->L[r], S));
+        return u;
+    };
+    int S = pr->key_block ? std::min(pr->key_block, round_L) : round_L;
+    if (!pr->key_block)
+        while (units_for(S) < kTargetUnits && S > 8192)
+            S = (int)std::max<int64_t>(8192, ceil_div(ceil_div(S, 2), kTileKeys) * kTileKeys);
+    p->split_keys = S;
+    p->n_splits.resize(R);
+    p->cap_k.resize(R);
+    p->cap_b.resize(R);
+    p->cnt_base.resize(R);
+    // Each of a split's four sub-lists receives 32 of every 128 keys (its warp's
+    // TMEM lanes), or 32 / cand_block blocks.  A sub-list holds a whole split when
+    // that is small; else room for the kept set plus two refresh intervals of
+    // appends, and at least 4 x keep so that compactions stay rare.
+    const int slack = 2 * kUpdateTiles * 32;
+    int64_t counts = 0;
+    for (int r = 0; r < R; ++r) {
+        const int ns = (int)std::max<int64_t>(1, ceil_div(p->L[r], S));
+        if ((int64_t)ns * kListsPerSplit > kMaxStreamSlots) {
+            delete p;
+            return IDX_ERR_UNSUPPORTED;
         }
+        p->n_splits[r] = ns;
+        const int split_tiles = (int)ceil_div(std::max(1, std::min(S, p->L[r])), kTileKeys);
+        p->cap_k[r] = std::min(split_tiles * 32, std::max(4 * p->topk, p->topk + slack));
+        p->cap_b[r] =
+            ct ? std::min(split_tiles * (32 / cb), std::max(4 * ct, ct + slack)) : 1;
+        p->cnt_base[r] = counts;
+        counts += (int64_t)(p->row_begin[r + 1] - p->row_begin[r]) * ns * kListsPerSplit;
     }
-    if (best_kb == 0) {
+    size_t off = kStatusBytes;
+    p->off_gtau = off;
+    off = align_up(off + (size_t)std::max(p->T, 1) * 4, 256);
+    p->off_counts = off;
+    off = align_up(off + (size_t)std::max<int64_t>(counts, 1) * 4, 256);
+    p->off_lists = off;
+    if (off >= p->budget) {
         delete p;
         return IDX_ERR_WORKSPACE;
     }
-    layout(*p, best_kb, best_rc);
+    const int64_t entries = (int64_t)((p->budget - off) / 8);
+    if (!build_passes(*p, p->cap_k, entries, p->passes_k, p->max_piece_rows) ||
+        (ct && !build_passes(*p, p->cap_b, entries, p->passes_b, p->max_piece_rows))) {
+        delete p;
+        return IDX_ERR_WORKSPACE;
+    }
+    int64_t need = pass_entries(*p, p->passes_k, p->cap_k);
+    if (ct)
+        need = std::max(need, pass_entries(*p, p->passes_b, p->cap_b));
+    p->ws_bytes = align_up(off + (size_t)std::max<int64_t>(need, 1) * 8, 256);
     *out = p;
     if (ws_bytes)
         *ws_bytes = p->ws_bytes;
@@ -537,9 +532,9 @@ int indexer_plan_info(indexer_plan_t p, int32_t* key_block, int32_t* row_chunk,
     if (!p)
         return IDX_ERR_INVALID_ARG;
     if (key_block)
-        *key_block = p->key_block;
+        *key_block = p->split_keys;
     if (row_chunk)
-        *row_chunk = p->row_chunk;
+        *row_chunk = p->max_piece_rows;
     if (max_splits)
         *max_splits = *std::max_element(p->n_splits.begin(), p->n_splits.end());
     return IDX_OK;
@@ -557,10 +552,10 @@ int indexer_logits(indexer_plan_t p, const void* q, const float* s_q, const floa
                    const void* k, const void* k_scale, const int32_t* clen, float* logits,
                    int64_t ld, void* ws, size_t ws_bytes, void* stream)
 {
-    int rc = check_common(p, ws, ws_bytes);
+    if (!p || !ws || !aligned(ws, 256) || ws_bytes < kStatusBytes)
+        return ws_bytes < kStatusBytes && p && ws ? IDX_ERR_WORKSPACE : IDX_ERR_INVALID_ARG;
+    int rc = check_inputs(p, q, s_q, w, k, k_scale, clen);
     if (rc != IDX_OK)
-        return rc;
-    if ((rc = check_inputs(p, q, s_q, w, k, k_scale, clen)) != IDX_OK)
         return rc;
     if (!logits || !aligned(logits, 4) || ld < std::max(p->max_L, 1) || ld > INT32_MAX)
         return IDX_ERR_INVALID_ARG;
@@ -572,6 +567,12 @@ int indexer_logits(indexer_plan_t p, const void* q, const float* s_q, const floa
     if ((rc = fill_maps(c, q, k)) != IDX_OK)
         return rc;
     set_inputs(c, s_q, w, k_scale, clen, ws);
+    c.lp.out = logits;
+    // key tiles per unit: enough units for every SM to get several
+    int64_t work = 0;
+    for (int r = 0; r < p->R; ++r)
+        work += ceil_div(p->row_begin[r + 1] - p->row_begin[r], p->G) * ceil_div(ld, kTileKeys);
+    const int chunk = (int)std::min<int64_t>(64, std::max<int64_t>(4, work / (8LL * c.sms)));
     std::vector<Segment> segs;
     for (int r = 0; r < p->R; ++r) {
         const int rb = p->row_begin[r], re = p->row_begin[r + 1];
@@ -585,28 +586,33 @@ int indexer_logits(indexer_plan_t p, const void* q, const float* s_q, const floa
         s.key_count = p->L[r];
         s.j_begin = 0;
         s.j_end = (int)ld;
+        s.unit_tiles = chunk;
+        s.n_row_groups = (int)ceil_div(s.nrows, p->G);
+        s.n_chunks = (int)ceil_div(ceil_div(ld, kTileKeys), chunk);
         s.out_offset = (int64_t)rb * ld;
         s.out_ld = ld;
         segs.push_back(s);
         if ((int)segs.size() == kMaxSegments) {
-            if ((rc = run_logits(c, segs, logits)) != IDX_OK)
+            if ((rc = run_logits(c, segs, kSinkLogits)) != IDX_OK)
                 return rc;
             segs.clear();
         }
     }
-    return segs.empty() ? IDX_OK : run_logits(c, segs, logits);
+    return segs.empty() ? IDX_OK : run_logits(c, segs, kSinkLogits);
 }
 
 int indexer_topk(indexer_plan_t p, const float* logits, int64_t ld, const int32_t* clen,
                  int32_t* out_idx, float* out_val, void* ws, size_t ws_bytes, void* stream)
 {
-    int rc = check_common(p, ws, ws_bytes);
-    if (rc != IDX_OK)
-        return rc;
+    if (!p || !ws || !aligned(ws, 256))
+        return IDX_ERR_INVALID_ARG;
+    if (ws_bytes < kStatusBytes)
+        return IDX_ERR_WORKSPACE;
     if (!logits || !clen || !out_idx || ld < std::max(p->max_L, 1) || !aligned(logits, 4) ||
         !aligned(out_idx, 4) || (out_val && !aligned(out_val, 4)))
         return IDX_ERR_INVALID_ARG;
     Ctx c;
+    int rc;
     if ((rc = begin_call(c, p, ws, stream)) != IDX_OK)
         return rc;
     TopkParams tp;
@@ -653,9 +659,9 @@ int indexer_fused_topk(indexer_plan_t p, const void* q, const float* s_q, const 
     c.lp.cand_mask = cand_mask;
     c.lp.ld_mask = ld_mask;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
-    if ((rc = run_blocked(c, wsb, 0)) != IDX_OK)
-        return rc;
-    return run_merge(c, wsb, 0, out_idx, out_val, nullptr, 0);
+    if (cudaMemsetAsync(wsb + p->off_gtau, 0, (size_t)p->T * 4, c.st) != cudaSuccess)
+        return IDX_ERR_CUDA;
+    return run_streamed(c, wsb, 0, out_idx, out_val, nullptr, 0);
 }
 
 int indexer_candidate_blocks(indexer_plan_t p, const void* q, const float* s_q, const float* w,
@@ -680,9 +686,9 @@ int indexer_candidate_blocks(indexer_plan_t p, const void* q, const float* s_q, 
         return rc;
     set_inputs(c, s_q, w, k_scale, clen, ws);
     uint8_t* wsb = static_cast<uint8_t*>(ws);
-    if ((rc = run_blocked(c, wsb, p->cand_block)) != IDX_OK)
-        return rc;
-    return run_merge(c, wsb, p->cand_block, nullptr, nullptr, cand_mask, ld_mask);
+    if (cudaMemsetAsync(wsb + p->off_gtau, 0, (size_t)p->T * 4, c.st) != cudaSuccess)
+        return IDX_ERR_CUDA;
+    return run_streamed(c, wsb, p->cand_block, nullptr, nullptr, cand_mask, ld_mask);
 }
 
 int indexer_expand_mask(indexer_plan_t p, const uint8_t* cand_mask, int64_t ld_mask,

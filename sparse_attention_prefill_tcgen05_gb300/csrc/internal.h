@@ -18,6 +18,7 @@ constexpr int kThreads = 384;    // warp 0 TMA, warp 1 MMA/TMEM, 2-3 spare, 4-11
 // Device status word bits (OR-ed by kernels, read by indexer_status).
 constexpr uint32_t kStatusTimeout = 1u << 0;
 constexpr uint32_t kStatusBadArg = 1u << 1;
+constexpr uint32_t kStatusListOverflow = 1u << 2;   // a streamed list lost entries
 
 // Key formats.
 constexpr int kKeyFp8 = 0;
@@ -25,6 +26,12 @@ constexpr int kKeyFp4 = 1;
 
 // What the logits kernel does with each (row, key) score.
 constexpr int kSinkLogits = 0;   // write fp32 to a [rows, ld] buffer
+constexpr int kSinkStream = 1;   // append threshold-passing (score, key) to per-row lists
+constexpr int kSinkPool = 2;     // same over cand_block-key block maxima (candidate blocks)
+
+constexpr int kListsPerSplit = 4;     // one candidate sub-list per epilogue warp quadrant
+constexpr int kMaxStreamSlots = 256;  // sub-lists per row (key splits x kListsPerSplit)
+constexpr int kMaxMergePieces = 64;   // row pieces per merge launch
 
 // A contiguous piece of work: some rows of one request against a key range
 // of that request.  Units (row group x key chunk) are numbered per launch.
@@ -38,9 +45,12 @@ struct Segment {
     int32_t unit_begin;  // first unit number of this segment in the launch
     int32_t n_row_groups;
     int32_t n_chunks;
-    int32_t pad_;
-    int64_t out_offset;  // element offset of (row_begin, j_begin) in the output
-    int64_t out_ld;      // elements between consecutive rows of the output
+    int32_t unit_tiles;  // key tiles per unit
+    int64_t out_offset;  // logits: element offset of (row_begin, j_begin) in the output;
+                         // streams: entry offset of row_begin's list for this split
+    int64_t out_ld;      // logits: elements between rows; streams: entries between rows
+    int64_t cnt_offset;  // streams: counts index of row_begin for this split
+    int64_t cnt_ld;      // streams: counts between rows
 };
 
 struct LogitsParams {
@@ -56,69 +66,55 @@ struct LogitsParams {
     int32_t mask_block;
     int32_t num_segments;
     int32_t total_units;
-    int32_t chunk_tiles;  // key tiles per unit
+    int32_t pad0_;
     long long timeout_cycles;
     float* out;
     uint32_t* status;
+    // streamed top-k
+    uint2* lists;         // (score bits, key or block index) entries
+    uint32_t* counts;     // entries appended per (row, split), clamped to cap
+    uint32_t* gtau;       // [rows] shared lower bound (ord of a score) per row
+    int32_t cap;          // list capacity per (row, split)
+    int32_t keep;         // k (keys) or cand_topk (blocks)
+    int32_t pool;         // keys per block for kSinkPool
+    int32_t update_tiles; // tiles between threshold refreshes
     Segment seg[kMaxSegments];
 };
 
-// One (row range, key split) piece of the selection kernels.
-struct SelSegment {
-    int32_t row_begin;    // first global row
-    int32_t nrows;
-    int32_t j_begin;      // request-local key (or block) index of entry 0
-    int32_t n_entries;    // entries in this piece (keys, or blocks when pooling)
-    int32_t key_count;    // keys of the request (clamps compress_len)
-    int32_t cand_slot;    // split index within the row's candidate slots
-    int32_t n_slots;      // candidate slots per row of this request
-    int32_t pad_;
-    int64_t src_offset;   // element offset of (row_begin, entry 0) in the dense source
-    int64_t src_ld;
-    int64_t cand_offset;  // entry offset of the request's first row in the candidate area
-    int32_t row_block;    // first CTA (= row) of this piece in the launch
-    int32_t pad2_;
-};
-
-struct SelParams {
-    const float* src;            // dense scores
-    const int32_t* compress_len;
-    int32_t k;                   // entries kept per row
-    int32_t pool;                // 0: entries are keys; >0: entries are blocks of `pool` keys
-    int32_t num_segments;
-    int32_t total_rows_launch;
-    float* cand_val;             // [.., k] per slot
-    int32_t* cand_idx;
-    SelSegment seg[kMaxSegments];
-};
-
 // Host-side launchers (defined in the .cu files).
-cudaError_t launch_logits(const LogitsParams& p, int H, int D, int kfmt, int grid,
+cudaError_t launch_logits(const LogitsParams& p, int H, int D, int kfmt, int sink, int grid,
                           cudaStream_t stream);
 size_t logits_smem_bytes(int H, int D, int kfmt);
 int logits_rows_per_group(int H, int kfmt);   // query rows per MMA tile
 
-// Per-row top-k of dense rows into candidate slots (rows = total of segs).
-cudaError_t launch_select_dense(const SelParams& p, cudaStream_t stream);
-
-// Final merge: per row, exact top-k of its n_slots*k candidates into out_idx/out_val,
-// or (blocks) into a 0/1 mask.
-struct MergeParams {
-    const float* cand_val;
-    const int32_t* cand_idx;
-    int32_t k;                 // kept per row
-    int32_t num_requests;
-    int32_t total_rows;
+// Exact selection over the lists appended by the streaming sinks.  A piece is
+// a row range of one request whose lists were filled by the same launch; one
+// CTA per row.
+struct MergePiece {
+    int32_t row_begin;      // first global row
+    int32_t nrows;
+    int32_t cta_begin;      // first CTA of the piece in the launch
+    int32_t slots;          // key splits (lists) per row
+    int32_t cap;            // entries per list
     int32_t pad_;
-    int32_t* out_idx;          // [rows, k] or null
-    float* out_val;            // [rows, k] or null
-    uint8_t* mask;             // [rows, ld_mask] or null (block selection)
-    int64_t ld_mask;
-    int32_t req_row_begin[kMaxRequests + 1];
-    int32_t req_slots[kMaxRequests];
-    int64_t req_cand_offset[kMaxRequests];
+    int64_t list_offset;    // entry offset of row_begin's first list
+    int64_t count_offset;   // counts index of row_begin's first list
 };
-cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+struct StreamMergeParams {
+    const uint2* lists;
+    const uint32_t* counts;
+    const uint32_t* gtau;   // per-row lower bound on the k-th key: entries below it are skipped
+    int32_t k;
+    int32_t num_pieces;
+    int32_t total_ctas;
+    int32_t pad_;
+    int32_t* out_idx;
+    float* out_val;
+    uint8_t* mask;             // blocks: [rows, ld_mask]
+    int64_t ld_mask;
+    MergePiece piece[kMaxMergePieces];
+};
+cudaError_t launch_stream_merge(const StreamMergeParams& p, cudaStream_t stream);
 
 // Standalone top-k over user logits [rows, ld].
 struct TopkParams {

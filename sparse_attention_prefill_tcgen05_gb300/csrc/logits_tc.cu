@@ -1,4 +1,5 @@
-// Indexer logits on the 5th-generation tensor cores (sm_103a).
+// Indexer logits on the 5th-generation tensor cores (sm_103a), with the
+// selection fused into the epilogue.
 //
 //   logit[t, j] = s_k[j] * sum_h c[t,h] * max(S[t,h,j], 0),   c = w * s_q,
 //   S[t,h,j]    = <q[t,h,:], k[j,:]>  (fp8 e4m3 x fp8 e4m3, fp32 accumulate)
@@ -7,59 +8,94 @@
 // positive ("[DeepSeek-V4.1] Bound the dense prefill indexer transient",
 // Motivation: the DeepGEMM fp8 MQA logits the indexer scores with;
 // "chunked-prefill-memory.md" section 1: T query rows against the whole
-// compressed prefix, [T, max_seqlen_k] fp32 output, -inf past the row's
-// causal length).
+// compressed prefix, -inf past the row's causal length).
 //
-// Mapping.  One MMA tile is M = 128 keys (TMEM lanes) x N = 256 (row, head)
-// columns (256/H query rows x H heads) x K = D.  With keys on the lanes, the
-// head reduction of one (row, key) is a run of H consecutive accumulator
-// columns held by ONE thread: no shuffles, no shared-memory reduction.
+// Mapping.  One MMA tile is M = 128 keys (TMEM lanes) x N = (rows x H heads)
+// columns x K = D.  With keys on the lanes, the head reduction of one
+// (row, key) is a run of H consecutive accumulator columns held by ONE
+// thread: no shuffles, no shared-memory reduction.
 //
 // Roles (384 threads, one CTA per SM, persistent over work units):
 //   warp 0      TMA producer: the unit's Q tile (double-buffered) and a ring
 //               of K tiles, 128-byte-swizzled for the MMA.
-//   warp 1      allocates 512 TMEM columns (two 256-column accumulators),
-//               issues tcgen05.mma (D/32 per tile) and tcgen05.commit.
-//   warps 4-11  epilogue: tcgen05.ld 32x32b, ReLU, head-weighted sum, key
-//               scale, causal mask (and candidate mask), coalesced store.
+//   warp 1      allocates 512 TMEM columns (two accumulators), issues
+//               tcgen05.mma (D/32 per tile) and tcgen05.commit.
+//   warps 4-11  epilogue: tcgen05.ld 32x32b (pipelined), ReLU, head-weighted
+//               sum (four independent partial sums per row), key scale,
+//               causal and candidate masks, then one of three sinks:
+//   * kSinkLogits: coalesced fp32 store of the [rows, ld] logits;
+//   * kSinkStream: streamed exact top-k ("chunked-prefill-memory.md" section
+//     2.3 scores key blocks and keeps per-block top-k; here the block top-k is
+//     kept on the fly).  A key is appended to its row's list only if it is at
+//     or above the row's threshold tau.  tau is always a valid lower bound of
+//     the row's k-th best (composite) score: it comes from a two-level
+//     histogram of the appended scores (256 bins of the top byte of the
+//     order-preserving image, then 256 bins of the next byte inside the
+//     boundary bin), from an exact compaction of the list when it fills, and
+//     from the other key splits of the same row through a per-row atomic max
+//     in global memory.  Nothing that can be in the row's top-k is ever
+//     skipped, so the exact selection over the lists (select.cu) equals the
+//     top-k over all keys.
+//   * kSinkPool: the same over the maximum of each cand_block-key block
+//     (candidate blocks, same section: 8-key block pooling, top-2048 blocks).
 // The accumulator is double-buffered so the epilogue of tile i overlaps the
 // MMAs of tile i+1.
+#include "groupsel.cuh"
 #include "internal.h"
-#include "ptx.cuh"
 
 namespace idx {
 namespace {
 
-template <int H, int D, int KFMT>
+constexpr int kHalfThreads = 128;
+
+template <int H, int D, int KFMT, int SINK>
 struct Cfg {
-    // fp4 keys need TMEM columns for the block scales, so their tiles are
-    // 192 columns wide (two accumulators of 192 + scale columns <= 512).
-    static constexpr int NMAX = KFMT == kKeyFp8 ? kTileN : 192;
+    // fp8 tiles are 256 columns (16 rows for small H); fp4 keys would need TMEM
+    // columns for block scales (192-column tiles).
+    static constexpr int NMAX = KFMT == kKeyFp8 ? (H >= 16 ? kTileN : 16 * H) : 192;
     static constexpr int G = NMAX / H;                 // query rows per tile
     static constexpr int N = G * H;                    // MMA N
     static constexpr int QBYTES = N * D;               // Q tile: N rows of D bytes
-    static constexpr int KBYTES = kTileKeys * D;       // K tile in smem (fp4 unpacked to bytes)
+    static constexpr int KBYTES = kTileKeys * D;       // K tile
     static constexpr int STAGES = (D >= 128) ? 6 : 8;
     static constexpr int KSTEPS = D / 32;              // MMA K = 32 elements
-    static constexpr int ROWS_PER_HALF = G / 2;        // rows one epilogue thread reduces
+    static constexpr int RPH = G / 2;                  // rows one epilogue thread reduces
     static constexpr int HALF_COLS = N / 2;
+    static constexpr int NCH = HALF_COLS / 32;         // 32-column TMEM loads per tile
     static constexpr int ACC_COLS = N;                 // TMEM columns per accumulator
     static constexpr int SF_BYTES = KFMT == kKeyFp4 ? kTileKeys * 16 : 0;  // per stage
     static constexpr int TMEM_SFA = 2 * ACC_COLS;      // 4 columns per stage
     static constexpr int TMEM_SFB = TMEM_SFA + 4 * STAGES;
+    static constexpr bool STREAM = SINK != kSinkLogits;
     static_assert(D == 32 || D == 64 || D == 128, "D must be 32, 64 or 128");
     static_assert(G >= 2 && G % 2 == 0 && N % 16 == 0, "H must leave an even row count");
     static_assert(HALF_COLS % 32 == 0, "half tile must be whole 32-column loads");
-    static_assert(KFMT == kKeyFp8 || (D == 128 && TMEM_SFB + 4 <= 512), "fp4 needs D=128");
+    static_assert(!STREAM || G <= 16, "streamed selection keeps at most 16 rows per CTA");
     // shared memory carve-up (offsets from a 1024-byte aligned base)
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + ((2 * QBYTES + 1023) / 1024) * 1024;
     static constexpr int OFF_SF = OFF_K + STAGES * KBYTES;
-    static constexpr int OFF_C = OFF_SF + STAGES * SF_BYTES;        // float c[2][N]
-    static constexpr int OFF_BAR = OFF_C + 2 * kTileN * 4;
+    static constexpr int OFF_C = OFF_SF + STAGES * SF_BYTES;        // float c[2][kTileN]
+    static constexpr int OFF_HIST = OFF_C + 2 * kTileN * 4;          // u32 [G][2][256]
+    static constexpr int HIST_BYTES = STREAM ? G * 2 * 256 * 4 : 0;
+    static constexpr int OFF_ROWS = OFF_HIST + HIST_BYTES;           // row state [G]
+    static constexpr int ROWS_BYTES = STREAM ? G * 32 : 0;
+    static constexpr int OFF_SEL = OFF_ROWS + ROWS_BYTES;            // compaction scratch x2
+    static constexpr int SEL_ONE = (int)((sizeof(SelScratch<kHalfThreads>) + 15) / 16 * 16);
+    static constexpr int SEL_BYTES = STREAM ? 2 * SEL_ONE : 0;
+    static constexpr int OFF_BAR = OFF_SEL + SEL_BYTES;
     static constexpr int NBARS = 2 + 2 + 2 * STAGES + 2 + 2 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;              // + alignment slack
+};
+
+// Per-row state of the streamed selection (shared memory, one per row of the group).
+struct RowState {
+    uint32_t wcnt[4];  // entries each epilogue warp of the half appended to its sub-list
+    uint32_t tau_hi;   // candidate iff (ord(score), ~index) >= (tau_hi, tau_lo)
+    uint32_t tau_lo;
+    uint32_t b1;       // boundary bin of the top-byte histogram (256 = none yet)
+    uint32_t compact;  // set by the threshold refresh: the lists must be compacted
 };
 
 struct UnitInfo {
@@ -67,7 +103,7 @@ struct UnitInfo {
     int t0;        // first global row of the row group
     int nr;        // valid rows in the group
     int j0;        // request-local first key of the unit
-    int jend;      // request-local end of keys written by the unit
+    int jend;      // request-local end of keys covered by the unit
     int ntiles;    // tiles covering [j0, jend)
     int ntiles_mma;
 };
@@ -88,8 +124,8 @@ __device__ __forceinline__ UnitInfo decode_unit(const LogitsParams& p, int u, in
     ui.seg = s;
     ui.t0 = sg.row_begin + g * G;
     ui.nr = min(G, sg.row_begin + sg.nrows - ui.t0);
-    ui.j0 = sg.j_begin + chunk * p.chunk_tiles * kTileKeys;
-    ui.jend = min(sg.j_end, ui.j0 + p.chunk_tiles * kTileKeys);
+    ui.j0 = sg.j_begin + chunk * sg.unit_tiles * kTileKeys;
+    ui.jend = min(sg.j_end, ui.j0 + sg.unit_tiles * kTileKeys);
     ui.ntiles = (ui.jend - ui.j0 + kTileKeys - 1) / kTileKeys;
     // longest causal length in the group (warp-cooperative), clamped to the request
     int m = 0;
@@ -110,11 +146,116 @@ __device__ __forceinline__ void report(const LogitsParams& p, volatile int* abor
     atomicOr(p.status, bits);
 }
 
-template <int H, int D, int KFMT>
+__device__ __forceinline__ void red_add_shared(uint32_t* addr, uint32_t v)
+{
+    asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(smem_u32(addr)), "r"(v) : "memory");
+}
+
+// Append this warp's threshold-passing entries of one row to the warp's own
+// sub-list (position from a register count: no atomics on the list) and
+// count them in the row's histograms with fire-and-forget shared reductions:
+// h1 counts by top byte while no boundary bin is known or above it, h2 counts
+// the next byte inside the boundary bin b1.  Returns the warp's new count.
+__device__ __forceinline__ uint32_t stream_push(uint32_t* h1, uint32_t* h2, uint2* sub,
+                                                uint32_t cap, uint32_t wcnt, uint32_t tau_hi,
+                                                uint32_t tau_lo, uint32_t b1, float v,
+                                                uint32_t idx, bool active, int lane)
+{
+    const uint32_t o = f2ord(v);
+    const bool cand =
+        active && o > kOrdNegInf && (o > tau_hi || (o == tau_hi && ~idx >= tau_lo));
+    const uint32_t m = __ballot_sync(0xffffffffu, cand);
+    if (m == 0)
+        return wcnt;
+    const uint32_t t8 = o >> 24;
+    if (cand) {
+        const uint32_t pos = wcnt + __popc(m & ((1u << lane) - 1u));
+        if (pos < cap)
+            sub[pos] = make_uint2(__float_as_uint(v), idx);
+    }
+    // level 2: inside the boundary bin (the common case once b1 is known)
+    const bool in_b1 = cand && t8 == b1;
+    if (in_b1)
+        red_add_shared(&h2[(o >> 16) & 255u], 1u);
+    // level 1: everything else, aggregated when the lanes share the leader's byte
+    const bool l1 = cand && !in_b1;
+    const uint32_t ml1 = __ballot_sync(0xffffffffu, l1);
+    if (ml1) {
+        const int leader = __ffs(ml1) - 1;
+        const uint32_t lt8 = __shfl_sync(0xffffffffu, t8, leader);
+        const uint32_t same = __ballot_sync(0xffffffffu, l1 && t8 == lt8);
+        if (lane == leader)
+            red_add_shared(&h1[lt8], static_cast<uint32_t>(__popc(same)));
+        else if (l1 && t8 != lt8)
+            red_add_shared(&h1[t8], 1u);
+    }
+    return wcnt + __popc(m);
+}
+
+// Suffix-count search over 256 bins held 8 per lane (lane L: bins 8L..8L+7),
+// with add_val added to bin add_bin: the highest bin b with sum(bins >= b) >=
+// need.  Returns 256 if the total is below need; *above gets sum(bins > b).
+// Warp-wide.
+__device__ __forceinline__ uint32_t boundary_bin(const uint32_t* hist, uint32_t need, int lane,
+                                                 uint32_t* above, uint32_t add_bin = 256u,
+                                                 uint32_t add_val = 0u)
+{
+    const uint4 a = reinterpret_cast<const uint4*>(hist)[lane * 2];
+    const uint4 b = reinterpret_cast<const uint4*>(hist)[lane * 2 + 1];
+    uint32_t c[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if (static_cast<uint32_t>(lane * 8 + i) == add_bin)
+            c[i] += add_val;
+    uint32_t lsum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        lsum += c[i];
+    uint32_t incl = lsum;  // sum over lanes >= this lane
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xffffffffu, incl, off);
+        if (lane + off < 32)
+            incl += y;
+    }
+    const uint32_t hit = __ballot_sync(0xffffffffu, incl >= need);
+    if (hit == 0) {
+        *above = 0;
+        return 256u;
+    }
+    const int bl = 31 - __clz(hit);
+    uint32_t bin = 0, abv = 0;
+    if (lane == bl) {
+        uint32_t cum = incl - lsum;
+        for (int i = 7; i >= 0; --i) {
+            if (cum + c[i] >= need) {
+                bin = static_cast<uint32_t>(bl * 8 + i);
+                abv = cum;
+                break;
+            }
+            cum += c[i];
+        }
+    }
+    *above = __shfl_sync(0xffffffffu, abv, bl);
+    return __shfl_sync(0xffffffffu, bin, bl);
+}
+
+__device__ __forceinline__ uint32_t warp_sum_bins(const uint32_t* hist, int lane)
+{
+    const uint4 a = reinterpret_cast<const uint4*>(hist)[lane * 2];
+    const uint4 b = reinterpret_cast<const uint4*>(hist)[lane * 2 + 1];
+    uint32_t s = a.x + a.y + a.z + a.w + b.x + b.y + b.z + b.w;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        s += __shfl_xor_sync(0xffffffffu, s, o);
+    return s;
+}
+
+template <int H, int D, int KFMT, int SINK>
 __global__ void __launch_bounds__(kThreads, 1)
     logits_tc_kernel(const __grid_constant__ LogitsParams p)
 {
-    using C = Cfg<H, D, KFMT>;
+    using C = Cfg<H, D, KFMT, SINK>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -122,6 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* k_s = smem + C::OFF_K;
     uint8_t* sf_s = smem + C::OFF_SF;
     float* c_s = reinterpret_cast<float*>(smem + C::OFF_C);
+    uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);
+    RowState* rows_s = reinterpret_cast<RowState*>(smem + C::OFF_ROWS);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* q_full = bars;
     uint64_t* q_empty = bars + 2;
@@ -157,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&p.tmap_k);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, 2 * C::ACC_COLS);
+        tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -226,9 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int r = 0; r < kTileKeys / 32; ++r) {
                         const int m = r * 32 + lane;
-                        const int key = key0 + m;
                         const int local = ui.j0 + i * kTileKeys + m;
-                        const uint32_t word = local < sg.key_count ? __ldg(src + key) : 0x7F7F7F7Fu;
+                        const uint32_t word =
+                            local < sg.key_count ? __ldg(src + key0 + m) : 0x7F7F7F7Fu;
                         *reinterpret_cast<uint32_t*>(sf + m * 16) = word;
                     }
                     fence_proxy_async_smem();
@@ -290,10 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_f8f6f4(d_tmem, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
                         }
                     } else {
-                        // key scales of this stage into TMEM, then one block-scaled MMA per
-                        // 32-element block (A = e2m1 keys, B = e4m3 queries)
                         const uint32_t sfa = tmem_base + C::TMEM_SFA + 4 * ks;
-                        tmem_cp_128x128b(sfa, smem_desc_noswizzle(smem_u32(sf_s + ks * C::SF_BYTES), 128));
+                        tmem_cp_128x128b(
+                            sfa, smem_desc_noswizzle(smem_u32(sf_s + ks * C::SF_BYTES), 128));
 #pragma unroll
                         for (int kk = 0; kk < C::KSTEPS; ++kk) {
                             const uint64_t adesc = smem_desc_kmajor(k_addr + kk * 32, D);
@@ -334,100 +476,363 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- epilogue
         const int ew = warp - 4;                 // 0..7
         const int quad = warp & 3;               // TMEM lane quadrant of this warp
-        const int half = ew >> 2;                // column half: rows [half*G/2, +G/2)
+        const int half = ew >> 2;                // column half: rows [half*RPH, +RPH)
         const int kq = quad * 32 + lane;         // key within the tile
         const int etid = ew * 32 + lane;         // 0..255
+        const int htid = quad * 32 + lane;       // 0..127 within the half
+        const NamedSync half_sync{2 + half, kHalfThreads};
+        SelScratch<kHalfThreads>* sel_s =
+            reinterpret_cast<SelScratch<kHalfThreads>*>(smem + C::OFF_SEL + half * C::SEL_ONE);
         int ab = 0, aph = 0, it = 0;
-        bool ok = true;
-        // Every epilogue warp walks every unit (also after an abort) so that the
-        // named barrier below always sees all 256 threads.
+        bool alive = true;
+        // Every epilogue warp walks every unit and every tile, also after a
+        // timeout ("not alive": waits are skipped), so the named barriers always
+        // see all of their threads.
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x, ++it) {
             const UnitInfo ui = decode_unit<C::G>(p, u, lane);
             const Segment& sg = p.seg[ui.seg];
             float* cbuf = c_s + (it & 1) * kTileN;
-            if (etid < C::N) {   // c[n] = w * s_q for column n = row * H + head
+            if (etid < C::N) {   // c[n] = w * s_q for column n = row * H + head,
+                                 // times 2^25 where the epilogue's relu is scaled (n % 4 >= 2)
                 const int rl = etid / H;
                 const int t = ui.t0 + rl;
-                cbuf[etid] = rl < ui.nr ? p.w[(size_t)t * H + (etid % H)] *
-                                              p.s_q[(size_t)t * H + (etid % H)]
-                                        : 0.0f;
+                const float cv = rl < ui.nr ? p.w[(size_t)t * H + (etid % H)] *
+                                                  p.s_q[(size_t)t * H + (etid % H)]
+                                            : 0.0f;
+                cbuf[etid] = (etid & 2) ? cv * 33554432.0f : cv;
+            }
+            if constexpr (C::STREAM) {
+                for (int i = etid; i < C::G * 512; i += kEpiWarps * 32)
+                    hist_s[i] = 0;
+                if (etid < C::G) {
+                    RowState& rs = rows_s[etid];
+                    for (int q = 0; q < 4; ++q)
+                        rs.wcnt[q] = 0;
+                    rs.tau_hi = etid < ui.nr ? p.gtau[ui.t0 + etid] : 0u;
+                    rs.tau_lo = 0;
+                    rs.b1 = 256;
+                    rs.compact = 0;
+                }
             }
             asm volatile("bar.sync 1, 256;" ::: "memory");
-            if (!ok)
-                continue;
-            int clen[C::ROWS_PER_HALF];
+            int clen[C::RPH];
+            uint32_t tau_hi[C::RPH], tau_lo[C::RPH], b1[C::RPH], wcnt[C::RPH];
 #pragma unroll
-            for (int r = 0; r < C::ROWS_PER_HALF; ++r) {
-                const int rl = half * C::ROWS_PER_HALF + r;
+            for (int r = 0; r < C::RPH; ++r) {
+                const int rl = half * C::RPH + r;
                 clen[r] = rl < ui.nr ? min(p.compress_len[ui.t0 + rl], sg.key_count) : 0;
+                tau_hi[r] = 0;
+                tau_lo[r] = 0;
+                b1[r] = 256;
+                wcnt[r] = 0;
+                if constexpr (C::STREAM) {
+                    tau_hi[r] = rows_s[rl].tau_hi;
+                    tau_lo[r] = rows_s[rl].tau_lo;
+                }
             }
-            float* out_base = p.out + sg.out_offset - sg.j_begin;
+            // the rows' shared thresholds, read one refresh interval ahead of use
+            constexpr int kOwned = (C::RPH + 3) / 4;
+            uint32_t gpre[kOwned];
+#pragma unroll
+            for (int oi = 0; oi < kOwned; ++oi) {
+                const int rl = half * C::RPH + quad + 4 * oi;
+                gpre[oi] = 0;
+                if (C::STREAM && quad + 4 * oi < C::RPH && rl < ui.nr)
+                    gpre[oi] = ld_relaxed_gpu(p.gtau + ui.t0 + rl);
+            }
+            // key scales one tile ahead (a global load whose latency the tile hides)
+            float sk_next = 1.0f;
+            if (KFMT == kKeyFp8 && ui.ntiles_mma > 0) {
+                const int j0 = ui.j0 + kq;
+                sk_next = j0 < sg.key_count ? __ldg(p.s_k + sg.key_base + j0) : 0.0f;
+            }
+            // a warp's sub-list sees 32 of every 128 keys (or its lanes' blocks)
+            const int unit_entries_warp =
+                SINK == kSinkPool ? ui.ntiles * (32 / (p.pool > 0 ? p.pool : 1)) : ui.ntiles * 32;
+            const bool no_overflow = unit_entries_warp <= p.cap;
             for (int i = 0; i < ui.ntiles; ++i) {
                 const int j = ui.j0 + i * kTileKeys + kq;
-                float acc[C::ROWS_PER_HALF];
-                bool have = false;
+                float acc[C::RPH];
+#pragma unroll
+                for (int r = 0; r < C::RPH; ++r)
+                    acc[r] = -INFINITY;
                 if (i < ui.ntiles_mma) {
-                    float sk = 1.0f;
-                    if (KFMT == kKeyFp8)
-                        sk = j < sg.key_count ? __ldg(p.s_k + sg.key_base + j) : 0.0f;
-                    const bool got = mbar_wait(&a_full[ab], aph, budget, abort_flag);
-                    if (!__all_sync(0xffffffffu, got)) {
+                    const float sk = sk_next;
+                    if (KFMT == kKeyFp8 && i + 1 < ui.ntiles_mma)
+                        sk_next = j + kTileKeys < sg.key_count
+                                      ? __ldg(p.s_k + sg.key_base + j + kTileKeys)
+                                      : 0.0f;
+                    bool got = alive && mbar_wait(&a_full[ab], aph, budget, abort_flag);
+                    got = __all_sync(0xffffffffu, got);
+                    if (!got && alive) {
                         if (lane == 0)
                             report(p, abort_flag, kStatusTimeout);
-                        ok = false;
-                        break;
+                        alive = false;
                     }
-                    tc_fence_after();
+                    if (got) {
+                        tc_fence_after();
+                        // four partial sums per row (heads h = 0,1,2,3 mod 4), two per
+                        // packed FMA.  Heads 0,1 mod 4: relu by max (ALU pipe); heads
+                        // 2,3 mod 4: relu(S) * 2^-25 by a saturating multiply (FMA pipe)
+                        // with c stored times 2^25, so every product and sum is
+                        // bit-identical to fmaf(c, max(S, 0), part).
+                        float2 part[C::RPH][2];
 #pragma unroll
-                    for (int r = 0; r < C::ROWS_PER_HALF; ++r)
-                        acc[r] = 0.0f;
-                    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                           ab * C::ACC_COLS + half * C::HALF_COLS;
-                    const float4* cc4 =
-                        reinterpret_cast<const float4*>(cbuf + half * C::HALF_COLS);
+                        for (int r = 0; r < C::RPH; ++r) {
+                            part[r][0] = make_float2(0.0f, 0.0f);
+                            part[r][1] = make_float2(0.0f, 0.0f);
+                        }
+                        const uint32_t tbase = tmem_base +
+                                               (static_cast<uint32_t>(quad * 32) << 16) +
+                                               ab * C::ACC_COLS + half * C::HALF_COLS;
+                        const float4* cc4 =
+                            reinterpret_cast<const float4*>(cbuf + half * C::HALF_COLS);
+                        // next 32 columns (TMEM) and their 32 head weights (shared memory)
+                        // in flight while the current ones are reduced
+                        float va[32], vb[32];
+                        float4 ca[8], cb[8];
+                        tmem_ld_32x32b_x32(tbase, va);
 #pragma unroll
-                    for (int ch = 0; ch < C::HALF_COLS / 32; ++ch) {
-                        float v[32];
-                        tmem_ld_32x32b_x32(tbase + ch * 32, v);
+                        for (int e4 = 0; e4 < 8; ++e4)
+                            ca[e4] = cc4[e4];
                         tmem_wait_ld();
 #pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {
-                            const float4 c4 = cc4[ch * 8 + e4];
-                            const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+                        for (int ch = 0; ch < C::NCH; ++ch) {
+                            float(&cur)[32] = (ch & 1) ? vb : va;
+                            float(&nxt)[32] = (ch & 1) ? va : vb;
+                            float4(&ccur)[8] = (ch & 1) ? cb : ca;
+                            float4(&cnxt)[8] = (ch & 1) ? ca : cb;
+                            if (ch + 1 < C::NCH) {
+                                tmem_ld_32x32b_x32(tbase + (ch + 1) * 32, nxt);
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int col = ch * 32 + e4 * 4 + e;
-                                acc[col / H] = fmaf(cv[e], fmaxf(v[e4 * 4 + e], 0.0f), acc[col / H]);
+                                for (int e4 = 0; e4 < 8; ++e4)
+                                    cnxt[e4] = cc4[(ch + 1) * 8 + e4];
                             }
+#pragma unroll
+                            for (int e4 = 0; e4 < 8; ++e4) {
+                                const float4 c4 = ccur[e4];
+                                const int r = (ch * 32 + e4 * 4) / H;
+                                const float2 r01 = make_float2(fmaxf(cur[e4 * 4 + 0], 0.0f),
+                                                               fmaxf(cur[e4 * 4 + 1], 0.0f));
+                                const float2 r23 = make_float2(relu_scaled(cur[e4 * 4 + 2]),
+                                                               relu_scaled(cur[e4 * 4 + 3]));
+                                part[r][0] = __ffma2_rn(make_float2(c4.x, c4.y), r01, part[r][0]);
+                                part[r][1] = __ffma2_rn(make_float2(c4.z, c4.w), r23, part[r][1]);
+                            }
+                            if (ch + 1 < C::NCH)
+                                tmem_wait_ld();
                         }
+#pragma unroll
+                        for (int r = 0; r < C::RPH; ++r)
+                            acc[r] = ((part[r][0].x + part[r][0].y) + (part[r][1].x + part[r][1].y)) * sk;
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0)
+                    if (lane == 0 && got)
                         mbar_arrive(&a_empty[ab]);
                     if (++ab == 2) {
                         ab = 0;
                         aph ^= 1;
                     }
-#pragma unroll
-                    for (int r = 0; r < C::ROWS_PER_HALF; ++r)
-                        acc[r] *= sk;
-                    have = true;
                 }
-                if (j < ui.jend) {
+                // causal and candidate masks
 #pragma unroll
-                    for (int r = 0; r < C::ROWS_PER_HALF; ++r) {
-                        const int rl = half * C::ROWS_PER_HALF + r;
-                        if (rl < ui.nr) {
-                            const int t = ui.t0 + rl;
-                            bool valid = have && j < clen[r];
-                            if (valid && p.cand_mask)
-                                valid = p.cand_mask[(size_t)t * p.ld_mask + j / p.mask_block] != 0;
-                            out_base[(size_t)(t - sg.row_begin) * sg.out_ld + j] =
-                                valid ? acc[r] : -INFINITY;
+                for (int r = 0; r < C::RPH; ++r) {
+                    const int rl = half * C::RPH + r;
+                    bool valid = rl < ui.nr && j < clen[r];
+                    if (valid && p.cand_mask)
+                        valid = p.cand_mask[(size_t)(ui.t0 + rl) * p.ld_mask + j / p.mask_block] != 0;
+                    if (!valid)
+                        acc[r] = -INFINITY;
+                }
+                if constexpr (SINK == kSinkLogits) {
+                    if (j < ui.jend) {
+                        float* out_base = p.out + sg.out_offset - sg.j_begin;
+#pragma unroll
+                        for (int r = 0; r < C::RPH; ++r) {
+                            const int rl = half * C::RPH + r;
+                            if (rl < ui.nr)
+                                out_base[(size_t)(ui.t0 + rl - sg.row_begin) * sg.out_ld + j] =
+                                    acc[r];
+                        }
+                    }
+                } else {
+                    const uint32_t cap = static_cast<uint32_t>(p.cap);
+#pragma unroll
+                    for (int r = 0; r < C::RPH; ++r) {
+                        const int rl = half * C::RPH + r;
+                        uint32_t* h1 = hist_s + rl * 512;
+                        uint2* sub = p.lists + sg.out_offset +
+                                     (int64_t)(ui.t0 + rl - sg.row_begin) * sg.out_ld +
+                                     (int64_t)quad * p.cap;
+                        if constexpr (SINK == kSinkStream) {
+                            wcnt[r] = stream_push(h1, h1 + 256, sub, cap, wcnt[r], tau_hi[r],
+                                                  tau_lo[r], b1[r], acc[r],
+                                                  static_cast<uint32_t>(j), rl < ui.nr, lane);
+                        } else {
+                            // block maximum over `pool` consecutive keys (lanes)
+                            float bm = acc[r];
+                            for (int o = 1; o < p.pool; o <<= 1)
+                                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+                            const bool lead = (kq % p.pool) == 0;
+                            wcnt[r] = stream_push(h1, h1 + 256, sub, cap, wcnt[r], tau_hi[r],
+                                                  tau_lo[r], b1[r], bm,
+                                                  static_cast<uint32_t>(j / p.pool),
+                                                  lead && rl < ui.nr, lane);
+                        }
+                    }
+                    const bool refresh = ((i + 1) % p.update_tiles) == 0 || i + 1 == ui.ntiles;
+                    if (refresh) {
+                        // publish this warp's counts, then the row owners refresh tau
+                        if (lane == 0) {
+#pragma unroll
+                            for (int r = 0; r < C::RPH; ++r)
+                                rows_s[half * C::RPH + r].wcnt[quad] = wcnt[r];
+                        }
+                        half_sync();
+                        // rows of this half: warp `quad` owns rows quad, quad+4, ...
+#pragma unroll
+                        for (int oi = 0; oi < kOwned; ++oi) {
+                            const int rr = quad + 4 * oi;
+                            const int rl = half * C::RPH + rr;
+                            if (rr >= C::RPH)
+                                continue;
+                            if (rl >= ui.nr)
+                                continue;
+                            RowState& rs = rows_s[rl];
+                            uint32_t* h1 = hist_s + rl * 512;
+                            uint32_t* h2 = h1 + 256;
+                            const uint32_t keep = static_cast<uint32_t>(p.keep);
+                            const uint32_t cur_b1 = rs.b1;
+                            const uint32_t sum2 = cur_b1 < 256 ? warp_sum_bins(h2, lane) : 0u;
+                            uint32_t above1 = 0, tau_new = 0;
+                            const uint32_t bin1 =
+                                boundary_bin(h1, keep, lane, &above1, cur_b1, sum2);
+                            if (bin1 < 256) {
+                                __syncwarp();
+                                if (cur_b1 == 256 || bin1 > cur_b1) {
+                                    for (int i2 = lane; i2 < 256; i2 += 32)
+                                        h2[i2] = 0;
+                                    __syncwarp();
+                                    tau_new = bin1 << 24;
+                                    if (lane == 0)
+                                        rs.b1 = bin1;
+                                } else {
+                                    uint32_t above2 = 0;
+                                    const uint32_t bin2 =
+                                        boundary_bin(h2, keep - above1, lane, &above2);
+                                    tau_new = (bin1 << 24) | (bin2 < 256 ? bin2 << 16 : 0u);
+                                }
+                            }
+                            if (lane == 0) {
+                                const int t = ui.t0 + rl;
+                                const uint32_t g = gpre[oi];
+                                if (tau_new > g)
+                                    atomicMax(p.gtau + t, tau_new);
+                                const uint32_t best = max(tau_new, g);
+                                if (best > rs.tau_hi) {
+                                    rs.tau_hi = best;
+                                    rs.tau_lo = 0;
+                                }
+                                // a sub-list must have room for the next refresh interval
+                                const uint32_t slack =
+                                    static_cast<uint32_t>(p.update_tiles) * 32u;
+                                bool full = false, lost = false;
+                                for (int q = 0; q < 4; ++q) {
+                                    full |= rs.wcnt[q] + slack > cap;
+                                    lost |= rs.wcnt[q] > cap;
+                                }
+                                rs.compact = (full && !no_overflow) ? 1u : 0u;
+                                if (lost)
+                                    atomicOr(p.status, kStatusListOverflow);
+                            }
+                        }
+                        half_sync();
+                        // exact compaction of any row whose sub-lists are about to fill
+                        // (all 128 threads): keep the top `keep` entries of the four
+                        // sub-lists, written to the front of sub-list 0
+                        for (int rr = 0; rr < C::RPH; ++rr) {
+                            const int rl = half * C::RPH + rr;
+                            if (rl >= ui.nr || rows_s[rl].compact == 0)
+                                continue;
+                            RowState& rs = rows_s[rl];
+                            uint2* list = p.lists + sg.out_offset +
+                                          (int64_t)(ui.t0 + rl - sg.row_begin) * sg.out_ld;
+                            const int n0 = static_cast<int>(min(rs.wcnt[0], cap));
+                            const int n1 = static_cast<int>(min(rs.wcnt[1], cap));
+                            const int n2 = static_cast<int>(min(rs.wcnt[2], cap));
+                            const int n3 = static_cast<int>(min(rs.wcnt[3], cap));
+                            const int o1 = n0, o2 = n0 + n1, o3 = n0 + n1 + n2;
+                            const int n = o3 + n3;
+                            auto at = [&](int e) -> uint2* {
+                                const int q = (e >= o1) + (e >= o2) + (e >= o3);
+                                const int base = q == 0 ? 0 : (q == 1 ? o1 : (q == 2 ? o2 : o3));
+                                return list + (int64_t)q * p.cap + (e - base);
+                            };
+                            auto load = [&](int e, uint32_t& hi, uint32_t& lo) {
+                                const uint2 ent = *at(e);
+                                hi = f2ord(__uint_as_float(ent.x));
+                                lo = ~ent.y;
+                            };
+                            const CompositeThr thr = group_threshold<kHalfThreads>(
+                                *sel_s, htid, n, static_cast<uint32_t>(p.keep), load, half_sync);
+                            // kept entry number pos goes to sub-list 0, index pos <= e
+                            auto emit = [&](int pos, int e, uint32_t hi, uint32_t lo) {
+                                (void)e;
+                                list[pos] = make_uint2(__float_as_uint(ord2f(hi)), ~lo);
+                            };
+                            const int kept = group_emit<kHalfThreads>(*sel_s, htid, n, thr, load,
+                                                                      emit, half_sync);
+                            if (htid == 0) {
+                                rs.wcnt[0] = static_cast<uint32_t>(kept);
+                                rs.wcnt[1] = rs.wcnt[2] = rs.wcnt[3] = 0;
+                                rs.compact = 0;
+                                // later entries must reach the kept set's threshold
+                                if (thr.phi > rs.tau_hi ||
+                                    (thr.phi == rs.tau_hi && thr.plo > rs.tau_lo)) {
+                                    rs.tau_hi = thr.phi;
+                                    rs.tau_lo = thr.plo;
+                                }
+                                const int t = ui.t0 + rl;
+                                const uint32_t g =
+                                    *reinterpret_cast<volatile uint32_t*>(p.gtau + t);
+                                if (thr.phi > g)
+                                    atomicMax(p.gtau + t, thr.phi);
+                            }
+                            half_sync();
+                        }
+#pragma unroll
+                        for (int oi = 0; oi < kOwned; ++oi) {
+                            const int rl = half * C::RPH + quad + 4 * oi;
+                            if (quad + 4 * oi < C::RPH && rl < ui.nr)
+                                gpre[oi] = ld_relaxed_gpu(p.gtau + ui.t0 + rl);
+                        }
+#pragma unroll
+                        for (int r = 0; r < C::RPH; ++r) {
+                            const int rl = half * C::RPH + r;
+                            tau_hi[r] = rows_s[rl].tau_hi;
+                            tau_lo[r] = rows_s[rl].tau_lo;
+                            b1[r] = rows_s[rl].b1;
+                            wcnt[r] = rows_s[rl].wcnt[quad];
                         }
                     }
                 }
+            }
+            if constexpr (C::STREAM) {
+                // unit end: every warp publishes its own sub-list lengths (also for
+                // units with no tiles)
+                if (lane == 0) {
+#pragma unroll
+                    for (int r = 0; r < C::RPH; ++r) {
+                        const int rl = half * C::RPH + r;
+                        if (rl < ui.nr)
+                            p.counts[sg.cnt_offset +
+                                     (int64_t)(ui.t0 + rl - sg.row_begin) * sg.cnt_ld + quad] =
+                                min(wcnt[r], static_cast<uint32_t>(p.cap));
+                    }
+                }
+                // both halves are done with the row state before the next unit resets it
+                asm volatile("bar.sync 1, 256;" ::: "memory");
             }
         }
     }
@@ -436,14 +841,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1)
-        tmem_dealloc(tmem_base, 2 * C::ACC_COLS);
+        tmem_dealloc(tmem_base, 512);
 }
 
-template <int H, int D, int KFMT>
+template <int H, int D, int KFMT, int SINK>
 cudaError_t launch_one(const LogitsParams& p, int grid, cudaStream_t stream)
 {
-    using C = Cfg<H, D, KFMT>;
-    auto kern = logits_tc_kernel<H, D, KFMT>;
+    using C = Cfg<H, D, KFMT, SINK>;
+    auto kern = logits_tc_kernel<H, D, KFMT, SINK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);
     if (e != cudaSuccess)
@@ -452,40 +857,39 @@ cudaError_t launch_one(const LogitsParams& p, int grid, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-}  // namespace
-
-size_t logits_smem_bytes(int H, int D, int kfmt)
+template <int H, int D, int KFMT>
+cudaError_t launch_sink(const LogitsParams& p, int sink, int grid, cudaStream_t stream)
 {
-    if (kfmt == kKeyFp4)
-        return (H == 32 && D == 128) ? Cfg<32, 128, kKeyFp4>::SMEM : 0;
-    if (H == 32 && D == 128)
-        return Cfg<32, 128, kKeyFp8>::SMEM;
-    if (H == 4 && D == 64)
-        return Cfg<4, 64, kKeyFp8>::SMEM;
-    if (H == 64 && D == 128)
-        return Cfg<64, 128, kKeyFp8>::SMEM;
-    if (H == 16 && D == 128)
-        return Cfg<16, 128, kKeyFp8>::SMEM;
-    return 0;
+    if (sink == kSinkLogits)
+        return launch_one<H, D, KFMT, kSinkLogits>(p, grid, stream);
+    if (sink == kSinkStream)
+        return launch_one<H, D, KFMT, kSinkStream>(p, grid, stream);
+    if (sink == kSinkPool)
+        return launch_one<H, D, KFMT, kSinkPool>(p, grid, stream);
+    return cudaErrorInvalidValue;
 }
 
-int logits_rows_per_group(int H, int kfmt) { return (kfmt == kKeyFp4 ? 192 : kTileN) / H; }
+}  // namespace
 
-cudaError_t launch_logits(const LogitsParams& p, int H, int D, int kfmt, int grid,
+int logits_rows_per_group(int H, int kfmt)
+{
+    if (kfmt == kKeyFp4)
+        return 192 / H;
+    return H >= 16 ? kTileN / H : 16;
+}
+
+cudaError_t launch_logits(const LogitsParams& p, int H, int D, int kfmt, int sink, int grid,
                           cudaStream_t stream)
 {
     if (kfmt == kKeyFp8) {
         if (H == 32 && D == 128)
-            return launch_one<32, 128, kKeyFp8>(p, grid, stream);
-        if (H == 4 && D == 64)
-            return launch_one<4, 64, kKeyFp8>(p, grid, stream);
-        if (H == 64 && D == 128)
-            return launch_one<64, 128, kKeyFp8>(p, grid, stream);
+            return launch_sink<32, 128, kKeyFp8>(p, sink, grid, stream);
         if (H == 16 && D == 128)
-            return launch_one<16, 128, kKeyFp8>(p, grid, stream);
-    } else if (kfmt == kKeyFp4) {
-        if (H == 32 && D == 128)
-            return launch_one<32, 128, kKeyFp4>(p, grid, stream);
+            return launch_sink<16, 128, kKeyFp8>(p, sink, grid, stream);
+        if (H == 64 && D == 128)
+            return launch_sink<64, 128, kKeyFp8>(p, sink, grid, stream);
+        if (H == 4 && D == 64)
+            return launch_sink<4, 64, kKeyFp8>(p, sink, grid, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -18,6 +18,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p)
 
 // ------------------------------------------------------------- mbarriers
 
+// Relaxed device-scope load of a value other CTAs update with atomics.
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
@@ -54,6 +62,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread until the phase completes
+// or `hint_ns` nanoseconds pass, instead of returning at once (a waiting warp
+// then takes no issue slots from the warps doing work).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed.  Returns false
 // when `budget` SM cycles pass first or when *abort becomes non-zero.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long budget,
@@ -63,9 +88,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
         return true;
     const long long t0 = clock64();
     while (true) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity))
-                return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000u))
+            return true;
         if (*abort)
             return false;
         if (clock64() - t0 > budget)
@@ -274,6 +298,17 @@ __host__ __device__ constexpr uint32_t idesc_mxf8f6f4(int M, int N, int a_fmt, i
            (static_cast<uint32_t>(b_fmt) << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
            (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) |
            (static_cast<uint32_t>(a_sf_id & 3) << 29);
+}
+
+// ReLU on the FMA pipe, scaled by 2^-25: sat(x * 2^-25) clamps to [0, 1],
+// which equals max(x, 0) * 2^-25 exactly whenever |x| < 2^25 (scaling by a
+// power of two is exact at these magnitudes).  FMNMX runs on the ALU pipe at
+// half the FMA rate, so the epilogue spreads its ReLUs over both pipes.
+__device__ __forceinline__ float relu_scaled(float x)
+{
+    float r;
+    asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(r) : "f"(x), "f"(2.98023223876953125e-08f));
+    return r;
 }
 
 // Order-preserving map of an fp32 value to uint32 (larger float -> larger key).

@@ -1,245 +1,24 @@
 // Exact per-row top-k selection kernels.
 //
 // Selection rule: among the eligible entries of a row (finite score, inside
-// the row's causal length), keep the k with the largest score; on equal
-// scores the lower key index wins.  Used three ways:
-//   * per key split: the top-k of one block of keys ("chunked-prefill-
-//     memory.md" section 2.3: score against key blocks, keep the per-block
-//     top-k values and indices);
-//   * merge: the top-k of the union of the per-block candidates, which is
-//     exactly the top-k of the whole row (same section: "topk(union) ==
-//     topk(union of per-block topk) holds exactly");
-//   * candidate blocks: the same, over the maximum score of each 8-key block
-//     (same section: block pooling over 8-key blocks, top-2048 blocks).
-//
-// Algorithm: radix select on the order-preserving 32-bit image of the fp32
-// score, 8 bits per pass from the top, stopping as soon as the boundary bin
-// is taken whole; exact ties at the k-th score are resolved by position
-// (= key order) in a final ordered pass.  The output lists the kept entries
-// in ascending key order, so results are bitwise reproducible.
+// the row's causal length, a candidate block for masked consumers) keep the
+// k with the largest score; on equal scores the lower key index wins.  Used
+// for
+//   * the ragged top-k over dense logits (indexer_topk, the ragged top-k that
+//     "chunked-prefill-memory.md" section 2.3 runs after the logits);
+//   * the exact merge of the candidate lists that the streaming logits kernel
+//     appends per key split: the top-k of the union of the splits' candidates
+//     is the top-k of the row (same section, "holds exactly");
+//   * candidate blocks: the same over 8-key block maxima, written as a mask.
+// The threshold search and ordered emission are in groupsel.cuh.
+#include "groupsel.cuh"
 #include "internal.h"
-#include "ptx.cuh"
 
 namespace idx {
 namespace {
 
 constexpr int kSelThreads = 512;
-constexpr int kSelWarps = kSelThreads / 32;
-
-struct SelShared {
-    uint32_t hist[256];
-    uint32_t warp_a[kSelWarps];
-    uint32_t warp_b[kSelWarps];
-    uint32_t bcast[4];
-};
-
-// Warp-aggregated histogram increment: lanes with the same digit add once.
-__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t digit, bool active)
-{
-    const uint32_t d = active ? digit : 256u;
-    const uint32_t peers = __match_any_sync(0xffffffffu, d);
-    const int leader = __ffs(peers) - 1;
-    if (active && (threadIdx.x & 31) == leader)
-        atomicAdd(&hist[d], static_cast<uint32_t>(__popc(peers)));
-}
-
-// Block-wide exclusive scan of two counters (one entry per thread).
-__device__ __forceinline__ void block_scan2(SelShared& sh, uint32_t a, uint32_t b, uint32_t& pa,
-                                            uint32_t& pb, uint32_t& ta, uint32_t& tb)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t ia = a, ib = b;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t xa = __shfl_up_sync(0xffffffffu, ia, o);
-        const uint32_t xb = __shfl_up_sync(0xffffffffu, ib, o);
-        if (lane >= o) {
-            ia += xa;
-            ib += xb;
-        }
-    }
-    if (lane == 31) {
-        sh.warp_a[warp] = ia;
-        sh.warp_b[warp] = ib;
-    }
-    __syncthreads();
-    uint32_t wa = 0, wb = 0;
-    ta = 0;
-    tb = 0;
-    for (int w = 0; w < kSelWarps; ++w) {
-        const uint32_t x = sh.warp_a[w], y = sh.warp_b[w];
-        if (w < warp) {
-            wa += x;
-            wb += y;
-        }
-        ta += x;
-        tb += y;
-    }
-    pa = wa + ia - a;
-    pb = wb + ib - b;
-    __syncthreads();
-}
-
-// Top-k of entries 0..n-1 of one row.  load(e) -> fp32 score (-inf = not
-// eligible).  emit(pos, e, v) writes output slot pos (0 <= pos < k) in
-// ascending e.  Returns the number of entries emitted (<= k).
-template <class Load, class Emit>
-__device__ int block_topk(SelShared& sh, int n, int k, const Load& load, const Emit& emit)
-{
-    const int tid = threadIdx.x;
-    uint32_t prefix = 0, pmask = 0;
-    uint32_t remaining = static_cast<uint32_t>(k);
-    bool take_all = false;     // every eligible entry is kept
-    bool resolved = false;     // boundary bin taken whole: keep (ord & pmask) >= prefix
-    uint32_t tie_quota = 0;    // after 32 bits: how many entries equal to prefix to keep
-
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        for (int i = tid; i < 256; i += kSelThreads)
-            sh.hist[i] = 0;
-        __syncthreads();
-        for (int base = 0; base < n; base += kSelThreads) {
-            const int e = base + tid;
-            bool act = false;
-            uint32_t dig = 0;
-            if (e < n) {
-                const uint32_t o = f2ord(load(e));
-                act = o > kOrdNegInf && (o & pmask) == prefix;
-                dig = (o >> shift) & 255u;
-            }
-            hist_add(sh.hist, dig, act);
-        }
-        __syncthreads();
-        if (tid == 0) {
-            uint32_t total = 0;
-            for (int b = 0; b < 256; ++b)
-                total += sh.hist[b];
-            uint32_t flag = 0, bin = 0, above = 0;
-            if (pass == 0 && total <= remaining) {
-                flag = 1;  // fewer eligible entries than k
-            } else {
-                uint32_t cum = 0;
-                for (int b = 255; b >= 0; --b) {
-                    const uint32_t c = sh.hist[b];
-                    if (cum + c >= remaining) {
-                        bin = static_cast<uint32_t>(b);
-                        above = cum;
-                        flag = (cum + c == remaining) ? 2 : 0;
-                        break;
-                    }
-                    cum += c;
-                }
-            }
-            sh.bcast[0] = flag;
-            sh.bcast[1] = bin;
-            sh.bcast[2] = above;
-        }
-        __syncthreads();
-        const uint32_t flag = sh.bcast[0];
-        if (flag == 1) {
-            take_all = true;
-            break;
-        }
-        prefix |= sh.bcast[1] << shift;
-        pmask |= 255u << shift;
-        remaining -= sh.bcast[2];
-        __syncthreads();
-        if (flag == 2) {
-            resolved = true;
-            break;
-        }
-    }
-    if (!take_all && !resolved)
-        tie_quota = remaining;   // keep > prefix, plus the first tie_quota entries == prefix
-
-    // ordered output pass
-    uint32_t sel_before = 0, ties_before = 0;
-    for (int base = 0; base < n; base += kSelThreads) {
-        const int e = base + tid;
-        uint32_t sel = 0, tie = 0;
-        float v = -INFINITY;
-        if (e < n) {
-            v = load(e);
-            const uint32_t o = f2ord(v);
-            if (o > kOrdNegInf) {
-                if (take_all)
-                    sel = 1;
-                else if (resolved)
-                    sel = (o & pmask) >= prefix ? 1u : 0u;
-                else if (o > prefix)
-                    sel = 1;
-                else if (o == prefix)
-                    tie = 1;
-            }
-        }
-        uint32_t ps, pt, ts, tt;
-        block_scan2(sh, sel, tie, ps, pt, ts, tt);
-        if (tie && ties_before + pt < tie_quota)
-            sel = 1;
-        // positions: entries are emitted in ascending e, so count kept entries before e
-        const uint32_t kept_tie_before =
-            min(tie_quota, ties_before + pt) - min(tie_quota, ties_before);
-        const uint32_t pos = sel_before + ps + kept_tie_before;
-        if (sel && pos < static_cast<uint32_t>(k))
-            emit(static_cast<int>(pos), e, v);
-        const uint32_t kept_ties_chunk = min(tie_quota, ties_before + tt) - min(tie_quota, ties_before);
-        sel_before += ts + kept_ties_chunk;
-        ties_before += tt;
-    }
-    return static_cast<int>(min(sel_before, static_cast<uint32_t>(k)));
-}
-
-// ------------------------------------------------------------ per-split
-
-__global__ void __launch_bounds__(kSelThreads) select_dense_kernel(const __grid_constant__ SelParams p)
-{
-    __shared__ SelShared sh;
-    const int cta = blockIdx.x;
-    int s = 0;
-    while (s + 1 < p.num_segments && p.seg[s + 1].row_block <= cta)
-        ++s;
-    const SelSegment& sg = p.seg[s];
-    const int tr = cta - sg.row_block;       // row within the segment
-    const int t = sg.row_begin + tr;
-    const int clen = min(p.compress_len[t], sg.key_count);
-    const float* src = p.src + sg.src_offset + (int64_t)tr * sg.src_ld;
-    const int64_t out_base = sg.cand_offset + ((int64_t)tr * sg.n_slots + sg.cand_slot) * p.k;
-    float* cv = p.cand_val + out_base;
-    int32_t* ci = p.cand_idx + out_base;
-    int count;
-    if (p.pool == 0) {
-        const int n = max(0, min(clen - sg.j_begin, sg.n_entries));
-        auto load = [&](int e) { return src[e]; };
-        auto emit = [&](int pos, int e, float v) {
-            cv[pos] = v;
-            ci[pos] = sg.j_begin + e;
-        };
-        count = block_topk(sh, n, p.k, load, emit);
-    } else {
-        const int pool = p.pool;
-        const int nkeys = max(0, min(clen - sg.j_begin * pool, sg.n_entries * pool));
-        const int n = (nkeys + pool - 1) / pool;
-        auto load = [&](int e) {
-            float m = -INFINITY;
-            const int k0 = e * pool;
-            const int k1 = min(k0 + pool, nkeys);
-            for (int kk = k0; kk < k1; ++kk)
-                m = fmaxf(m, src[kk]);
-            return m;
-        };
-        auto emit = [&](int pos, int e, float v) {
-            cv[pos] = v;
-            ci[pos] = sg.j_begin + e;
-        };
-        count = block_topk(sh, n, p.k, load, emit);
-    }
-    for (int i = count + threadIdx.x; i < p.k; i += kSelThreads) {
-        cv[i] = -INFINITY;
-        ci[i] = -1;
-    }
-}
-
-// ---------------------------------------------------------------- merge
+using Scratch = SelScratch<kSelThreads>;
 
 __device__ __forceinline__ int find_request(const int32_t* row_begin, int nreq, int t)
 {
@@ -254,45 +33,191 @@ __device__ __forceinline__ int find_request(const int32_t* row_begin, int nreq, 
     return lo;
 }
 
-__global__ void __launch_bounds__(kSelThreads) merge_kernel(const __grid_constant__ MergeParams p)
+// Top-k of entries 0..n-1; load(e) -> (score, index).  Emits in ascending e.
+template <class LoadVJ, class Emit>
+__device__ int cta_topk(Scratch& sh, int n, int k, const LoadVJ& load_vj, const Emit& emit)
 {
-    __shared__ SelShared sh;
-    const int t = blockIdx.x;
-    const int r = find_request(p.req_row_begin, p.num_requests, t);
-    const int tr = t - p.req_row_begin[r];
-    const int nslots = p.req_slots[r];
-    const int64_t base = p.req_cand_offset[r] + (int64_t)tr * nslots * p.k;
-    const float* cv = p.cand_val + base;
-    const int32_t* ci = p.cand_idx + base;
-    const int n = nslots * p.k;
-    auto load = [&](int e) { return cv[e]; };
+    auto load = [&](int e, uint32_t& hi, uint32_t& lo) {
+        float v;
+        int32_t j;
+        load_vj(e, v, j);
+        hi = f2ord(v);
+        lo = ~static_cast<uint32_t>(j);
+    };
+    const CompositeThr thr =
+        group_threshold<kSelThreads>(sh, threadIdx.x, n, static_cast<uint32_t>(k), load, CtaSync{});
+    auto emit_e = [&](int pos, int e, uint32_t hi, uint32_t lo) {
+        if (pos < k)
+            emit(pos, e, ord2f(hi), static_cast<int32_t>(~lo));
+    };
+    const int count = group_emit<kSelThreads>(sh, threadIdx.x, n, thr, load, emit_e, CtaSync{});
+    return min(count, k);
+}
+
+// --------------------------------------------------- streamed-list merge
+
+// Bitonic sort of n2 (a power of two) (key, value) pairs in shared memory,
+// ascending by key.
+__device__ void bitonic_sort(int32_t* key, float* val, int n2)
+{
+    for (int size = 2; size <= n2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            __syncthreads();
+            for (int i = threadIdx.x; i < n2 / 2; i += kSelThreads) {
+                const int lo = 2 * i - (i & (stride - 1));
+                const int hi = lo + stride;
+                const bool up = (lo & size) == 0;
+                const int32_t a = key[lo], b = key[hi];
+                if ((a > b) == up) {
+                    key[lo] = b;
+                    key[hi] = a;
+                    const float fa = val[lo];
+                    val[lo] = val[hi];
+                    val[hi] = fa;
+                }
+            }
+        }
+    }
+    __syncthreads();
+}
+
+constexpr int kMaxSortK = 4096;
+constexpr int kStageEntries = 7168;   // candidates staged in shared memory per row (56 KB)
+
+__global__ void __launch_bounds__(kSelThreads)
+    stream_merge_kernel(const __grid_constant__ StreamMergeParams p)
+{
+    __shared__ Scratch sh;
+    __shared__ int32_t s_off[kMaxStreamSlots + 1];
+    extern __shared__ __align__(16) uint8_t dyn[];
+    // [stage: kStageEntries x 8 B][keys: n2 x 4 B][values: n2 x 4 B], n2 = k rounded up
+    // to a power of two
+    int n2 = 1;
+    while (n2 < p.k)
+        n2 <<= 1;
+    uint2* stage = reinterpret_cast<uint2*>(dyn);
+    int32_t* skey = reinterpret_cast<int32_t*>(dyn + sizeof(uint2) * kStageEntries);
+    float* sval = reinterpret_cast<float*>(dyn + sizeof(uint2) * kStageEntries + sizeof(int32_t) * n2);
+
+    __shared__ int32_t s_staged;
+    const int cta = blockIdx.x;
+    int pi = 0;
+    while (pi + 1 < p.num_pieces && p.piece[pi + 1].cta_begin <= cta)
+        ++pi;
+    const MergePiece& pc = p.piece[pi];
+    const int tr = cta - pc.cta_begin;
+    const int t = pc.row_begin + tr;
+    const int nslots = pc.slots;
+    const int64_t lbase = pc.list_offset + (int64_t)tr * nslots * pc.cap;
+    const int64_t cbase = pc.count_offset + (int64_t)tr * nslots;
+    // entries below the row's final threshold bound cannot be among its top k
+    const uint32_t floor_ord = p.gtau ? p.gtau[t] : 0u;
+    if (threadIdx.x < 32) {
+        // exclusive prefix of the sub-list lengths, 32 slots per step
+        int carry = 0;
+        for (int s0 = 0; s0 < nslots; s0 += 32) {
+            const int s = s0 + static_cast<int>(threadIdx.x);
+            const int c = s < nslots ? min(static_cast<int>(p.counts[cbase + s]), pc.cap) : 0;
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if ((threadIdx.x & 31) >= static_cast<unsigned>(o))
+                    incl += y;
+            }
+            if (s < nslots)
+                s_off[s] = carry + incl - c;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (threadIdx.x == 0) {
+            s_off[nslots] = carry;
+            s_staged = 0;
+        }
+    }
+    __syncthreads();
+    const int n_all = s_off[nslots];
+    // copy the entries that pass the floor into shared memory (order is irrelevant:
+    // the selection is by unique composite keys); every radix pass reads them there
+    for (int s = 0; s < nslots; ++s) {
+        const uint2* src = p.lists + lbase + (int64_t)s * pc.cap;
+        const int c = s_off[s + 1] - s_off[s];
+        for (int i0 = 0; i0 < c; i0 += kSelThreads) {
+            const int i = i0 + threadIdx.x;
+            uint2 ent = make_uint2(0u, 0u);
+            bool pass = false;
+            if (i < c) {
+                ent = src[i];
+                pass = f2ord(__uint_as_float(ent.x)) >= floor_ord;
+            }
+            const uint32_t m = __ballot_sync(0xffffffffu, pass);
+            int base = 0;
+            if ((threadIdx.x & 31) == 0 && m)
+                base = atomicAdd(&s_staged, __popc(m));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            const int pos = base + __popc(m & ((1u << (threadIdx.x & 31)) - 1u));
+            if (pass && pos < kStageEntries)
+                stage[pos] = ent;
+        }
+    }
+    __syncthreads();
+    const bool staged = s_staged <= kStageEntries;
+    const int n = staged ? s_staged : n_all;
+    const int k = p.k;
+    for (int i = threadIdx.x; i < n2; i += kSelThreads) {
+        skey[i] = INT32_MAX;
+        sval[i] = -INFINITY;
+    }
+    __syncthreads();
+    auto emit = [&](int pos, int e, float v, int32_t j) {
+        (void)e;
+        skey[pos] = j;
+        sval[pos] = v;
+    };
+    int count;
+    if (staged) {
+        auto load = [&](int e, float& v, int32_t& j) {
+            const uint2 ent = stage[e];
+            v = __uint_as_float(ent.x);
+            j = static_cast<int32_t>(ent.y);
+        };
+        count = cta_topk(sh, n, k, load, emit);
+    } else {
+        auto load = [&](int e, float& v, int32_t& j) {
+            int lo = 0, hi = nslots - 1;   // the slot s with s_off[s] <= e < s_off[s + 1]
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_off[mid] <= e)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            const uint2 ent = p.lists[lbase + (int64_t)lo * pc.cap + (e - s_off[lo])];
+            v = __uint_as_float(ent.x);
+            if (f2ord(v) < floor_ord)
+                v = -INFINITY;
+            j = static_cast<int32_t>(ent.y);
+        };
+        count = cta_topk(sh, n, k, load, emit);
+    }
+    __syncthreads();
     if (p.mask) {
         uint8_t* m = p.mask + (int64_t)t * p.ld_mask;
         for (int64_t b = threadIdx.x; b < p.ld_mask; b += kSelThreads)
             m[b] = 0;
         __syncthreads();
-        auto emit = [&](int pos, int e, float v) {
-            (void)pos;
-            (void)v;
-            const int b = ci[e];
-            if (b >= 0 && b < p.ld_mask)
-                m[b] = 1;
-        };
-        block_topk(sh, n, p.k, load, emit);
-    } else {
-        int32_t* oi = p.out_idx + (int64_t)t * p.k;
-        float* ov = p.out_val ? p.out_val + (int64_t)t * p.k : nullptr;
-        auto emit = [&](int pos, int e, float v) {
-            oi[pos] = ci[e];
-            if (ov)
-                ov[pos] = v;
-        };
-        const int count = block_topk(sh, n, p.k, load, emit);
-        for (int i = count + threadIdx.x; i < p.k; i += kSelThreads) {
-            oi[i] = -1;
-            if (ov)
-                ov[i] = -INFINITY;
-        }
+        for (int i = threadIdx.x; i < count; i += kSelThreads)
+            if (skey[i] >= 0 && skey[i] < p.ld_mask)
+                m[skey[i]] = 1;
+        return;
+    }
+    bitonic_sort(skey, sval, n2);
+    int32_t* oi = p.out_idx + (int64_t)t * k;
+    float* ov = p.out_val ? p.out_val + (int64_t)t * k : nullptr;
+    for (int i = threadIdx.x; i < k; i += kSelThreads) {
+        const bool have = i < count;
+        oi[i] = have ? skey[i] : -1;
+        if (ov)
+            ov[i] = have ? sval[i] : -INFINITY;
     }
 }
 
@@ -300,20 +225,24 @@ __global__ void __launch_bounds__(kSelThreads) merge_kernel(const __grid_constan
 
 __global__ void __launch_bounds__(kSelThreads) topk_dense_kernel(const __grid_constant__ TopkParams p)
 {
-    __shared__ SelShared sh;
+    __shared__ Scratch sh;
     const int t = blockIdx.x;
     const int r = find_request(p.req_row_begin, p.num_requests, t);
     const int n = max(0, min(p.compress_len[t], p.req_key_count[r]));
     const float* row = p.logits + (int64_t)t * p.ld;
     int32_t* oi = p.out_idx + (int64_t)t * p.k;
     float* ov = p.out_val ? p.out_val + (int64_t)t * p.k : nullptr;
-    auto load = [&](int e) { return row[e]; };
-    auto emit = [&](int pos, int e, float v) {
-        oi[pos] = e;
+    auto load = [&](int e, float& v, int32_t& j) {
+        v = row[e];
+        j = e;
+    };
+    auto emit = [&](int pos, int e, float v, int32_t j) {
+        (void)e;
+        oi[pos] = j;
         if (ov)
             ov[pos] = v;
     };
-    const int count = block_topk(sh, n, p.k, load, emit);
+    const int count = cta_topk(sh, n, p.k, load, emit);
     for (int i = count + threadIdx.x; i < p.k; i += kSelThreads) {
         oi[i] = -1;
         if (ov)
@@ -323,19 +252,21 @@ __global__ void __launch_bounds__(kSelThreads) topk_dense_kernel(const __grid_co
 
 }  // namespace
 
-cudaError_t launch_select_dense(const SelParams& p, cudaStream_t stream)
+cudaError_t launch_stream_merge(const StreamMergeParams& p, cudaStream_t stream)
 {
-    if (p.total_rows_launch <= 0)
+    if (p.total_ctas <= 0)
         return cudaSuccess;
-    select_dense_kernel<<<p.total_rows_launch, kSelThreads, 0, stream>>>(p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream)
-{
-    if (p.total_rows <= 0)
-        return cudaSuccess;
-    merge_kernel<<<p.total_rows, kSelThreads, 0, stream>>>(p);
+    if (p.k > kMaxSortK)
+        return cudaErrorInvalidValue;
+    int n2 = 1;
+    while (n2 < p.k)
+        n2 <<= 1;
+    const size_t dyn = sizeof(uint2) * kStageEntries + (sizeof(int32_t) + sizeof(float)) * n2;
+    cudaError_t e = cudaFuncSetAttribute(stream_merge_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    if (e != cudaSuccess)
+        return e;
+    stream_merge_kernel<<<p.total_ctas, kSelThreads, dyn, stream>>>(p);
     return cudaGetLastError();
 }
 

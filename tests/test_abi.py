@@ -91,7 +91,7 @@ def test_plan_rejects_bad_problems():
            kdtype=K.IDX_K_FP4_E2M1_UE8M0)
     expect(K.IDX_ERR_INVALID_ARG, K.indexer_plan, cu_q, cu_k, cl, 32, 128, 8, key_block=100)
     expect(K.IDX_ERR_WORKSPACE, K.indexer_plan, cu_q, cu_k, cl, 32, 128, 8,
-           transient_budget_bytes=1024)
+           transient_budget_bytes=512)
 
 
 def test_plan_with_empty_rows_and_requests():

@@ -160,6 +160,50 @@ def test_row_chunking_is_bitwise_invariant():
         assert torch.equal(part, full[a:b])
 
 
+def _structured_problem(L, rows, topk, key_scale):
+    """H=32, D=128 with q = 1.0 everywhere, k = 2.0 everywhere, w = 1/32, s_q = 1 and a
+    chosen per-key scale, so logit[t, j] = 128 * 2 * key_scale[j] exactly."""
+    spec = W.ProblemSpec("structured", (W.RequestSpec(rows, L - rows, 1),), H=32, D=128,
+                         topk=topk, seed=0)
+    p = W.make_problem(spec)
+    T = rows
+    q = torch.full((T, 32, 128), 0x38, dtype=torch.uint8)
+    k = torch.full((L, 128), 0x40, dtype=torch.uint8)
+    return dataclasses.replace(p, q=q, s_q=torch.ones(T, 32), w=torch.full((T, 32), 1.0 / 32),
+                               k=k, k_scale=key_scale.float())
+
+
+def test_increasing_scores_force_list_compaction():
+    """Scores rise with the key index, so every key passes the running threshold and the
+    per-row lists must be compacted many times inside the kernel."""
+    L, rows, topk = 8192, 24, 64
+    p = _structured_problem(L, rows, topk, 1.0 + torch.arange(L, dtype=torch.float64) / L)
+    plan = Hp.make_plan(p)
+    assert plan.info()["max_splits"] == 1
+    d = Hp.device_inputs(p)
+    fi, fv = Hp.gpu_fused(p, plan, d)
+    ref = oracle_rows(p, np.arange(rows))
+    cl = p.compress_len.numpy()
+    fi = fi.cpu().numpy()
+    for t in range(rows):
+        want = list(range(int(cl[t]) - topk, int(cl[t])))
+        assert fi[t].tolist() == want, t
+        Hp.check_topk_row(fi[t], ref[t], int(cl[t]), topk)
+
+
+def test_all_equal_scores_keep_the_lowest_indices():
+    """Every key ties: the top-k is the k lowest key indices, through compaction too."""
+    L, rows, topk = 8192, 20, 100
+    p = _structured_problem(L, rows, topk, torch.ones(L, dtype=torch.float64))
+    plan = Hp.make_plan(p)
+    d = Hp.device_inputs(p)
+    fi, fv = Hp.gpu_fused(p, plan, d)
+    fi = fi.cpu().numpy()
+    for t in range(rows):
+        assert fi[t].tolist() == list(range(topk)), t
+    assert torch.all(fv == 256.0)
+
+
 # ------------------------------------------------------------- candidates
 
 def test_candidate_blocks_and_masked_consumer_scaled():
@@ -262,10 +306,11 @@ def test_bounded_wait_reports_timeout_instead_of_hanging():
 def test_workspace_too_small_is_rejected():
     p = W.make_problem(W.CONFIGS["tiny"])
     plan = Hp.make_plan(p)
+    assert plan.workspace_bytes > 256
     d = Hp.device_inputs(p)
     ws = torch.empty(256, dtype=torch.uint8, device="cuda")
-    out = torch.empty((64, 1024), dtype=torch.float32, device="cuda")
+    idx = torch.empty((64, p.topk), dtype=torch.int32, device="cuda")
     with pytest.raises(K.IndexerError) as e:
-        K.indexer_logits(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"],
-                         d["compress_len"], out, ws)
+        K.indexer_fused_topk(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"],
+                             d["compress_len"], None, idx, None, ws)
     assert e.value.code == K.IDX_ERR_WORKSPACE
