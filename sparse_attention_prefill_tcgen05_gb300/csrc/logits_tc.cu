@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const UnitInfo ui = decode_unit<C::G>(p, u, lane);
             if (ui.ntiles_mma == 0)
                 continue;
-            const Segment& sg = p.seg[ui.seg];
+            const Segment sg = p.seg[ui.seg];   // by value: loop-invariant registers
             if (lane == 0) {
                 if (!mbar_wait(&q_empty[qb], qph ^ 1, budget, abort_flag)) {
                     report(p, abort_flag, kStatusTimeout);
@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // see all of their threads.
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x, ++it) {
             const UnitInfo ui = decode_unit<C::G>(p, u, lane);
-            const Segment& sg = p.seg[ui.seg];
+            const Segment sg = p.seg[ui.seg];   // by value: loop-invariant registers
             float* cbuf = c_s + (it & 1) * kTileN;
             if (etid < C::N) {   // c[n] = w * s_q for column n = row * H + head,
                                  // times 2^25 where the epilogue's relu is scaled (n % 4 >= 2)
@@ -530,6 +530,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tau_lo[r] = rows_s[rl].tau_lo;
                 }
             }
+            // smallest causal length among this half's rows (rows past nr are never
+            // stored or selected)
+            int clen_min = INT_MAX;
+#pragma unroll
+            for (int r = 0; r < C::RPH; ++r)
+                if (half * C::RPH + r < ui.nr)
+                    clen_min = min(clen_min, clen[r]);
             // the rows' shared thresholds, read one refresh interval ahead of use
             constexpr int kOwned = (C::RPH + 3) / 4;
             uint32_t gpre[kOwned];
@@ -635,15 +642,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         aph ^= 1;
                     }
                 }
-                // causal and candidate masks
+                // causal and candidate masks (most tiles lie below every row's causal
+                // length: one warp-uniform test skips the per-row work there)
+                if (p.cand_mask != nullptr || ui.j0 + (i + 1) * kTileKeys > clen_min) {
 #pragma unroll
-                for (int r = 0; r < C::RPH; ++r) {
-                    const int rl = half * C::RPH + r;
-                    bool valid = rl < ui.nr && j < clen[r];
-                    if (valid && p.cand_mask)
-                        valid = p.cand_mask[(size_t)(ui.t0 + rl) * p.ld_mask + j / p.mask_block] != 0;
-                    if (!valid)
-                        acc[r] = -INFINITY;
+                    for (int r = 0; r < C::RPH; ++r) {
+                        const int rl = half * C::RPH + r;
+                        bool valid = rl < ui.nr && j < clen[r];
+                        if (valid && p.cand_mask)
+                            valid = p.cand_mask[(size_t)(ui.t0 + rl) * p.ld_mask +
+                                                j / p.mask_block] != 0;
+                        if (!valid)
+                            acc[r] = -INFINITY;
+                    }
                 }
                 if constexpr (SINK == kSinkLogits) {
                     if (j < ui.jend) {
