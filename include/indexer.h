@@ -78,14 +78,14 @@ extern "C" {
  *   num_requests  R >= 1 (at most 256)
  *   total_rows    T = cu_seqlens_q[R];  total_keys = cu_seqlens_k[R]
  *   H, D          heads and head dim of q; k has D too.  Built shapes:
- *                 (H, D) in {(32,128), (16,128), (64,128), (4,64)}
+ *                 (H, D) in {(32,128), (16,128), (64,128), (8,64)}
  *   topk          keys kept per row, 1 <= topk <= 2048
  *   cu_seqlens_q  [R+1] non-decreasing row offsets, starts at 0
  *   cu_seqlens_k  [R+1] non-decreasing key offsets, starts at 0
  *   compress_len  [T] causal length of every row, 0 <= compress_len[t] <= the
  *                 keys of its request (e.g. floor((pos+1)/ratio))
  *   kdtype        IDX_K_FP8_E4M3 or IDX_K_FP4_E2M1_UE8M0
- *   cand_block    keys per candidate block (0 means 8)
+ *   cand_block    keys per candidate block: 1, 2, 4 or 8 (0 means 8)
  *   cand_topk     candidate blocks kept per row by indexer_candidate_blocks,
  *                 1..4096 (e.g. 2048); 0 = the plan makes no candidate-block
  *                 calls and reserves no workspace for them

@@ -72,7 +72,7 @@ bool supported_shape(int H, int D, int kdtype)
     if (kdtype == IDX_K_FP4_E2M1_UE8M0)
         return false;
     return (H == 32 && D == 128) || (H == 16 && D == 128) || (H == 64 && D == 128) ||
-           (H == 4 && D == 64);
+           (H == 8 && D == 64);
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -412,7 +412,7 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
         return IDX_ERR_INVALID_ARG;
     const int cb = pr->cand_block ? pr->cand_block : 8;
     const int ct = pr->cand_topk;
-    if (cb < 1 || cb > 32 || (32 % cb) != 0 || ct < 0 || ct > 4096)
+    if (cb < 1 || cb > 8 || (cb & (cb - 1)) != 0 || ct < 0 || ct > 4096)
         return IDX_ERR_INVALID_ARG;
     if (pr->key_block < 0 || (pr->key_block % kTileKeys) != 0)
         return IDX_ERR_INVALID_ARG;

@@ -59,9 +59,9 @@ struct Cfg {
     static constexpr int KBYTES = kTileKeys * D;       // K tile
     static constexpr int STAGES = (D >= 128) ? 6 : 8;
     static constexpr int KSTEPS = D / 32;              // MMA K = 32 elements
-    static constexpr int RPH = G / 2;                  // rows one epilogue thread reduces
+    static constexpr int RPH = G / 2;                  // rows of one column half
     static constexpr int HALF_COLS = N / 2;
-    static constexpr int NCH = HALF_COLS / 32;         // 32-column TMEM loads per tile
+    static constexpr int NCH = HALF_COLS / 32;         // 32-column chunks per half
     static constexpr int ACC_COLS = N;                 // TMEM columns per accumulator
     static constexpr int SF_BYTES = KFMT == kKeyFp4 ? kTileKeys * 16 : 0;  // per stage
     static constexpr int TMEM_SFA = 2 * ACC_COLS;      // 4 columns per stage
@@ -70,6 +70,8 @@ struct Cfg {
     static_assert(D == 32 || D == 64 || D == 128, "D must be 32, 64 or 128");
     static_assert(G >= 2 && G % 2 == 0 && N % 16 == 0, "H must leave an even row count");
     static_assert(HALF_COLS % 32 == 0, "half tile must be whole 32-column loads");
+    static_assert(H >= 8 && (RPH == 2 || RPH == 4 || RPH == 8),
+                  "the epilogue's head split needs 8..64 heads");
     static_assert(!STREAM || G <= 16, "streamed selection keeps at most 16 rows per CTA");
     // shared memory carve-up (offsets from a 1024-byte aligned base)
     static constexpr int OFF_Q = 0;
@@ -152,41 +154,31 @@ __device__ __forceinline__ void red_add_shared(uint32_t* addr, uint32_t v)
 }
 
 // Append this warp's threshold-passing entries of one row to the warp's own
-// sub-list (position from a register count: no atomics on the list) and
-// count them in the row's histograms with fire-and-forget shared reductions:
-// h1 counts by top byte while no boundary bin is known or above it, h2 counts
-// the next byte inside the boundary bin b1.  Returns the warp's new count.
+// sub-list and count them in the row's histograms.  The lanes set in
+// `rowmask` hold entries of this row (other lanes hold other rows); the
+// append position comes from the warp-uniform count `wcnt` and a ballot
+// prefix, so no atomics touch the list.  Histogram counts are fire-and-forget
+// shared reductions: h2 counts the second byte of entries whose top byte is
+// the boundary bin b1, h1 counts the top byte of all other entries.  Returns
+// the new count.
 __device__ __forceinline__ uint32_t stream_push(uint32_t* h1, uint32_t* h2, uint2* sub,
                                                 uint32_t cap, uint32_t wcnt, uint32_t tau_hi,
                                                 uint32_t tau_lo, uint32_t b1, float v,
-                                                uint32_t idx, bool active, int lane)
+                                                uint32_t idx, bool active, uint32_t rowmask,
+                                                int lane)
 {
     const uint32_t o = f2ord(v);
     const bool cand =
         active && o > kOrdNegInf && (o > tau_hi || (o == tau_hi && ~idx >= tau_lo));
-    const uint32_t m = __ballot_sync(0xffffffffu, cand);
-    if (m == 0)
-        return wcnt;
-    const uint32_t t8 = o >> 24;
+    const uint32_t m = __ballot_sync(0xffffffffu, cand) & rowmask;
     if (cand) {
         const uint32_t pos = wcnt + __popc(m & ((1u << lane) - 1u));
         if (pos < cap)
             sub[pos] = make_uint2(__float_as_uint(v), idx);
-    }
-    // level 2: inside the boundary bin (the common case once b1 is known)
-    const bool in_b1 = cand && t8 == b1;
-    if (in_b1)
-        red_add_shared(&h2[(o >> 16) & 255u], 1u);
-    // level 1: everything else, aggregated when the lanes share the leader's byte
-    const bool l1 = cand && !in_b1;
-    const uint32_t ml1 = __ballot_sync(0xffffffffu, l1);
-    if (ml1) {
-        const int leader = __ffs(ml1) - 1;
-        const uint32_t lt8 = __shfl_sync(0xffffffffu, t8, leader);
-        const uint32_t same = __ballot_sync(0xffffffffu, l1 && t8 == lt8);
-        if (lane == leader)
-            red_add_shared(&h1[lt8], static_cast<uint32_t>(__popc(same)));
-        else if (l1 && t8 != lt8)
+        const uint32_t t8 = o >> 24;
+        if (t8 == b1)
+            red_add_shared(&h2[(o >> 16) & 255u], 1u);
+        else
             red_add_shared(&h1[t8], 1u);
     }
     return wcnt + __popc(m);
@@ -474,12 +466,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 4) {
         // ---------------------------------------------------------- epilogue
+        // Warp (half, quad) reduces TMEM lanes [32 quad, +32) (keys) x columns
+        // [half * HALF_COLS, +HALF_COLS) (RPH rows x H heads).  It reads them with
+        // the 16x256b shape: thread (g = lane / 4, q = lane % 4) gets, for each
+        // 8-column group, columns 2q and 2q + 1 of the lanes g and g + 8 of a
+        // 16-lane block.  Each thread therefore needs only 2 head weights per
+        // group (one 8-byte shared load that four lanes share, instead of a
+        // broadcast of every weight to all 32 lanes), and the head sums are
+        // finished by a reduce-scatter over the four q lanes.
         const int ew = warp - 4;                 // 0..7
         const int quad = warp & 3;               // TMEM lane quadrant of this warp
         const int half = ew >> 2;                // column half: rows [half*RPH, +RPH)
-        const int kq = quad * 32 + lane;         // key within the tile
         const int etid = ew * 32 + lane;         // 0..255
         const int htid = quad * 32 + lane;       // 0..127 within the half
+        const int g = lane >> 2;
+        const int q = lane & 3;
+        constexpr int RPH = C::RPH;
+        constexpr int F = 4 * RPH;               // partial sums per thread per tile
+        constexpr int RO = RPH >= 4 ? RPH / 4 : 1;   // rows a thread finishes
+        constexpr int NK = RPH >= 4 ? 4 : RPH;       // key slots a thread finishes
+        constexpr int NLD = 2 * C::NCH;          // 16-lane x 32-column loads per tile
+        // finished value m: f = q * RPH + m = rr * 4 + slot-in-row, rr = f / 4
+        auto own_rr = [&](int ro) { return RPH >= 4 ? q * (RPH / 4) + ro : (q >> 1); };
+        auto slot_bl = [&](int s) { return RPH >= 4 ? s : ((2 * q + s) & 3); };
+        // lanes that finish the same rows as this one
+        const uint32_t rowmask = RPH >= 4 ? (0x11111111u << q) : (0x33333333u << (q & 2));
+        const bool row_leader = g == 0 && (RPH >= 4 || (q & 1) == 0);
         const NamedSync half_sync{2 + half, kHalfThreads};
         SelScratch<kHalfThreads>* sel_s =
             reinterpret_cast<SelScratch<kHalfThreads>*>(smem + C::OFF_SEL + half * C::SEL_ONE);
@@ -491,23 +503,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x, ++it) {
             const UnitInfo ui = decode_unit<C::G>(p, u, lane);
             const Segment sg = p.seg[ui.seg];   // by value: loop-invariant registers
+            // head weights c[n] = w * s_q of column n = row * H + head; odd columns
+            // carry 2^25 (their relu is a saturating multiply by 2^-25).  Double
+            // buffered by unit: the other half may still read the previous one.
             float* cbuf = c_s + (it & 1) * kTileN;
-            if (etid < C::N) {   // c[n] = w * s_q for column n = row * H + head,
-                                 // times 2^25 where the epilogue's relu is scaled (n % 4 >= 2)
+            if (etid < C::N) {
                 const int rl = etid / H;
-                const int t = ui.t0 + rl;
-                const float cv = rl < ui.nr ? p.w[(size_t)t * H + (etid % H)] *
-                                                  p.s_q[(size_t)t * H + (etid % H)]
-                                            : 0.0f;
-                cbuf[etid] = (etid & 2) ? cv * 33554432.0f : cv;
+                const size_t o = (size_t)(ui.t0 + rl) * H + (etid % H);
+                const float cv = rl < ui.nr ? p.w[o] * p.s_q[o] : 0.0f;
+                cbuf[etid] = (etid & 1) ? cv * 33554432.0f : cv;
             }
+            const float2* cw = reinterpret_cast<const float2*>(cbuf + half * C::HALF_COLS) + q;
             if constexpr (C::STREAM) {
                 for (int i = etid; i < C::G * 512; i += kEpiWarps * 32)
                     hist_s[i] = 0;
                 if (etid < C::G) {
                     RowState& rs = rows_s[etid];
-                    for (int q = 0; q < 4; ++q)
-                        rs.wcnt[q] = 0;
+                    for (int w4 = 0; w4 < 4; ++w4)
+                        rs.wcnt[w4] = 0;
                     rs.tau_hi = etid < ui.nr ? p.gtau[ui.t0 + etid] : 0u;
                     rs.tau_lo = 0;
                     rs.b1 = 256;
@@ -515,60 +528,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             asm volatile("bar.sync 1, 256;" ::: "memory");
-            int clen[C::RPH];
-            uint32_t tau_hi[C::RPH], tau_lo[C::RPH], b1[C::RPH], wcnt[C::RPH];
+            // the rows this thread finishes
+            int clen[RO];
+            uint32_t tau_hi[RO], tau_lo[RO], b1[RO], wcnt[RO];
 #pragma unroll
-            for (int r = 0; r < C::RPH; ++r) {
-                const int rl = half * C::RPH + r;
-                clen[r] = rl < ui.nr ? min(p.compress_len[ui.t0 + rl], sg.key_count) : 0;
-                tau_hi[r] = 0;
-                tau_lo[r] = 0;
-                b1[r] = 256;
-                wcnt[r] = 0;
+            for (int ro = 0; ro < RO; ++ro) {
+                const int rl = half * RPH + own_rr(ro);
+                clen[ro] = rl < ui.nr ? min(p.compress_len[ui.t0 + rl], sg.key_count) : 0;
+                tau_hi[ro] = 0;
+                tau_lo[ro] = 0;
+                b1[ro] = 256;
+                wcnt[ro] = 0;
                 if constexpr (C::STREAM) {
-                    tau_hi[r] = rows_s[rl].tau_hi;
-                    tau_lo[r] = rows_s[rl].tau_lo;
+                    tau_hi[ro] = rows_s[rl].tau_hi;
+                    tau_lo[ro] = rows_s[rl].tau_lo;
                 }
             }
-            // smallest causal length among this half's rows (rows past nr are never
+            // smallest causal length among the half's rows (rows past nr are never
             // stored or selected)
             int clen_min = INT_MAX;
-#pragma unroll
-            for (int r = 0; r < C::RPH; ++r)
-                if (half * C::RPH + r < ui.nr)
-                    clen_min = min(clen_min, clen[r]);
-            // the rows' shared thresholds, read one refresh interval ahead of use
-            constexpr int kOwned = (C::RPH + 3) / 4;
+            for (int r = 0; r < RPH; ++r)
+                if (half * RPH + r < ui.nr)
+                    clen_min = min(clen_min, min(p.compress_len[ui.t0 + half * RPH + r],
+                                                 sg.key_count));
+            // the shared thresholds of the rows this warp refreshes, read one
+            // refresh interval ahead of use
+            constexpr int kOwned = (RPH + 3) / 4;
             uint32_t gpre[kOwned];
 #pragma unroll
             for (int oi = 0; oi < kOwned; ++oi) {
-                const int rl = half * C::RPH + quad + 4 * oi;
+                const int rl = half * RPH + quad + 4 * oi;
                 gpre[oi] = 0;
-                if (C::STREAM && quad + 4 * oi < C::RPH && rl < ui.nr)
+                if (C::STREAM && quad + 4 * oi < RPH && rl < ui.nr)
                     gpre[oi] = ld_relaxed_gpu(p.gtau + ui.t0 + rl);
             }
-            // key scales one tile ahead (a global load whose latency the tile hides)
-            float sk_next = 1.0f;
-            if (KFMT == kKeyFp8 && ui.ntiles_mma > 0) {
-                const int j0 = ui.j0 + kq;
-                sk_next = j0 < sg.key_count ? __ldg(p.s_k + sg.key_base + j0) : 0.0f;
+            // key scale of key (quadrant base + lane), one tile ahead; the owners
+            // of each key fetch it by a shuffle
+            float sk_next = 0.0f;
+            {
+                const int j0 = ui.j0 + quad * 32 + lane;
+                if (KFMT == kKeyFp8 && ui.ntiles_mma > 0 && j0 < sg.key_count)
+                    sk_next = __ldg(p.s_k + sg.key_base + j0);
             }
             // a warp's sub-list sees 32 of every 128 keys (or its lanes' blocks)
             const int unit_entries_warp =
                 SINK == kSinkPool ? ui.ntiles * (32 / (p.pool > 0 ? p.pool : 1)) : ui.ntiles * 32;
             const bool no_overflow = unit_entries_warp <= p.cap;
             for (int i = 0; i < ui.ntiles; ++i) {
-                const int j = ui.j0 + i * kTileKeys + kq;
-                float acc[C::RPH];
+                const int jt = ui.j0 + i * kTileKeys + quad * 32;   // first key of the quadrant
+                float val[RPH];
 #pragma unroll
-                for (int r = 0; r < C::RPH; ++r)
-                    acc[r] = -INFINITY;
+                for (int m = 0; m < RPH; ++m)
+                    val[m] = -INFINITY;
                 if (i < ui.ntiles_mma) {
-                    const float sk = sk_next;
-                    if (KFMT == kKeyFp8 && i + 1 < ui.ntiles_mma)
-                        sk_next = j + kTileKeys < sg.key_count
-                                      ? __ldg(p.s_k + sg.key_base + j + kTileKeys)
-                                      : 0.0f;
+                    const float sk_lane = sk_next;
+                    {
+                        const int jn = jt + kTileKeys + lane;
+                        if (KFMT == kKeyFp8 && i + 1 < ui.ntiles_mma)
+                            sk_next = jn < sg.key_count ? __ldg(p.s_k + sg.key_base + jn) : 0.0f;
+                    }
                     bool got = alive && mbar_wait(&a_full[ab], aph, budget, abort_flag);
                     got = __all_sync(0xffffffffu, got);
                     if (!got && alive) {
@@ -578,135 +596,167 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (got) {
                         tc_fence_after();
-                        // four partial sums per row (heads h = 0,1,2,3 mod 4), two per
-                        // packed FMA.  Heads 0,1 mod 4: relu by max (ALU pipe); heads
-                        // 2,3 mod 4: relu(S) * 2^-25 by a saturating multiply (FMA pipe)
-                        // with c stored times 2^25, so every product and sum is
-                        // bit-identical to fmaf(c, max(S, 0), part).
-                        float2 part[C::RPH][2];
+                        // partial sums [row][block][lane g or g+8], two heads per packed
+                        // FMA: relu by max (ALU pipe) for column 2q, by a saturating
+                        // multiply with 2^-25 (FMA pipe) for column 2q + 1, whose weight
+                        // carries 2^25; every product and sum is bit-identical to
+                        // fmaf(c, max(S, 0), part).
+                        float2 part[RPH][2][2];
 #pragma unroll
-                        for (int r = 0; r < C::RPH; ++r) {
-                            part[r][0] = make_float2(0.0f, 0.0f);
-                            part[r][1] = make_float2(0.0f, 0.0f);
-                        }
+                        for (int r = 0; r < RPH; ++r)
+#pragma unroll
+                            for (int b2 = 0; b2 < 2; ++b2) {
+                                part[r][b2][0] = make_float2(0.0f, 0.0f);
+                                part[r][b2][1] = make_float2(0.0f, 0.0f);
+                            }
                         const uint32_t tbase = tmem_base +
                                                (static_cast<uint32_t>(quad * 32) << 16) +
                                                ab * C::ACC_COLS + half * C::HALF_COLS;
-                        const float4* cc4 =
-                            reinterpret_cast<const float4*>(cbuf + half * C::HALF_COLS);
-                        // next 32 columns (TMEM) and their 32 head weights (shared memory)
-                        // in flight while the current ones are reduced
-                        float va[32], vb[32];
-                        float4 ca[8], cb[8];
-                        tmem_ld_32x32b_x32(tbase, va);
-#pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4)
-                            ca[e4] = cc4[e4];
+                        // load ld = (chunk, block): 16 lanes x 32 columns; the next one
+                        // is in flight while the current one is reduced
+                        float va[16], vb[16];
+                        tmem_ld_16x256b_x4(tbase, va);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int ch = 0; ch < C::NCH; ++ch) {
-                            float(&cur)[32] = (ch & 1) ? vb : va;
-                            float(&nxt)[32] = (ch & 1) ? va : vb;
-                            float4(&ccur)[8] = (ch & 1) ? cb : ca;
-                            float4(&cnxt)[8] = (ch & 1) ? ca : cb;
-                            if (ch + 1 < C::NCH) {
-                                tmem_ld_32x32b_x32(tbase + (ch + 1) * 32, nxt);
-#pragma unroll
-                                for (int e4 = 0; e4 < 8; ++e4)
-                                    cnxt[e4] = cc4[(ch + 1) * 8 + e4];
+                        for (int ld = 0; ld < NLD; ++ld) {
+                            float(&cur)[16] = (ld & 1) ? vb : va;
+                            float(&nxt)[16] = (ld & 1) ? va : vb;
+                            if (ld + 1 < NLD) {
+                                const int ch1 = (ld + 1) >> 1, b1n = (ld + 1) & 1;
+                                tmem_ld_16x256b_x4(
+                                    tbase + (static_cast<uint32_t>(16 * b1n) << 16) + ch1 * 32, nxt);
                             }
+                            const int ch = ld >> 1, blk = ld & 1;
 #pragma unroll
-                            for (int e4 = 0; e4 < 8; ++e4) {
-                                const float4 c4 = ccur[e4];
-                                const int r = (ch * 32 + e4 * 4) / H;
-                                const float2 r01 = make_float2(fmaxf(cur[e4 * 4 + 0], 0.0f),
-                                                               fmaxf(cur[e4 * 4 + 1], 0.0f));
-                                const float2 r23 = make_float2(relu_scaled(cur[e4 * 4 + 2]),
-                                                               relu_scaled(cur[e4 * 4 + 3]));
-                                part[r][0] = __ffma2_rn(make_float2(c4.x, c4.y), r01, part[r][0]);
-                                part[r][1] = __ffma2_rn(make_float2(c4.z, c4.w), r23, part[r][1]);
+                            for (int k = 0; k < 4; ++k) {
+                                const int r = (ch * 32 + 8 * k) / H;
+                                const float2 c2 = cw[(ch * 4 + k) * 4];
+                                const float2 lo = make_float2(fmaxf(cur[4 * k + 0], 0.0f),
+                                                              relu_scaled(cur[4 * k + 1]));
+                                const float2 hi = make_float2(fmaxf(cur[4 * k + 2], 0.0f),
+                                                              relu_scaled(cur[4 * k + 3]));
+                                part[r][blk][0] = __ffma2_rn(c2, lo, part[r][blk][0]);
+                                part[r][blk][1] = __ffma2_rn(c2, hi, part[r][blk][1]);
                             }
-                            if (ch + 1 < C::NCH)
+                            if (ld + 1 < NLD)
                                 tmem_wait_ld();
+                            if (ld + 2 == NLD) {
+                                // every column of the accumulator is in registers: hand
+                                // it back to the MMA before the last chunk's arithmetic
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0)
+                                    mbar_arrive(&a_empty[ab]);
+                            }
+                        }
+                        // reduce-scatter over the four q lanes: thread q keeps the
+                        // sums f = q * RPH + m, f = row * 4 + block * 2 + (g or g+8)
+                        float pf[F];
+#pragma unroll
+                        for (int r = 0; r < RPH; ++r)
+#pragma unroll
+                            for (int b2 = 0; b2 < 2; ++b2)
+#pragma unroll
+                                for (int l2 = 0; l2 < 2; ++l2)
+                                    pf[r * 4 + b2 * 2 + l2] =
+                                        part[r][b2][l2].x + part[r][b2][l2].y;
+                        float rs1[F / 2];
+#pragma unroll
+                        for (int x = 0; x < F / 2; ++x) {
+                            const float keep = (q & 2) ? pf[F / 2 + x] : pf[x];
+                            const float send = (q & 2) ? pf[x] : pf[F / 2 + x];
+                            rs1[x] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
                         }
 #pragma unroll
-                        for (int r = 0; r < C::RPH; ++r)
-                            acc[r] = ((part[r][0].x + part[r][0].y) + (part[r][1].x + part[r][1].y)) * sk;
+                        for (int x = 0; x < F / 4; ++x) {
+                            const float keep = (q & 1) ? rs1[F / 4 + x] : rs1[x];
+                            const float send = (q & 1) ? rs1[x] : rs1[F / 4 + x];
+                            val[x] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+                        }
+#pragma unroll
+                        for (int s2 = 0; s2 < NK; ++s2) {
+                            const float skv =
+                                __shfl_sync(0xffffffffu, sk_lane, 8 * slot_bl(s2) + g);
+#pragma unroll
+                            for (int x = s2; x < F / 4; x += NK)
+                                val[x] *= skv;
+                        }
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0 && got)
-                        mbar_arrive(&a_empty[ab]);
                     if (++ab == 2) {
                         ab = 0;
                         aph ^= 1;
                     }
                 }
                 // causal and candidate masks (most tiles lie below every row's causal
-                // length: one warp-uniform test skips the per-row work there)
+                // length: one warp-uniform test skips the per-value work there)
                 if (p.cand_mask != nullptr || ui.j0 + (i + 1) * kTileKeys > clen_min) {
 #pragma unroll
-                    for (int r = 0; r < C::RPH; ++r) {
-                        const int rl = half * C::RPH + r;
-                        bool valid = rl < ui.nr && j < clen[r];
+                    for (int m = 0; m < RPH; ++m) {
+                        const int ro = RPH >= 4 ? (m >> 2) : 0;
+                        const int rl = half * RPH + own_rr(ro);
+                        const int j = jt + 8 * slot_bl(RPH >= 4 ? (m & 3) : m) + g;
+                        bool valid = rl < ui.nr && j < clen[ro];
                         if (valid && p.cand_mask)
                             valid = p.cand_mask[(size_t)(ui.t0 + rl) * p.ld_mask +
                                                 j / p.mask_block] != 0;
                         if (!valid)
-                            acc[r] = -INFINITY;
+                            val[m] = -INFINITY;
                     }
                 }
                 if constexpr (SINK == kSinkLogits) {
-                    if (j < ui.jend) {
-                        float* out_base = p.out + sg.out_offset - sg.j_begin;
+                    float* out_base = p.out + sg.out_offset - sg.j_begin;
 #pragma unroll
-                        for (int r = 0; r < C::RPH; ++r) {
-                            const int rl = half * C::RPH + r;
-                            if (rl < ui.nr)
-                                out_base[(size_t)(ui.t0 + rl - sg.row_begin) * sg.out_ld + j] =
-                                    acc[r];
-                        }
+                    for (int m = 0; m < RPH; ++m) {
+                        const int ro = RPH >= 4 ? (m >> 2) : 0;
+                        const int rl = half * RPH + own_rr(ro);
+                        const int j = jt + 8 * slot_bl(RPH >= 4 ? (m & 3) : m) + g;
+                        if (rl < ui.nr && j < ui.jend)
+                            out_base[(size_t)(ui.t0 + rl - sg.row_begin) * sg.out_ld + j] =
+                                val[m];
                     }
                 } else {
                     const uint32_t cap = static_cast<uint32_t>(p.cap);
 #pragma unroll
-                    for (int r = 0; r < C::RPH; ++r) {
-                        const int rl = half * C::RPH + r;
+                    for (int m = 0; m < RPH; ++m) {
+                        const int ro = RPH >= 4 ? (m >> 2) : 0;
+                        const int rl = half * RPH + own_rr(ro);
+                        const int j = jt + 8 * slot_bl(RPH >= 4 ? (m & 3) : m) + g;
                         uint32_t* h1 = hist_s + rl * 512;
                         uint2* sub = p.lists + sg.out_offset +
                                      (int64_t)(ui.t0 + rl - sg.row_begin) * sg.out_ld +
                                      (int64_t)quad * p.cap;
                         if constexpr (SINK == kSinkStream) {
-                            wcnt[r] = stream_push(h1, h1 + 256, sub, cap, wcnt[r], tau_hi[r],
-                                                  tau_lo[r], b1[r], acc[r],
-                                                  static_cast<uint32_t>(j), rl < ui.nr, lane);
+                            wcnt[ro] = stream_push(h1, h1 + 256, sub, cap, wcnt[ro], tau_hi[ro],
+                                                   tau_lo[ro], b1[ro], val[m],
+                                                   static_cast<uint32_t>(j), rl < ui.nr,
+                                                   rowmask, lane);
                         } else {
-                            // block maximum over `pool` consecutive keys (lanes)
-                            float bm = acc[r];
+                            // block maximum over `pool` consecutive keys: lanes g..
+                            float bm = val[m];
                             for (int o = 1; o < p.pool; o <<= 1)
-                                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
-                            const bool lead = (kq % p.pool) == 0;
-                            wcnt[r] = stream_push(h1, h1 + 256, sub, cap, wcnt[r], tau_hi[r],
-                                                  tau_lo[r], b1[r], bm,
-                                                  static_cast<uint32_t>(j / p.pool),
-                                                  lead && rl < ui.nr, lane);
+                                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4 * o));
+                            const bool lead = (g % p.pool) == 0;
+                            wcnt[ro] = stream_push(h1, h1 + 256, sub, cap, wcnt[ro], tau_hi[ro],
+                                                   tau_lo[ro], b1[ro], bm,
+                                                   static_cast<uint32_t>(j / p.pool),
+                                                   lead && rl < ui.nr, rowmask, lane);
                         }
                     }
                     const bool refresh = ((i + 1) % p.update_tiles) == 0 || i + 1 == ui.ntiles;
                     if (refresh) {
                         // publish this warp's counts, then the row owners refresh tau
-                        if (lane == 0) {
+                        if (row_leader) {
 #pragma unroll
-                            for (int r = 0; r < C::RPH; ++r)
-                                rows_s[half * C::RPH + r].wcnt[quad] = wcnt[r];
+                            for (int ro = 0; ro < RO; ++ro)
+                                rows_s[half * RPH + own_rr(ro)].wcnt[quad] = wcnt[ro];
                         }
                         half_sync();
-                        // rows of this half: warp `quad` owns rows quad, quad+4, ...
+                        // rows of this half: warp `quad` refreshes rows quad, quad+4, ...
 #pragma unroll
                         for (int oi = 0; oi < kOwned; ++oi) {
                             const int rr = quad + 4 * oi;
-                            const int rl = half * C::RPH + rr;
-                            if (rr >= C::RPH)
+                            const int rl = half * RPH + rr;
+                            if (rr >= RPH)
                                 continue;
                             if (rl >= ui.nr)
                                 continue;
@@ -737,10 +787,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             if (lane == 0) {
                                 const int t = ui.t0 + rl;
-                                const uint32_t g = gpre[oi];
-                                if (tau_new > g)
+                                const uint32_t gv = gpre[oi];
+                                if (tau_new > gv)
                                     atomicMax(p.gtau + t, tau_new);
-                                const uint32_t best = max(tau_new, g);
+                                const uint32_t best = max(tau_new, gv);
                                 if (best > rs.tau_hi) {
                                     rs.tau_hi = best;
                                     rs.tau_lo = 0;
@@ -749,9 +799,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const uint32_t slack =
                                     static_cast<uint32_t>(p.update_tiles) * 32u;
                                 bool full = false, lost = false;
-                                for (int q = 0; q < 4; ++q) {
-                                    full |= rs.wcnt[q] + slack > cap;
-                                    lost |= rs.wcnt[q] > cap;
+                                for (int w4 = 0; w4 < 4; ++w4) {
+                                    full |= rs.wcnt[w4] + slack > cap;
+                                    lost |= rs.wcnt[w4] > cap;
                                 }
                                 rs.compact = (full && !no_overflow) ? 1u : 0u;
                                 if (lost)
@@ -762,8 +812,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // exact compaction of any row whose sub-lists are about to fill
                         // (all 128 threads): keep the top `keep` entries of the four
                         // sub-lists, written to the front of sub-list 0
-                        for (int rr = 0; rr < C::RPH; ++rr) {
-                            const int rl = half * C::RPH + rr;
+                        for (int rr = 0; rr < RPH; ++rr) {
+                            const int rl = half * RPH + rr;
                             if (rl >= ui.nr || rows_s[rl].compact == 0)
                                 continue;
                             RowState& rs = rows_s[rl];
@@ -776,9 +826,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int o1 = n0, o2 = n0 + n1, o3 = n0 + n1 + n2;
                             const int n = o3 + n3;
                             auto at = [&](int e) -> uint2* {
-                                const int q = (e >= o1) + (e >= o2) + (e >= o3);
-                                const int base = q == 0 ? 0 : (q == 1 ? o1 : (q == 2 ? o2 : o3));
-                                return list + (int64_t)q * p.cap + (e - base);
+                                const int w4 = (e >= o1) + (e >= o2) + (e >= o3);
+                                const int base =
+                                    w4 == 0 ? 0 : (w4 == 1 ? o1 : (w4 == 2 ? o2 : o3));
+                                return list + (int64_t)w4 * p.cap + (e - base);
                             };
                             auto load = [&](int e, uint32_t& hi, uint32_t& lo) {
                                 const uint2 ent = *at(e);
@@ -805,26 +856,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     rs.tau_lo = thr.plo;
                                 }
                                 const int t = ui.t0 + rl;
-                                const uint32_t g =
+                                const uint32_t gv =
                                     *reinterpret_cast<volatile uint32_t*>(p.gtau + t);
-                                if (thr.phi > g)
+                                if (thr.phi > gv)
                                     atomicMax(p.gtau + t, thr.phi);
                             }
                             half_sync();
                         }
 #pragma unroll
                         for (int oi = 0; oi < kOwned; ++oi) {
-                            const int rl = half * C::RPH + quad + 4 * oi;
-                            if (quad + 4 * oi < C::RPH && rl < ui.nr)
+                            const int rl = half * RPH + quad + 4 * oi;
+                            if (quad + 4 * oi < RPH && rl < ui.nr)
                                 gpre[oi] = ld_relaxed_gpu(p.gtau + ui.t0 + rl);
                         }
 #pragma unroll
-                        for (int r = 0; r < C::RPH; ++r) {
-                            const int rl = half * C::RPH + r;
-                            tau_hi[r] = rows_s[rl].tau_hi;
-                            tau_lo[r] = rows_s[rl].tau_lo;
-                            b1[r] = rows_s[rl].b1;
-                            wcnt[r] = rows_s[rl].wcnt[quad];
+                        for (int ro = 0; ro < RO; ++ro) {
+                            const int rl = half * RPH + own_rr(ro);
+                            tau_hi[ro] = rows_s[rl].tau_hi;
+                            tau_lo[ro] = rows_s[rl].tau_lo;
+                            b1[ro] = rows_s[rl].b1;
+                            wcnt[ro] = rows_s[rl].wcnt[quad];
                         }
                     }
                 }
@@ -832,14 +883,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (C::STREAM) {
                 // unit end: every warp publishes its own sub-list lengths (also for
                 // units with no tiles)
-                if (lane == 0) {
+                if (row_leader) {
 #pragma unroll
-                    for (int r = 0; r < C::RPH; ++r) {
-                        const int rl = half * C::RPH + r;
+                    for (int ro = 0; ro < RO; ++ro) {
+                        const int rl = half * RPH + own_rr(ro);
                         if (rl < ui.nr)
                             p.counts[sg.cnt_offset +
                                      (int64_t)(ui.t0 + rl - sg.row_begin) * sg.cnt_ld + quad] =
-                                min(wcnt[r], static_cast<uint32_t>(p.cap));
+                                min(wcnt[ro], static_cast<uint32_t>(p.cap));
                     }
                 }
                 // both halves are done with the row state before the next unit resets it
@@ -899,8 +950,8 @@ cudaError_t launch_logits(const LogitsParams& p, int H, int D, int kfmt, int sin
             return launch_sink<16, 128, kKeyFp8>(p, sink, grid, stream);
         if (H == 64 && D == 128)
             return launch_sink<64, 128, kKeyFp8>(p, sink, grid, stream);
-        if (H == 4 && D == 64)
-            return launch_sink<4, 64, kKeyFp8>(p, sink, grid, stream);
+        if (H == 8 && D == 64)
+            return launch_sink<8, 64, kKeyFp8>(p, sink, grid, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -224,6 +224,25 @@ __device__ __forceinline__ void tmem_wait_ld()
 
 // 32 lanes x 32 columns of 32-bit: thread i of the warp receives lane
 // (quadrant base + i), columns [col, col+32).
+// 16 lanes x 256 bits, repeated 4 times along the columns (32 columns): thread
+// t = 4g + q gets, for repetition k, columns 8k + 2q and 8k + 2q + 1 of lane g
+// (v[4k], v[4k+1]) and of lane g + 8 (v[4k+2], v[4k+3]), lanes counted from
+// the address's lane field.
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, float (&v)[32])
 {
     uint32_t r[32];
