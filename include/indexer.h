@@ -73,6 +73,11 @@ extern "C" {
 #define IDX_K_FP4_E2M1_UE8M0 1     /* k: e2m1 [keys, D/2], element 2i in the low nibble;
                                       k_scale: uint8 ue8m0 [keys, D/32]; s_k is 1 */
 
+/* Row selection strategies of indexer_fused_topk (both exact). */
+#define IDX_SELECT_AUTO 0          /* sampled row thresholds where rows are long enough,
+                                      the running-threshold stream for undecided rows */
+#define IDX_SELECT_STREAM 1        /* the running-threshold stream for every row */
+
 /*
  * Problem description, read only by indexer_plan (host memory, copied).
  *   num_requests  R >= 1 (at most 256)
@@ -95,6 +100,12 @@ extern "C" {
  *                 calls (0 means 2 GiB); the planner shrinks key blocks and
  *                 row chunks to fit and fails with IDX_ERR_WORKSPACE if it
  *                 cannot.
+ *   select_mode   IDX_SELECT_AUTO or IDX_SELECT_STREAM.  AUTO scores every
+ *                 32nd-or-so key tile first and takes, per row, a threshold a
+ *                 little below the expected k-th score; the lists then hold every
+ *                 key at or above it, and a row whose lists hold fewer than k
+ *                 keys (or overflow) is selected again by the stream.  Results
+ *                 are identical; only the work differs.
  */
 typedef struct indexer_problem {
     int32_t num_requests;
@@ -111,6 +122,8 @@ typedef struct indexer_problem {
     int32_t cand_topk;
     int32_t key_block;
     uint64_t transient_budget_bytes;
+    int32_t select_mode;
+    int32_t reserved_;
 } indexer_problem;
 
 typedef struct indexer_plan_s* indexer_plan_t;
@@ -127,9 +140,11 @@ int indexer_plan(const indexer_problem* problem, indexer_plan_t* out_plan,
                  size_t* workspace_bytes);
 void indexer_plan_destroy(indexer_plan_t plan);
 
-/* Key-block size and row-chunk size the plan chose (for reporting). */
+/* Key-block size, row-chunk size, key splits per row and key-tile sampling
+ * stride (0 = no sampled thresholds) the plan chose (for reporting); any
+ * pointer may be NULL. */
 int indexer_plan_info(indexer_plan_t plan, int32_t* key_block, int32_t* row_chunk,
-                      int32_t* max_splits);
+                      int32_t* max_splits, int32_t* sample_stride);
 
 /*
  * Dense logits ("chunked-prefill-memory.md" section 1: [T, max_seqlen_k] fp32).

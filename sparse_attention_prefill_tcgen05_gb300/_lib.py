@@ -27,6 +27,8 @@ IDX_ERR_TIMEOUT = -5
 IDX_ERR_DEVICE_CHECK = -6
 IDX_K_FP8_E4M3 = 0
 IDX_K_FP4_E2M1_UE8M0 = 1
+IDX_SELECT_AUTO = 0
+IDX_SELECT_STREAM = 1
 
 EXPORTED = ("indexer_plan", "indexer_plan_destroy", "indexer_plan_info", "indexer_logits",
             "indexer_topk", "indexer_fused_topk", "indexer_candidate_blocks",
@@ -53,6 +55,7 @@ class _Problem(ctypes.Structure):
         ("kdtype", ctypes.c_int32), ("cand_block", ctypes.c_int32),
         ("cand_topk", ctypes.c_int32), ("key_block", ctypes.c_int32),
         ("transient_budget_bytes", ctypes.c_uint64),
+        ("select_mode", ctypes.c_int32), ("reserved_", ctypes.c_int32),
     ]
 
 
@@ -73,6 +76,7 @@ def lib():
         L.indexer_plan_destroy.argtypes = [P]
         L.indexer_plan_destroy.restype = None
         L.indexer_plan_info.argtypes = [P, ctypes.POINTER(ctypes.c_int32),
+                                        ctypes.POINTER(ctypes.c_int32),
                                         ctypes.POINTER(ctypes.c_int32),
                                         ctypes.POINTER(ctypes.c_int32)]
         L.indexer_logits.argtypes = [P, P, P, P, P, P, P, P, i64, P, sz, P]
@@ -127,10 +131,11 @@ class Plan:
         self._keep = keepalive
 
     def info(self):
-        kb, rc, ns = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
-        _check("indexer_plan_info", lib().indexer_plan_info(self.handle, ctypes.byref(kb),
-                                                             ctypes.byref(rc), ctypes.byref(ns)))
-        return {"key_block": kb.value, "row_chunk": rc.value, "max_splits": ns.value}
+        kb, rc, ns, st = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        _check("indexer_plan_info", lib().indexer_plan_info(
+            self.handle, ctypes.byref(kb), ctypes.byref(rc), ctypes.byref(ns), ctypes.byref(st)))
+        return {"key_block": kb.value, "row_chunk": rc.value, "max_splits": ns.value,
+                "sample_stride": st.value}
 
     def __del__(self):
         h, self.handle = getattr(self, "handle", None), None
@@ -140,7 +145,8 @@ class Plan:
 
 def indexer_plan(cu_seqlens_q, cu_seqlens_k, compress_len, H: int, D: int, topk: int,
                  kdtype: int = IDX_K_FP8_E4M3, cand_block: int = 0, cand_topk: int = 0,
-                 key_block: int = 0, transient_budget_bytes: int = 0) -> Plan:
+                 key_block: int = 0, transient_budget_bytes: int = 0,
+                 select_mode: int = 0) -> Plan:
     """Host-only planning: lengths are host (CPU) int32 arrays/tensors."""
     def host_i32(x):
         t = torch.as_tensor(x).to(device="cpu", dtype=torch.int32).contiguous()
@@ -152,7 +158,8 @@ def indexer_plan(cu_seqlens_q, cu_seqlens_k, compress_len, H: int, D: int, topk:
     prob = _Problem(num_requests=cq.numel() - 1, total_rows=int(cq[-1]), total_keys=int(ck[-1]),
                     H=H, D=D, topk=topk, cu_seqlens_q=pq, cu_seqlens_k=pk, compress_len=pl,
                     kdtype=kdtype, cand_block=cand_block, cand_topk=cand_topk,
-                    key_block=key_block, transient_budget_bytes=transient_budget_bytes)
+                    key_block=key_block, transient_budget_bytes=transient_budget_bytes,
+                    select_mode=select_mode)
     handle = ctypes.c_void_p()
     ws = ctypes.c_size_t()
     _check("indexer_plan", lib().indexer_plan(ctypes.byref(prob), ctypes.byref(handle),

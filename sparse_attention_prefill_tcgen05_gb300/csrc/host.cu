@@ -29,6 +29,7 @@ struct Pass {
 };
 
 constexpr int kUpdateTiles = 4;          // tiles between threshold refreshes
+constexpr int kSampleTiles = 32;         // sampled key tiles per row (at most)
 constexpr int64_t kTargetUnits = 1024;   // units per launch wanted for load balance
 
 }  // namespace
@@ -52,7 +53,10 @@ struct indexer_plan_s {
     std::vector<Pass> passes_k, passes_b;
     int max_piece_rows = 0;
     // workspace layout (bytes)
-    size_t off_gtau = 0, off_counts = 0, off_lists = 0, ws_bytes = 0;
+    // sampled thresholds (top-k): every sample_stride-th key tile, sample_cols
+    // columns per row, threshold at the sample_rank-th largest; stride 0 = off
+    int sample_stride = 0, sample_cols = 0, sample_rank = 0;
+    size_t off_gtau = 0, off_fail = 0, off_tau = 0, off_counts = 0, off_lists = 0, ws_bytes = 0;
     long long wait_budget = 4000000000LL;
 };
 
@@ -259,9 +263,135 @@ int run_logits(Ctx& c, std::vector<Segment>& segs, int sink)
                : IDX_ERR_CUDA;
 }
 
-// Streamed top-k (pool = 0) or candidate blocks (pool > 0): every pass scores
-// its rows against every key split, appending threshold-passing entries to the
-// lists, then selects exactly from the lists.
+// Segments and merge pieces of one pass for a list-filling sink: every piece
+// against every key split of its request.
+int pass_launches(Ctx& c, const Pass& ps, const std::vector<int32_t>& cap, int sink,
+                  StreamMergeParams& mp)
+{
+    const indexer_plan_s* p = c.p;
+    LogitsParams& lp = c.lp;
+    std::memset(&mp, 0, sizeof(mp));
+    std::vector<Segment> segs;
+    int ctas = 0;
+    int launch_cap = -1;
+    auto flush = [&]() -> int {
+        if (segs.empty())
+            return IDX_OK;
+        lp.cap = launch_cap;
+        int rc = run_logits(c, segs, sink);
+        segs.clear();
+        return rc;
+    };
+    for (const PassPiece& pc : ps.pieces) {
+        const int r = pc.r;
+        const int ns = p->n_splits[r];
+        // one launch per distinct capacity (capacity is a launch parameter)
+        if (cap[r] != launch_cap || (int)segs.size() + ns > kMaxSegments) {
+            int rc = flush();
+            if (rc != IDX_OK)
+                return rc;
+            launch_cap = cap[r];
+        }
+        for (int s = 0; s < ns; ++s) {
+            Segment sg;
+            std::memset(&sg, 0, sizeof(sg));
+            sg.row_begin = pc.a;
+            sg.nrows = pc.b - pc.a;
+            sg.key_base = p->key_begin[r];
+            sg.key_count = p->L[r];
+            sg.j_begin = s * p->split_keys;
+            sg.j_end = std::min(p->L[r], (s + 1) * p->split_keys);
+            sg.unit_tiles = (int)ceil_div(std::max(0, sg.j_end - sg.j_begin), kTileKeys);
+            sg.tile_stride = 1;
+            sg.n_row_groups = (int)ceil_div(sg.nrows, p->G);
+            sg.n_chunks = 1;
+            // row-major [row][split][quadrant][cap]
+            sg.out_offset = pc.list_off + (int64_t)s * kListsPerSplit * cap[r];
+            sg.out_ld = (int64_t)ns * kListsPerSplit * cap[r];
+            sg.cnt_offset = p->cnt_base[r] +
+                            (int64_t)(pc.a - p->row_begin[r]) * ns * kListsPerSplit +
+                            (int64_t)s * kListsPerSplit;
+            sg.cnt_ld = ns * kListsPerSplit;
+            segs.push_back(sg);
+        }
+        MergePiece& mpc = mp.piece[mp.num_pieces++];
+        mpc.row_begin = pc.a;
+        mpc.nrows = pc.b - pc.a;
+        mpc.cta_begin = ctas;
+        mpc.slots = ns * kListsPerSplit;
+        mpc.cap = cap[r];
+        mpc.list_offset = pc.list_off;
+        mpc.count_offset = p->cnt_base[r] + (int64_t)(pc.a - p->row_begin[r]) * ns * kListsPerSplit;
+        ctas += pc.b - pc.a;
+    }
+    mp.total_ctas = ctas;
+    mp.lists = lp.lists;
+    mp.counts = lp.counts;
+    return flush();
+}
+
+int launch_merge(Ctx& c, StreamMergeParams& mp)
+{
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return launch_stream_merge(mp, c.st) == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+}
+
+// Sampled logits of the pass's rows (every sample_stride-th key tile of each
+// request) into `samples` [rows, sample_cols], then each row's threshold.
+int pass_thresholds(Ctx& c, const Pass& ps, float* samples, uint32_t* tau_row)
+{
+    const indexer_plan_s* p = c.p;
+    LogitsParams& lp = c.lp;
+    const int first = ps.pieces.front().a;
+    std::vector<Segment> segs;
+    int rows = 0;
+    for (const PassPiece& pc : ps.pieces) {
+        const int r = pc.r;
+        Segment sg;
+        std::memset(&sg, 0, sizeof(sg));
+        sg.row_begin = pc.a;
+        sg.nrows = pc.b - pc.a;
+        sg.key_base = p->key_begin[r];
+        sg.key_count = p->L[r];
+        sg.j_begin = 0;
+        sg.j_end = p->L[r];
+        sg.tile_stride = p->sample_stride;
+        sg.unit_tiles = (int)ceil_div(ceil_div(std::max(1, p->L[r]), kTileKeys), p->sample_stride);
+        sg.n_row_groups = (int)ceil_div(sg.nrows, p->G);
+        sg.n_chunks = 1;
+        sg.out_offset = (int64_t)(pc.a - first) * p->sample_cols;
+        sg.out_ld = p->sample_cols;
+        segs.push_back(sg);
+        rows = pc.b - first;
+        if ((int)segs.size() == kMaxSegments) {
+            lp.out = samples;
+            int rc = run_logits(c, segs, kSinkLogits);
+            if (rc != IDX_OK)
+                return rc;
+            segs.clear();
+        }
+    }
+    if (!segs.empty()) {
+        lp.out = samples;
+        int rc = run_logits(c, segs, kSinkLogits);
+        if (rc != IDX_OK)
+            return rc;
+    }
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return launch_sample_threshold(samples, p->sample_cols, rows, p->sample_rank,
+                                   tau_row + first, c.st) == cudaSuccess
+               ? IDX_OK
+               : IDX_ERR_CUDA;
+}
+
+// Streamed top-k (pool = 0) or candidate blocks (pool > 0), pass by pass.
+//   exact:   the logits kernel appends entries that pass each row's running
+//            threshold (histograms, compaction, shared bound), then the merge
+//            selects exactly from the lists;
+//   sampled: (top-k, when the plan samples) a threshold per row from sampled
+//            logits, lists of every entry at or above it, a merge that
+//            decides the rows whose lists hold at least k entries and did not
+//            overflow, and the exact path for the rows it could not decide.
 int run_streamed(Ctx& c, uint8_t* ws, int pool, int32_t* out_idx, float* out_val,
                  uint8_t* mask, int64_t ld_mask)
 {
@@ -269,84 +399,58 @@ int run_streamed(Ctx& c, uint8_t* ws, int pool, int32_t* out_idx, float* out_val
     const std::vector<Pass>& passes = pool ? p->passes_b : p->passes_k;
     const std::vector<int32_t>& cap = pool ? p->cap_b : p->cap_k;
     const int keep = pool ? p->cand_topk : p->topk;
+    const bool sampled = pool == 0 && p->sample_stride > 0;
     LogitsParams& lp = c.lp;
     lp.lists = reinterpret_cast<uint2*>(ws + p->off_lists);
     lp.counts = reinterpret_cast<uint32_t*>(ws + p->off_counts);
     lp.gtau = reinterpret_cast<uint32_t*>(ws + p->off_gtau);
+    uint32_t* row_fail = reinterpret_cast<uint32_t*>(ws + p->off_fail);
+    uint32_t* tau_row = reinterpret_cast<uint32_t*>(ws + p->off_tau);
     lp.keep = keep;
     lp.pool = pool ? pool : 1;
     lp.update_tiles = kUpdateTiles;
-    for (const Pass& ps : passes) {
-        // one launch per distinct capacity (capacity is a launch parameter)
-        std::vector<Segment> segs;
-        StreamMergeParams mp;
-        std::memset(&mp, 0, sizeof(mp));
-        int ctas = 0;
-        int launch_cap = -1;
-        auto flush = [&]() -> int {
-            if (segs.empty())
-                return IDX_OK;
-            lp.cap = launch_cap;
-            int rc = run_logits(c, segs, pool ? kSinkPool : kSinkStream);
-            segs.clear();
-            return rc;
-        };
-        for (const PassPiece& pc : ps.pieces) {
-            const int r = pc.r;
-            const int ns = p->n_splits[r];
-            if (cap[r] != launch_cap || (int)segs.size() + ns > kMaxSegments) {
-                int rc = flush();
-                if (rc != IDX_OK)
-                    return rc;
-                launch_cap = cap[r];
-            }
-            for (int s = 0; s < ns; ++s) {
-                Segment sg;
-                std::memset(&sg, 0, sizeof(sg));
-                sg.row_begin = pc.a;
-                sg.nrows = pc.b - pc.a;
-                sg.key_base = p->key_begin[r];
-                sg.key_count = p->L[r];
-                sg.j_begin = s * p->split_keys;
-                sg.j_end = std::min(p->L[r], (s + 1) * p->split_keys);
-                sg.unit_tiles = (int)ceil_div(std::max(0, sg.j_end - sg.j_begin), kTileKeys);
-                sg.n_row_groups = (int)ceil_div(sg.nrows, p->G);
-                sg.n_chunks = 1;
-                // row-major [row][split][quadrant][cap]
-                sg.out_offset = pc.list_off + (int64_t)s * kListsPerSplit * cap[r];
-                sg.out_ld = (int64_t)ns * kListsPerSplit * cap[r];
-                sg.cnt_offset = p->cnt_base[r] +
-                                (int64_t)(pc.a - p->row_begin[r]) * ns * kListsPerSplit +
-                                (int64_t)s * kListsPerSplit;
-                sg.cnt_ld = ns * kListsPerSplit;
-                segs.push_back(sg);
-            }
-            MergePiece& mpc = mp.piece[mp.num_pieces++];
-            mpc.row_begin = pc.a;
-            mpc.nrows = pc.b - pc.a;
-            mpc.cta_begin = ctas;
-            mpc.slots = ns * kListsPerSplit;
-            mpc.cap = cap[r];
-            mpc.list_offset = pc.list_off;
-            mpc.count_offset = p->cnt_base[r] + (int64_t)(pc.a - p->row_begin[r]) * ns * kListsPerSplit;
-            ctas += pc.b - pc.a;
-        }
-        int rc = flush();
-        if (rc != IDX_OK)
-            return rc;
-        mp.lists = lp.lists;
-        mp.counts = lp.counts;
-        mp.gtau = lp.gtau;
+    auto finish = [&](StreamMergeParams& mp) {
         mp.k = keep;
-        mp.total_ctas = ctas;
         mp.out_idx = out_idx;
         mp.out_val = out_val;
         mp.mask = mask;
         mp.ld_mask = ld_mask;
-        g_launches.fetch_add(1, std::memory_order_relaxed);
-        if (launch_stream_merge(mp, c.st) != cudaSuccess)
-            return IDX_ERR_CUDA;
+        mp.bitmap_words = pool ? 0 : (int)ceil_div(std::max(1, p->max_L), 32);
+    };
+    for (const Pass& ps : passes) {
+        StreamMergeParams mp;
+        int rc;
+        if (sampled) {
+            if ((rc = pass_thresholds(c, ps, reinterpret_cast<float*>(lp.lists), tau_row)) !=
+                IDX_OK)
+                return rc;
+            lp.tau_row = tau_row;
+            lp.row_fail = nullptr;
+            if ((rc = pass_launches(c, ps, cap, kSinkFilter, mp)) != IDX_OK)
+                return rc;
+            finish(mp);
+            mp.gtau = nullptr;
+            mp.verify = 1;
+            mp.tau_row = tau_row;
+            mp.row_fail = row_fail;
+            if ((rc = launch_merge(c, mp)) != IDX_OK)
+                return rc;
+            // the exact path, for the undecided rows only
+            lp.row_fail = row_fail;
+        } else {
+            lp.row_fail = nullptr;
+        }
+        if ((rc = pass_launches(c, ps, cap, pool ? kSinkPool : kSinkStream, mp)) != IDX_OK)
+            return rc;
+        finish(mp);
+        mp.gtau = lp.gtau;
+        mp.verify = 0;
+        mp.only_failed = sampled ? 1 : 0;
+        mp.row_fail = row_fail;
+        if ((rc = launch_merge(c, mp)) != IDX_OK)
+            return rc;
     }
+    lp.row_fail = nullptr;
     return IDX_OK;
 }
 
@@ -498,8 +602,29 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
         p->cnt_base[r] = counts;
         counts += (int64_t)(p->row_begin[r + 1] - p->row_begin[r]) * ns * kListsPerSplit;
     }
+    // Sampled thresholds for rows with at least 2 x kSampleTiles key tiles: tiles
+    // 0, s, 2s, ... (at most kSampleTiles per row).  With mu = k / s samples
+    // expected among a row's top k (keys in random order), the threshold is the
+    // sample of rank mu + 6.5 sqrt(mu) + 8, so that a row whose lists end up
+    // with fewer than k entries (decided again by the exact path) is rare.
+    const int max_tiles = (int)ceil_div(std::max(1, p->max_L), kTileKeys);
+    if (pr->select_mode == IDX_SELECT_AUTO && max_tiles >= 2 * kSampleTiles) {
+        const int st = (int)ceil_div(max_tiles, kSampleTiles);
+        const double mu = (double)p->topk / st;
+        p->sample_stride = st;
+        p->sample_cols = (int)ceil_div(max_tiles, st) * kTileKeys;
+        p->sample_rank = (int)std::ceil(mu + 6.5 * std::sqrt(mu) + 8.0);
+        // the samples of a pass live in its list area
+        for (int r = 0; r < R; ++r)
+            if ((int64_t)p->sample_cols * 4 >
+                (int64_t)p->n_splits[r] * kListsPerSplit * p->cap_k[r] * 8)
+                p->sample_stride = 0;
+    }
     size_t off = kStatusBytes;
-    p->off_gtau = off;
+    p->off_gtau = off;                       // [T] shared bound, then [T] row flags
+    p->off_fail = off + (size_t)std::max(p->T, 1) * 4;
+    off = align_up(p->off_fail + (size_t)std::max(p->T, 1) * 4, 256);
+    p->off_tau = off;
     off = align_up(off + (size_t)std::max(p->T, 1) * 4, 256);
     p->off_counts = off;
     off = align_up(off + (size_t)std::max<int64_t>(counts, 1) * 4, 256);
@@ -527,10 +652,12 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
 void indexer_plan_destroy(indexer_plan_t p) { delete p; }
 
 int indexer_plan_info(indexer_plan_t p, int32_t* key_block, int32_t* row_chunk,
-                      int32_t* max_splits)
+                      int32_t* max_splits, int32_t* sample_stride)
 {
     if (!p)
         return IDX_ERR_INVALID_ARG;
+    if (sample_stride)
+        *sample_stride = p->sample_stride;
     if (key_block)
         *key_block = p->split_keys;
     if (row_chunk)
@@ -659,7 +786,8 @@ int indexer_fused_topk(indexer_plan_t p, const void* q, const float* s_q, const 
     c.lp.cand_mask = cand_mask;
     c.lp.ld_mask = ld_mask;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
-    if (cudaMemsetAsync(wsb + p->off_gtau, 0, (size_t)p->T * 4, c.st) != cudaSuccess)
+    // shared bounds and row flags
+    if (cudaMemsetAsync(wsb + p->off_gtau, 0, (size_t)p->T * 8, c.st) != cudaSuccess)
         return IDX_ERR_CUDA;
     return run_streamed(c, wsb, 0, out_idx, out_val, nullptr, 0);
 }

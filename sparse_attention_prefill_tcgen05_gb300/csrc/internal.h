@@ -28,6 +28,7 @@ constexpr int kKeyFp4 = 1;
 constexpr int kSinkLogits = 0;   // write fp32 to a [rows, ld] buffer
 constexpr int kSinkStream = 1;   // append threshold-passing (score, key) to per-row lists
 constexpr int kSinkPool = 2;     // same over cand_block-key block maxima (candidate blocks)
+constexpr int kSinkFilter = 3;   // append entries at or above a fixed per-row threshold
 
 constexpr int kListsPerSplit = 4;     // one candidate sub-list per epilogue warp quadrant
 constexpr int kMaxStreamSlots = 256;  // sub-lists per row (key splits x kListsPerSplit)
@@ -46,6 +47,9 @@ struct Segment {
     int32_t n_row_groups;
     int32_t n_chunks;
     int32_t unit_tiles;  // key tiles per unit
+    int32_t tile_stride; // 1: every key tile; s: tiles 0, s, 2s, ... (sampled keys, whose
+                         // logits go to consecutive output columns)
+    int32_t pad_;
     int64_t out_offset;  // logits: element offset of (row_begin, j_begin) in the output;
                          // streams: entry offset of row_begin's list for this split
     int64_t out_ld;      // logits: elements between rows; streams: entries between rows
@@ -78,6 +82,8 @@ struct LogitsParams {
     int32_t keep;         // k (keys) or cand_topk (blocks)
     int32_t pool;         // keys per block for kSinkPool
     int32_t update_tiles; // tiles between threshold refreshes
+    const uint32_t* tau_row;   // kSinkFilter: [rows] fixed threshold (ord of a score)
+    const uint32_t* row_fail;  // nullable [rows]: only row groups with a set row run
     Segment seg[kMaxSegments];
 };
 
@@ -104,10 +110,15 @@ struct StreamMergeParams {
     const uint2* lists;
     const uint32_t* counts;
     const uint32_t* gtau;   // per-row lower bound on the k-th key: entries below it are skipped
+    uint32_t* row_fail;     // [rows] verify: set for rows the lists cannot decide;
+                            // only_failed: rows with a clear entry are skipped
+    const uint32_t* tau_row;  // verify: the threshold the lists were filled with
+    int32_t verify;
+    int32_t only_failed;
     int32_t k;
     int32_t num_pieces;
     int32_t total_ctas;
-    int32_t pad_;
+    int32_t bitmap_words;      // ceil(largest key count / 32): index-order output by bitmap
     int32_t* out_idx;
     float* out_val;
     uint8_t* mask;             // blocks: [rows, ld_mask]
@@ -131,6 +142,11 @@ struct TopkParams {
     int32_t req_key_count[kMaxRequests];
 };
 cudaError_t launch_topk_dense(const TopkParams& p, cudaStream_t stream);
+
+// Per-row threshold from sampled logits [rows, ld]: the ord of the rank-th
+// largest sample, or 0 (everything passes) when a row has fewer samples.
+cudaError_t launch_sample_threshold(const float* samples, int64_t ld, int rows, int rank,
+                                    uint32_t* tau_row, cudaStream_t stream);
 
 cudaError_t launch_expand_mask(const uint8_t* cand_mask, int64_t ld_mask, const int32_t* clen,
                                uint8_t* key_mask, int64_t ld, int block, int rows,

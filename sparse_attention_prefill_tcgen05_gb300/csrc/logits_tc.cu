@@ -105,6 +105,8 @@ struct UnitInfo {
     int t0;        // first global row of the row group
     int nr;        // valid rows in the group
     int j0;        // request-local first key of the unit
+    int col0;      // output column of the unit's first key (sampled segments)
+    int step;      // keys between consecutive tiles (tile_stride * 128)
     int jend;      // request-local end of keys covered by the unit
     int ntiles;    // tiles covering [j0, jend)
     int ntiles_mma;
@@ -123,12 +125,15 @@ __device__ __forceinline__ UnitInfo decode_unit(const LogitsParams& p, int u, in
     const int local = u - sg.unit_begin;
     const int chunk = local / sg.n_row_groups;
     const int g = local - chunk * sg.n_row_groups;
+    const int step = (sg.tile_stride > 0 ? sg.tile_stride : 1) * kTileKeys;   // tile to tile
     ui.seg = s;
     ui.t0 = sg.row_begin + g * G;
     ui.nr = min(G, sg.row_begin + sg.nrows - ui.t0);
-    ui.j0 = sg.j_begin + chunk * sg.unit_tiles * kTileKeys;
-    ui.jend = min(sg.j_end, ui.j0 + sg.unit_tiles * kTileKeys);
-    ui.ntiles = (ui.jend - ui.j0 + kTileKeys - 1) / kTileKeys;
+    ui.j0 = sg.j_begin + chunk * sg.unit_tiles * step;
+    ui.col0 = chunk * sg.unit_tiles * kTileKeys;
+    ui.step = step;
+    ui.jend = min(sg.j_end, ui.j0 + sg.unit_tiles * step);
+    ui.ntiles = (ui.jend - ui.j0 + step - 1) / step;
     // longest causal length in the group (warp-cooperative), clamped to the request
     int m = 0;
     for (int r = lane; r < ui.nr; r += 32)
@@ -137,7 +142,18 @@ __device__ __forceinline__ UnitInfo decode_unit(const LogitsParams& p, int u, in
     for (int o = 16; o > 0; o >>= 1)
         m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
     const int mma_end = min(ui.jend, m);
-    ui.ntiles_mma = mma_end > ui.j0 ? (mma_end - ui.j0 + kTileKeys - 1) / kTileKeys : 0;
+    ui.ntiles_mma = mma_end > ui.j0 ? (mma_end - ui.j0 + step - 1) / step : 0;
+    if (p.row_fail != nullptr) {
+        // second pass over the rows the first one could not decide: other row
+        // groups have no work
+        bool any = false;
+        for (int r = lane; r < ui.nr; r += 32)
+            any |= p.row_fail[ui.t0 + r] != 0;
+        if (!__any_sync(0xffffffffu, any)) {
+            ui.ntiles = 0;
+            ui.ntiles_mma = 0;
+        }
+    }
     return ui;
 }
 
@@ -339,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             for (int i = 0; i < ui.ntiles_mma && ok; ++i) {
-                const int key0 = sg.key_base + ui.j0 + i * kTileKeys;
+                const int key0 = sg.key_base + ui.j0 + i * ui.step;
                 if (lane == 0) {
                     if (!mbar_wait(&k_empty[ks], kph ^ 1, budget, abort_flag)) {
                         report(p, abort_flag, kStatusTimeout);
@@ -361,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int r = 0; r < kTileKeys / 32; ++r) {
                         const int m = r * 32 + lane;
-                        const int local = ui.j0 + i * kTileKeys + m;
+                        const int local = ui.j0 + i * ui.step + m;
                         const uint32_t word =
                             local < sg.key_count ? __ldg(src + key0 + m) : 0x7F7F7F7Fu;
                         *reinterpret_cast<uint32_t*>(sf + m * 16) = word;
@@ -539,7 +555,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tau_lo[ro] = 0;
                 b1[ro] = 256;
                 wcnt[ro] = 0;
-                if constexpr (C::STREAM) {
+                if constexpr (SINK == kSinkFilter) {
+                    tau_hi[ro] = rl < ui.nr ? p.tau_row[ui.t0 + rl] : 0u;
+                } else if constexpr (C::STREAM) {
                     tau_hi[ro] = rows_s[rl].tau_hi;
                     tau_lo[ro] = rows_s[rl].tau_lo;
                 }
@@ -575,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 SINK == kSinkPool ? ui.ntiles * (32 / (p.pool > 0 ? p.pool : 1)) : ui.ntiles * 32;
             const bool no_overflow = unit_entries_warp <= p.cap;
             for (int i = 0; i < ui.ntiles; ++i) {
-                const int jt = ui.j0 + i * kTileKeys + quad * 32;   // first key of the quadrant
+                const int jt = ui.j0 + i * ui.step + quad * 32;   // first key of the quadrant
                 float val[RPH];
 #pragma unroll
                 for (int m = 0; m < RPH; ++m)
@@ -583,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (i < ui.ntiles_mma) {
                     const float sk_lane = sk_next;
                     {
-                        const int jn = jt + kTileKeys + lane;
+                        const int jn = jt + ui.step + lane;
                         if (KFMT == kKeyFp8 && i + 1 < ui.ntiles_mma)
                             sk_next = jn < sg.key_count ? __ldg(p.s_k + sg.key_base + jn) : 0.0f;
                     }
@@ -689,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // causal and candidate masks (most tiles lie below every row's causal
                 // length: one warp-uniform test skips the per-value work there)
-                if (p.cand_mask != nullptr || ui.j0 + (i + 1) * kTileKeys > clen_min) {
+                if (p.cand_mask != nullptr || ui.j0 + i * ui.step + kTileKeys > clen_min) {
 #pragma unroll
                     for (int m = 0; m < RPH; ++m) {
                         const int ro = RPH >= 4 ? (m >> 2) : 0;
@@ -704,15 +722,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if constexpr (SINK == kSinkLogits) {
-                    float* out_base = p.out + sg.out_offset - sg.j_begin;
+                    // column of key j: (j - j_begin) for every tile, or the sample
+                    // number for a sampled segment
+                    float* out_base = p.out + sg.out_offset + ui.col0 + i * kTileKeys + quad * 32;
+#pragma unroll
+                    for (int m = 0; m < RPH; ++m) {
+                        const int ro = RPH >= 4 ? (m >> 2) : 0;
+                        const int rl = half * RPH + own_rr(ro);
+                        const int kk = 8 * slot_bl(RPH >= 4 ? (m & 3) : m) + g;
+                        if (rl < ui.nr && jt + kk < ui.jend)
+                            out_base[(size_t)(ui.t0 + rl - sg.row_begin) * sg.out_ld + kk] =
+                                val[m];
+                    }
+                } else if constexpr (SINK == kSinkFilter) {
+                    // fixed threshold: append, no histograms, no refresh (a sub-list
+                    // that overflows is detected by the merge from its count)
 #pragma unroll
                     for (int m = 0; m < RPH; ++m) {
                         const int ro = RPH >= 4 ? (m >> 2) : 0;
                         const int rl = half * RPH + own_rr(ro);
                         const int j = jt + 8 * slot_bl(RPH >= 4 ? (m & 3) : m) + g;
-                        if (rl < ui.nr && j < ui.jend)
-                            out_base[(size_t)(ui.t0 + rl - sg.row_begin) * sg.out_ld + j] =
-                                val[m];
+                        const uint32_t o = f2ord(val[m]);
+                        const bool cand = rl < ui.nr && o > kOrdNegInf && o >= tau_hi[ro];
+                        const uint32_t mb = __ballot_sync(0xffffffffu, cand) & rowmask;
+                        if (cand) {
+                            const uint32_t pos = wcnt[ro] + __popc(mb & ((1u << lane) - 1u));
+                            if (pos < static_cast<uint32_t>(p.cap))
+                                p.lists[sg.out_offset +
+                                        (int64_t)(ui.t0 + rl - sg.row_begin) * sg.out_ld +
+                                        (int64_t)quad * p.cap + pos] =
+                                    make_uint2(__float_as_uint(val[m]), static_cast<uint32_t>(j));
+                        }
+                        wcnt[ro] += __popc(mb);
                     }
                 } else {
                     const uint32_t cap = static_cast<uint32_t>(p.cap);
@@ -890,7 +931,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (rl < ui.nr)
                             p.counts[sg.cnt_offset +
                                      (int64_t)(ui.t0 + rl - sg.row_begin) * sg.cnt_ld + quad] =
-                                min(wcnt[ro], static_cast<uint32_t>(p.cap));
+                                SINK == kSinkFilter ? wcnt[ro]
+                                                    : min(wcnt[ro], static_cast<uint32_t>(p.cap));
                     }
                 }
                 // both halves are done with the row state before the next unit resets it
@@ -928,6 +970,8 @@ cudaError_t launch_sink(const LogitsParams& p, int sink, int grid, cudaStream_t 
         return launch_one<H, D, KFMT, kSinkStream>(p, grid, stream);
     if (sink == kSinkPool)
         return launch_one<H, D, KFMT, kSinkPool>(p, grid, stream);
+    if (sink == kSinkFilter)
+        return launch_one<H, D, KFMT, kSinkFilter>(p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

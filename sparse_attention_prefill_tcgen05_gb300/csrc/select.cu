@@ -82,7 +82,30 @@ __device__ void bitonic_sort(int32_t* key, float* val, int n2)
 }
 
 constexpr int kMaxSortK = 4096;
+constexpr int kBitmapWords = 2048;    // index-order output by bitmap for keys < 65536
+
+// Exclusive prefix sum of one value per thread over the CTA.
+__device__ uint32_t block_exclusive_sum(uint32_t v, Scratch& sh)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    if (lane == 31)
+        sh.warp_sum[warp] = incl;
+    __syncthreads();
+    uint32_t wbefore = 0;
+    for (int w = 0; w < warp; ++w)
+        wbefore += sh.warp_sum[w];
+    __syncthreads();
+    return wbefore + incl - v;
+}
 constexpr int kStageEntries = 7168;   // candidates staged in shared memory per row (56 KB)
+static_assert(kStageEntries * 8 >= kBitmapWords * 8, "the bitmap reuses the staging area");
 
 __global__ void __launch_bounds__(kSelThreads)
     stream_merge_kernel(const __grid_constant__ StreamMergeParams p)
@@ -100,6 +123,10 @@ __global__ void __launch_bounds__(kSelThreads)
     float* sval = reinterpret_cast<float*>(dyn + sizeof(uint2) * kStageEntries + sizeof(int32_t) * n2);
 
     __shared__ int32_t s_staged;
+    __shared__ int32_t s_overflow;
+    if (threadIdx.x == 0)
+        s_overflow = 0;
+    __syncthreads();
     const int cta = blockIdx.x;
     int pi = 0;
     while (pi + 1 < p.num_pieces && p.piece[pi + 1].cta_begin <= cta)
@@ -110,6 +137,8 @@ __global__ void __launch_bounds__(kSelThreads)
     const int nslots = pc.slots;
     const int64_t lbase = pc.list_offset + (int64_t)tr * nslots * pc.cap;
     const int64_t cbase = pc.count_offset + (int64_t)tr * nslots;
+    if (p.only_failed && p.row_fail[t] == 0)
+        return;   // decided by the first pass
     // entries below the row's final threshold bound cannot be among its top k
     const uint32_t floor_ord = p.gtau ? p.gtau[t] : 0u;
     if (threadIdx.x < 32) {
@@ -117,7 +146,10 @@ __global__ void __launch_bounds__(kSelThreads)
         int carry = 0;
         for (int s0 = 0; s0 < nslots; s0 += 32) {
             const int s = s0 + static_cast<int>(threadIdx.x);
-            const int c = s < nslots ? min(static_cast<int>(p.counts[cbase + s]), pc.cap) : 0;
+            const uint32_t raw = s < nslots ? p.counts[cbase + s] : 0u;
+            const int c = static_cast<int>(min(raw, static_cast<uint32_t>(pc.cap)));
+            if (raw > static_cast<uint32_t>(pc.cap))
+                s_overflow = 1;   // benign race: every writer stores 1
             int incl = c;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -136,6 +168,17 @@ __global__ void __launch_bounds__(kSelThreads)
     }
     __syncthreads();
     const int n_all = s_off[nslots];
+    if (p.verify) {
+        // the lists hold every entry at or above the row's threshold unless a
+        // sub-list overflowed; they decide the row iff that holds and they have
+        // at least k entries (or the threshold let everything through)
+        const bool decided = s_overflow == 0 && (p.tau_row[t] == 0u || n_all >= p.k);
+        if (!decided) {
+            if (threadIdx.x == 0)
+                p.row_fail[t] = 1u;
+            return;
+        }
+    }
     // copy the entries that pass the floor into shared memory (order is irrelevant:
     // the selection is by unique composite keys); every radix pass reads them there
     for (int s = 0; s < nslots; ++s) {
@@ -210,15 +253,97 @@ __global__ void __launch_bounds__(kSelThreads)
                 m[skey[i]] = 1;
         return;
     }
-    bitonic_sort(skey, sval, n2);
     int32_t* oi = p.out_idx + (int64_t)t * k;
     float* ov = p.out_val ? p.out_val + (int64_t)t * k : nullptr;
+    if (p.bitmap_words > 0 && p.bitmap_words <= kBitmapWords) {
+        // ascending key order without a sort: a bitmap of the kept keys (in the
+        // staging area, free now) and an exclusive scan of its word popcounts give
+        // every kept key its output position directly
+        uint32_t* bits = reinterpret_cast<uint32_t*>(stage);
+        uint32_t* wpre = bits + kBitmapWords;
+        const int nw = p.bitmap_words;
+        for (int w = threadIdx.x; w < nw; w += kSelThreads)
+            bits[w] = 0;
+        __syncthreads();
+        for (int i = threadIdx.x; i < count; i += kSelThreads)
+            atomicOr(&bits[skey[i] >> 5], 1u << (skey[i] & 31));
+        __syncthreads();
+        constexpr int kPer = kBitmapWords / kSelThreads;   // consecutive words per thread
+        const int w0 = threadIdx.x * kPer;
+        uint32_t local = 0;
+#pragma unroll
+        for (int w = 0; w < kPer; ++w)
+            local += w0 + w < nw ? __popc(bits[w0 + w]) : 0u;
+        const uint32_t before = block_exclusive_sum(local, sh);
+        uint32_t run = before;
+#pragma unroll
+        for (int w = 0; w < kPer; ++w) {
+            if (w0 + w < nw) {
+                wpre[w0 + w] = run;
+                run += __popc(bits[w0 + w]);
+            }
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < count; i += kSelThreads) {
+            const int j = skey[i];
+            const int pos = static_cast<int>(wpre[j >> 5] +
+                                             __popc(bits[j >> 5] & ((1u << (j & 31)) - 1u)));
+            oi[pos] = j;
+            if (ov)
+                ov[pos] = sval[i];
+        }
+        for (int i = count + threadIdx.x; i < k; i += kSelThreads) {
+            oi[i] = -1;
+            if (ov)
+                ov[i] = -INFINITY;
+        }
+        return;
+    }
+    bitonic_sort(skey, sval, n2);
     for (int i = threadIdx.x; i < k; i += kSelThreads) {
         const bool have = i < count;
         oi[i] = have ? skey[i] : -1;
         if (ov)
             ov[i] = have ? sval[i] : -INFINITY;
     }
+}
+
+// ------------------------------------------------- sampled row thresholds
+
+// tau[t] = ord of the rank-th largest finite sample of row t (the rank-th
+// largest composite key, ties to the lower sample position), or 0 when the
+// row has fewer than rank finite samples.
+__global__ void __launch_bounds__(kSelThreads)
+    sample_threshold_kernel(const float* samples, int64_t ld, int rank, uint32_t* tau_row)
+{
+    __shared__ Scratch sh;
+    __shared__ uint32_t s_min;
+    const int t = blockIdx.x;
+    const float* row = samples + (int64_t)t * ld;
+    auto load = [&](int e, uint32_t& hi, uint32_t& lo) {
+        hi = f2ord(row[e]);
+        lo = ~static_cast<uint32_t>(e);
+    };
+    const int n = static_cast<int>(ld);
+    const CompositeThr thr =
+        group_threshold<kSelThreads>(sh, threadIdx.x, n, static_cast<uint32_t>(rank), load, CtaSync{});
+    if (threadIdx.x == 0)
+        s_min = 0xFFFFFFFFu;
+    __syncthreads();
+    uint32_t mn = 0xFFFFFFFFu, cnt = 0;
+    for (int e = threadIdx.x; e < n; e += kSelThreads) {
+        uint32_t hi, lo;
+        load(e, hi, lo);
+        if (hi > kOrdNegInf && thr.kept(hi, lo)) {
+            mn = min(mn, hi);
+            ++cnt;
+        }
+    }
+    atomicMin(&s_min, mn);
+    const uint32_t kept = block_exclusive_sum(cnt, sh) + cnt;   // inclusive
+    __syncthreads();
+    if (threadIdx.x == kSelThreads - 1)
+        tau_row[t] = kept >= static_cast<uint32_t>(rank) ? s_min : 0u;
 }
 
 // ------------------------------------------------------- standalone top-k
@@ -267,6 +392,15 @@ cudaError_t launch_stream_merge(const StreamMergeParams& p, cudaStream_t stream)
     if (e != cudaSuccess)
         return e;
     stream_merge_kernel<<<p.total_ctas, kSelThreads, dyn, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sample_threshold(const float* samples, int64_t ld, int rows, int rank,
+                                    uint32_t* tau_row, cudaStream_t stream)
+{
+    if (rows <= 0)
+        return cudaSuccess;
+    sample_threshold_kernel<<<rows, kSelThreads, 0, stream>>>(samples, ld, rank, tau_row);
     return cudaGetLastError();
 }
 

@@ -26,12 +26,12 @@ def device_inputs(p, layer=1, dev="cuda"):
                 k_scale=p.k_scale.to(dev), compress_len=p.compress_len.to(dev))
 
 
-def make_plan(p, key_block=0, budget=0, topk=None):
+def make_plan(p, key_block=0, budget=0, topk=None, select_mode=K.IDX_SELECT_AUTO):
     kd = K.IDX_K_FP8_E4M3 if p.spec.kdtype == "fp8" else K.IDX_K_FP4_E2M1_UE8M0
     return K.indexer_plan(p.cu_seqlens_q, p.cu_seqlens_k, p.compress_len, p.H, p.D,
                           topk or p.topk, kdtype=kd, cand_block=p.spec.cand_block,
                           cand_topk=p.spec.cand_topk, key_block=key_block,
-                          transient_budget_bytes=budget)
+                          transient_budget_bytes=budget, select_mode=select_mode)
 
 
 def workspace(plan, dev="cuda"):

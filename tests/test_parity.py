@@ -48,6 +48,10 @@ def check_all(p, key_block=0):
     sel_ref = O.topk_rows(g.astype(np.float64), cl, p.topk)
     ti, tv = Hp.gpu_topk(p, plan, torch.from_numpy(g).cuda(), d)
     fi, fv = Hp.gpu_fused(p, plan, d)
+    # both selection strategies give the same result, bit for bit
+    si, sv = Hp.gpu_fused(p, Hp.make_plan(p, key_block=key_block,
+                                          select_mode=K.IDX_SELECT_STREAM), d)
+    assert torch.equal(si, fi) and torch.equal(sv, fv)
     ti, fi = ti.cpu().numpy(), fi.cpu().numpy()
     for t in range(T):
         want = sorted(x for x in sel_ref[t].tolist() if x >= 0)
@@ -173,12 +177,14 @@ def _structured_problem(L, rows, topk, key_scale):
                                k=k, k_scale=key_scale.float())
 
 
-def test_increasing_scores_force_list_compaction():
+@pytest.mark.parametrize("mode", [K.IDX_SELECT_STREAM, K.IDX_SELECT_AUTO])
+def test_increasing_scores_force_list_compaction(mode):
     """Scores rise with the key index, so every key passes the running threshold and the
-    per-row lists must be compacted many times inside the kernel."""
+    per-row lists must be compacted many times inside the kernel (stream); the sampled
+    threshold lets only the top few hundred through (auto)."""
     L, rows, topk = 8192, 24, 64
     p = _structured_problem(L, rows, topk, 1.0 + torch.arange(L, dtype=torch.float64) / L)
-    plan = Hp.make_plan(p)
+    plan = Hp.make_plan(p, select_mode=mode)
     assert plan.info()["max_splits"] == 1
     d = Hp.device_inputs(p)
     fi, fv = Hp.gpu_fused(p, plan, d)
@@ -191,17 +197,60 @@ def test_increasing_scores_force_list_compaction():
         Hp.check_topk_row(fi[t], ref[t], int(cl[t]), topk)
 
 
-def test_all_equal_scores_keep_the_lowest_indices():
+@pytest.mark.parametrize("mode", [K.IDX_SELECT_STREAM, K.IDX_SELECT_AUTO])
+def test_all_equal_scores_keep_the_lowest_indices(mode):
     """Every key ties: the top-k is the k lowest key indices, through compaction too."""
     L, rows, topk = 8192, 20, 100
     p = _structured_problem(L, rows, topk, torch.ones(L, dtype=torch.float64))
-    plan = Hp.make_plan(p)
+    plan = Hp.make_plan(p, select_mode=mode)
     d = Hp.device_inputs(p)
     fi, fv = Hp.gpu_fused(p, plan, d)
     fi = fi.cpu().numpy()
     for t in range(rows):
         assert fi[t].tolist() == list(range(topk)), t
     assert torch.all(fv == 256.0)
+
+
+def _sampled_tiles_scores(L, stride, sampled_high):
+    """Distinct scores rising with the key index, every key of the sampled tiles
+    (0, stride, 2 stride, ...) one unit above (or below) every other key."""
+    j = torch.arange(L, dtype=torch.float64)
+    on = ((j // 128) % stride) == 0
+    hi, lo = 2.0 + j / L, 1.0 + j / L
+    return torch.where(on, hi, lo) if sampled_high else torch.where(on, lo, hi)
+
+
+def _check_structured_topk(p, plan, rows, topk):
+    d = Hp.device_inputs(p)
+    fi, fv = Hp.gpu_fused(p, plan, d)
+    ref = oracle_rows(p, np.arange(rows))
+    cl = p.compress_len.numpy()
+    fi = fi.cpu().numpy()
+    for t in range(rows):
+        want = np.sort(np.argsort(-ref[t][: int(cl[t])], kind="stable")[:topk])
+        assert fi[t].tolist() == want.tolist(), t
+        Hp.check_topk_row(fi[t], ref[t], int(cl[t]), topk)
+    return fi
+
+
+def test_sampled_threshold_too_high_falls_back_to_the_stream():
+    """The sampled tiles hold the highest scores, so each row's threshold (the rank-th
+    sample) lets fewer than k keys through: every row is decided again by the stream."""
+    L, rows, topk = 16384, 24, 1024
+    p = _structured_problem(L, rows, topk, _sampled_tiles_scores(L, 4, True))
+    plan = Hp.make_plan(p)
+    assert plan.info()["sample_stride"] == 4
+    _check_structured_topk(p, plan, rows, topk)
+
+
+def test_sampled_threshold_too_low_overflows_and_falls_back():
+    """The sampled tiles hold the lowest scores, so three quarters of every row pass the
+    threshold and the lists overflow: the stream decides every row again."""
+    L, rows, topk = 16384, 24, 64
+    p = _structured_problem(L, rows, topk, _sampled_tiles_scores(L, 4, False))
+    plan = Hp.make_plan(p)
+    assert plan.info()["sample_stride"] == 4
+    _check_structured_topk(p, plan, rows, topk)
 
 
 # ------------------------------------------------------------- candidates
