@@ -59,18 +59,20 @@ struct Cfg {
     static constexpr int KBYTES = kTileKeys * D;       // K tile
     static constexpr int STAGES = (D >= 128) ? 6 : 8;
     static constexpr int KSTEPS = D / 32;              // MMA K = 32 elements
-    static constexpr int RPH = G / 2;                  // rows of one column half
-    static constexpr int HALF_COLS = N / 2;
-    static constexpr int NCH = HALF_COLS / 32;         // 32-column chunks per half
+    static constexpr int NPART = kEpiWarps / 4;        // column parts (4 warps each)
+    static constexpr int RPH = G / NPART;              // rows of one column part
+    static constexpr int HALF_COLS = N / NPART;        // columns of one column part
+    static constexpr int NCH = HALF_COLS / 32;         // 32-column chunks per part
     static constexpr int ACC_COLS = N;                 // TMEM columns per accumulator
     static constexpr int SF_BYTES = KFMT == kKeyFp4 ? kTileKeys * 16 : 0;  // per stage
     static constexpr int TMEM_SFA = 2 * ACC_COLS;      // 4 columns per stage
     static constexpr int TMEM_SFB = TMEM_SFA + 4 * STAGES;
     static constexpr bool STREAM = SINK != kSinkLogits;
     static_assert(D == 32 || D == 64 || D == 128, "D must be 32, 64 or 128");
-    static_assert(G >= 2 && G % 2 == 0 && N % 16 == 0, "H must leave an even row count");
-    static_assert(HALF_COLS % 32 == 0, "half tile must be whole 32-column loads");
-    static_assert(H >= 8 && (RPH == 2 || RPH == 4 || RPH == 8),
+    static_assert(G >= 2 && N % 16 == 0, "H must leave at least two rows per tile");
+    static_assert(G % NPART == 0 && HALF_COLS % 32 == 0,
+                  "a column part must be whole rows and whole 32-column loads");
+    static_assert(H >= 8 && (RPH == 1 || RPH == 2 || RPH == 4 || RPH == 8),
                   "the epilogue's head split needs 8..64 heads");
     static_assert(!STREAM || G <= 16, "streamed selection keeps at most 16 rows per CTA");
     // shared memory carve-up (offsets from a 1024-byte aligned base)
@@ -84,7 +86,7 @@ struct Cfg {
     static constexpr int ROWS_BYTES = STREAM ? G * 32 : 0;
     static constexpr int OFF_SEL = OFF_ROWS + ROWS_BYTES;            // compaction scratch x2
     static constexpr int SEL_ONE = (int)((sizeof(SelScratch<kHalfThreads>) + 15) / 16 * 16);
-    static constexpr int SEL_BYTES = STREAM ? 2 * SEL_ONE : 0;
+    static constexpr int SEL_BYTES = STREAM ? NPART * SEL_ONE : 0;
     static constexpr int OFF_BAR = OFF_SEL + SEL_BYTES;
     static constexpr int NBARS = 2 + 2 + 2 * STAGES + 2 + 2 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
@@ -93,7 +95,7 @@ struct Cfg {
 
 // Per-row state of the streamed selection (shared memory, one per row of the group).
 struct RowState {
-    uint32_t wcnt[4];  // entries each epilogue warp of the half appended to its sub-list
+    uint32_t wcnt[4];  // entries each epilogue warp of the row's column part appended
     uint32_t tau_hi;   // candidate iff (ord(score), ~index) >= (tau_hi, tau_lo)
     uint32_t tau_lo;
     uint32_t b1;       // boundary bin of the top-byte histogram (256 = none yet)
@@ -492,9 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // finished by a reduce-scatter over the four q lanes.
         const int ew = warp - 4;                 // 0..7
         const int quad = warp & 3;               // TMEM lane quadrant of this warp
-        const int half = ew >> 2;                // column half: rows [half*RPH, +RPH)
+        const int half = ew >> 2;                // column part: rows [half*RPH, +RPH)
         const int etid = ew * 32 + lane;         // 0..255
-        const int htid = quad * 32 + lane;       // 0..127 within the half
+        const int htid = quad * 32 + lane;       // 0..127 within the column part
         const int g = lane >> 2;
         const int q = lane & 3;
         constexpr int RPH = C::RPH;
@@ -503,12 +505,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int NK = RPH >= 4 ? 4 : RPH;       // key slots a thread finishes
         constexpr int NLD = 2 * C::NCH;          // 16-lane x 32-column loads per tile
         // finished value m: f = q * RPH + m = rr * 4 + slot-in-row, rr = f / 4
-        auto own_rr = [&](int ro) { return RPH >= 4 ? q * (RPH / 4) + ro : (q >> 1); };
-        auto slot_bl = [&](int s) { return RPH >= 4 ? s : ((2 * q + s) & 3); };
+        auto own_rr = [&](int ro) { return RPH >= 4 ? q * (RPH / 4) + ro : (q * RPH) >> 2; };
+        auto slot_bl = [&](int s) { return RPH >= 4 ? s : ((q * RPH + s) & 3); };
         // lanes that finish the same rows as this one
-        const uint32_t rowmask = RPH >= 4 ? (0x11111111u << q) : (0x33333333u << (q & 2));
-        const bool row_leader = g == 0 && (RPH >= 4 || (q & 1) == 0);
+        const uint32_t rowmask = RPH >= 4   ? (0x11111111u << q)
+                                 : RPH == 2 ? (0x33333333u << (q & 2))
+                                            : 0xFFFFFFFFu;
+        const bool row_leader = g == 0 && (RPH >= 4 || (q & (4 / RPH - 1)) == 0);
         const NamedSync half_sync{2 + half, kHalfThreads};
+        const NamedSync epi_sync{1, kEpiWarps * 32};
         SelScratch<kHalfThreads>* sel_s =
             reinterpret_cast<SelScratch<kHalfThreads>*>(smem + C::OFF_SEL + half * C::SEL_ONE);
         int ab = 0, aph = 0, it = 0;
@@ -543,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rs.compact = 0;
                 }
             }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
+            epi_sync();
             // the rows this thread finishes
             int clen[RO];
             uint32_t tau_hi[RO], tau_lo[RO], b1[RO], wcnt[RO];
@@ -619,13 +624,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // multiply with 2^-25 (FMA pipe) for column 2q + 1, whose weight
                         // carries 2^25; every product and sum is bit-identical to
                         // fmaf(c, max(S, 0), part).
-                        float2 part[RPH][2][2];
+                        float2 acc2[RPH][2][2];
 #pragma unroll
                         for (int r = 0; r < RPH; ++r)
 #pragma unroll
                             for (int b2 = 0; b2 < 2; ++b2) {
-                                part[r][b2][0] = make_float2(0.0f, 0.0f);
-                                part[r][b2][1] = make_float2(0.0f, 0.0f);
+                                acc2[r][b2][0] = make_float2(0.0f, 0.0f);
+                                acc2[r][b2][1] = make_float2(0.0f, 0.0f);
                             }
                         const uint32_t tbase = tmem_base +
                                                (static_cast<uint32_t>(quad * 32) << 16) +
@@ -653,8 +658,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                               relu_scaled(cur[4 * k + 1]));
                                 const float2 hi = make_float2(fmaxf(cur[4 * k + 2], 0.0f),
                                                               relu_scaled(cur[4 * k + 3]));
-                                part[r][blk][0] = __ffma2_rn(c2, lo, part[r][blk][0]);
-                                part[r][blk][1] = __ffma2_rn(c2, hi, part[r][blk][1]);
+                                acc2[r][blk][0] = __ffma2_rn(c2, lo, acc2[r][blk][0]);
+                                acc2[r][blk][1] = __ffma2_rn(c2, hi, acc2[r][blk][1]);
                             }
                             if (ld + 1 < NLD)
                                 tmem_wait_ld();
@@ -677,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                                 for (int l2 = 0; l2 < 2; ++l2)
                                     pf[r * 4 + b2 * 2 + l2] =
-                                        part[r][b2][l2].x + part[r][b2][l2].y;
+                                        acc2[r][b2][l2].x + acc2[r][b2][l2].y;
                         float rs1[F / 2];
 #pragma unroll
                         for (int x = 0; x < F / 2; ++x) {
@@ -936,7 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 // both halves are done with the row state before the next unit resets it
-                asm volatile("bar.sync 1, 256;" ::: "memory");
+                epi_sync();
             }
         }
     }
