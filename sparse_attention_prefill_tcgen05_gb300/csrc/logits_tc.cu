@@ -534,7 +534,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float cv = rl < ui.nr ? p.w[o] * p.s_q[o] : 0.0f;
                 cbuf[etid] = (etid & 1) ? cv * 33554432.0f : cv;
             }
-            const float2* cw = reinterpret_cast<const float2*>(cbuf + half * C::HALF_COLS) + q;
             if constexpr (C::STREAM) {
                 for (int i = etid; i < C::G * 512; i += kEpiWarps * 32)
                     hist_s[i] = 0;
@@ -549,6 +548,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             epi_sync();
+            // this thread's head weights: columns 2q, 2q + 1 of every 8-column group
+            float2 cw[C::NCH * 4];
+#pragma unroll
+            for (int gi = 0; gi < C::NCH * 4; ++gi)
+                cw[gi] = reinterpret_cast<const float2*>(cbuf + half * C::HALF_COLS)[gi * 4 + q];
             // the rows this thread finishes
             int clen[RO];
             uint32_t tau_hi[RO], tau_lo[RO], b1[RO], wcnt[RO];
@@ -561,7 +565,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 b1[ro] = 256;
                 wcnt[ro] = 0;
                 if constexpr (SINK == kSinkFilter) {
-                    tau_hi[ro] = rl < ui.nr ? p.tau_row[ui.t0 + rl] : 0u;
+                    // as a float: v >= it <=> ord(v) >= tau for every v but -0.0 against
+                    // tau = ord(+0.0), which only lets -0.0 entries through as well (still
+                    // every entry at or above a threshold); tau = 0 passes every finite v
+                    const uint32_t tr = rl < ui.nr ? p.tau_row[ui.t0 + rl] : 0u;
+                    tau_hi[ro] = tr > kOrdNegInf ? __float_as_uint(ord2f(tr))
+                                                 : 0xFF7FFFFFu;   // -FLT_MAX
                 } else if constexpr (C::STREAM) {
                     tau_hi[ro] = rows_s[rl].tau_hi;
                     tau_lo[ro] = rows_s[rl].tau_lo;
@@ -653,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
                                 const int r = (ch * 32 + 8 * k) / H;
-                                const float2 c2 = cw[(ch * 4 + k) * 4];
+                                const float2 c2 = cw[ch * 4 + k];
                                 const float2 lo = make_float2(fmaxf(cur[4 * k + 0], 0.0f),
                                                               relu_scaled(cur[4 * k + 1]));
                                 const float2 hi = make_float2(fmaxf(cur[4 * k + 2], 0.0f),
@@ -747,8 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int ro = RPH >= 4 ? (m >> 2) : 0;
                         const int rl = half * RPH + own_rr(ro);
                         const int j = jt + 8 * slot_bl(RPH >= 4 ? (m & 3) : m) + g;
-                        const uint32_t o = f2ord(val[m]);
-                        const bool cand = rl < ui.nr && o > kOrdNegInf && o >= tau_hi[ro];
+                        const bool cand = rl < ui.nr && val[m] >= __uint_as_float(tau_hi[ro]);
                         const uint32_t mb = __ballot_sync(0xffffffffu, cand) & rowmask;
                         if (cand) {
                             const uint32_t pos = wcnt[ro] + __popc(mb & ((1u << lane) - 1u));
