@@ -60,11 +60,12 @@ __device__ __forceinline__ void hist_add_aggregated(uint32_t* hist, uint32_t dig
 // this (tid in [0, NT)).
 template <int NT, class Sync, class Load>
 __device__ CompositeThr group_threshold(SelScratch<NT>& sh, int tid, int n, uint32_t k,
-                                        const Load& load, const Sync& sync)
+                                        const Load& load, const Sync& sync, int max_passes = 8,
+                                        uint32_t* eligible = nullptr)
 {
     CompositeThr thr{0u, 0u, 0u, 0u};
     uint32_t remaining = k;
-    for (int pass = 0; pass < 8; ++pass) {
+    for (int pass = 0; pass < max_passes; ++pass) {
         const bool in_hi = pass < 4;
         const int shift = 24 - 8 * (pass & 3);
         for (int i = tid; i < 256; i += NT)
@@ -98,6 +99,8 @@ __device__ CompositeThr group_threshold(SelScratch<NT>& sh, int tid, int n, uint
                     suf += y;
             }
             const uint32_t total = __shfl_sync(0xffffffffu, suf, 0);
+            if (pass == 0 && lane == 0)
+                sh.bcast[3] = total;
             const uint32_t holders = __ballot_sync(0xffffffffu, suf >= remaining);
             if (total <= remaining) {
                 if (lane == 0) {
@@ -127,6 +130,8 @@ __device__ CompositeThr group_threshold(SelScratch<NT>& sh, int tid, int n, uint
         const uint32_t flag = sh.bcast[0];
         const uint32_t bin = sh.bcast[1];
         const uint32_t above = sh.bcast[2];
+        if (pass == 0 && eligible)
+            *eligible = sh.bcast[3];
         sync();
         if (flag == 1)
             break;  // the current prefix already keeps exactly what must be kept

@@ -112,6 +112,7 @@ struct UnitInfo {
     int jend;      // request-local end of keys covered by the unit
     int ntiles;    // tiles covering [j0, jend)
     int ntiles_mma;
+    bool skip;     // second pass: no row of the group needs it
 };
 
 // Decode a unit number.  Units run chunk-major inside a segment so that the
@@ -128,6 +129,7 @@ __device__ __forceinline__ UnitInfo decode_unit(const LogitsParams& p, int u, in
     const int chunk = local / sg.n_row_groups;
     const int g = local - chunk * sg.n_row_groups;
     const int step = (sg.tile_stride > 0 ? sg.tile_stride : 1) * kTileKeys;   // tile to tile
+    ui.skip = false;
     ui.seg = s;
     ui.t0 = sg.row_begin + g * G;
     ui.nr = min(G, sg.row_begin + sg.nrows - ui.t0);
@@ -154,6 +156,7 @@ __device__ __forceinline__ UnitInfo decode_unit(const LogitsParams& p, int u, in
         if (!__any_sync(0xffffffffu, any)) {
             ui.ntiles = 0;
             ui.ntiles_mma = 0;
+            ui.skip = true;
         }
     }
     return ui;
@@ -936,8 +939,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if constexpr (C::STREAM) {
                 // unit end: every warp publishes its own sub-list lengths (also for
-                // units with no tiles)
-                if (row_leader) {
+                // units with no tiles; not for units a second pass skips, whose rows
+                // keep the first pass's lists)
+                if (row_leader && !ui.skip) {
 #pragma unroll
                     for (int ro = 0; ro < RO; ++ro) {
                         const int rl = half * RPH + own_rr(ro);

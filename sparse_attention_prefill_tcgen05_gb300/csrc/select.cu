@@ -104,6 +104,31 @@ __device__ uint32_t block_exclusive_sum(uint32_t v, Scratch& sh)
     __syncthreads();
     return wbefore + incl - v;
 }
+// wpre[w] = set bits in bits[0, w); returns the total.  All threads call.
+__device__ int bitmap_prefix(const uint32_t* bits, uint32_t* wpre, int nw, Scratch& sh,
+                             int& s_total)
+{
+    constexpr int kPer = kBitmapWords / kSelThreads;   // consecutive words per thread
+    const int w0 = threadIdx.x * kPer;
+    uint32_t local = 0;
+#pragma unroll
+    for (int w = 0; w < kPer; ++w)
+        local += w0 + w < nw ? __popc(bits[w0 + w]) : 0u;
+    const uint32_t before = block_exclusive_sum(local, sh);
+    uint32_t run = before;
+#pragma unroll
+    for (int w = 0; w < kPer; ++w) {
+        if (w0 + w < nw) {
+            wpre[w0 + w] = run;
+            run += __popc(bits[w0 + w]);
+        }
+    }
+    if (threadIdx.x == kSelThreads - 1)
+        s_total = static_cast<int>(run);
+    __syncthreads();
+    return s_total;
+}
+
 constexpr int kStageEntries = 7168;   // candidates staged in shared memory per row (56 KB)
 static_assert(kStageEntries * 8 >= kBitmapWords * 8, "the bitmap reuses the staging area");
 
@@ -124,6 +149,7 @@ __global__ void __launch_bounds__(kSelThreads)
 
     __shared__ int32_t s_staged;
     __shared__ int32_t s_overflow;
+    __shared__ int s_total;
     if (threadIdx.x == 0)
         s_overflow = 0;
     __syncthreads();
@@ -181,31 +207,81 @@ __global__ void __launch_bounds__(kSelThreads)
     }
     // copy the entries that pass the floor into shared memory (order is irrelevant:
     // the selection is by unique composite keys); every radix pass reads them there
-    for (int s = 0; s < nslots; ++s) {
-        const uint2* src = p.lists + lbase + (int64_t)s * pc.cap;
-        const int c = s_off[s + 1] - s_off[s];
-        for (int i0 = 0; i0 < c; i0 += kSelThreads) {
-            const int i = i0 + threadIdx.x;
-            uint2 ent = make_uint2(0u, 0u);
-            bool pass = false;
-            if (i < c) {
-                ent = src[i];
-                pass = f2ord(__uint_as_float(ent.x)) >= floor_ord;
+    // (one warp per sub-list, so the sub-lists' loads are in flight together)
+    {
+        const int lane = threadIdx.x & 31;
+        for (int s = threadIdx.x >> 5; s < nslots; s += kSelThreads / 32) {
+            const uint2* src = p.lists + lbase + (int64_t)s * pc.cap;
+            const int c = s_off[s + 1] - s_off[s];
+            for (int i0 = 0; i0 < c; i0 += 32) {
+                const int i = i0 + lane;
+                uint2 ent = make_uint2(0u, 0u);
+                bool pass = false;
+                if (i < c) {
+                    ent = src[i];
+                    pass = f2ord(__uint_as_float(ent.x)) >= floor_ord;
+                }
+                const uint32_t m = __ballot_sync(0xffffffffu, pass);
+                int base = 0;
+                if (lane == 0 && m)
+                    base = atomicAdd(&s_staged, __popc(m));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                const int pos = base + __popc(m & ((1u << lane) - 1u));
+                if (pass && pos < kStageEntries)
+                    stage[pos] = ent;
             }
-            const uint32_t m = __ballot_sync(0xffffffffu, pass);
-            int base = 0;
-            if ((threadIdx.x & 31) == 0 && m)
-                base = atomicAdd(&s_staged, __popc(m));
-            base = __shfl_sync(0xffffffffu, base, 0);
-            const int pos = base + __popc(m & ((1u << (threadIdx.x & 31)) - 1u));
-            if (pass && pos < kStageEntries)
-                stage[pos] = ent;
         }
     }
     __syncthreads();
     const bool staged = s_staged <= kStageEntries;
     const int n = staged ? s_staged : n_all;
     const int k = p.k;
+    if (staged && !p.mask && p.bitmap_words > 0 && p.bitmap_words <= kBitmapWords) {
+        // threshold over the staged entries, then the kept keys in ascending order
+        // straight from a bitmap: no ordered emission, no sort
+        auto load = [&](int e, uint32_t& hi, uint32_t& lo) {
+            const uint2 ent = stage[e];
+            hi = f2ord(__uint_as_float(ent.x));
+            lo = ~ent.y;
+        };
+        const CompositeThr thr =
+            group_threshold<kSelThreads>(sh, threadIdx.x, n, static_cast<uint32_t>(k), load,
+                                         CtaSync{});
+        uint32_t* bits = reinterpret_cast<uint32_t*>(skey);
+        uint32_t* wpre = bits + kBitmapWords;
+        const int nw = p.bitmap_words;
+        for (int w = threadIdx.x; w < nw; w += kSelThreads)
+            bits[w] = 0;
+        __syncthreads();
+        for (int e = threadIdx.x; e < n; e += kSelThreads) {
+            uint32_t hi, lo;
+            load(e, hi, lo);
+            if (hi > kOrdNegInf && thr.kept(hi, lo))
+                atomicOr(&bits[(~lo) >> 5], 1u << ((~lo) & 31));
+        }
+        __syncthreads();
+        const int total = bitmap_prefix(bits, wpre, nw, sh, s_total);
+        int32_t* oi = p.out_idx + (int64_t)t * k;
+        float* ov = p.out_val ? p.out_val + (int64_t)t * k : nullptr;
+        for (int e = threadIdx.x; e < n; e += kSelThreads) {
+            uint32_t hi, lo;
+            load(e, hi, lo);
+            if (hi > kOrdNegInf && thr.kept(hi, lo)) {
+                const uint32_t j = ~lo;
+                const int pos = static_cast<int>(wpre[j >> 5] +
+                                                 __popc(bits[j >> 5] & ((1u << (j & 31)) - 1u)));
+                oi[pos] = static_cast<int32_t>(j);
+                if (ov)
+                    ov[pos] = ord2f(hi);
+            }
+        }
+        for (int i = total + threadIdx.x; i < k; i += kSelThreads) {
+            oi[i] = -1;
+            if (ov)
+                ov[i] = -INFINITY;
+        }
+        return;
+    }
     for (int i = threadIdx.x; i < n2; i += kSelThreads) {
         skey[i] = INT32_MAX;
         sval[i] = -INFINITY;
@@ -268,22 +344,7 @@ __global__ void __launch_bounds__(kSelThreads)
         for (int i = threadIdx.x; i < count; i += kSelThreads)
             atomicOr(&bits[skey[i] >> 5], 1u << (skey[i] & 31));
         __syncthreads();
-        constexpr int kPer = kBitmapWords / kSelThreads;   // consecutive words per thread
-        const int w0 = threadIdx.x * kPer;
-        uint32_t local = 0;
-#pragma unroll
-        for (int w = 0; w < kPer; ++w)
-            local += w0 + w < nw ? __popc(bits[w0 + w]) : 0u;
-        const uint32_t before = block_exclusive_sum(local, sh);
-        uint32_t run = before;
-#pragma unroll
-        for (int w = 0; w < kPer; ++w) {
-            if (w0 + w < nw) {
-                wpre[w0 + w] = run;
-                run += __popc(bits[w0 + w]);
-            }
-        }
-        __syncthreads();
+        bitmap_prefix(bits, wpre, nw, sh, s_total);
         for (int i = threadIdx.x; i < count; i += kSelThreads) {
             const int j = skey[i];
             const int pos = static_cast<int>(wpre[j >> 5] +
@@ -310,40 +371,26 @@ __global__ void __launch_bounds__(kSelThreads)
 
 // ------------------------------------------------- sampled row thresholds
 
-// tau[t] = ord of the rank-th largest finite sample of row t (the rank-th
-// largest composite key, ties to the lower sample position), or 0 when the
-// row has fewer than rank finite samples.
+// tau[t] = the rank-th largest finite sample of row t rounded down to its top
+// 16 bits (two radix passes), or 0 when the row has fewer than rank finite
+// samples.  Any threshold keeps the selection exact (rows the lists cannot
+// decide are selected again); this one lets at least rank samples through.
 __global__ void __launch_bounds__(kSelThreads)
     sample_threshold_kernel(const float* samples, int64_t ld, int rank, uint32_t* tau_row)
 {
     __shared__ Scratch sh;
-    __shared__ uint32_t s_min;
     const int t = blockIdx.x;
     const float* row = samples + (int64_t)t * ld;
     auto load = [&](int e, uint32_t& hi, uint32_t& lo) {
         hi = f2ord(row[e]);
         lo = ~static_cast<uint32_t>(e);
     };
-    const int n = static_cast<int>(ld);
-    const CompositeThr thr =
-        group_threshold<kSelThreads>(sh, threadIdx.x, n, static_cast<uint32_t>(rank), load, CtaSync{});
+    uint32_t eligible = 0;
+    const CompositeThr thr = group_threshold<kSelThreads>(
+        sh, threadIdx.x, static_cast<int>(ld), static_cast<uint32_t>(rank), load, CtaSync{}, 2,
+        &eligible);
     if (threadIdx.x == 0)
-        s_min = 0xFFFFFFFFu;
-    __syncthreads();
-    uint32_t mn = 0xFFFFFFFFu, cnt = 0;
-    for (int e = threadIdx.x; e < n; e += kSelThreads) {
-        uint32_t hi, lo;
-        load(e, hi, lo);
-        if (hi > kOrdNegInf && thr.kept(hi, lo)) {
-            mn = min(mn, hi);
-            ++cnt;
-        }
-    }
-    atomicMin(&s_min, mn);
-    const uint32_t kept = block_exclusive_sum(cnt, sh) + cnt;   // inclusive
-    __syncthreads();
-    if (threadIdx.x == kSelThreads - 1)
-        tau_row[t] = kept >= static_cast<uint32_t>(rank) ? s_min : 0u;
+        tau_row[t] = eligible >= static_cast<uint32_t>(rank) ? (thr.phi & thr.mhi) : 0u;
 }
 
 // ------------------------------------------------------- standalone top-k
@@ -386,7 +433,8 @@ cudaError_t launch_stream_merge(const StreamMergeParams& p, cudaStream_t stream)
     int n2 = 1;
     while (n2 < p.k)
         n2 <<= 1;
-    const size_t dyn = sizeof(uint2) * kStageEntries + (sizeof(int32_t) + sizeof(float)) * n2;
+    const size_t dyn = sizeof(uint2) * kStageEntries +
+                       std::max<size_t>((sizeof(int32_t) + sizeof(float)) * n2, 8 * kBitmapWords);
     cudaError_t e = cudaFuncSetAttribute(stream_merge_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
     if (e != cudaSuccess)
