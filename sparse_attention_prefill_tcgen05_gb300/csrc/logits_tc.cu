@@ -515,6 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  : RPH == 2 ? (0x33333333u << (q & 2))
                                             : 0xFFFFFFFFu;
         const bool row_leader = g == 0 && (RPH >= 4 || (q & (4 / RPH - 1)) == 0);
+        const uint32_t lanes_below = (1u << lane) - 1u;
         const NamedSync half_sync{2 + half, kHalfThreads};
         const NamedSync epi_sync{1, kEpiWarps * 32};
         SelScratch<kHalfThreads>* sel_s =
@@ -578,6 +579,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tau_hi[ro] = rows_s[rl].tau_hi;
                     tau_lo[ro] = rows_s[rl].tau_lo;
                 }
+            }
+            // this warp's sub-list of each row the thread finishes
+            uint2* sub_own[RO];
+#pragma unroll
+            for (int ro = 0; ro < RO; ++ro) {
+                const int rl = half * RPH + own_rr(ro);
+                sub_own[ro] = p.lists + sg.out_offset +
+                              (int64_t)(ui.t0 + rl - sg.row_begin) * sg.out_ld +
+                              (int64_t)quad * p.cap;
             }
             // smallest causal length among the half's rows (rows past nr are never
             // stored or selected)
@@ -762,11 +772,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const bool cand = rl < ui.nr && val[m] >= __uint_as_float(tau_hi[ro]);
                         const uint32_t mb = __ballot_sync(0xffffffffu, cand) & rowmask;
                         if (cand) {
-                            const uint32_t pos = wcnt[ro] + __popc(mb & ((1u << lane) - 1u));
+                            const uint32_t pos = wcnt[ro] + __popc(mb & lanes_below);
                             if (pos < static_cast<uint32_t>(p.cap))
-                                p.lists[sg.out_offset +
-                                        (int64_t)(ui.t0 + rl - sg.row_begin) * sg.out_ld +
-                                        (int64_t)quad * p.cap + pos] =
+                                sub_own[ro][pos] =
                                     make_uint2(__float_as_uint(val[m]), static_cast<uint32_t>(j));
                         }
                         wcnt[ro] += __popc(mb);

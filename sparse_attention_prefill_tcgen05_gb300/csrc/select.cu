@@ -213,22 +213,29 @@ __global__ void __launch_bounds__(kSelThreads)
         for (int s = threadIdx.x >> 5; s < nslots; s += kSelThreads / 32) {
             const uint2* src = p.lists + lbase + (int64_t)s * pc.cap;
             const int c = s_off[s + 1] - s_off[s];
-            for (int i0 = 0; i0 < c; i0 += 32) {
-                const int i = i0 + lane;
-                uint2 ent = make_uint2(0u, 0u);
-                bool pass = false;
-                if (i < c) {
-                    ent = src[i];
-                    pass = f2ord(__uint_as_float(ent.x)) >= floor_ord;
+            for (int i0 = 0; i0 < c; i0 += 32 * 8) {
+                // eight loads in flight per lane before any of them is used
+                uint2 ent[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + u * 32 + lane;
+                    ent[u] = i < c ? src[i] : make_uint2(0u, 0u);
                 }
-                const uint32_t m = __ballot_sync(0xffffffffu, pass);
-                int base = 0;
-                if (lane == 0 && m)
-                    base = atomicAdd(&s_staged, __popc(m));
-                base = __shfl_sync(0xffffffffu, base, 0);
-                const int pos = base + __popc(m & ((1u << lane) - 1u));
-                if (pass && pos < kStageEntries)
-                    stage[pos] = ent;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + u * 32 + lane;
+                    const bool pass = i < c && f2ord(__uint_as_float(ent[u].x)) >= floor_ord;
+                    const uint32_t m = __ballot_sync(0xffffffffu, pass);
+                    if (m == 0)
+                        continue;
+                    int base = 0;
+                    if (lane == 0)
+                        base = atomicAdd(&s_staged, __popc(m));
+                    base = __shfl_sync(0xffffffffu, base, 0);
+                    const int pos = base + __popc(m & ((1u << lane) - 1u));
+                    if (pass && pos < kStageEntries)
+                        stage[pos] = ent[u];
+                }
             }
         }
     }
@@ -379,10 +386,15 @@ __global__ void __launch_bounds__(kSelThreads)
     sample_threshold_kernel(const float* samples, int64_t ld, int rank, uint32_t* tau_row)
 {
     __shared__ Scratch sh;
+    extern __shared__ __align__(16) float srow[];
     const int t = blockIdx.x;
     const float* row = samples + (int64_t)t * ld;
+    // the row once into shared memory (ld is a multiple of 128: float4 loads)
+    for (int e = threadIdx.x; e < static_cast<int>(ld) / 4; e += kSelThreads)
+        reinterpret_cast<float4*>(srow)[e] = reinterpret_cast<const float4*>(row)[e];
+    __syncthreads();
     auto load = [&](int e, uint32_t& hi, uint32_t& lo) {
-        hi = f2ord(row[e]);
+        hi = f2ord(srow[e]);
         lo = ~static_cast<uint32_t>(e);
     };
     uint32_t eligible = 0;
@@ -448,7 +460,10 @@ cudaError_t launch_sample_threshold(const float* samples, int64_t ld, int rows, 
 {
     if (rows <= 0)
         return cudaSuccess;
-    sample_threshold_kernel<<<rows, kSelThreads, 0, stream>>>(samples, ld, rank, tau_row);
+    if (ld % 4 != 0 || ld > 16384)
+        return cudaErrorInvalidValue;
+    sample_threshold_kernel<<<rows, kSelThreads, ld * sizeof(float), stream>>>(samples, ld, rank,
+                                                                             tau_row);
     return cudaGetLastError();
 }
 
