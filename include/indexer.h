@@ -258,6 +258,14 @@ int indexer_fused_topk_noalloc(indexer_plan_t plan, const void* q, const float* 
    diagnostic counter for benchmarks; never reset). */
 long long indexer_launch_count(void);
 
+/* Benchmark diagnostic: while set, every indexer_fused_topk /
+   indexer_candidate_blocks call records start_event (a cudaEvent_t) on its
+   stream just before the first list-filling logits launch of its first pass
+   and stop_event just after it, so the caller can time the dominant kernel
+   inside a step.  NULL, NULL turns it off.  Process-wide, not thread-safe;
+   the events are owned by the caller. */
+void indexer_profile_main_kernel(void* start_event, void* stop_event);
+
 const char* indexer_error_string(int status);
 int indexer_version(void);
 

@@ -34,7 +34,7 @@ EXPORTED = ("indexer_plan", "indexer_plan_destroy", "indexer_plan_info", "indexe
             "indexer_topk", "indexer_fused_topk", "indexer_candidate_blocks",
             "indexer_expand_mask", "indexer_status", "indexer_selftest_timeout",
             "indexer_set_wait_budget", "indexer_launch_count", "indexer_error_string",
-            "indexer_version", "indexer_fused_topk_noalloc")
+            "indexer_version", "indexer_fused_topk_noalloc", "indexer_profile_main_kernel")
 IDX_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -88,6 +88,8 @@ def lib():
         L.indexer_selftest_timeout.argtypes = [P, ctypes.c_longlong, P]
         L.indexer_set_wait_budget.argtypes = [P, ctypes.c_longlong]
         L.indexer_launch_count.argtypes = []
+        L.indexer_profile_main_kernel.argtypes = [P, P]
+        L.indexer_profile_main_kernel.restype = None
         L.indexer_fused_topk_noalloc.argtypes = [P, P, P, P, P, P, P, P, i64, P, P, P]
         L.indexer_error_string.argtypes = [i32]
         L.indexer_error_string.restype = ctypes.c_char_p
@@ -228,6 +230,13 @@ def indexer_fused_topk_noalloc(plan: Plan, q, s_q, w, k, k_scale, compress_len, 
 
 def indexer_launch_count() -> int:
     return int(lib().indexer_launch_count())
+
+
+def indexer_profile_main_kernel(start_event=None, stop_event=None):
+    """Record two torch.cuda.Event (already created, timing enabled) around the main
+    logits launch of the following top-k calls; no arguments turns it off."""
+    h = lambda e: ctypes.c_void_p(e.cuda_event) if e is not None else None
+    lib().indexer_profile_main_kernel(h(start_event), h(stop_event))
 
 
 def indexer_version() -> int:

@@ -63,6 +63,8 @@ struct indexer_plan_s {
 namespace {
 
 std::atomic<long long> g_launches{0};  // kernels launched by this library (diagnostic)
+// events recorded around the main logits launch of the next top-k calls (diagnostic)
+std::atomic<void*> g_prof_start{nullptr}, g_prof_stop{nullptr};
 
 constexpr size_t kStatusBytes = 256;
 constexpr uint64_t kDefaultBudget = 2ull << 30;
@@ -330,6 +332,13 @@ int pass_launches(Ctx& c, const Pass& ps, const std::vector<int32_t>& cap, int s
     return flush();
 }
 
+void record_prof(Ctx& c, std::atomic<void*>& ev)
+{
+    void* e = ev.load(std::memory_order_relaxed);
+    if (e)
+        cudaEventRecord(static_cast<cudaEvent_t>(e), c.st);
+}
+
 int launch_merge(Ctx& c, StreamMergeParams& mp)
 {
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -426,8 +435,11 @@ int run_streamed(Ctx& c, uint8_t* ws, int pool, int32_t* out_idx, float* out_val
                 return rc;
             lp.tau_row = tau_row;
             lp.row_fail = nullptr;
+            const bool prof = &ps == &passes.front();
+            if (prof) record_prof(c, g_prof_start);
             if ((rc = pass_launches(c, ps, cap, kSinkFilter, mp)) != IDX_OK)
                 return rc;
+            if (prof) record_prof(c, g_prof_stop);
             finish(mp);
             mp.gtau = nullptr;
             mp.verify = 1;
@@ -440,8 +452,11 @@ int run_streamed(Ctx& c, uint8_t* ws, int pool, int32_t* out_idx, float* out_val
         } else {
             lp.row_fail = nullptr;
         }
+        const bool prof = !sampled && &ps == &passes.front();
+        if (prof) record_prof(c, g_prof_start);
         if ((rc = pass_launches(c, ps, cap, pool ? kSinkPool : kSinkStream, mp)) != IDX_OK)
             return rc;
+        if (prof) record_prof(c, g_prof_stop);
         finish(mp);
         mp.gtau = lp.gtau;
         mp.verify = 0;
@@ -486,6 +501,12 @@ extern "C" {
 int indexer_version(void) { return 2; }
 
 long long indexer_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void indexer_profile_main_kernel(void* start_event, void* stop_event)
+{
+    g_prof_start.store(start_event, std::memory_order_relaxed);
+    g_prof_stop.store(stop_event, std::memory_order_relaxed);
+}
 
 const char* indexer_error_string(int s)
 {
