@@ -83,7 +83,8 @@ extern "C" {
  *   num_requests  R >= 1 (at most 256)
  *   total_rows    T = cu_seqlens_q[R];  total_keys = cu_seqlens_k[R]
  *   H, D          heads and head dim of q; k has D too.  Built shapes:
- *                 (H, D) in {(32,128), (16,128), (64,128), (8,64)}
+ *                 (H, D) in {(32,128), (16,128), (64,128), (8,64), (4,64)}; 4 heads run
+ *                 as 8 (zero-padded into the workspace, which adds exactly 0)
  *   topk          keys kept per row, 1 <= topk <= 2048
  *   cu_seqlens_q  [R+1] non-decreasing row offsets, starts at 0
  *   cu_seqlens_k  [R+1] non-decreasing key offsets, starts at 0

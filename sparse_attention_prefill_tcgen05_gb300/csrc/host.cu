@@ -36,6 +36,8 @@ constexpr int64_t kTargetUnits = 1024;   // units per launch wanted for load bal
 
 struct indexer_plan_s {
     int R = 0, T = 0, Lk = 0, H = 0, D = 0, topk = 0, kdtype = 0;
+    int kH = 0;                       // heads the kernels run with (H, or H padded with zero heads)
+    size_t off_pad = 0, pad_end = 0;  // padded q / s_q / w when kH != H
     int cand_block = 8, cand_topk = 0;
     int G = 8;                        // query rows per MMA tile
     std::vector<int32_t> row_begin;   // [R+1]
@@ -78,7 +80,7 @@ bool supported_shape(int H, int D, int kdtype)
     if (kdtype == IDX_K_FP4_E2M1_UE8M0)
         return false;
     return (H == 32 && D == 128) || (H == 16 && D == 128) || (H == 64 && D == 128) ||
-           (H == 8 && D == 64);
+           (H == 8 && D == 64) || (H == 4 && D == 64);
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -233,7 +235,7 @@ int fill_maps(Ctx& c, const void* q, const void* k)
 {
     const indexer_plan_s* p = c.p;
     std::memset(&c.lp, 0, sizeof(c.lp));
-    if (!make_map(&c.lp.tmap_q, q, (uint64_t)p->T * p->H, p->D, p->G * p->H))
+    if (!make_map(&c.lp.tmap_q, q, (uint64_t)p->T * p->kH, p->D, p->G * p->kH))
         return IDX_ERR_CUDA;
     const uint64_t krows = (uint64_t)std::max(p->Lk, 1);
     if (!make_map(&c.lp.tmap_k, k, krows, p->D, kTileKeys))
@@ -260,7 +262,7 @@ int run_logits(Ctx& c, std::vector<Segment>& segs, int sink)
         return IDX_OK;
     const int grid = std::min(units, c.sms);
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    return launch_logits(lp, p->H, p->D, p->kdtype, sink, grid, c.st) == cudaSuccess
+    return launch_logits(lp, p->kH, p->D, p->kdtype, sink, grid, c.st) == cudaSuccess
                ? IDX_OK
                : IDX_ERR_CUDA;
 }
@@ -494,6 +496,32 @@ void set_inputs(Ctx& c, const float* s_q, const float* w, const void* k_scale,
     c.lp.mask_block = c.p->cand_block;
 }
 
+// Tensor maps and input pointers of a call; pads the heads first when the
+// kernels run with more heads than the problem has.
+int prepare(Ctx& c, const void* q, const float* s_q, const float* w, const void* k,
+            const void* k_scale, const int32_t* clen, void* ws)
+{
+    const indexer_plan_s* p = c.p;
+    if (p->kH != p->H) {
+        uint8_t* base = static_cast<uint8_t*>(ws) + p->off_pad;
+        void* q_pad = base;
+        float* s_q_pad = reinterpret_cast<float*>(base + (size_t)p->T * p->kH * p->D);
+        float* w_pad = s_q_pad + (size_t)p->T * p->kH;
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        if (launch_pad_heads(q, s_q, w, q_pad, s_q_pad, w_pad, p->T, p->H, p->kH, p->D, c.st) !=
+            cudaSuccess)
+            return IDX_ERR_CUDA;
+        q = q_pad;
+        s_q = s_q_pad;
+        w = w_pad;
+    }
+    int rc = fill_maps(c, q, k);
+    if (rc != IDX_OK)
+        return rc;
+    set_inputs(c, s_q, w, k_scale, clen, ws);
+    return IDX_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -581,7 +609,9 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
         delete p;
         return IDX_ERR_UNSUPPORTED;
     }
-    p->G = logits_rows_per_group(p->H, p->kdtype);
+    // 4 heads run as 8 (zero heads 4..7 add exactly 0 to every logit)
+    p->kH = p->H == 4 ? 8 : p->H;
+    p->G = logits_rows_per_group(p->kH, p->kdtype);
     const int G = p->G;
 
     // Key splits: the caller's size, else the largest multiple of 128 that still
@@ -642,6 +672,10 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
                 p->sample_stride = 0;
     }
     size_t off = kStatusBytes;
+    p->off_pad = off;
+    if (p->kH != p->H)
+        off = align_up(off + (size_t)p->T * p->kH * (p->D + 8), 256);
+    p->pad_end = off;
     p->off_gtau = off;                       // [T] shared bound, then [T] row flags
     p->off_fail = off + (size_t)std::max(p->T, 1) * 4;
     off = align_up(p->off_fail + (size_t)std::max(p->T, 1) * 4, 256);
@@ -700,8 +734,10 @@ int indexer_logits(indexer_plan_t p, const void* q, const float* s_q, const floa
                    const void* k, const void* k_scale, const int32_t* clen, float* logits,
                    int64_t ld, void* ws, size_t ws_bytes, void* stream)
 {
-    if (!p || !ws || !aligned(ws, 256) || ws_bytes < kStatusBytes)
-        return ws_bytes < kStatusBytes && p && ws ? IDX_ERR_WORKSPACE : IDX_ERR_INVALID_ARG;
+    if (!p || !ws || !aligned(ws, 256))
+        return IDX_ERR_INVALID_ARG;
+    if (ws_bytes < p->pad_end)
+        return IDX_ERR_WORKSPACE;
     int rc = check_inputs(p, q, s_q, w, k, k_scale, clen);
     if (rc != IDX_OK)
         return rc;
@@ -712,9 +748,8 @@ int indexer_logits(indexer_plan_t p, const void* q, const float* s_q, const floa
         return rc;
     if (p->T == 0)
         return IDX_OK;
-    if ((rc = fill_maps(c, q, k)) != IDX_OK)
+    if ((rc = prepare(c, q, s_q, w, k, k_scale, clen, ws)) != IDX_OK)
         return rc;
-    set_inputs(c, s_q, w, k_scale, clen, ws);
     c.lp.out = logits;
     // key tiles per unit: enough units for every SM to get several
     int64_t work = 0;
@@ -801,9 +836,8 @@ int indexer_fused_topk(indexer_plan_t p, const void* q, const float* s_q, const 
         return rc;
     if (p->T == 0)
         return IDX_OK;
-    if ((rc = fill_maps(c, q, k)) != IDX_OK)
+    if ((rc = prepare(c, q, s_q, w, k, k_scale, clen, ws)) != IDX_OK)
         return rc;
-    set_inputs(c, s_q, w, k_scale, clen, ws);
     c.lp.cand_mask = cand_mask;
     c.lp.ld_mask = ld_mask;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
@@ -831,9 +865,8 @@ int indexer_candidate_blocks(indexer_plan_t p, const void* q, const float* s_q, 
         return rc;
     if (p->T == 0)
         return IDX_OK;
-    if ((rc = fill_maps(c, q, k)) != IDX_OK)
+    if ((rc = prepare(c, q, s_q, w, k, k_scale, clen, ws)) != IDX_OK)
         return rc;
-    set_inputs(c, s_q, w, k_scale, clen, ws);
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     if (cudaMemsetAsync(wsb + p->off_gtau, 0, (size_t)p->T * 4, c.st) != cudaSuccess)
         return IDX_ERR_CUDA;

@@ -153,5 +153,8 @@ cudaError_t launch_expand_mask(const uint8_t* cand_mask, int64_t ld_mask, const 
                                uint8_t* key_mask, int64_t ld, int block, int rows,
                                cudaStream_t st);
 cudaError_t launch_selftest_timeout(uint32_t* status, long long cycles, cudaStream_t st);
+cudaError_t launch_pad_heads(const void* q, const float* s_q, const float* w, void* q_out,
+                             float* s_q_out, float* w_out, int rows, int h_in, int h_out, int D,
+                             cudaStream_t st);
 
 }  // namespace idx

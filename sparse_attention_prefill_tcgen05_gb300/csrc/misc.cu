@@ -24,6 +24,33 @@ __global__ void expand_mask_kernel(const uint8_t* __restrict__ cand_mask, int64_
     }
 }
 
+// Head padding: q [rows, h_in, D] bytes -> q_out [rows, h_out, D] with zero
+// heads past h_in, and s_q / w [rows, h_in] -> [rows, h_out] with zeros.  A
+// zero head contributes exactly 0 to every logit (its weight is 0 and its
+// dot product is 0), so the padded problem scores every key identically.
+__global__ void pad_heads_kernel(const uint4* __restrict__ q, const float* __restrict__ s_q,
+                                 const float* __restrict__ w, uint4* __restrict__ q_out,
+                                 float* __restrict__ s_q_out, float* __restrict__ w_out, int rows,
+                                 int h_in, int h_out, int d16)
+{
+    const int64_t nq = (int64_t)rows * h_out * d16;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nq;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row_head = i / d16;
+        const int h = static_cast<int>(row_head % h_out);
+        const int64_t t = row_head / h_out;
+        q_out[i] = h < h_in ? q[(t * h_in + h) * d16 + i % d16] : make_uint4(0u, 0u, 0u, 0u);
+    }
+    const int64_t ns = (int64_t)rows * h_out;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < ns;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int h = static_cast<int>(i % h_out);
+        const int64_t t = i / h_out;
+        s_q_out[i] = h < h_in ? s_q[t * h_in + h] : 0.0f;
+        w_out[i] = h < h_in ? w[t * h_in + h] : 0.0f;
+    }
+}
+
 // Waits on a barrier that nothing arrives on; must give up after `cycles`.
 __global__ void selftest_timeout_kernel(uint32_t* status, long long cycles)
 {
@@ -52,6 +79,20 @@ cudaError_t launch_expand_mask(const uint8_t* cand_mask, int64_t ld_mask, const 
     const int64_t per_row = (ld + 255) / 256;
     dim3 grid((unsigned)std::min<int64_t>(per_row, 64), (unsigned)rows);
     expand_mask_kernel<<<grid, 256, 0, st>>>(cand_mask, ld_mask, clen, key_mask, ld, block, rows);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pad_heads(const void* q, const float* s_q, const float* w, void* q_out,
+                             float* s_q_out, float* w_out, int rows, int h_in, int h_out, int D,
+                             cudaStream_t st)
+{
+    if (rows <= 0)
+        return cudaSuccess;
+    const int64_t nq = (int64_t)rows * h_out * (D / 16);
+    const int blocks = (int)std::min<int64_t>((nq + 255) / 256, 4096);
+    pad_heads_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(q), s_q, w,
+                                             static_cast<uint4*>(q_out), s_q_out, w_out, rows,
+                                             h_in, h_out, D / 16);
     return cudaGetLastError();
 }
 

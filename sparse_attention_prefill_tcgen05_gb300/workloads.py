@@ -94,8 +94,8 @@ class ProblemSpec:
 # The five workloads: a tiny oracle-sized case and four shaped like the pages'.
 CONFIGS = {
     "tiny": ProblemSpec(
-        "tiny: T=64 rows at pos 960..1023, L=1024, H=8, D=64, fp8, top-32",
-        (RequestSpec(64, 960, 1),), H=8, D=64, topk=32, seed=0),
+        "tiny: T=64 rows at pos 960..1023, L=1024, H=4, D=64, fp8, top-32",
+        (RequestSpec(64, 960, 1),), H=4, D=64, topk=32, seed=0),
     "cold64k": ProblemSpec(
         "cold chunk: T=2048 rows ending a 65,536-token prefix, L=65,536, H=32, D=128, fp8, "
         "5% of keys x4, top-2048",
