@@ -11,19 +11,26 @@
 // compressed prefix, -inf past the row's causal length).
 //
 // Mapping.  One MMA tile is M = 128 keys (TMEM lanes) x N = (rows x H heads)
-// columns x K = D.  With keys on the lanes, the head reduction of one
-// (row, key) is a run of H consecutive accumulator columns held by ONE
-// thread: no shuffles, no shared-memory reduction.
+// columns x K = D.  The head reduction of one (row, key) is a run of H
+// accumulator columns on one TMEM lane.
 //
-// Roles (384 threads, one CTA per SM, persistent over work units):
-//   warp 0      TMA producer: the unit's Q tile (double-buffered) and a ring
-//               of K tiles, 128-byte-swizzled for the MMA.
-//   warp 1      allocates 512 TMEM columns (two accumulators), issues
-//               tcgen05.mma (D/32 per tile) and tcgen05.commit.
-//   warps 4-11  epilogue: tcgen05.ld 32x32b (pipelined), ReLU, head-weighted
-//               sum (four independent partial sums per row), key scale,
-//               causal and candidate masks, then one of three sinks:
-//   * kSinkLogits: coalesced fp32 store of the [rows, ld] logits;
+// Roles (640 threads, one CTA per SM, persistent over work units):
+//   warp 0       TMA producer: the unit's Q tile (double-buffered) and a ring
+//                of K tiles, 128-byte-swizzled for the MMA.
+//   warp 1       allocates 512 TMEM columns (two accumulators), issues
+//                tcgen05.mma (D/32 per tile) and tcgen05.commit.
+//   warps 4-19   epilogue: four column parts x four TMEM lane quadrants.  A
+//                warp reads its 32 keys x N/4 columns with tcgen05.ld 16x256b,
+//                which gives thread (g, q) columns 2q and 2q+1 of every 8-column
+//                group for two keys, so its head weights stay in registers; the
+//                head sums are finished by a shuffle reduce-scatter over the four
+//                q lanes of a key.  Then key scale, causal and candidate masks,
+//                and one of four sinks:
+//   * kSinkLogits: fp32 store of the [rows, ld] logits (also used, with a key
+//     tile stride, for the sampled keys of the fused top-k);
+//   * kSinkFilter: append every entry at or above the row's fixed threshold to
+//     the warp's sub-list of its (row, key split); the merge checks that the
+//     lists decide the row;
 //   * kSinkStream: streamed exact top-k ("chunked-prefill-memory.md" section
 //     2.3 scores key blocks and keeps per-block top-k; here the block top-k is
 //     kept on the fly).  A key is appended to its row's list only if it is at
@@ -39,7 +46,8 @@
 //   * kSinkPool: the same over the maximum of each cand_block-key block
 //     (candidate blocks, same section: 8-key block pooling, top-2048 blocks).
 // The accumulator is double-buffered so the epilogue of tile i overlaps the
-// MMAs of tile i+1.
+// MMAs of tile i+1, and it is handed back as soon as its last column is in
+// registers.
 #include "groupsel.cuh"
 #include "internal.h"
 
