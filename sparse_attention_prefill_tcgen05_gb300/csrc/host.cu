@@ -37,7 +37,9 @@ constexpr int64_t kTargetUnits = 1024;   // units per launch wanted for load bal
 struct indexer_plan_s {
     int R = 0, T = 0, Lk = 0, H = 0, D = 0, topk = 0, kdtype = 0;
     int kH = 0;                       // heads the kernels run with (H, or H padded with zero heads)
-    size_t off_pad = 0, pad_end = 0;  // padded q / s_q / w when kH != H
+    size_t off_pad = 0;               // padded q / s_q / w when kH != H
+    size_t off_k8 = 0;                // e4m3 keys [Lk, D] + s_k [Lk] converted from e2m1
+    size_t pad_end = 0;               // end of the per-call input preparation area
     int cand_block = 8, cand_topk = 0;
     int G = 8;                        // query rows per MMA tile
     std::vector<int32_t> row_begin;   // [R+1]
@@ -75,10 +77,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool supported_shape(int H, int D, int kdtype)
 {
-    // e2m1 keys: the block-scaled MMA kernel raised an illegal instruction on its
-    // first GB300 run and is not launched until that is understood.
-    if (kdtype == IDX_K_FP4_E2M1_UE8M0)
-        return false;
+    // e2m1 keys are converted to e4m3 exactly (misc.cu) and scored like fp8 keys
+    (void)kdtype;
     return (H == 32 && D == 128) || (H == 16 && D == 128) || (H == 64 && D == 128) ||
            (H == 8 && D == 64) || (H == 4 && D == 64);
 }
@@ -262,7 +262,7 @@ int run_logits(Ctx& c, std::vector<Segment>& segs, int sink)
         return IDX_OK;
     const int grid = std::min(units, c.sms);
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    return launch_logits(lp, p->kH, p->D, p->kdtype, sink, grid, c.st) == cudaSuccess
+    return launch_logits(lp, p->kH, p->D, kKeyFp8, sink, grid, c.st) == cudaSuccess
                ? IDX_OK
                : IDX_ERR_CUDA;
 }
@@ -489,8 +489,9 @@ void set_inputs(Ctx& c, const float* s_q, const float* w, const void* k_scale,
 {
     c.lp.s_q = s_q;
     c.lp.w = w;
-    c.lp.s_k = c.p->kdtype == IDX_K_FP8_E4M3 ? static_cast<const float*>(k_scale) : nullptr;
-    c.lp.k_sf = c.p->kdtype == IDX_K_FP8_E4M3 ? nullptr : static_cast<const uint8_t*>(k_scale);
+    // (e2m1 keys arrive here already converted to e4m3 + s_k)
+    c.lp.s_k = static_cast<const float*>(k_scale);
+    c.lp.k_sf = nullptr;
     c.lp.compress_len = clen;
     c.lp.status = static_cast<uint32_t*>(ws);
     c.lp.mask_block = c.p->cand_block;
@@ -514,6 +515,17 @@ int prepare(Ctx& c, const void* q, const float* s_q, const float* w, const void*
         q = q_pad;
         s_q = s_q_pad;
         w = w_pad;
+    }
+    if (p->kdtype == IDX_K_FP4_E2M1_UE8M0) {
+        uint8_t* k8 = static_cast<uint8_t*>(ws) + p->off_k8;
+        float* s_k = reinterpret_cast<float*>(k8 + (size_t)std::max(p->Lk, 1) * p->D);
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        if (launch_fp4_to_fp8(static_cast<const uint8_t*>(k), static_cast<const uint8_t*>(k_scale),
+                              p->Lk, p->D, k8, s_k, static_cast<uint32_t*>(ws), c.st) !=
+            cudaSuccess)
+            return IDX_ERR_CUDA;
+        k = k8;
+        k_scale = s_k;
     }
     int rc = fill_maps(c, q, k);
     if (rc != IDX_OK)
@@ -611,7 +623,7 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
     }
     // 4 heads run as 8 (zero heads 4..7 add exactly 0 to every logit)
     p->kH = p->H == 4 ? 8 : p->H;
-    p->G = logits_rows_per_group(p->kH, p->kdtype);
+    p->G = logits_rows_per_group(p->kH, kKeyFp8);
     const int G = p->G;
 
     // Key splits: the caller's size, else the largest multiple of 128 that still
@@ -675,6 +687,9 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
     p->off_pad = off;
     if (p->kH != p->H)
         off = align_up(off + (size_t)p->T * p->kH * (p->D + 8), 256);
+    p->off_k8 = off;
+    if (p->kdtype == IDX_K_FP4_E2M1_UE8M0)
+        off = align_up(off + (size_t)std::max(p->Lk, 1) * (p->D + 4), 256);
     p->pad_end = off;
     p->off_gtau = off;                       // [T] shared bound, then [T] row flags
     p->off_fail = off + (size_t)std::max(p->T, 1) * 4;

@@ -20,6 +20,7 @@ constexpr int kThreads = 128 + 32 * kEpiWarps;   // warp 0 TMA, warp 1 MMA/TMEM,
 constexpr uint32_t kStatusTimeout = 1u << 0;
 constexpr uint32_t kStatusBadArg = 1u << 1;
 constexpr uint32_t kStatusListOverflow = 1u << 2;   // a streamed list lost entries
+constexpr uint32_t kStatusFp4Range = 1u << 3;       // an e2m1 key has no exact e4m3 form
 
 // Key formats.
 constexpr int kKeyFp8 = 0;
@@ -153,6 +154,12 @@ cudaError_t launch_expand_mask(const uint8_t* cand_mask, int64_t ld_mask, const 
                                uint8_t* key_mask, int64_t ld, int block, int rows,
                                cudaStream_t st);
 cudaError_t launch_selftest_timeout(uint32_t* status, long long cycles, cudaStream_t st);
+// e2m1 keys [keys, D/2] (element 2i in the low nibble) with ue8m0 scales
+// [keys, D/32] -> e4m3 keys [keys, D] and fp32 s_k [keys] = 2^(largest block
+// exponent - 127), exactly; a key whose smaller blocks would need more than
+// e4m3's range sets kStatusFp4Range in *status.
+cudaError_t launch_fp4_to_fp8(const uint8_t* k4, const uint8_t* sf, int keys, int D, uint8_t* k8,
+                              float* s_k, uint32_t* status, cudaStream_t st);
 cudaError_t launch_pad_heads(const void* q, const float* s_q, const float* w, void* q_out,
                              float* s_q_out, float* w_out, int rows, int h_in, int h_out, int D,
                              cudaStream_t st);

@@ -51,6 +51,62 @@ __global__ void pad_heads_kernel(const uint4* __restrict__ q, const float* __res
     }
 }
 
+// e2m1 (OCP MX): sign, 2 exponent bits (bias 1), 1 mantissa bit; codes 0..7 are
+// 0, 0.5, 1, 1.5, 2, 3, 4, 6.  A nonzero magnitude is m * 2^E with m in {1, 1.5}.
+// Scaled by 2^-n (n >= 0: its block exponent below the key's largest) it is an
+// e4m3 value iff E - n >= -6 (normal: exponent field E - n + 7, mantissa 0 or
+// 0b100) or it is a subnormal multiple of 2^-9 (m = 1: E - n >= -9; m = 1.5:
+// E - n >= -8).  One thread per (key, 8 elements).
+__global__ void fp4_to_fp8_kernel(const uint8_t* __restrict__ k4, const uint8_t* __restrict__ sf,
+                                  int keys, int D, uint8_t* __restrict__ k8,
+                                  float* __restrict__ s_k, uint32_t* status)
+{
+    const int per_key = D / 8;
+    const int64_t n = (int64_t)keys * per_key;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t j = i / per_key;
+        const int part = static_cast<int>(i % per_key);      // elements 8*part .. 8*part+7
+        const uint8_t* sfj = sf + j * (D / 32);
+        int emax = 0;
+        for (int b = 0; b < D / 32; ++b)
+            emax = max(emax, static_cast<int>(sfj[b]));
+        if (part == 0)
+            s_k[j] = ldexpf(1.0f, emax - 127);
+        const int shift = emax - static_cast<int>(sfj[(part * 8) / 32]);   // n
+        const uint32_t packed = *reinterpret_cast<const uint32_t*>(k4 + j * (D / 2) + part * 4);
+        uint32_t lo = 0, hi = 0;
+        bool ok = true;
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t code = (packed >> (4 * e)) & 15u;
+            const uint32_t sign = code >> 3, mag = code & 7u;
+            uint32_t out = sign << 7;
+            if (mag != 0) {
+                // mag 1: 0.5 = 1*2^-1; 2: 1; 3: 1.5; 4: 2; 5: 3 = 1.5*2; 6: 4; 7: 6 = 1.5*4
+                const int E = mag == 1 ? -1 : static_cast<int>((mag - 2) >> 1);
+                const bool half = mag >= 2 && (mag & 1u);    // m = 1.5
+                const int Es = E - shift;
+                if (Es >= -6) {
+                    out |= static_cast<uint32_t>(Es + 7) << 3 | (half ? 4u : 0u);
+                } else if (!half && Es >= -9) {
+                    out |= 1u << (Es + 9);
+                } else if (half && Es >= -8) {
+                    out |= 3u << (Es + 8);
+                } else {
+                    ok = false;
+                }
+            }
+            if (e < 4)
+                lo |= out << (8 * e);
+            else
+                hi |= out << (8 * (e - 4));
+        }
+        *reinterpret_cast<uint2*>(k8 + j * D + part * 8) = make_uint2(lo, hi);
+        if (!ok)
+            atomicOr(status, kStatusFp4Range);
+    }
+}
+
 // Waits on a barrier that nothing arrives on; must give up after `cycles`.
 __global__ void selftest_timeout_kernel(uint32_t* status, long long cycles)
 {
@@ -79,6 +135,17 @@ cudaError_t launch_expand_mask(const uint8_t* cand_mask, int64_t ld_mask, const 
     const int64_t per_row = (ld + 255) / 256;
     dim3 grid((unsigned)std::min<int64_t>(per_row, 64), (unsigned)rows);
     expand_mask_kernel<<<grid, 256, 0, st>>>(cand_mask, ld_mask, clen, key_mask, ld, block, rows);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fp4_to_fp8(const uint8_t* k4, const uint8_t* sf, int keys, int D, uint8_t* k8,
+                              float* s_k, uint32_t* status, cudaStream_t st)
+{
+    if (keys <= 0)
+        return cudaSuccess;
+    const int64_t n = (int64_t)keys * (D / 8);
+    const int blocks = (int)std::min<int64_t>((n + 255) / 256, 8192);
+    fp4_to_fp8_kernel<<<blocks, 256, 0, st>>>(k4, sf, keys, D, k8, s_k, status);
     return cudaGetLastError();
 }
 

@@ -97,18 +97,13 @@ def test_ragged_requests_parity():
     check_all(p, key_block=1024)
 
 
-FP4_OFF = pytest.mark.skip(reason="e2m1 keys are not enabled in this build (the planner "
-                                   "returns IDX_ERR_UNSUPPORTED)")
-
-
-@FP4_OFF
 def test_fp4_keys_scaled_parity():
-    """fp8 queries x e2m1 keys with one ue8m0 scale per 32 elements (block-scaled MMA)."""
+    """fp8 queries x e2m1 keys with one ue8m0 scale per 32 elements (converted exactly to
+    e4m3 keys with a per-key power-of-two scale, then the fp8 MMA)."""
     p = small("v4ratio2", 16, 32, topk=64)
     check_all(p, key_block=1024)
 
 
-@FP4_OFF
 def test_fp4_exact_arithmetic_inputs_are_bit_exact():
     spec = dataclasses.replace(W.scaled(W.CONFIGS["v4ratio2"], 32, 64), topk=50, exact=True)
     p = W.make_problem(spec)
@@ -118,6 +113,25 @@ def test_fp4_exact_arithmetic_inputs_are_bit_exact():
     ref = oracle_rows(p, np.arange(T))
     g = Hp.gpu_logits(p, plan, d).cpu().numpy().astype(np.float64)
     assert np.array_equal(g, ref)
+
+
+def test_fp4_key_outside_the_e4m3_range_is_reported():
+    """A key whose block scales span 2^10 with a 0.5 code in the small block has no exact
+    e4m3 form: the call reports IDX_ERR_DEVICE_CHECK through indexer_status."""
+    p = small("v4ratio2", 64, 256, topk=16)
+    k, ks = p.k.clone(), p.k_scale.clone()
+    ks[0, 0] = 127 + 10
+    ks[0, 1] = 127
+    k[0, 16] = 0x11                       # elements 32, 33 (block 1): code 1 = 0.5
+    p = dataclasses.replace(p, k=k, k_scale=ks)
+    plan = Hp.make_plan(p)
+    d = Hp.device_inputs(p)
+    out = torch.empty((int(p.cu_seqlens_q[-1]), Hp.max_keys(p)), dtype=torch.float32,
+                      device="cuda")
+    ws = Hp.workspace(plan)
+    K.indexer_logits(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"], d["compress_len"],
+                     out, ws)
+    assert K.indexer_status(plan, ws) == K.IDX_ERR_DEVICE_CHECK
 
 
 def test_exact_arithmetic_inputs_are_bit_exact():
@@ -309,7 +323,6 @@ def test_full_cold_chunk_t2048_l65536_top2048():
     assert exact >= n // 2
 
 
-@FP4_OFF
 def test_full_v4_low_ratio_fp4_t2048_l100000_top512():
     _, _, _, exact, n = full_size_check("v4ratio2", 48)
     assert exact >= n // 2
