@@ -262,7 +262,7 @@ int run_logits(Ctx& c, std::vector<Segment>& segs, int sink)
         return IDX_OK;
     const int grid = std::min(units, c.sms);
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    return launch_logits(lp, p->kH, p->D, kKeyFp8, sink, grid, c.st) == cudaSuccess
+    return launch_logits(lp, p->kH, p->D, sink, grid, c.st) == cudaSuccess
                ? IDX_OK
                : IDX_ERR_CUDA;
 }
@@ -491,7 +491,6 @@ void set_inputs(Ctx& c, const float* s_q, const float* w, const void* k_scale,
     c.lp.w = w;
     // (e2m1 keys arrive here already converted to e4m3 + s_k)
     c.lp.s_k = static_cast<const float*>(k_scale);
-    c.lp.k_sf = nullptr;
     c.lp.compress_len = clen;
     c.lp.status = static_cast<uint32_t*>(ws);
     c.lp.mask_block = c.p->cand_block;
@@ -623,7 +622,7 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
     }
     // 4 heads run as 8 (zero heads 4..7 add exactly 0 to every logit)
     p->kH = p->H == 4 ? 8 : p->H;
-    p->G = logits_rows_per_group(p->kH, kKeyFp8);
+    p->G = logits_rows_per_group(p->kH);
     const int G = p->G;
 
     // Key splits: the caller's size, else the largest multiple of 128 that still

@@ -23,8 +23,6 @@ constexpr uint32_t kStatusListOverflow = 1u << 2;   // a streamed list lost entr
 constexpr uint32_t kStatusFp4Range = 1u << 3;       // an e2m1 key has no exact e4m3 form
 
 // Key formats.
-constexpr int kKeyFp8 = 0;
-constexpr int kKeyFp4 = 1;
 
 // What the logits kernel does with each (row, key) score.
 constexpr int kSinkLogits = 0;   // write fp32 to a [rows, ld] buffer
@@ -65,7 +63,6 @@ struct LogitsParams {
     const float* s_q;    // [rows, H]
     const float* w;      // [rows, H]
     const float* s_k;    // fp8 keys: [keys]
-    const uint8_t* k_sf; // fp4 keys: ue8m0 [keys, D/32]
     const int32_t* compress_len;  // [rows]
     const uint8_t* cand_mask;     // nullable [rows, ld_mask] 0/1 per key block
     int64_t ld_mask;
@@ -90,10 +87,9 @@ struct LogitsParams {
 };
 
 // Host-side launchers (defined in the .cu files).
-cudaError_t launch_logits(const LogitsParams& p, int H, int D, int kfmt, int sink, int grid,
+cudaError_t launch_logits(const LogitsParams& p, int H, int D, int sink, int grid,
                           cudaStream_t stream);
-size_t logits_smem_bytes(int H, int D, int kfmt);
-int logits_rows_per_group(int H, int kfmt);   // query rows per MMA tile
+int logits_rows_per_group(int H);   // query rows per MMA tile
 
 // Exact selection over the lists appended by the streaming sinks.  A piece is
 // a row range of one request whose lists were filled by the same launch; one

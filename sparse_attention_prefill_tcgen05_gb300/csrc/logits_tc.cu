@@ -56,11 +56,10 @@ namespace {
 
 constexpr int kHalfThreads = 128;
 
-template <int H, int D, int KFMT, int SINK>
+template <int H, int D, int SINK>
 struct Cfg {
-    // fp8 tiles are 256 columns (16 rows for small H); fp4 keys would need TMEM
-    // columns for block scales (192-column tiles).
-    static constexpr int NMAX = KFMT == kKeyFp8 ? (H >= 16 ? kTileN : 16 * H) : 192;
+    // tiles are 256 columns (16 rows for small H)
+    static constexpr int NMAX = H >= 16 ? kTileN : 16 * H;
     static constexpr int G = NMAX / H;                 // query rows per tile
     static constexpr int N = G * H;                    // MMA N
     static constexpr int QBYTES = N * D;               // Q tile: N rows of D bytes
@@ -72,9 +71,6 @@ struct Cfg {
     static constexpr int HALF_COLS = N / NPART;        // columns of one column part
     static constexpr int NCH = HALF_COLS / 32;         // 32-column chunks per part
     static constexpr int ACC_COLS = N;                 // TMEM columns per accumulator
-    static constexpr int SF_BYTES = KFMT == kKeyFp4 ? kTileKeys * 16 : 0;  // per stage
-    static constexpr int TMEM_SFA = 2 * ACC_COLS;      // 4 columns per stage
-    static constexpr int TMEM_SFB = TMEM_SFA + 4 * STAGES;
     static constexpr bool STREAM = SINK != kSinkLogits;
     static_assert(D == 32 || D == 64 || D == 128, "D must be 32, 64 or 128");
     static_assert(G >= 2 && N % 16 == 0, "H must leave at least two rows per tile");
@@ -86,8 +82,7 @@ struct Cfg {
     // shared memory carve-up (offsets from a 1024-byte aligned base)
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + ((2 * QBYTES + 1023) / 1024) * 1024;
-    static constexpr int OFF_SF = OFF_K + STAGES * KBYTES;
-    static constexpr int OFF_C = OFF_SF + STAGES * SF_BYTES;        // float c[2][kTileN]
+    static constexpr int OFF_C = OFF_K + STAGES * KBYTES;           // float c[2][kTileN]
     static constexpr int OFF_HIST = OFF_C + 2 * kTileN * 4;          // u32 [G][2][256]
     static constexpr int HIST_BYTES = STREAM ? G * 2 * 256 * 4 : 0;
     static constexpr int OFF_ROWS = OFF_HIST + HIST_BYTES;           // row state [G]
@@ -272,17 +267,16 @@ __device__ __forceinline__ uint32_t warp_sum_bins(const uint32_t* hist, int lane
     return s;
 }
 
-template <int H, int D, int KFMT, int SINK>
+template <int H, int D, int SINK>
 __global__ void __launch_bounds__(kThreads, 1)
     logits_tc_kernel(const __grid_constant__ LogitsParams p)
 {
-    using C = Cfg<H, D, KFMT, SINK>;
+    using C = Cfg<H, D, SINK>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* q_s = smem + C::OFF_Q;
     uint8_t* k_s = smem + C::OFF_K;
-    uint8_t* sf_s = smem + C::OFF_SF;
     float* c_s = reinterpret_cast<float*>(smem + C::OFF_C);
     uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);
     RowState* rows_s = reinterpret_cast<RowState*>(smem + C::OFF_ROWS);
@@ -308,8 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&a_empty[i], kEpiWarps);
         }
         for (int i = 0; i < C::STAGES; ++i) {
-            // fp4: one arrival with the TMA bytes plus one after the scales are staged
-            mbar_init(&k_full[i], KFMT == kKeyFp4 ? 2 : 1);
+            mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
         }
         mbar_init(drain, 1);
@@ -329,20 +322,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const long long budget = p.timeout_cycles;
-    if (KFMT == kKeyFp4) {
-        // q carries no block scale: every B scale is 2^0 (ue8m0 127) in all bytes
-        if (warp >= 4 && warp < 8) {
-            const uint32_t one = 0x7F7F7F7Fu;
-            tmem_st_32x32b_x4(tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) +
-                                  C::TMEM_SFB,
-                              one, one, one, one);
-            tmem_wait_st();
-        }
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-    }
-
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         int issued[C::STAGES];
@@ -382,24 +361,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok)
                     break;
-                if (KFMT == kKeyFp4) {
-                    // stage the tile's ue8m0 scales, one 32-bit word (4 blocks of 32
-                    // elements) per key, at a 16-byte row pitch for tcgen05.cp
-                    uint8_t* sf = sf_s + ks * C::SF_BYTES;
-                    const uint32_t* src = reinterpret_cast<const uint32_t*>(p.k_sf);
-#pragma unroll
-                    for (int r = 0; r < kTileKeys / 32; ++r) {
-                        const int m = r * 32 + lane;
-                        const int local = ui.j0 + i * ui.step + m;
-                        const uint32_t word =
-                            local < sg.key_count ? __ldg(src + key0 + m) : 0x7F7F7F7Fu;
-                        *reinterpret_cast<uint32_t*>(sf + m * 16) = word;
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&k_full[ks]);
-                }
                 if (++ks == C::STAGES) {
                     ks = 0;
                     kph ^= 1;
@@ -446,25 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t k_addr = smem_u32(k_s + ks * C::KBYTES);
                     const uint32_t d_tmem = tmem_base + ab * C::ACC_COLS;
-                    if (KFMT == kKeyFp8) {
 #pragma unroll
-                        for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                            const uint64_t adesc = smem_desc_kmajor(k_addr + kk * 32, D);
-                            const uint64_t bdesc = smem_desc_kmajor(q_addr + kk * 32, D);
-                            mma_f8f6f4(d_tmem, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
-                        }
-                    } else {
-                        const uint32_t sfa = tmem_base + C::TMEM_SFA + 4 * ks;
-                        tmem_cp_128x128b(
-                            sfa, smem_desc_noswizzle(smem_u32(sf_s + ks * C::SF_BYTES), 128));
-#pragma unroll
-                        for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                            const uint64_t adesc = smem_desc_kmajor(k_addr + kk * 32, D);
-                            const uint64_t bdesc = smem_desc_kmajor(q_addr + kk * 32, D);
-                            mma_mxf8f6f4(d_tmem, adesc, bdesc,
-                                         idesc_mxf8f6f4(kTileKeys, C::N, 5, 0, kk, kk), sfa,
-                                         tmem_base + C::TMEM_SFB, kk > 0 ? 1u : 0u);
-                        }
+                    for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                        const uint64_t adesc = smem_desc_kmajor(k_addr + kk * 32, D);
+                        const uint64_t bdesc = smem_desc_kmajor(q_addr + kk * 32, D);
+                        mma_f8f6f4(d_tmem, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(&k_empty[ks]);
                     mma_commit(&a_full[ab]);
@@ -620,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float sk_next = 0.0f;
             {
                 const int j0 = ui.j0 + quad * 32 + lane;
-                if (KFMT == kKeyFp8 && ui.ntiles_mma > 0 && j0 < sg.key_count)
+                if (ui.ntiles_mma > 0 && j0 < sg.key_count)
                     sk_next = __ldg(p.s_k + sg.key_base + j0);
             }
             // a warp's sub-list sees 32 of every 128 keys (or its lanes' blocks)
@@ -637,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float sk_lane = sk_next;
                     {
                         const int jn = jt + ui.step + lane;
-                        if (KFMT == kKeyFp8 && i + 1 < ui.ntiles_mma)
+                        if (i + 1 < ui.ntiles_mma)
                             sk_next = jn < sg.key_count ? __ldg(p.s_k + sg.key_base + jn) : 0.0f;
                     }
                     bool got = alive && mbar_wait(&a_full[ab], aph, budget, abort_flag);
@@ -981,11 +928,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem_base, 512);
 }
 
-template <int H, int D, int KFMT, int SINK>
+template <int H, int D, int SINK>
 cudaError_t launch_one(const LogitsParams& p, int grid, cudaStream_t stream)
 {
-    using C = Cfg<H, D, KFMT, SINK>;
-    auto kern = logits_tc_kernel<H, D, KFMT, SINK>;
+    using C = Cfg<H, D, SINK>;
+    auto kern = logits_tc_kernel<H, D, SINK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);
     if (e != cudaSuccess)
@@ -994,42 +941,35 @@ cudaError_t launch_one(const LogitsParams& p, int grid, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-template <int H, int D, int KFMT>
+template <int H, int D>
 cudaError_t launch_sink(const LogitsParams& p, int sink, int grid, cudaStream_t stream)
 {
     if (sink == kSinkLogits)
-        return launch_one<H, D, KFMT, kSinkLogits>(p, grid, stream);
+        return launch_one<H, D, kSinkLogits>(p, grid, stream);
     if (sink == kSinkStream)
-        return launch_one<H, D, KFMT, kSinkStream>(p, grid, stream);
+        return launch_one<H, D, kSinkStream>(p, grid, stream);
     if (sink == kSinkPool)
-        return launch_one<H, D, KFMT, kSinkPool>(p, grid, stream);
+        return launch_one<H, D, kSinkPool>(p, grid, stream);
     if (sink == kSinkFilter)
-        return launch_one<H, D, KFMT, kSinkFilter>(p, grid, stream);
+        return launch_one<H, D, kSinkFilter>(p, grid, stream);
     return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-int logits_rows_per_group(int H, int kfmt)
-{
-    if (kfmt == kKeyFp4)
-        return 192 / H;
-    return H >= 16 ? kTileN / H : 16;
-}
+int logits_rows_per_group(int H) { return H >= 16 ? kTileN / H : 16; }
 
-cudaError_t launch_logits(const LogitsParams& p, int H, int D, int kfmt, int sink, int grid,
+cudaError_t launch_logits(const LogitsParams& p, int H, int D, int sink, int grid,
                           cudaStream_t stream)
 {
-    if (kfmt == kKeyFp8) {
-        if (H == 32 && D == 128)
-            return launch_sink<32, 128, kKeyFp8>(p, sink, grid, stream);
-        if (H == 16 && D == 128)
-            return launch_sink<16, 128, kKeyFp8>(p, sink, grid, stream);
-        if (H == 64 && D == 128)
-            return launch_sink<64, 128, kKeyFp8>(p, sink, grid, stream);
-        if (H == 8 && D == 64)
-            return launch_sink<8, 64, kKeyFp8>(p, sink, grid, stream);
-    }
+    if (H == 32 && D == 128)
+        return launch_sink<32, 128>(p, sink, grid, stream);
+    if (H == 16 && D == 128)
+        return launch_sink<16, 128>(p, sink, grid, stream);
+    if (H == 64 && D == 128)
+        return launch_sink<64, 128>(p, sink, grid, stream);
+    if (H == 8 && D == 64)
+        return launch_sink<8, 64>(p, sink, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -164,49 +164,6 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint
         : "memory");
 }
 
-// Block-scaled variant, kind::mxf8f6f4 with one ue8m0 scale per 32 elements of
-// K for every row of A and of B; the scales live in TMEM (sfa, sfb) and the
-// instruction descriptor selects the byte of the 32-bit TMEM cell to use.
-__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                             uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                             uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
-        "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
-}
-
-// Copy a 128-row x 128-bit matrix from shared memory (no-swizzle canonical
-// layout, row r at byte 16*r) into TMEM: row r lands in lane r, 4 columns.
-__device__ __forceinline__ void tmem_cp_128x128b(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc)
-                 : "memory");
-}
-
-// 32 lanes x 4 columns of 32-bit from registers into TMEM (warp quadrant lanes).
-__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t a, uint32_t b,
-                                                  uint32_t c, uint32_t d)
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
-                 "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_st()
-{
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Arrive once on `bar` when every tcgen05 operation this thread issued so
 // far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar)
@@ -222,8 +179,6 @@ __device__ __forceinline__ void tmem_wait_ld()
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// 32 lanes x 32 columns of 32-bit: thread i of the warp receives lane
-// (quadrant base + i), columns [col, col+32).
 // 16 lanes x 256 bits, repeated 4 times along the columns (32 columns): thread
 // t = 4g + q gets, for repetition k, columns 8k + 2q and 8k + 2q + 1 of lane g
 // (v[4k], v[4k+1]) and of lane g + 8 (v[4k+2], v[4k+3]), lanes counted from
@@ -240,27 +195,6 @@ __device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, float (&v)[16
         : "r"(taddr));
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-        v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, float (&v)[32])
-{
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
-        "[%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
         v[i] = __uint_as_float(r[i]);
 }
 
@@ -295,29 +229,6 @@ __host__ __device__ constexpr uint32_t idesc_f8f6f4(int M, int N, int a_fmt, int
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Shared-memory descriptor of a no-swizzle K-major matrix whose 8-row core
-// matrices (16 bytes per row) are `sbo` bytes apart.
-__device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t saddr, uint32_t sbo)
-{
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= 1ull << 16;
-    d |= static_cast<uint64_t>(sbo >> 4) << 32;
-    d |= 1ull << 46;
-    return d;
-}
-
-// Instruction descriptor, kind::mxf8f6f4 block-scaled with ue8m0 scales:
-// B scale byte id (bits 4-5), A format (7-9), B format (10-12), N >> 3
-// (17-22), scale type ue8m0 (bit 23), M >> 4 (24-28), A scale byte id (29-30).
-__host__ __device__ constexpr uint32_t idesc_mxf8f6f4(int M, int N, int a_fmt, int b_fmt,
-                                                      int a_sf_id, int b_sf_id)
-{
-    return (static_cast<uint32_t>(b_sf_id & 3) << 4) | (static_cast<uint32_t>(a_fmt) << 7) |
-           (static_cast<uint32_t>(b_fmt) << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-           (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) |
-           (static_cast<uint32_t>(a_sf_id & 3) << 29);
-}
 
 // ReLU on the FMA pipe, scaled by 2^-25: sat(x * 2^-25) clamps to [0, 1],
 // which equals max(x, 0) * 2^-25 exactly whenever |x| < 2^25 (scaling by a
