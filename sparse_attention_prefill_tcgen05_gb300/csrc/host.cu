@@ -417,6 +417,8 @@ int run_streamed(Ctx& c, uint8_t* ws, int pool, int32_t* out_idx, float* out_val
     lp.gtau = reinterpret_cast<uint32_t*>(ws + p->off_gtau);
     uint32_t* row_fail = reinterpret_cast<uint32_t*>(ws + p->off_fail);
     uint32_t* tau_row = reinterpret_cast<uint32_t*>(ws + p->off_tau);
+    // second word of the per-call status area (zeroed at the start of every call)
+    uint32_t* fail_any = reinterpret_cast<uint32_t*>(ws) + 1;
     lp.keep = keep;
     lp.pool = pool ? pool : 1;
     lp.update_tiles = kUpdateTiles;
@@ -447,12 +449,16 @@ int run_streamed(Ctx& c, uint8_t* ws, int pool, int32_t* out_idx, float* out_val
             mp.verify = 1;
             mp.tau_row = tau_row;
             mp.row_fail = row_fail;
+            mp.fail_any = fail_any;
             if ((rc = launch_merge(c, mp)) != IDX_OK)
                 return rc;
-            // the exact path, for the undecided rows only
+            // the exact path, for the undecided rows only (no work at all when the
+            // merge flagged none)
             lp.row_fail = row_fail;
+            lp.fail_any = fail_any;
         } else {
             lp.row_fail = nullptr;
+            lp.fail_any = nullptr;
         }
         const bool prof = !sampled && &ps == &passes.front();
         if (prof) record_prof(c, g_prof_start);
@@ -464,10 +470,12 @@ int run_streamed(Ctx& c, uint8_t* ws, int pool, int32_t* out_idx, float* out_val
         mp.verify = 0;
         mp.only_failed = sampled ? 1 : 0;
         mp.row_fail = row_fail;
+        mp.fail_any = fail_any;
         if ((rc = launch_merge(c, mp)) != IDX_OK)
             return rc;
     }
     lp.row_fail = nullptr;
+    lp.fail_any = nullptr;
     return IDX_OK;
 }
 

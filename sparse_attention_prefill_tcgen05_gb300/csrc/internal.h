@@ -83,6 +83,7 @@ struct LogitsParams {
     int32_t update_tiles; // tiles between threshold refreshes
     const uint32_t* tau_row;   // kSinkFilter: [rows] fixed threshold (ord of a score)
     const uint32_t* row_fail;  // nullable [rows]: only row groups with a set row run
+    const uint32_t* fail_any;  // nullable: the whole launch has no work while it reads 0
     Segment seg[kMaxSegments];
 };
 
@@ -111,6 +112,7 @@ struct StreamMergeParams {
     uint32_t* row_fail;     // [rows] verify: set for rows the lists cannot decide;
                             // only_failed: rows with a clear entry are skipped
     const uint32_t* tau_row;  // verify: the threshold the lists were filled with
+    uint32_t* fail_any;       // verify: set when any row is flagged; only_failed: 0 = no work
     int32_t verify;
     int32_t only_failed;
     int32_t k;

@@ -293,6 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // a second pass with no flagged row anywhere has nothing to do (the flag was
+    // written by an earlier launch, so every thread reads the same value)
+    if (p.fail_any != nullptr && *p.fail_any == 0u)
+        return;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {

@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kSelThreads)
     const int nslots = pc.slots;
     const int64_t lbase = pc.list_offset + (int64_t)tr * nslots * pc.cap;
     const int64_t cbase = pc.count_offset + (int64_t)tr * nslots;
-    if (p.only_failed && p.row_fail[t] == 0)
+    if (p.only_failed && (*p.fail_any == 0u || p.row_fail[t] == 0))
         return;   // decided by the first pass
     // entries below the row's final threshold bound cannot be among its top k
     const uint32_t floor_ord = p.gtau ? p.gtau[t] : 0u;
@@ -200,8 +200,10 @@ __global__ void __launch_bounds__(kSelThreads)
         // at least k entries (or the threshold let everything through)
         const bool decided = s_overflow == 0 && (p.tau_row[t] == 0u || n_all >= p.k);
         if (!decided) {
-            if (threadIdx.x == 0)
+            if (threadIdx.x == 0) {
                 p.row_fail[t] = 1u;
+                atomicOr(p.fail_any, 1u);
+            }
             return;
         }
     }
