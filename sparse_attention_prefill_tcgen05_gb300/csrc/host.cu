@@ -29,7 +29,7 @@ struct Pass {
 };
 
 constexpr int kUpdateTiles = 4;          // tiles between threshold refreshes
-constexpr int kSampleTiles = 32;         // sampled key tiles per row (at most)
+constexpr int kSampleTiles = 16;         // sampled key tiles per row (at most)
 constexpr int64_t kTargetUnits = 1024;   // units per launch wanted for load balance
 
 }  // namespace
@@ -675,15 +675,15 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
     // Sampled thresholds for rows with at least 2 x kSampleTiles key tiles: tiles
     // 0, s, 2s, ... (at most kSampleTiles per row).  With mu = k / s samples
     // expected among a row's top k (keys in random order), the threshold is the
-    // sample of rank mu + 6.5 sqrt(mu) + 8, so that a row whose lists end up
-    // with fewer than k entries (decided again by the exact path) is rare.
+    // sample of rank mu + 5 sqrt(mu) + 4, so that a row whose lists end up with
+    // fewer than k entries (decided again by the exact path) is rare.
     const int max_tiles = (int)ceil_div(std::max(1, p->max_L), kTileKeys);
     if (pr->select_mode == IDX_SELECT_AUTO && max_tiles >= 2 * kSampleTiles) {
         const int st = (int)ceil_div(max_tiles, kSampleTiles);
         const double mu = (double)p->topk / st;
         p->sample_stride = st;
         p->sample_cols = (int)ceil_div(max_tiles, st) * kTileKeys;
-        p->sample_rank = (int)std::ceil(mu + 6.5 * std::sqrt(mu) + 8.0);
+        p->sample_rank = (int)std::ceil(mu + 5.0 * std::sqrt(mu) + 4.0);
         // the samples of a pass live in its list area
         for (int r = 0; r < R; ++r)
             if ((int64_t)p->sample_cols * 4 >

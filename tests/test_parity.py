@@ -247,23 +247,29 @@ def _check_structured_topk(p, plan, rows, topk):
     return fi
 
 
+def _sampled_problem(L, rows, topk, sampled_high):
+    """A structured problem whose sampled tiles (at the plan's stride) score above (or
+    below) every other key."""
+    probe = _structured_problem(L, rows, topk, torch.ones(L, dtype=torch.float64))
+    stride = Hp.make_plan(probe).info()["sample_stride"]
+    assert stride >= 2
+    p = _structured_problem(L, rows, topk, _sampled_tiles_scores(L, stride, sampled_high))
+    return p, Hp.make_plan(p)
+
+
 def test_sampled_threshold_too_high_falls_back_to_the_stream():
     """The sampled tiles hold the highest scores, so each row's threshold (the rank-th
     sample) lets fewer than k keys through: every row is decided again by the stream."""
     L, rows, topk = 16384, 24, 1024
-    p = _structured_problem(L, rows, topk, _sampled_tiles_scores(L, 4, True))
-    plan = Hp.make_plan(p)
-    assert plan.info()["sample_stride"] == 4
+    p, plan = _sampled_problem(L, rows, topk, True)
     _check_structured_topk(p, plan, rows, topk)
 
 
 def test_sampled_threshold_too_low_overflows_and_falls_back():
-    """The sampled tiles hold the lowest scores, so three quarters of every row pass the
+    """The sampled tiles hold the lowest scores, so most of every row passes the
     threshold and the lists overflow: the stream decides every row again."""
     L, rows, topk = 16384, 24, 64
-    p = _structured_problem(L, rows, topk, _sampled_tiles_scores(L, 4, False))
-    plan = Hp.make_plan(p)
-    assert plan.info()["sample_stride"] == 4
+    p, plan = _sampled_problem(L, rows, topk, False)
     _check_structured_topk(p, plan, rows, topk)
 
 
