@@ -123,15 +123,44 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def replica_env():
+    """(world size, rank, local rank) from the launcher's environment."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_replicas(backend: str):
+    """One process per GPU; the ranks only meet at barriers and the final max."""
+    import torch.distributed as dist
+    ws, rank, local = replica_env()
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest value over all ranks (the slowest replica's time)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> float:
+    """Weak scaling: every rank processes the same units; the job rate is all units
+    over the slowest rank's time."""
+    return world * units_per_rank / (slowest_ms / 1e3)
+
+
 def dist_setup():
     import torch
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    ws, rank, local = replica_env()
     if ws > 1:
-        import torch.distributed as dist
         torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        init_replicas("nccl")
     else:
         torch.cuda.set_device(0)
     return ws, rank, local
@@ -284,14 +313,10 @@ def main():
     if ws_n > 1:
         torch.distributed.barrier()
     assert K.indexer_status(plan, wsb) == K.IDX_OK
-    total_ms = sum(times)
-    if ws_n > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(times), dev)
     ms = total_ms / args.steps
     pairs = spec.dense_pairs
-    value = ws_n * pairs / (ms / 1e3)
+    value = whole_job_rate(pairs, ws_n, ms)
 
     # roofline: the step's dominant kernel, the fixed-threshold logits launch
     # (tcgen05 contraction + fused ReLU/head-sum/scale/mask epilogue + list append),
