@@ -567,13 +567,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     gpre[oi] = ld_relaxed_gpu(p.gtau + ui.t0 + rl);
             }
             // key scale of key (quadrant base + lane), one tile ahead; the owners
-            // of each key fetch it by a shuffle
+            // of each key fetch it by a shuffle.  The index is clamped instead of
+            // tested, so no instruction waits on the load before its use: keys at
+            // or past key_count are masked to -inf whatever scale they get.
+            const float* sk_row = p.s_k + sg.key_base;
+            const int sk_last = max(sg.key_count - 1, 0);
             float sk_next = 0.0f;
-            {
-                const int j0 = ui.j0 + quad * 32 + lane;
-                if (ui.ntiles_mma > 0 && j0 < sg.key_count)
-                    sk_next = __ldg(p.s_k + sg.key_base + j0);
-            }
+            if (ui.ntiles_mma > 0)
+                sk_next = __ldg(sk_row + min(ui.j0 + quad * 32 + lane, sk_last));
             // a warp's sub-list sees 32 of every 128 keys (or its lanes' blocks)
             const int unit_entries_warp =
                 SINK == kSinkPool ? ui.ntiles * (32 / (p.pool > 0 ? p.pool : 1)) : ui.ntiles * 32;
@@ -586,11 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     val[m] = -INFINITY;
                 if (i < ui.ntiles_mma) {
                     const float sk_lane = sk_next;
-                    {
-                        const int jn = jt + ui.step + lane;
-                        if (i + 1 < ui.ntiles_mma)
-                            sk_next = jn < sg.key_count ? __ldg(p.s_k + sg.key_base + jn) : 0.0f;
-                    }
+                    if (i + 1 < ui.ntiles_mma)
+                        sk_next = __ldg(sk_row + min(jt + ui.step + lane, sk_last));
                     bool got = alive && mbar_wait(&a_full[ab], aph, budget, abort_flag);
                     got = __all_sync(0xffffffffu, got);
                     if (!got && alive) {
