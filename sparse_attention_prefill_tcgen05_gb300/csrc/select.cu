@@ -217,12 +217,12 @@ __global__ void __launch_bounds__(kSelThreads)
             const int c = s_off[s + 1] - s_off[s];
             for (int i0 = 0; i0 < c; i0 += 32 * 8) {
                 // eight loads in flight per lane before any of them is used
+                // (clamped indices: no load result is selected on, so all eight
+                // are in flight at once; entries past c are dropped below)
                 uint2 ent[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int i = i0 + u * 32 + lane;
-                    ent[u] = i < c ? src[i] : make_uint2(0u, 0u);
-                }
+                for (int u = 0; u < 8; ++u)
+                    ent[u] = src[min(i0 + u * 32 + lane, c - 1)];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int i = i0 + u * 32 + lane;
