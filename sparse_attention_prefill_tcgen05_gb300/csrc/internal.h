@@ -12,9 +12,6 @@ constexpr int kTileKeys = 128;   // MMA M: keys per tile (one TMEM lane each)
 constexpr int kTileN = 256;      // MMA N: (row, head) columns per tile
 constexpr int kMaxSegments = 48;
 constexpr int kMaxRequests = 256;
-constexpr int kEpiWarps = 16;
-constexpr int kThreads = 128 + 32 * kEpiWarps;   // warp 0 TMA, warp 1 MMA/TMEM, 2-3 spare,
-                                                 // 4.. epilogue
 
 // Device status word bits (OR-ed by kernels, read by indexer_status).
 constexpr uint32_t kStatusTimeout = 1u << 0;

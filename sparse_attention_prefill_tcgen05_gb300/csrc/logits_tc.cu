@@ -14,13 +14,15 @@
 // columns x K = D.  The head reduction of one (row, key) is a run of H
 // accumulator columns on one TMEM lane.
 //
-// Roles (640 threads, one CTA per SM, persistent over work units):
+// Roles (one CTA per SM, persistent over work units; 640 threads for the list
+// sinks, 384 for plain logits):
 //   warp 0       TMA producer: the unit's Q tile (double-buffered) and a ring
 //                of K tiles, 128-byte-swizzled for the MMA.
 //   warp 1       allocates 512 TMEM columns (two accumulators), issues
 //                tcgen05.mma (D/32 per tile) and tcgen05.commit.
-//   warps 4-19   epilogue: four column parts x four TMEM lane quadrants.  A
-//                warp reads its 32 keys x N/4 columns with tcgen05.ld 16x256b,
+//   warps 4..    epilogue: four (list sinks) or two (logits) column parts x
+//                four TMEM lane quadrants.  A warp reads its 32 keys x its
+//                part's columns with tcgen05.ld 16x256b,
 //                which gives thread (g, q) columns 2q and 2q+1 of every 8-column
 //                group for two keys, so its head weights stay in registers; the
 //                head sums are finished by a shuffle reduce-scatter over the four
@@ -66,7 +68,11 @@ struct Cfg {
     static constexpr int KBYTES = kTileKeys * D;       // K tile
     static constexpr int STAGES = (D >= 128) ? 6 : 8;
     static constexpr int KSTEPS = D / 32;              // MMA K = 32 elements
-    static constexpr int NPART = kEpiWarps / 4;        // column parts (4 warps each)
+    // epilogue warps: 16 for the list sinks (their per-tile selection work needs the
+    // latency hiding), 8 for plain logits (fewer instructions per tile, 168 registers)
+    static constexpr int EPI = SINK == kSinkLogits ? 8 : 16;
+    static constexpr int THREADS = 128 + 32 * EPI;
+    static constexpr int NPART = EPI / 4;              // column parts (4 warps each)
     static constexpr int RPH = G / NPART;              // rows of one column part
     static constexpr int HALF_COLS = N / NPART;        // columns of one column part
     static constexpr int NCH = HALF_COLS / 32;         // 32-column chunks per part
@@ -268,7 +274,7 @@ __device__ __forceinline__ uint32_t warp_sum_bins(const uint32_t* hist, int lane
 }
 
 template <int H, int D, int SINK>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
     logits_tc_kernel(const __grid_constant__ LogitsParams p)
 {
     using C = Cfg<H, D, SINK>;
@@ -303,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 1);
             mbar_init(&a_full[i], 1);
-            mbar_init(&a_empty[i], kEpiWarps);
+            mbar_init(&a_empty[i], C::EPI);
         }
         for (int i = 0; i < C::STAGES; ++i) {
             mbar_init(&k_full[i], 1);
@@ -476,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_leader = g == 0 && (RPH >= 4 || (q & (4 / RPH - 1)) == 0);
         const uint32_t lanes_below = (1u << lane) - 1u;
         const NamedSync half_sync{2 + half, kHalfThreads};
-        const NamedSync epi_sync{1, kEpiWarps * 32};
+        const NamedSync epi_sync{1, C::EPI * 32};
         SelScratch<kHalfThreads>* sel_s =
             reinterpret_cast<SelScratch<kHalfThreads>*>(smem + C::OFF_SEL + half * C::SEL_ONE);
         int ab = 0, aph = 0, it = 0;
@@ -498,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cbuf[etid] = (etid & 1) ? cv * 33554432.0f : cv;
             }
             if constexpr (C::STREAM) {
-                for (int i = etid; i < C::G * 512; i += kEpiWarps * 32)
+                for (int i = etid; i < C::G * 512; i += C::EPI * 32)
                     hist_s[i] = 0;
                 if (etid < C::G) {
                     RowState& rs = rows_s[etid];
@@ -939,7 +945,7 @@ cudaError_t launch_one(const LogitsParams& p, int grid, cudaStream_t stream)
                                          C::SMEM);
     if (e != cudaSuccess)
         return e;
-    kern<<<grid, kThreads, C::SMEM, stream>>>(p);
+    kern<<<grid, C::THREADS, C::SMEM, stream>>>(p);
     return cudaGetLastError();
 }
 
