@@ -29,7 +29,7 @@ struct NamedSync {
 
 template <int NT>
 struct SelScratch {
-    alignas(16) uint32_t hist[256];
+    alignas(16) uint32_t hist[2][256];   // alternate passes: one is counted, the other zeroed
     uint32_t warp_sum[NT / 32];
     uint32_t bcast[4];
 };
@@ -65,12 +65,17 @@ __device__ CompositeThr group_threshold(SelScratch<NT>& sh, int tid, int n, uint
 {
     CompositeThr thr{0u, 0u, 0u, 0u};
     uint32_t remaining = k;
+    for (int i = tid; i < 256; i += NT)
+        sh.hist[0][i] = 0;
+    sync();
+    // two barriers per pass: after counting (this pass's histogram complete, the
+    // other one zeroed for the next pass) and after the boundary search
     for (int pass = 0; pass < max_passes; ++pass) {
         const bool in_hi = pass < 4;
         const int shift = 24 - 8 * (pass & 3);
+        uint32_t* hist = sh.hist[pass & 1];
         for (int i = tid; i < 256; i += NT)
-            sh.hist[i] = 0;
-        sync();
+            sh.hist[(pass + 1) & 1][i] = 0;
         for (int base = 0; base < n; base += NT) {
             const int e = base + tid;
             bool act = false;
@@ -81,14 +86,14 @@ __device__ CompositeThr group_threshold(SelScratch<NT>& sh, int tid, int n, uint
                 act = hi > kOrdNegInf && (hi & thr.mhi) == thr.phi && (lo & thr.mlo) == thr.plo;
                 dig = ((in_hi ? hi : lo) >> shift) & 255u;
             }
-            hist_add_aggregated(sh.hist, dig, act);
+            hist_add_aggregated(hist, dig, act);
         }
         sync();
         if (tid < 32) {
             // boundary bin by one warp: 8 bins per lane, suffix sums across lanes
             const int lane = tid;
-            const uint4 a = reinterpret_cast<const uint4*>(sh.hist)[lane * 2];
-            const uint4 b = reinterpret_cast<const uint4*>(sh.hist)[lane * 2 + 1];
+            const uint4 a = reinterpret_cast<const uint4*>(hist)[lane * 2];
+            const uint4 b = reinterpret_cast<const uint4*>(hist)[lane * 2 + 1];
             const uint32_t c[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
             const uint32_t lsum = c[0] + c[1] + c[2] + c[3] + c[4] + c[5] + c[6] + c[7];
             uint32_t suf = lsum;  // sum over lanes >= this one
@@ -127,12 +132,12 @@ __device__ CompositeThr group_threshold(SelScratch<NT>& sh, int tid, int n, uint
             }
         }
         sync();
+        // (bcast is rewritten only after the next pass's counting barrier)
         const uint32_t flag = sh.bcast[0];
         const uint32_t bin = sh.bcast[1];
         const uint32_t above = sh.bcast[2];
         if (pass == 0 && eligible)
             *eligible = sh.bcast[3];
-        sync();
         if (flag == 1)
             break;  // the current prefix already keeps exactly what must be kept
         if (in_hi) {

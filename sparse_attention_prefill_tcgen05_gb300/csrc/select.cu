@@ -129,7 +129,7 @@ __device__ int bitmap_prefix(const uint32_t* bits, uint32_t* wpre, int nw, Scrat
     return s_total;
 }
 
-constexpr int kStageEntries = 7168;   // candidates staged in shared memory per row (56 KB)
+constexpr int kStageEntries = 6400;   // candidates staged in shared memory per row (50 KB)
 static_assert(kStageEntries * 8 >= kBitmapWords * 8, "the bitmap reuses the staging area");
 
 __global__ void __launch_bounds__(kSelThreads)
