@@ -129,6 +129,36 @@ __device__ int bitmap_prefix(const uint32_t* bits, uint32_t* wpre, int nw, Scrat
     return s_total;
 }
 
+// Threshold by value buckets (one counting pass instead of up to eight radix
+// passes): 2048 equal-width buckets between the smallest and largest staged
+// score, the boundary bucket by a suffix scan, and the composite keys of that
+// bucket's entries ranked directly when it holds few of them.  kept(v, j) is
+// then "bucket(v) above the boundary, or in it with a composite key at least
+// the cut".  bucket() is one exact subtraction and one multiplication, the
+// same instructions wherever it is evaluated, and monotone in v.
+constexpr int kBuckets = 2048;
+constexpr int kBucketCands = 256;
+
+struct BucketThr {
+    float vmin, scale;
+    int boundary;          // -1: every entry is kept
+    uint64_t cut;          // composite key cut inside the boundary bucket
+    __device__ __forceinline__ int bucket(float v) const
+    {
+        const float x = __fmul_rn(__fsub_rn(v, vmin), scale);
+        return min(kBuckets - 1, static_cast<int>(x));
+    }
+    __device__ __forceinline__ bool kept(float v, uint32_t j) const
+    {
+        if (boundary < 0)
+            return true;
+        const int b = bucket(v);
+        if (b != boundary)
+            return b > boundary;
+        return ((static_cast<uint64_t>(f2ord(v)) << 32) | ~j) >= cut;
+    }
+};
+
 constexpr int kStageEntries = 6400;   // candidates staged in shared memory per row (50 KB)
 static_assert(kStageEntries * 8 >= kBitmapWords * 8, "the bitmap reuses the staging area");
 
@@ -150,6 +180,8 @@ __global__ void __launch_bounds__(kSelThreads)
     __shared__ int32_t s_staged;
     __shared__ int32_t s_overflow;
     __shared__ int s_total;
+    __shared__ int s_bnd, s_need, s_bsize, s_bcount;
+    __shared__ uint64_t s_cut;
     if (threadIdx.x == 0)
         s_overflow = 0;
     __syncthreads();
@@ -253,9 +285,106 @@ __global__ void __launch_bounds__(kSelThreads)
             hi = f2ord(__uint_as_float(ent.x));
             lo = ~ent.y;
         };
-        const CompositeThr thr =
-            group_threshold<kSelThreads>(sh, threadIdx.x, n, static_cast<uint32_t>(k), load,
-                                         CtaSync{});
+        // --- value buckets (the scratch below is the bitmap's, free until then)
+        uint32_t* bhist = reinterpret_cast<uint32_t*>(skey);
+        uint64_t* bcand = reinterpret_cast<uint64_t*>(bhist + kBuckets);
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        uint32_t omin = 0xFFFFFFFFu, omax = 0u;
+        for (int e = threadIdx.x; e < n; e += kSelThreads) {
+            const uint32_t o = f2ord(__uint_as_float(stage[e].x));
+            omin = min(omin, o);
+            omax = max(omax, o);
+        }
+        omin = __reduce_min_sync(0xffffffffu, omin);
+        omax = __reduce_max_sync(0xffffffffu, omax);
+        if (lane == 0) {
+            sh.hist[0][warp] = omin;
+            sh.hist[1][warp] = omax;
+        }
+        for (int i = threadIdx.x; i < kBuckets; i += kSelThreads)
+            bhist[i] = 0;
+        if (threadIdx.x == 0)
+            s_bcount = 0;
+        __syncthreads();
+        BucketThr bt;
+        {
+            uint32_t a = 0xFFFFFFFFu, b = 0u;
+            for (int w = 0; w < kSelThreads / 32; ++w) {
+                a = min(a, sh.hist[0][w]);
+                b = max(b, sh.hist[1][w]);
+            }
+            bt.vmin = ord2f(a);
+            const float range = __fsub_rn(ord2f(b), bt.vmin);
+            bt.scale = range > 0.0f ? __fdiv_rn(static_cast<float>(kBuckets), range) : 0.0f;
+        }
+        const bool use_buckets = n > k && bt.scale > 0.0f && bt.scale < INFINITY;
+        bool resolved = false;
+        if (use_buckets) {
+            for (int e = threadIdx.x; e < n; e += kSelThreads)
+                atomicAdd(&bhist[bt.bucket(__uint_as_float(stage[e].x))], 1u);
+            __syncthreads();
+            // suffix counts: thread t owns buckets [2048 - 4(t+1), 2048 - 4t)
+            constexpr int kPer = kBuckets / kSelThreads;
+            const int top = kBuckets - kPer * threadIdx.x;
+            uint32_t c[kPer], local = 0;
+#pragma unroll
+            for (int x = 0; x < kPer; ++x) {
+                c[x] = bhist[top - 1 - x];
+                local += c[x];
+            }
+            const uint32_t above_me = block_exclusive_sum(local, sh);
+            if (above_me < static_cast<uint32_t>(k) && above_me + local >= static_cast<uint32_t>(k)) {
+                uint32_t cum = above_me;
+#pragma unroll
+                for (int x = 0; x < kPer; ++x) {
+                    if (cum + c[x] >= static_cast<uint32_t>(k)) {
+                        s_bnd = top - 1 - x;
+                        s_need = static_cast<int>(k - cum);
+                        s_bsize = static_cast<int>(c[x]);
+                        break;
+                    }
+                    cum += c[x];
+                }
+            }
+            __syncthreads();
+            bt.boundary = s_bnd;
+            const int need = s_need, bsize = s_bsize;
+            if (bsize == need) {
+                bt.cut = 0;                   // the whole boundary bucket is kept
+                resolved = true;
+            } else if (bsize <= kBucketCands) {
+                for (int e = threadIdx.x; e < n; e += kSelThreads) {
+                    const uint2 ent = stage[e];
+                    const float v = __uint_as_float(ent.x);
+                    if (bt.bucket(v) == bt.boundary)
+                        bcand[atomicAdd(&s_bcount, 1)] =
+                            (static_cast<uint64_t>(f2ord(v)) << 32) | ~ent.y;
+                }
+                __syncthreads();
+                // the need-th largest candidate: the one with exactly need-1 above it
+                for (int i = threadIdx.x; i < bsize; i += kSelThreads) {
+                    const uint64_t mine = bcand[i];
+                    int rank = 0;
+                    for (int x = 0; x < bsize; ++x)
+                        rank += bcand[x] > mine;
+                    if (rank == need - 1)
+                        s_cut = mine;
+                }
+                __syncthreads();
+                bt.cut = s_cut;
+                resolved = true;
+            }
+        }
+        CompositeThr thr{0u, 0u, 0u, 0u};
+        if (!resolved) {
+            bt.boundary = -1;                 // not used: the radix threshold decides
+            thr = group_threshold<kSelThreads>(sh, threadIdx.x, n, static_cast<uint32_t>(k),
+                                               load, CtaSync{});
+        }
+        auto keep_entry = [&](uint32_t hi, uint32_t lo) {
+            return resolved ? bt.kept(ord2f(hi), ~lo) : thr.kept(hi, lo);
+        };
+        __syncthreads();                      // the bucket scratch becomes the bitmap
         uint32_t* bits = reinterpret_cast<uint32_t*>(skey);
         uint32_t* wpre = bits + kBitmapWords;
         const int nw = p.bitmap_words;
@@ -265,7 +394,7 @@ __global__ void __launch_bounds__(kSelThreads)
         for (int e = threadIdx.x; e < n; e += kSelThreads) {
             uint32_t hi, lo;
             load(e, hi, lo);
-            if (hi > kOrdNegInf && thr.kept(hi, lo))
+            if (hi > kOrdNegInf && keep_entry(hi, lo))
                 atomicOr(&bits[(~lo) >> 5], 1u << ((~lo) & 31));
         }
         __syncthreads();
@@ -275,7 +404,7 @@ __global__ void __launch_bounds__(kSelThreads)
         for (int e = threadIdx.x; e < n; e += kSelThreads) {
             uint32_t hi, lo;
             load(e, hi, lo);
-            if (hi > kOrdNegInf && thr.kept(hi, lo)) {
+            if (hi > kOrdNegInf && keep_entry(hi, lo)) {
                 const uint32_t j = ~lo;
                 const int pos = static_cast<int>(wpre[j >> 5] +
                                                  __popc(bits[j >> 5] & ((1u << (j & 31)) - 1u)));
