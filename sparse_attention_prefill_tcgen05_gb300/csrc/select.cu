@@ -509,31 +509,115 @@ __global__ void __launch_bounds__(kSelThreads)
 
 // ------------------------------------------------- sampled row thresholds
 
-// tau[t] = the rank-th largest finite sample of row t rounded down to its top
-// 16 bits (two radix passes), or 0 when the row has fewer than rank finite
-// samples.  Any threshold keeps the selection exact (rows the lists cannot
-// decide are selected again); this one lets at least rank samples through.
+// tau[t] = the smallest ord among the samples of row t that lie in or above
+// the value bucket holding its rank-th largest finite sample (2048 equal-width
+// buckets between the row's smallest and largest finite sample), or 0 when the
+// row has fewer than rank finite samples.  At least rank samples are at or
+// above it.  Any threshold keeps the selection exact (rows the lists cannot
+// decide are selected again); this one is close to the rank-th sample.
 __global__ void __launch_bounds__(kSelThreads)
     sample_threshold_kernel(const float* samples, int64_t ld, int rank, uint32_t* tau_row)
 {
     __shared__ Scratch sh;
+    __shared__ uint32_t bhist[kBuckets];
+    __shared__ int s_bnd;
     extern __shared__ __align__(16) float srow[];
     const int t = blockIdx.x;
+    const int n = static_cast<int>(ld);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float* row = samples + (int64_t)t * ld;
-    // the row once into shared memory (ld is a multiple of 128: float4 loads)
-    for (int e = threadIdx.x; e < static_cast<int>(ld) / 4; e += kSelThreads)
-        reinterpret_cast<float4*>(srow)[e] = reinterpret_cast<const float4*>(row)[e];
+    // the row once into shared memory (ld is a multiple of 128: float4 loads), with
+    // the range and the count of its finite samples
+    uint32_t omin = 0xFFFFFFFFu, omax = 0u, cnt = 0;
+    for (int e = threadIdx.x; e < n / 4; e += kSelThreads) {
+        const float4 v4 = reinterpret_cast<const float4*>(row)[e];
+        reinterpret_cast<float4*>(srow)[e] = v4;
+        const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const uint32_t o = f2ord(v[x]);
+            if (o > kOrdNegInf) {
+                omin = min(omin, o);
+                omax = max(omax, o);
+                ++cnt;
+            }
+        }
+    }
+    for (int i = threadIdx.x; i < kBuckets; i += kSelThreads)
+        bhist[i] = 0;
+    omin = __reduce_min_sync(0xffffffffu, omin);
+    omax = __reduce_max_sync(0xffffffffu, omax);
+    cnt = __reduce_add_sync(0xffffffffu, cnt);
+    if (lane == 0) {
+        sh.hist[0][warp] = omin;
+        sh.hist[1][warp] = omax;
+        sh.warp_sum[warp] = cnt;
+    }
     __syncthreads();
-    auto load = [&](int e, uint32_t& hi, uint32_t& lo) {
-        hi = f2ord(srow[e]);
-        lo = ~static_cast<uint32_t>(e);
-    };
-    uint32_t eligible = 0;
-    const CompositeThr thr = group_threshold<kSelThreads>(
-        sh, threadIdx.x, static_cast<int>(ld), static_cast<uint32_t>(rank), load, CtaSync{}, 2,
-        &eligible);
-    if (threadIdx.x == 0)
-        tau_row[t] = eligible >= static_cast<uint32_t>(rank) ? (thr.phi & thr.mhi) : 0u;
+    uint32_t a = 0xFFFFFFFFu, b = 0u, m = 0;
+    for (int w = 0; w < kSelThreads / 32; ++w) {
+        a = min(a, sh.hist[0][w]);
+        b = max(b, sh.hist[1][w]);
+        m += sh.warp_sum[w];
+    }
+    if (m < static_cast<uint32_t>(rank)) {
+        if (threadIdx.x == 0)
+            tau_row[t] = 0u;
+        return;
+    }
+    BucketThr bt;
+    bt.vmin = ord2f(a);
+    const float range = __fsub_rn(ord2f(b), bt.vmin);
+    bt.scale = range > 0.0f ? __fdiv_rn(static_cast<float>(kBuckets), range) : 0.0f;
+    if (!(bt.scale < INFINITY))
+        bt.scale = 0.0f;                      // degenerate range: one bucket
+    __syncthreads();                          // (sh is reused by the scan below)
+    for (int e = threadIdx.x; e < n; e += kSelThreads) {
+        const float v = srow[e];
+        if (f2ord(v) > kOrdNegInf)
+            atomicAdd(&bhist[bt.bucket(v)], 1u);
+    }
+    __syncthreads();
+    constexpr int kPer = kBuckets / kSelThreads;
+    const int top = kBuckets - kPer * threadIdx.x;
+    uint32_t c[kPer], local = 0;
+#pragma unroll
+    for (int x = 0; x < kPer; ++x) {
+        c[x] = bhist[top - 1 - x];
+        local += c[x];
+    }
+    const uint32_t above_me = block_exclusive_sum(local, sh);
+    const uint32_t r = static_cast<uint32_t>(rank);
+    if (above_me < r && above_me + local >= r) {
+        uint32_t cum = above_me;
+#pragma unroll
+        for (int x = 0; x < kPer; ++x) {
+            if (cum + c[x] >= r) {
+                s_bnd = top - 1 - x;
+                break;
+            }
+            cum += c[x];
+        }
+    }
+    __syncthreads();
+    const int bnd = s_bnd;
+    uint32_t tmin = 0xFFFFFFFFu;
+    for (int e = threadIdx.x; e < n; e += kSelThreads) {
+        const float v = srow[e];
+        const uint32_t o = f2ord(v);
+        if (o > kOrdNegInf && bt.bucket(v) >= bnd)
+            tmin = min(tmin, o);
+    }
+    tmin = __reduce_min_sync(0xffffffffu, tmin);
+    if (lane == 0)
+        sh.hist[0][warp] = tmin;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t x = 0xFFFFFFFFu;
+        for (int w = 0; w < kSelThreads / 32; ++w)
+            x = min(x, sh.hist[0][w]);
+        tau_row[t] = x;
+    }
 }
 
 // ------------------------------------------------------- standalone top-k
