@@ -30,7 +30,8 @@ struct Pass {
 
 constexpr int kUpdateTiles = 4;          // tiles between threshold refreshes
 constexpr int kSampleTiles = 16;         // sampled key tiles per row (at most)
-constexpr int64_t kTargetUnits = 1024;   // units per launch wanted for load balance
+constexpr int64_t kPlanSms = 152;        // SMs the planner balances for (GB300)
+constexpr int64_t kUnitsPerSm = 6;       // work units per SM wanted for load balance
 
 }  // namespace
 
@@ -49,7 +50,8 @@ struct indexer_plan_s {
     int max_L = 0;
     uint64_t budget = 0;
     // streamed selection
-    int split_keys = 0;               // keys per split (multiple of 128)
+    int split_keys = 0;               // largest key split of any request (for reporting)
+    std::vector<int32_t> split_r;     // keys per split of each request (multiple of 128)
     std::vector<int32_t> n_splits;    // per request
     std::vector<int32_t> cap_k;       // sub-list capacity per (row, split, quadrant), keys
     std::vector<int32_t> cap_b;       // sub-list capacity per (row, split, quadrant), blocks
@@ -57,9 +59,12 @@ struct indexer_plan_s {
     std::vector<Pass> passes_k, passes_b;
     int max_piece_rows = 0;
     // workspace layout (bytes)
-    // sampled thresholds (top-k): every sample_stride-th key tile, sample_cols
-    // columns per row, threshold at the sample_rank-th largest; stride 0 = off
-    int sample_stride = 0, sample_cols = 0, sample_rank = 0;
+    // sampled thresholds (top-k): per request every stride_r-th key tile, the
+    // threshold at the rank_r-th largest sample (rank 0: the request is not
+    // sampled and its rows keep everything); sample_cols columns per row;
+    // sample_stride = the largest stride, 0 = no request is sampled
+    int sample_stride = 0, sample_cols = 0;
+    std::vector<int32_t> sample_stride_r, sample_rank_r;
     size_t off_gtau = 0, off_fail = 0, off_tau = 0, off_counts = 0, off_lists = 0, ws_bytes = 0;
     long long wait_budget = 4000000000LL;
 };
@@ -277,11 +282,9 @@ int pass_launches(Ctx& c, const Pass& ps, const std::vector<int32_t>& cap, int s
     std::memset(&mp, 0, sizeof(mp));
     std::vector<Segment> segs;
     int ctas = 0;
-    int launch_cap = -1;
     auto flush = [&]() -> int {
         if (segs.empty())
             return IDX_OK;
-        lp.cap = launch_cap;
         int rc = run_logits(c, segs, sink);
         segs.clear();
         return rc;
@@ -289,12 +292,10 @@ int pass_launches(Ctx& c, const Pass& ps, const std::vector<int32_t>& cap, int s
     for (const PassPiece& pc : ps.pieces) {
         const int r = pc.r;
         const int ns = p->n_splits[r];
-        // one launch per distinct capacity (capacity is a launch parameter)
-        if (cap[r] != launch_cap || (int)segs.size() + ns > kMaxSegments) {
+        if ((int)segs.size() + ns > kMaxSegments) {
             int rc = flush();
             if (rc != IDX_OK)
                 return rc;
-            launch_cap = cap[r];
         }
         for (int s = 0; s < ns; ++s) {
             Segment sg;
@@ -303,10 +304,11 @@ int pass_launches(Ctx& c, const Pass& ps, const std::vector<int32_t>& cap, int s
             sg.nrows = pc.b - pc.a;
             sg.key_base = p->key_begin[r];
             sg.key_count = p->L[r];
-            sg.j_begin = s * p->split_keys;
-            sg.j_end = std::min(p->L[r], (s + 1) * p->split_keys);
+            sg.j_begin = s * p->split_r[r];
+            sg.j_end = std::min(p->L[r], (s + 1) * p->split_r[r]);
             sg.unit_tiles = (int)ceil_div(std::max(0, sg.j_end - sg.j_begin), kTileKeys);
             sg.tile_stride = 1;
+            sg.cap = cap[r];
             sg.n_row_groups = (int)ceil_div(sg.nrows, p->G);
             sg.n_chunks = 1;
             // row-major [row][split][quadrant][cap]
@@ -355,7 +357,6 @@ int pass_thresholds(Ctx& c, const Pass& ps, float* samples, uint32_t* tau_row)
     LogitsParams& lp = c.lp;
     const int first = ps.pieces.front().a;
     std::vector<Segment> segs;
-    int rows = 0;
     for (const PassPiece& pc : ps.pieces) {
         const int r = pc.r;
         Segment sg;
@@ -366,14 +367,16 @@ int pass_thresholds(Ctx& c, const Pass& ps, float* samples, uint32_t* tau_row)
         sg.key_count = p->L[r];
         sg.j_begin = 0;
         sg.j_end = p->L[r];
-        sg.tile_stride = p->sample_stride;
-        sg.unit_tiles = (int)ceil_div(ceil_div(std::max(1, p->L[r]), kTileKeys), p->sample_stride);
+        if (p->sample_rank_r[r] == 0)
+            continue;                          // its rows keep every entry (threshold 0)
+        sg.tile_stride = p->sample_stride_r[r];
+        sg.unit_tiles =
+            (int)ceil_div(ceil_div(std::max(1, p->L[r]), kTileKeys), p->sample_stride_r[r]);
         sg.n_row_groups = (int)ceil_div(sg.nrows, p->G);
         sg.n_chunks = 1;
         sg.out_offset = (int64_t)(pc.a - first) * p->sample_cols;
         sg.out_ld = p->sample_cols;
         segs.push_back(sg);
-        rows = pc.b - first;
         if ((int)segs.size() == kMaxSegments) {
             lp.out = samples;
             int rc = run_logits(c, segs, kSinkLogits);
@@ -388,11 +391,25 @@ int pass_thresholds(Ctx& c, const Pass& ps, float* samples, uint32_t* tau_row)
         if (rc != IDX_OK)
             return rc;
     }
+    const int rows = ps.pieces.back().b - first;
+    SampleParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    sp.samples = samples;
+    sp.ld = p->sample_cols;
+    sp.row0 = first;
+    sp.rows = rows;
+    sp.k = p->topk;
+    sp.compress_len = c.lp.compress_len;
+    sp.tau_row = tau_row;
+    sp.num_requests = p->R;
+    for (int r = 0; r < p->R; ++r) {
+        sp.req_row_begin[r] = p->row_begin[r];
+        sp.req_rank[r] = p->sample_rank_r[r] > 0 ? p->sample_stride_r[r] : 0;
+        sp.req_key_count[r] = p->L[r];
+    }
+    sp.req_row_begin[p->R] = p->row_begin[p->R];
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    return launch_sample_threshold(samples, p->sample_cols, rows, p->sample_rank,
-                                   tau_row + first, c.st) == cudaSuccess
-               ? IDX_OK
-               : IDX_ERR_CUDA;
+    return launch_sample_threshold(sp, c.st) == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 
 // Streamed top-k (pool = 0) or candidate blocks (pool > 0), pass by pass.
@@ -633,20 +650,31 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
     p->G = logits_rows_per_group(p->kH);
     const int G = p->G;
 
-    // Key splits: the caller's size, else the largest multiple of 128 that still
-    // gives about kTargetUnits (row group x split) units, but not below 8K keys.
+    // Key splits: the caller's size, else per request the fewest splits that keep
+    // every (row group x split) unit within 1/(kUnitsPerSm x kPlanSms) of the whole
+    // batch's work (row groups x key tiles), and splits of at least 8K keys, so that
+    // one long request among short ones does not leave most SMs idle at the end.
     const int round_L = (int)std::max<int64_t>(kTileKeys, ceil_div(p->max_L, kTileKeys) * kTileKeys);
-    auto units_for = [&](int S) {
-        int64_t u = 0;
-        for (int r = 0; r < R; ++r)
-            u += ceil_div(p->row_begin[r + 1] - p->row_begin[r], G) *
-                 std::max<int64_t>(1, ceil_div(p->L[r], S));
-        return u;
-    };
-    int S = pr->key_block ? std::min(pr->key_block, round_L) : round_L;
-    if (!pr->key_block)
-        while (units_for(S) < kTargetUnits && S > 8192)
-            S = (int)std::max<int64_t>(8192, ceil_div(ceil_div(S, 2), kTileKeys) * kTileKeys);
+    int64_t total_tiles = 0;
+    for (int r = 0; r < R; ++r)
+        total_tiles += ceil_div(p->row_begin[r + 1] - p->row_begin[r], G) *
+                       std::max<int64_t>(1, ceil_div(p->L[r], kTileKeys));
+    const int64_t unit_tiles_max =
+        std::max<int64_t>(8192 / kTileKeys, ceil_div(total_tiles, kUnitsPerSm * kPlanSms));
+    p->split_r.resize(R);
+    int S = 0;
+    for (int r = 0; r < R; ++r) {
+        int Sr;
+        if (pr->key_block) {
+            Sr = std::min(pr->key_block, round_L);
+        } else {
+            const int64_t tiles = std::max<int64_t>(1, ceil_div(p->L[r], kTileKeys));
+            const int64_t ns = ceil_div(tiles, unit_tiles_max);
+            Sr = (int)(ceil_div(ceil_div(tiles, ns), 1) * kTileKeys);
+        }
+        p->split_r[r] = std::max(Sr, (int)kTileKeys);
+        S = std::max(S, p->split_r[r]);
+    }
     p->split_keys = S;
     p->n_splits.resize(R);
     p->cap_k.resize(R);
@@ -659,36 +687,52 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
     const int slack = 2 * kUpdateTiles * 32;
     int64_t counts = 0;
     for (int r = 0; r < R; ++r) {
-        const int ns = (int)std::max<int64_t>(1, ceil_div(p->L[r], S));
+        const int ns = (int)std::max<int64_t>(1, ceil_div(p->L[r], p->split_r[r]));
         if ((int64_t)ns * kListsPerSplit > kMaxStreamSlots) {
             delete p;
             return IDX_ERR_UNSUPPORTED;
         }
         p->n_splits[r] = ns;
-        const int split_tiles = (int)ceil_div(std::max(1, std::min(S, p->L[r])), kTileKeys);
+        const int split_tiles =
+            (int)ceil_div(std::max(1, std::min(p->split_r[r], p->L[r])), kTileKeys);
         p->cap_k[r] = std::min(split_tiles * 32, std::max(4 * p->topk, p->topk + slack));
         p->cap_b[r] =
             ct ? std::min(split_tiles * (32 / cb), std::max(4 * ct, ct + slack)) : 1;
         p->cnt_base[r] = counts;
         counts += (int64_t)(p->row_begin[r + 1] - p->row_begin[r]) * ns * kListsPerSplit;
     }
-    // Sampled thresholds for rows with at least 2 x kSampleTiles key tiles: tiles
-    // 0, s, 2s, ... (at most kSampleTiles per row).  With mu = k / s samples
+    // Sampled thresholds, per request with at least 2 x kSampleTiles key tiles:
+    // tiles 0, s, 2s, ... (at most kSampleTiles per row).  With mu = k / s samples
     // expected among a row's top k (keys in random order), the threshold is the
     // sample of rank mu + 5 sqrt(mu) + 4, so that a row whose lists end up with
-    // fewer than k entries (decided again by the exact path) is rare.
-    const int max_tiles = (int)ceil_div(std::max(1, p->max_L), kTileKeys);
-    if (pr->select_mode == IDX_SELECT_AUTO && max_tiles >= 2 * kSampleTiles) {
-        const int st = (int)ceil_div(max_tiles, kSampleTiles);
-        const double mu = (double)p->topk / st;
-        p->sample_stride = st;
-        p->sample_cols = (int)ceil_div(max_tiles, st) * kTileKeys;
-        p->sample_rank = (int)std::ceil(mu + 5.0 * std::sqrt(mu) + 4.0);
-        // the samples of a pass live in its list area
-        for (int r = 0; r < R; ++r)
+    // fewer than k entries (decided again by the exact path) is rare.  Shorter
+    // requests are not sampled: their lists hold every entry.
+    p->sample_stride_r.assign(R, 0);
+    p->sample_rank_r.assign(R, 0);
+    if (pr->select_mode == IDX_SELECT_AUTO) {
+        for (int r = 0; r < R; ++r) {
+            const int tiles = (int)ceil_div(std::max(1, p->L[r]), kTileKeys);
+            if (tiles < 2 * kSampleTiles)
+                continue;
+            const int st = (int)ceil_div(tiles, kSampleTiles);
+            const double mu = (double)p->topk / st;
+            const int cols = (int)ceil_div(tiles, st) * kTileKeys;
+            // the samples of a pass live in its list area
+            if ((int64_t)cols * 4 > (int64_t)p->n_splits[r] * kListsPerSplit * p->cap_k[r] * 8)
+                continue;
+            p->sample_stride_r[r] = st;
+            p->sample_rank_r[r] = (int)std::ceil(mu + 5.0 * std::sqrt(mu) + 4.0);   // (nonzero:
+            // sampled; the kernel ranks each row by its own sample fraction)
+            p->sample_stride = std::max(p->sample_stride, st);
+            p->sample_cols = std::max(p->sample_cols, cols);
+        }
+        // every row of a sampled pass has a sample row, sampled or not
+        for (int r = 0; r < R && p->sample_stride > 0; ++r)
             if ((int64_t)p->sample_cols * 4 >
-                (int64_t)p->n_splits[r] * kListsPerSplit * p->cap_k[r] * 8)
+                (int64_t)p->n_splits[r] * kListsPerSplit * p->cap_k[r] * 8) {
                 p->sample_stride = 0;
+                p->sample_rank_r.assign(R, 0);
+            }
     }
     size_t off = kStatusBytes;
     p->off_pad = off;

@@ -46,7 +46,7 @@ struct Segment {
     int32_t unit_tiles;  // key tiles per unit
     int32_t tile_stride; // 1: every key tile; s: tiles 0, s, 2s, ... (sampled keys, whose
                          // logits go to consecutive output columns)
-    int32_t pad_;
+    int32_t cap;         // list sinks: entries per sub-list
     int64_t out_offset;  // logits: element offset of (row_begin, j_begin) in the output;
                          // streams: entry offset of row_begin's list for this split
     int64_t out_ld;      // logits: elements between rows; streams: entries between rows
@@ -74,7 +74,6 @@ struct LogitsParams {
     uint2* lists;         // (score bits, key or block index) entries
     uint32_t* counts;     // entries appended per (row, split), clamped to cap
     uint32_t* gtau;       // [rows] shared lower bound (ord of a score) per row
-    int32_t cap;          // list capacity per (row, split)
     int32_t keep;         // k (keys) or cand_topk (blocks)
     int32_t pool;         // keys per block for kSinkPool
     int32_t update_tiles; // tiles between threshold refreshes
@@ -140,10 +139,24 @@ struct TopkParams {
 };
 cudaError_t launch_topk_dense(const TopkParams& p, cudaStream_t stream);
 
-// Per-row threshold from sampled logits [rows, ld]: the ord of the rank-th
-// largest sample, or 0 (everything passes) when a row has fewer samples.
-cudaError_t launch_sample_threshold(const float* samples, int64_t ld, int rows, int rank,
-                                    uint32_t* tau_row, cudaStream_t stream);
+// Per-row thresholds from sampled logits [rows, ld] (row t at t - row0): about
+// the largest sample of rank mu + 5 sqrt(mu) + 4, mu = k * the row's sampled
+// fraction, or 0 (everything passes) for rows of unsampled requests (stride 0),
+// rows with at most k valid keys and rows with fewer samples.
+struct SampleParams {
+    const float* samples;
+    int64_t ld;
+    int32_t row0;
+    int32_t rows;
+    int32_t k;
+    int32_t num_requests;
+    const int32_t* compress_len;
+    uint32_t* tau_row;           // [total rows], written at row0 .. row0 + rows - 1
+    int32_t req_row_begin[kMaxRequests + 1];
+    int32_t req_rank[kMaxRequests];    // sampling stride of the request, 0: not sampled
+    int32_t req_key_count[kMaxRequests];
+};
+cudaError_t launch_sample_threshold(const SampleParams& p, cudaStream_t stream);
 
 cudaError_t launch_expand_mask(const uint8_t* cand_mask, int64_t ld_mask, const int32_t* clen,
                                uint8_t* key_mask, int64_t ld, int block, int rows,

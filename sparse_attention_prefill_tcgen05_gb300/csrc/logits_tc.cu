@@ -552,7 +552,7 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                 const int rl = half * RPH + own_rr(ro);
                 sub_own[ro] = p.lists + sg.out_offset +
                               (int64_t)(ui.t0 + rl - sg.row_begin) * sg.out_ld +
-                              (int64_t)quad * p.cap;
+                              (int64_t)quad * sg.cap;
             }
             // smallest causal length among the half's rows (rows past nr are never
             // stored or selected)
@@ -584,7 +584,7 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
             // a warp's sub-list sees 32 of every 128 keys (or its lanes' blocks)
             const int unit_entries_warp =
                 SINK == kSinkPool ? ui.ntiles * (32 / (p.pool > 0 ? p.pool : 1)) : ui.ntiles * 32;
-            const bool no_overflow = unit_entries_warp <= p.cap;
+            const bool no_overflow = unit_entries_warp <= sg.cap;
             for (int i = 0; i < ui.ntiles; ++i) {
                 const int jt = ui.j0 + i * ui.step + quad * 32;   // first key of the quadrant
                 float val[RPH];
@@ -736,14 +736,14 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                         const uint32_t mb = __ballot_sync(0xffffffffu, cand) & rowmask;
                         if (cand) {
                             const uint32_t pos = wcnt[ro] + __popc(mb & lanes_below);
-                            if (pos < static_cast<uint32_t>(p.cap))
+                            if (pos < static_cast<uint32_t>(sg.cap))
                                 sub_own[ro][pos] =
                                     make_uint2(__float_as_uint(val[m]), static_cast<uint32_t>(j));
                         }
                         wcnt[ro] += __popc(mb);
                     }
                 } else {
-                    const uint32_t cap = static_cast<uint32_t>(p.cap);
+                    const uint32_t cap = static_cast<uint32_t>(sg.cap);
 #pragma unroll
                     for (int m = 0; m < RPH; ++m) {
                         const int ro = RPH >= 4 ? (m >> 2) : 0;
@@ -752,7 +752,7 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                         uint32_t* h1 = hist_s + rl * 512;
                         uint2* sub = p.lists + sg.out_offset +
                                      (int64_t)(ui.t0 + rl - sg.row_begin) * sg.out_ld +
-                                     (int64_t)quad * p.cap;
+                                     (int64_t)quad * sg.cap;
                         if constexpr (SINK == kSinkStream) {
                             wcnt[ro] = stream_push(h1, h1 + 256, sub, cap, wcnt[ro], tau_hi[ro],
                                                    tau_lo[ro], b1[ro], val[m],
@@ -857,7 +857,7 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                                 const int w4 = (e >= o1) + (e >= o2) + (e >= o3);
                                 const int base =
                                     w4 == 0 ? 0 : (w4 == 1 ? o1 : (w4 == 2 ? o2 : o3));
-                                return list + (int64_t)w4 * p.cap + (e - base);
+                                return list + (int64_t)w4 * sg.cap + (e - base);
                             };
                             auto load = [&](int e, uint32_t& hi, uint32_t& lo) {
                                 const uint2 ent = *at(e);
@@ -920,7 +920,7 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                             p.counts[sg.cnt_offset +
                                      (int64_t)(ui.t0 + rl - sg.row_begin) * sg.cnt_ld + quad] =
                                 SINK == kSinkFilter ? wcnt[ro]
-                                                    : min(wcnt[ro], static_cast<uint32_t>(p.cap));
+                                                    : min(wcnt[ro], static_cast<uint32_t>(sg.cap));
                     }
                 }
                 // both halves are done with the row state before the next unit resets it

@@ -516,16 +516,27 @@ __global__ void __launch_bounds__(kSelThreads)
 // above it.  Any threshold keeps the selection exact (rows the lists cannot
 // decide are selected again); this one is close to the rank-th sample.
 __global__ void __launch_bounds__(kSelThreads)
-    sample_threshold_kernel(const float* samples, int64_t ld, int rank, uint32_t* tau_row)
+    sample_threshold_kernel(const __grid_constant__ SampleParams p)
 {
     __shared__ Scratch sh;
     __shared__ uint32_t bhist[kBuckets];
     __shared__ int s_bnd;
     extern __shared__ __align__(16) float srow[];
-    const int t = blockIdx.x;
+    const int t = p.row0 + blockIdx.x;
+    const int req = find_request(p.req_row_begin, p.num_requests, t);
+    const int stride = p.req_rank[req];     // sampling stride (0: not sampled)
+    const int clen = min(p.compress_len[t], p.req_key_count[req]);
+    uint32_t* tau_out = p.tau_row + t;
+    // rows that keep every entry: unsampled requests and rows with at most k keys
+    if (stride == 0 || clen <= p.k) {
+        if (threadIdx.x == 0)
+            *tau_out = 0u;
+        return;
+    }
+    const int64_t ld = p.ld;
     const int n = static_cast<int>(ld);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const float* row = samples + (int64_t)t * ld;
+    const float* row = p.samples + (int64_t)blockIdx.x * ld;
     // the row once into shared memory (ld is a multiple of 128: float4 loads), with
     // the range and the count of its finite samples
     uint32_t omin = 0xFFFFFFFFu, omax = 0u, cnt = 0;
@@ -560,9 +571,17 @@ __global__ void __launch_bounds__(kSelThreads)
         b = max(b, sh.hist[1][w]);
         m += sh.warp_sum[w];
     }
+    // mu = samples expected among the row's top k: k times the sampled fraction,
+    // which is m / clen for a short row (its first tile is always sampled) and
+    // 1 / stride when a candidate mask leaves fewer eligible keys than clen; the
+    // threshold is the sample of rank mu + 5 sqrt(mu) + 4
+    const float frac = fmaxf(static_cast<float>(m) / static_cast<float>(clen),
+                             1.0f / static_cast<float>(stride));
+    const float mu = static_cast<float>(p.k) * frac;
+    const int rank = static_cast<int>(ceilf(mu + 5.0f * sqrtf(mu) + 4.0f));
     if (m < static_cast<uint32_t>(rank)) {
         if (threadIdx.x == 0)
-            tau_row[t] = 0u;
+            *tau_out = 0u;
         return;
     }
     BucketThr bt;
@@ -616,7 +635,7 @@ __global__ void __launch_bounds__(kSelThreads)
         uint32_t x = 0xFFFFFFFFu;
         for (int w = 0; w < kSelThreads / 32; ++w)
             x = min(x, sh.hist[0][w]);
-        tau_row[t] = x;
+        *tau_out = x;
     }
 }
 
@@ -670,15 +689,13 @@ cudaError_t launch_stream_merge(const StreamMergeParams& p, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-cudaError_t launch_sample_threshold(const float* samples, int64_t ld, int rows, int rank,
-                                    uint32_t* tau_row, cudaStream_t stream)
+cudaError_t launch_sample_threshold(const SampleParams& p, cudaStream_t stream)
 {
-    if (rows <= 0)
+    if (p.rows <= 0)
         return cudaSuccess;
-    if (ld % 4 != 0 || ld > 16384)
+    if (p.ld % 4 != 0 || p.ld > 16384)
         return cudaErrorInvalidValue;
-    sample_threshold_kernel<<<rows, kSelThreads, ld * sizeof(float), stream>>>(samples, ld, rank,
-                                                                             tau_row);
+    sample_threshold_kernel<<<p.rows, kSelThreads, p.ld * sizeof(float), stream>>>(p);
     return cudaGetLastError();
 }
 
