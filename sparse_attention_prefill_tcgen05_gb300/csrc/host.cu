@@ -326,6 +326,7 @@ int pass_launches(Ctx& c, const Pass& ps, const std::vector<int32_t>& cap, int s
         mpc.cta_begin = ctas;
         mpc.slots = ns * kListsPerSplit;
         mpc.cap = cap[r];
+        mpc.key_count = p->L[r];
         mpc.list_offset = pc.list_off;
         mpc.count_offset = p->cnt_base[r] + (int64_t)(pc.a - p->row_begin[r]) * ns * kListsPerSplit;
         ctas += pc.b - pc.a;
@@ -445,7 +446,7 @@ int run_streamed(Ctx& c, uint8_t* ws, int pool, int32_t* out_idx, float* out_val
         mp.out_val = out_val;
         mp.mask = mask;
         mp.ld_mask = ld_mask;
-        mp.bitmap_words = pool ? 0 : (int)ceil_div(std::max(1, p->max_L), 32);
+        mp.bitmap = pool ? 0 : 1;
     };
     for (const Pass& ps : passes) {
         StreamMergeParams mp;

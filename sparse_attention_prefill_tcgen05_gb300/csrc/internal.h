@@ -97,7 +97,7 @@ struct MergePiece {
     int32_t cta_begin;      // first CTA of the piece in the launch
     int32_t slots;          // key splits (lists) per row
     int32_t cap;            // entries per list
-    int32_t pad_;
+    int32_t key_count;      // keys (or blocks) of the piece's request: indices are below it
     int64_t list_offset;    // entry offset of row_begin's first list
     int64_t count_offset;   // counts index of row_begin's first list
 };
@@ -114,7 +114,7 @@ struct StreamMergeParams {
     int32_t k;
     int32_t num_pieces;
     int32_t total_ctas;
-    int32_t bitmap_words;      // ceil(largest key count / 32): index-order output by bitmap
+    int32_t bitmap;            // 1: index-order output by bitmap where a row's keys allow
     int32_t* out_idx;
     float* out_val;
     uint8_t* mask;             // blocks: [rows, ld_mask]

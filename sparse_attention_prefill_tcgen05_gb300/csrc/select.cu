@@ -277,7 +277,10 @@ __global__ void __launch_bounds__(kSelThreads)
     const bool staged = s_staged <= kStageEntries;
     const int n = staged ? s_staged : n_all;
     const int k = p.k;
-    if (staged && !p.mask && p.bitmap_words > 0 && p.bitmap_words <= kBitmapWords) {
+    // bitmap words for this row's key indices (0: too many keys, sort instead)
+    const int row_words = (pc.key_count + 31) / 32;
+    const int nw_row = p.bitmap && row_words <= kBitmapWords ? max(row_words, 1) : 0;
+    if (staged && !p.mask && nw_row > 0) {
         // threshold over the staged entries, then the kept keys in ascending order
         // straight from a bitmap: no ordered emission, no sort
         auto load = [&](int e, uint32_t& hi, uint32_t& lo) {
@@ -319,6 +322,10 @@ __global__ void __launch_bounds__(kSelThreads)
         }
         const bool use_buckets = n > k && bt.scale > 0.0f && bt.scale < INFINITY;
         bool resolved = false;
+        if (n <= k) {
+            bt.boundary = -1;                 // every staged entry is kept
+            resolved = true;
+        }
         if (use_buckets) {
             for (int e = threadIdx.x; e < n; e += kSelThreads)
                 atomicAdd(&bhist[bt.bucket(__uint_as_float(stage[e].x))], 1u);
@@ -387,7 +394,7 @@ __global__ void __launch_bounds__(kSelThreads)
         __syncthreads();                      // the bucket scratch becomes the bitmap
         uint32_t* bits = reinterpret_cast<uint32_t*>(skey);
         uint32_t* wpre = bits + kBitmapWords;
-        const int nw = p.bitmap_words;
+        const int nw = nw_row;
         for (int w = threadIdx.x; w < nw; w += kSelThreads)
             bits[w] = 0;
         __syncthreads();
@@ -469,13 +476,13 @@ __global__ void __launch_bounds__(kSelThreads)
     }
     int32_t* oi = p.out_idx + (int64_t)t * k;
     float* ov = p.out_val ? p.out_val + (int64_t)t * k : nullptr;
-    if (p.bitmap_words > 0 && p.bitmap_words <= kBitmapWords) {
+    if (nw_row > 0) {
         // ascending key order without a sort: a bitmap of the kept keys (in the
         // staging area, free now) and an exclusive scan of its word popcounts give
         // every kept key its output position directly
         uint32_t* bits = reinterpret_cast<uint32_t*>(stage);
         uint32_t* wpre = bits + kBitmapWords;
-        const int nw = p.bitmap_words;
+        const int nw = nw_row;
         for (int w = threadIdx.x; w < nw; w += kSelThreads)
             bits[w] = 0;
         __syncthreads();
