@@ -178,12 +178,16 @@ __global__ void __launch_bounds__(kSelThreads)
     float* sval = reinterpret_cast<float*>(dyn + sizeof(uint2) * kStageEntries + sizeof(int32_t) * n2);
 
     __shared__ int32_t s_staged;
+    __shared__ int32_t s_nall;
     __shared__ int32_t s_overflow;
     __shared__ int s_total;
     __shared__ int s_bnd, s_need, s_bsize, s_bcount;
     __shared__ uint64_t s_cut;
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
         s_overflow = 0;
+        s_staged = 0;
+        s_nall = 0;
+    }
     __syncthreads();
     const int cta = blockIdx.x;
     int pi = 0;
@@ -199,54 +203,21 @@ __global__ void __launch_bounds__(kSelThreads)
         return;   // decided by the first pass
     // entries below the row's final threshold bound cannot be among its top k
     const uint32_t floor_ord = p.gtau ? p.gtau[t] : 0u;
-    if (threadIdx.x < 32) {
-        // exclusive prefix of the sub-list lengths, 32 slots per step
-        int carry = 0;
-        for (int s0 = 0; s0 < nslots; s0 += 32) {
-            const int s = s0 + static_cast<int>(threadIdx.x);
-            const uint32_t raw = s < nslots ? p.counts[cbase + s] : 0u;
-            const int c = static_cast<int>(min(raw, static_cast<uint32_t>(pc.cap)));
-            if (raw > static_cast<uint32_t>(pc.cap))
-                s_overflow = 1;   // benign race: every writer stores 1
-            int incl = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if ((threadIdx.x & 31) >= static_cast<unsigned>(o))
-                    incl += y;
-            }
-            if (s < nslots)
-                s_off[s] = carry + incl - c;
-            carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (threadIdx.x == 0) {
-            s_off[nslots] = carry;
-            s_staged = 0;
-        }
-    }
-    __syncthreads();
-    const int n_all = s_off[nslots];
-    if (p.verify) {
-        // the lists hold every entry at or above the row's threshold unless a
-        // sub-list overflowed; they decide the row iff that holds and they have
-        // at least k entries (or the threshold let everything through)
-        const bool decided = s_overflow == 0 && (p.tau_row[t] == 0u || n_all >= p.k);
-        if (!decided) {
-            if (threadIdx.x == 0) {
-                p.row_fail[t] = 1u;
-                atomicOr(p.fail_any, 1u);
-            }
-            return;
-        }
-    }
     // copy the entries that pass the floor into shared memory (order is irrelevant:
-    // the selection is by unique composite keys); every radix pass reads them there
-    // (one warp per sub-list, so the sub-lists' loads are in flight together)
+    // the selection is by unique composite keys); every pass below reads them there.
+    // One warp per sub-list, which reads its own length, so the sub-lists' loads
+    // are in flight together.
     {
         const int lane = threadIdx.x & 31;
         for (int s = threadIdx.x >> 5; s < nslots; s += kSelThreads / 32) {
+            const uint32_t raw = p.counts[cbase + s];
+            const int c = static_cast<int>(min(raw, static_cast<uint32_t>(pc.cap)));
+            if (lane == 0) {
+                if (raw > static_cast<uint32_t>(pc.cap))
+                    s_overflow = 1;   // benign race: every writer stores 1
+                atomicAdd(&s_nall, c);
+            }
             const uint2* src = p.lists + lbase + (int64_t)s * pc.cap;
-            const int c = s_off[s + 1] - s_off[s];
             for (int i0 = 0; i0 < c; i0 += 32 * 8) {
                 // eight loads in flight per lane before any of them is used
                 // (clamped indices: no load result is selected on, so all eight
@@ -274,8 +245,47 @@ __global__ void __launch_bounds__(kSelThreads)
         }
     }
     __syncthreads();
+    const int n_all = s_nall;
+    if (p.verify) {
+        // the lists hold every entry at or above the row's threshold unless a
+        // sub-list overflowed; they decide the row iff that holds and they have
+        // at least k entries (or the threshold let everything through)
+        const bool decided = s_overflow == 0 && (p.tau_row[t] == 0u || n_all >= p.k);
+        if (!decided) {
+            if (threadIdx.x == 0) {
+                p.row_fail[t] = 1u;
+                atomicOr(p.fail_any, 1u);
+            }
+            return;
+        }
+    }
     const bool staged = s_staged <= kStageEntries;
     const int n = staged ? s_staged : n_all;
+    if (!staged) {
+        // the entries stay in the lists: exclusive prefix of the sub-list lengths
+        if (threadIdx.x < 32) {
+            int carry = 0;
+            for (int s0 = 0; s0 < nslots; s0 += 32) {
+                const int s = s0 + static_cast<int>(threadIdx.x);
+                const int c = s < nslots ? static_cast<int>(min(p.counts[cbase + s],
+                                                                static_cast<uint32_t>(pc.cap)))
+                                         : 0;
+                int incl = c;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if ((threadIdx.x & 31) >= static_cast<unsigned>(o))
+                        incl += y;
+                }
+                if (s < nslots)
+                    s_off[s] = carry + incl - c;
+                carry += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (threadIdx.x == 0)
+                s_off[nslots] = carry;
+        }
+        __syncthreads();
+    }
     const int k = p.k;
     // bitmap words for this row's key indices (0: too many keys, sort instead)
     const int row_words = (pc.key_count + 31) / 32;
