@@ -89,6 +89,16 @@ def test_long_context_scaled_parity_with_ties():
     check_all(p, key_block=1024)
 
 
+@pytest.mark.parametrize("H", [16, 64])
+def test_other_head_counts_parity(H):
+    """The other built head counts (16 rows x 16 heads and 4 rows x 64 heads per MMA tile),
+    several tiles and a ragged tail, sampled thresholds on."""
+    spec = W.ProblemSpec(f"H={H}", (W.RequestSpec(72, 4100, 1),), H=H, D=128, topk=100,
+                         seed=40 + H)
+    p = W.make_problem(spec)
+    check_all(p)
+
+
 def test_ragged_requests_parity():
     spec = dataclasses.replace(W.CONFIGS["ragged_cand"], topk=64, cand_topk=48, requests=(
         W.RequestSpec(100, 0, 1), W.RequestSpec(37, 0, 2), W.RequestSpec(0, 0, 1),
