@@ -86,6 +86,16 @@ def fp8_peak_tflops():
     return FALLBACK_BF16_TFLOPS * FP8_PER_BF16, "fallback 1.9 PF bf16 x2, of fallback"
 
 
+def epilogue_ceiling(pairs, H, kernel_ms, clk):
+    """The epilogue's own bound: ReLU and one weighted add per (row, head, key), 2*H
+    FP32 operations per pair on 128 FP32 lanes per SM (152 SMs) at the sampled SM clock."""
+    mhz = clk.get("sm_mhz") or clk.get("sm_max_mhz") or 2070.0
+    peak_ops = 152 * 128 * float(mhz) * 1e6
+    achieved = 2.0 * H * pairs / (kernel_ms / 1e3)
+    return {"ops_per_pair": 2 * H, "achieved_ops": achieved, "peak_ops": peak_ops,
+            "frac": achieved / peak_ops, "sm_mhz": mhz}
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
 
@@ -373,12 +383,13 @@ def main():
         "peak_transient_bytes": plan.workspace_bytes,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "logits_tc_kernel<32,128,fp8,fixed-threshold sink> in "
+                     "kernel": "logits_tc_kernel<32,128,fixed-threshold sink> in "
                                "indexer_fused_topk",
                      "kernel_ms": kms, "kernel_share_of_step": kms / ms,
                      "flops_per_launch": flops, "peak_source": peak_note,
                      "dense_logits_kernel_ms": lms,
-                     "dense_logits_frac": flops / (lms / 1e3) / 1e12 / peak},
+                     "dense_logits_frac": flops / (lms / 1e3) / 1e12 / peak,
+                     "cuda_core_co_ceiling": epilogue_ceiling(pairs, spec.H, kms, clk)},
         "e2e": {"value": pairs / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ems},
         "gpu_launches": launches,
