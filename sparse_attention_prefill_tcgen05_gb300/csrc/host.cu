@@ -64,6 +64,8 @@ struct indexer_plan_s {
     // sampled and its rows keep everything); sample_cols columns per row;
     // sample_stride = the largest stride, 0 = no request is sampled
     int sample_stride = 0, sample_cols = 0;
+    // the candidate-block path samples too (its pass list areas hold the samples)
+    bool sample_blocks = false;
     std::vector<int32_t> sample_stride_r, sample_rank_r;
     size_t off_gtau = 0, off_fail = 0, off_tau = 0, off_counts = 0, off_lists = 0, ws_bytes = 0;
     long long wait_budget = 4000000000LL;
@@ -351,8 +353,10 @@ int launch_merge(Ctx& c, StreamMergeParams& mp)
 }
 
 // Sampled logits of the pass's rows (every sample_stride-th key tile of each
-// request) into `samples` [rows, sample_cols], then each row's threshold.
-int pass_thresholds(Ctx& c, const Pass& ps, float* samples, uint32_t* tau_row)
+// request) into `samples` [rows, sample_cols], then each row's threshold for its
+// top `keep` keys (pool = 1) or its top `keep` pool-key blocks.
+int pass_thresholds(Ctx& c, const Pass& ps, float* samples, uint32_t* tau_row, int pool,
+                    int keep)
 {
     const indexer_plan_s* p = c.p;
     LogitsParams& lp = c.lp;
@@ -399,7 +403,8 @@ int pass_thresholds(Ctx& c, const Pass& ps, float* samples, uint32_t* tau_row)
     sp.ld = p->sample_cols;
     sp.row0 = first;
     sp.rows = rows;
-    sp.k = p->topk;
+    sp.k = keep;
+    sp.pool = pool > 1 ? pool : 1;
     sp.compress_len = c.lp.compress_len;
     sp.tau_row = tau_row;
     sp.num_requests = p->R;
@@ -428,7 +433,7 @@ int run_streamed(Ctx& c, uint8_t* ws, int pool, int32_t* out_idx, float* out_val
     const std::vector<Pass>& passes = pool ? p->passes_b : p->passes_k;
     const std::vector<int32_t>& cap = pool ? p->cap_b : p->cap_k;
     const int keep = pool ? p->cand_topk : p->topk;
-    const bool sampled = pool == 0 && p->sample_stride > 0;
+    const bool sampled = pool == 0 ? p->sample_stride > 0 : p->sample_blocks;
     LogitsParams& lp = c.lp;
     lp.lists = reinterpret_cast<uint2*>(ws + p->off_lists);
     lp.counts = reinterpret_cast<uint32_t*>(ws + p->off_counts);
@@ -452,14 +457,15 @@ int run_streamed(Ctx& c, uint8_t* ws, int pool, int32_t* out_idx, float* out_val
         StreamMergeParams mp;
         int rc;
         if (sampled) {
-            if ((rc = pass_thresholds(c, ps, reinterpret_cast<float*>(lp.lists), tau_row)) !=
-                IDX_OK)
+            if ((rc = pass_thresholds(c, ps, reinterpret_cast<float*>(lp.lists), tau_row, pool,
+                                      keep)) != IDX_OK)
                 return rc;
             lp.tau_row = tau_row;
             lp.row_fail = nullptr;
             const bool prof = &ps == &passes.front();
             if (prof) record_prof(c, g_prof_start);
-            if ((rc = pass_launches(c, ps, cap, kSinkFilter, mp)) != IDX_OK)
+            if ((rc = pass_launches(c, ps, cap, pool ? kSinkPoolFilter : kSinkFilter, mp)) !=
+                IDX_OK)
                 return rc;
             if (prof) record_prof(c, g_prof_stop);
             finish(mp);
@@ -718,9 +724,6 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
             const int st = (int)ceil_div(tiles, kSampleTiles);
             const double mu = (double)p->topk / st;
             const int cols = (int)ceil_div(tiles, st) * kTileKeys;
-            // the samples of a pass live in its list area
-            if ((int64_t)cols * 4 > (int64_t)p->n_splits[r] * kListsPerSplit * p->cap_k[r] * 8)
-                continue;
             p->sample_stride_r[r] = st;
             p->sample_rank_r[r] = (int)std::ceil(mu + 5.0 * std::sqrt(mu) + 4.0);   // (nonzero:
             // sampled; the kernel ranks each row by its own sample fraction)
@@ -728,12 +731,7 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
             p->sample_cols = std::max(p->sample_cols, cols);
         }
         // every row of a sampled pass has a sample row, sampled or not
-        for (int r = 0; r < R && p->sample_stride > 0; ++r)
-            if ((int64_t)p->sample_cols * 4 >
-                (int64_t)p->n_splits[r] * kListsPerSplit * p->cap_k[r] * 8) {
-                p->sample_stride = 0;
-                p->sample_rank_r.assign(R, 0);
-            }
+        p->sample_blocks = ct > 0 && p->sample_stride > 0;
     }
     size_t off = kStatusBytes;
     p->off_pad = off;
@@ -764,6 +762,32 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
     int64_t need = pass_entries(*p, p->passes_k, p->cap_k);
     if (ct)
         need = std::max(need, pass_entries(*p, p->passes_b, p->cap_b));
+    // a pass's sampled logits [rows, sample_cols] go to the list area first; a path
+    // whose samples do not fit the budget is not sampled
+    auto sample_entries = [&](const std::vector<Pass>& passes) {
+        int64_t m = 0;
+        for (const Pass& ps : passes)
+            m = std::max<int64_t>(m, (int64_t)(ps.pieces.back().b - ps.pieces.front().a) *
+                                         p->sample_cols / 2);
+        return m;
+    };
+    if (p->sample_stride > 0) {
+        const int64_t sk = sample_entries(p->passes_k);
+        if (sk <= entries) {
+            need = std::max(need, sk);
+        } else {
+            p->sample_stride = 0;
+            p->sample_rank_r.assign(R, 0);
+            p->sample_blocks = false;
+        }
+    }
+    if (p->sample_blocks) {
+        const int64_t sb = sample_entries(p->passes_b);
+        if (sb <= entries)
+            need = std::max(need, sb);
+        else
+            p->sample_blocks = false;
+    }
     p->ws_bytes = align_up(off + (size_t)std::max<int64_t>(need, 1) * 8, 256);
     *out = p;
     if (ws_bytes)
@@ -935,7 +959,8 @@ int indexer_candidate_blocks(indexer_plan_t p, const void* q, const float* s_q, 
     if ((rc = prepare(c, q, s_q, w, k, k_scale, clen, ws)) != IDX_OK)
         return rc;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
-    if (cudaMemsetAsync(wsb + p->off_gtau, 0, (size_t)p->T * 4, c.st) != cudaSuccess)
+    // shared bounds and row flags (contiguous)
+    if (cudaMemsetAsync(wsb + p->off_gtau, 0, (size_t)p->T * 8, c.st) != cudaSuccess)
         return IDX_ERR_CUDA;
     return run_streamed(c, wsb, p->cand_block, nullptr, nullptr, cand_mask, ld_mask);
 }

@@ -26,6 +26,7 @@ constexpr int kSinkLogits = 0;   // write fp32 to a [rows, ld] buffer
 constexpr int kSinkStream = 1;   // append threshold-passing (score, key) to per-row lists
 constexpr int kSinkPool = 2;     // same over cand_block-key block maxima (candidate blocks)
 constexpr int kSinkFilter = 3;   // append entries at or above a fixed per-row threshold
+constexpr int kSinkPoolFilter = 4;  // the same over cand_block-key block maxima
 
 constexpr int kListsPerSplit = 4;     // one candidate sub-list per epilogue warp quadrant
 constexpr int kMaxStreamSlots = 256;  // sub-lists per row (key splits x kListsPerSplit)
@@ -142,7 +143,9 @@ cudaError_t launch_topk_dense(const TopkParams& p, cudaStream_t stream);
 // Per-row thresholds from sampled logits [rows, ld] (row t at t - row0): about
 // the largest sample of rank mu + 5 sqrt(mu) + 4, mu = k * the row's sampled
 // fraction, or 0 (everything passes) for rows of unsampled requests (stride 0),
-// rows with at most k valid keys and rows with fewer samples.
+// rows with at most k valid keys and rows with fewer samples.  With pool > 1 the
+// ranked samples are the maxima of aligned pool-key blocks of the sampled keys
+// and k counts blocks.
 struct SampleParams {
     const float* samples;
     int64_t ld;
@@ -150,6 +153,8 @@ struct SampleParams {
     int32_t rows;
     int32_t k;
     int32_t num_requests;
+    int32_t pool;                // keys per ranked entry (1: keys; 2, 4, 8: block maxima)
+    int32_t pad_;
     const int32_t* compress_len;
     uint32_t* tau_row;           // [total rows], written at row0 .. row0 + rows - 1
     int32_t req_row_begin[kMaxRequests + 1];

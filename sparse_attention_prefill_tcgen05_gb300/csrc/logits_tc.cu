@@ -46,7 +46,8 @@
 //     skipped, so the exact selection over the lists (select.cu) equals the
 //     top-k over all keys.
 //   * kSinkPool: the same over the maximum of each cand_block-key block
-//     (candidate blocks, same section: 8-key block pooling, top-2048 blocks).
+//     (candidate blocks, same section: 8-key block pooling, top-2048 blocks);
+//   * kSinkPoolFilter: kSinkFilter over those block maxima.
 // The accumulator is double-buffered so the epilogue of tile i overlaps the
 // MMAs of tile i+1, and it is handed back as soon as its last column is in
 // registers.
@@ -273,7 +274,9 @@ __device__ __forceinline__ uint32_t warp_sum_bins(const uint32_t* hist, int lane
     return s;
 }
 
-template <int H, int D, int SINK>
+// MASK: the launch applies a candidate-block mask (a separate instantiation, so that
+// the unmasked kernels carry none of its registers).
+template <int H, int D, int SINK, bool MASK>
 __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
     logits_tc_kernel(const __grid_constant__ LogitsParams p)
 {
@@ -533,7 +536,7 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                 tau_lo[ro] = 0;
                 b1[ro] = 256;
                 wcnt[ro] = 0;
-                if constexpr (SINK == kSinkFilter) {
+                if constexpr (SINK == kSinkFilter || SINK == kSinkPoolFilter) {
                     // as a float: v >= it <=> ord(v) >= tau for every v but -0.0 against
                     // tau = ord(+0.0), which only lets -0.0 entries through as well (still
                     // every entry at or above a threshold); tau = 0 passes every finite v
@@ -581,20 +584,56 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
             float sk_next = 0.0f;
             if (ui.ntiles_mma > 0)
                 sk_next = __ldg(sk_row + min(ui.j0 + quad * 32 + lane, sk_last));
+            // candidate-mask bytes of this thread's keys, one tile ahead like the key
+            // scales (row and key indices clamped: a byte read for a key that the
+            // causal test drops does not matter)
+            constexpr bool has_mask = MASK;
+            const int mshift = has_mask ? __ffs(p.mask_block) - 1 : 0;
+            const uint8_t* mrow[RO];
+#pragma unroll
+            for (int ro = 0; ro < RO; ++ro) {
+                const int rl = half * RPH + own_rr(ro);
+                mrow[ro] = has_mask ? p.cand_mask + (size_t)(ui.t0 + min(rl, ui.nr - 1)) * p.ld_mask
+                                    : nullptr;
+            }
+            auto mask_at = [&](int m, int jt0) -> uint32_t {
+                const int ro = RPH >= 4 ? (m >> 2) : 0;
+                const int j = min(jt0 + 8 * slot_bl(RPH >= 4 ? (m & 3) : m) + g, sk_last);
+                return __ldg(mrow[ro] + (j >> mshift));
+            };
+            uint32_t mk_next[RPH];
+#pragma unroll
+            for (int m = 0; m < RPH; ++m)
+                mk_next[m] = (has_mask && ui.ntiles_mma > 0) ? mask_at(m, ui.j0 + quad * 32) : 1u;
             // a warp's sub-list sees 32 of every 128 keys (or its lanes' blocks)
             const int unit_entries_warp =
-                SINK == kSinkPool ? ui.ntiles * (32 / (p.pool > 0 ? p.pool : 1)) : ui.ntiles * 32;
+                (SINK == kSinkPool || SINK == kSinkPoolFilter)
+                    ? ui.ntiles * (32 / (p.pool > 0 ? p.pool : 1))
+                    : ui.ntiles * 32;
             const bool no_overflow = unit_entries_warp <= sg.cap;
             for (int i = 0; i < ui.ntiles; ++i) {
                 const int jt = ui.j0 + i * ui.step + quad * 32;   // first key of the quadrant
                 float val[RPH];
+                uint32_t mk_cur[RPH];
 #pragma unroll
-                for (int m = 0; m < RPH; ++m)
+                for (int m = 0; m < RPH; ++m) {
                     val[m] = -INFINITY;
+                    mk_cur[m] = 1u;
+                }
                 if (i < ui.ntiles_mma) {
                     const float sk_lane = sk_next;
                     if (i + 1 < ui.ntiles_mma)
                         sk_next = __ldg(sk_row + min(jt + ui.step + lane, sk_last));
+                    if constexpr (has_mask) {
+#pragma unroll
+                        for (int m = 0; m < RPH; ++m)
+                            mk_cur[m] = mk_next[m];
+                        if (i + 1 < ui.ntiles_mma) {
+#pragma unroll
+                            for (int m = 0; m < RPH; ++m)
+                                mk_next[m] = mask_at(m, jt + ui.step);
+                        }
+                    }
                     bool got = alive && mbar_wait(&a_full[ab], aph, budget, abort_flag);
                     got = __all_sync(0xffffffffu, got);
                     if (!got && alive) {
@@ -697,17 +736,13 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                 }
                 // causal and candidate masks (most tiles lie below every row's causal
                 // length: one warp-uniform test skips the per-value work there)
-                if (p.cand_mask != nullptr || ui.j0 + i * ui.step + kTileKeys > clen_min) {
+                if (has_mask || ui.j0 + i * ui.step + kTileKeys > clen_min) {
 #pragma unroll
                     for (int m = 0; m < RPH; ++m) {
                         const int ro = RPH >= 4 ? (m >> 2) : 0;
                         const int rl = half * RPH + own_rr(ro);
                         const int j = jt + 8 * slot_bl(RPH >= 4 ? (m & 3) : m) + g;
-                        bool valid = rl < ui.nr && j < clen[ro];
-                        if (valid && p.cand_mask)
-                            valid = p.cand_mask[(size_t)(ui.t0 + rl) * p.ld_mask +
-                                                j / p.mask_block] != 0;
-                        if (!valid)
+                        if (!(rl < ui.nr && j < clen[ro] && mk_cur[m] != 0u))
                             val[m] = -INFINITY;
                     }
                 }
@@ -739,6 +774,29 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                             if (pos < static_cast<uint32_t>(sg.cap))
                                 sub_own[ro][pos] =
                                     make_uint2(__float_as_uint(val[m]), static_cast<uint32_t>(j));
+                        }
+                        wcnt[ro] += __popc(mb);
+                    }
+                } else if constexpr (SINK == kSinkPoolFilter) {
+                    // the same over the maxima of cand_block-key blocks: the keys of a
+                    // block are lanes g of one q (xor over the g bits), its first lane
+                    // appends (block maximum, block index)
+#pragma unroll
+                    for (int m = 0; m < RPH; ++m) {
+                        const int ro = RPH >= 4 ? (m >> 2) : 0;
+                        const int rl = half * RPH + own_rr(ro);
+                        const int j = jt + 8 * slot_bl(RPH >= 4 ? (m & 3) : m) + g;
+                        float bm = val[m];
+                        for (int o = 1; o < p.pool; o <<= 1)
+                            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4 * o));
+                        const bool cand = (g % p.pool) == 0 && rl < ui.nr &&
+                                          bm >= __uint_as_float(tau_hi[ro]);
+                        const uint32_t mb = __ballot_sync(0xffffffffu, cand) & rowmask;
+                        if (cand) {
+                            const uint32_t pos = wcnt[ro] + __popc(mb & lanes_below);
+                            if (pos < static_cast<uint32_t>(sg.cap))
+                                sub_own[ro][pos] = make_uint2(__float_as_uint(bm),
+                                                              static_cast<uint32_t>(j / p.pool));
                         }
                         wcnt[ro] += __popc(mb);
                     }
@@ -919,7 +977,8 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                         if (rl < ui.nr)
                             p.counts[sg.cnt_offset +
                                      (int64_t)(ui.t0 + rl - sg.row_begin) * sg.cnt_ld + quad] =
-                                SINK == kSinkFilter ? wcnt[ro]
+                                (SINK == kSinkFilter || SINK == kSinkPoolFilter)
+                                    ? wcnt[ro]
                                                     : min(wcnt[ro], static_cast<uint32_t>(sg.cap));
                     }
                 }
@@ -936,11 +995,11 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
         tmem_dealloc(tmem_base, 512);
 }
 
-template <int H, int D, int SINK>
+template <int H, int D, int SINK, bool MASK>
 cudaError_t launch_one(const LogitsParams& p, int grid, cudaStream_t stream)
 {
     using C = Cfg<H, D, SINK>;
-    auto kern = logits_tc_kernel<H, D, SINK>;
+    auto kern = logits_tc_kernel<H, D, SINK, MASK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);
     if (e != cudaSuccess)
@@ -952,14 +1011,24 @@ cudaError_t launch_one(const LogitsParams& p, int grid, cudaStream_t stream)
 template <int H, int D>
 cudaError_t launch_sink(const LogitsParams& p, int sink, int grid, cudaStream_t stream)
 {
+    // masked launches: the consumer's key paths (samples, fixed threshold, stream);
+    // the candidate producer itself is never masked
+    const bool m = p.cand_mask != nullptr;
     if (sink == kSinkLogits)
-        return launch_one<H, D, kSinkLogits>(p, grid, stream);
+        return m ? launch_one<H, D, kSinkLogits, true>(p, grid, stream)
+                 : launch_one<H, D, kSinkLogits, false>(p, grid, stream);
     if (sink == kSinkStream)
-        return launch_one<H, D, kSinkStream>(p, grid, stream);
-    if (sink == kSinkPool)
-        return launch_one<H, D, kSinkPool>(p, grid, stream);
+        return m ? launch_one<H, D, kSinkStream, true>(p, grid, stream)
+                 : launch_one<H, D, kSinkStream, false>(p, grid, stream);
     if (sink == kSinkFilter)
-        return launch_one<H, D, kSinkFilter>(p, grid, stream);
+        return m ? launch_one<H, D, kSinkFilter, true>(p, grid, stream)
+                 : launch_one<H, D, kSinkFilter, false>(p, grid, stream);
+    if (m)
+        return cudaErrorInvalidValue;
+    if (sink == kSinkPool)
+        return launch_one<H, D, kSinkPool, false>(p, grid, stream);
+    if (sink == kSinkPoolFilter)
+        return launch_one<H, D, kSinkPoolFilter, false>(p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

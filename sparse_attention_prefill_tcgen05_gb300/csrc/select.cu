@@ -543,32 +543,45 @@ __global__ void __launch_bounds__(kSelThreads)
     const int req = find_request(p.req_row_begin, p.num_requests, t);
     const int stride = p.req_rank[req];     // sampling stride (0: not sampled)
     const int clen = min(p.compress_len[t], p.req_key_count[req]);
+    const int pool = p.pool > 1 ? p.pool : 1;
+    const int units = (clen + pool - 1) / pool;   // keys, or blocks, the row ranks
     uint32_t* tau_out = p.tau_row + t;
     // rows that keep every entry: unsampled requests and rows with at most k keys
-    if (stride == 0 || clen <= p.k) {
+    // (blocks)
+    if (stride == 0 || units <= p.k) {
         if (threadIdx.x == 0)
             *tau_out = 0u;
         return;
     }
     const int64_t ld = p.ld;
-    const int n = static_cast<int>(ld);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float* row = p.samples + (int64_t)blockIdx.x * ld;
-    // the row once into shared memory (ld is a multiple of 128: float4 loads), with
-    // the range and the count of its finite samples
+    // the row once into shared memory (ld is a multiple of 128: float4 loads)
+    for (int e = threadIdx.x; e < static_cast<int>(ld) / 4; e += kSelThreads)
+        reinterpret_cast<float4*>(srow)[e] = reinterpret_cast<const float4*>(row)[e];
+    // blocks: the maximum of each aligned pool-key group (sampled tiles are whole
+    // 128-key tiles, so every group is a whole block of the row)
+    const int n = static_cast<int>(ld) / pool;
+    float* vals = srow;
+    __syncthreads();
+    if (pool > 1) {
+        vals = srow + ld;
+        for (int b = threadIdx.x; b < n; b += kSelThreads) {
+            float m = -INFINITY;
+            for (int x = 0; x < pool; ++x)
+                m = fmaxf(m, srow[b * pool + x]);
+            vals[b] = m;
+        }
+        __syncthreads();
+    }
+    // the range and the count of the finite samples
     uint32_t omin = 0xFFFFFFFFu, omax = 0u, cnt = 0;
-    for (int e = threadIdx.x; e < n / 4; e += kSelThreads) {
-        const float4 v4 = reinterpret_cast<const float4*>(row)[e];
-        reinterpret_cast<float4*>(srow)[e] = v4;
-        const float v[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            const uint32_t o = f2ord(v[x]);
-            if (o > kOrdNegInf) {
-                omin = min(omin, o);
-                omax = max(omax, o);
-                ++cnt;
-            }
+    for (int e = threadIdx.x; e < n; e += kSelThreads) {
+        const uint32_t o = f2ord(vals[e]);
+        if (o > kOrdNegInf) {
+            omin = min(omin, o);
+            omax = max(omax, o);
+            ++cnt;
         }
     }
     for (int i = threadIdx.x; i < kBuckets; i += kSelThreads)
@@ -589,10 +602,10 @@ __global__ void __launch_bounds__(kSelThreads)
         m += sh.warp_sum[w];
     }
     // mu = samples expected among the row's top k: k times the sampled fraction,
-    // which is m / clen for a short row (its first tile is always sampled) and
+    // which is m / units for a short row (its first tile is always sampled) and
     // 1 / stride when a candidate mask leaves fewer eligible keys than clen; the
     // threshold is the sample of rank mu + 5 sqrt(mu) + 4
-    const float frac = fmaxf(static_cast<float>(m) / static_cast<float>(clen),
+    const float frac = fmaxf(static_cast<float>(m) / static_cast<float>(units),
                              1.0f / static_cast<float>(stride));
     const float mu = static_cast<float>(p.k) * frac;
     const int rank = static_cast<int>(ceilf(mu + 5.0f * sqrtf(mu) + 4.0f));
@@ -609,7 +622,7 @@ __global__ void __launch_bounds__(kSelThreads)
         bt.scale = 0.0f;                      // degenerate range: one bucket
     __syncthreads();                          // (sh is reused by the scan below)
     for (int e = threadIdx.x; e < n; e += kSelThreads) {
-        const float v = srow[e];
+        const float v = vals[e];
         if (f2ord(v) > kOrdNegInf)
             atomicAdd(&bhist[bt.bucket(v)], 1u);
     }
@@ -639,7 +652,7 @@ __global__ void __launch_bounds__(kSelThreads)
     const int bnd = s_bnd;
     uint32_t tmin = 0xFFFFFFFFu;
     for (int e = threadIdx.x; e < n; e += kSelThreads) {
-        const float v = srow[e];
+        const float v = vals[e];
         const uint32_t o = f2ord(v);
         if (o > kOrdNegInf && bt.bucket(v) >= bnd)
             tmin = min(tmin, o);
@@ -712,7 +725,16 @@ cudaError_t launch_sample_threshold(const SampleParams& p, cudaStream_t stream)
         return cudaSuccess;
     if (p.ld % 4 != 0 || p.ld > 16384)
         return cudaErrorInvalidValue;
-    sample_threshold_kernel<<<p.rows, kSelThreads, p.ld * sizeof(float), stream>>>(p);
+    const int pool = p.pool > 1 ? p.pool : 1;
+    const size_t dyn = (p.ld + (pool > 1 ? p.ld / pool : 0)) * sizeof(float);
+    if (dyn > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(sample_threshold_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)dyn);
+        if (e != cudaSuccess)
+            return e;
+    }
+    sample_threshold_kernel<<<p.rows, kSelThreads, dyn, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -318,6 +318,55 @@ def test_candidate_blocks_and_masked_consumer_scaled():
         assert np.array_equal(km[t], ((j < cl[t]) & (mask[t][j // 8] != 0)).astype(np.uint8))
 
 
+@pytest.mark.parametrize("block,cand_topk", [(8, 64), (4, 200)])
+def test_sampled_candidate_blocks_match_the_stream(block, cand_topk):
+    """Requests long enough to be sampled: the block threshold from pooled samples, the
+    fixed-threshold block lists and the verify merge give the same masks, bit for bit,
+    as the exact stream, and the oracle's (also on the GPU's own logits)."""
+    spec = dataclasses.replace(
+        W.CONFIGS["ragged_cand"], topk=64, cand_block=block, cand_topk=cand_topk,
+        requests=(W.RequestSpec(20, 16364, 1), W.RequestSpec(12, 9000, 2)), seed=11)
+    p = W.make_problem(spec)
+    plan = Hp.make_plan(p)
+    assert plan.info()["sample_stride"] >= 2
+    d = Hp.device_inputs(p)
+    n0 = K.indexer_launch_count()
+    mask = Hp.gpu_candidates(p, plan, d).cpu().numpy()
+    n1 = K.indexer_launch_count()
+    mask_s = Hp.gpu_candidates(p, Hp.make_plan(p, select_mode=K.IDX_SELECT_STREAM),
+                               d).cpu().numpy()
+    # the sampled flow (samples, thresholds, filter, verify) launches more kernels
+    assert n1 - n0 > K.indexer_launch_count() - n1
+    assert np.array_equal(mask, mask_s)
+    T = int(p.cu_seqlens_q[-1])
+    ref = oracle_rows(p, np.arange(T))
+    cl = p.compress_len.numpy()
+    for t in range(T):
+        Hp.check_mask_row(mask[t], ref[t], int(cl[t]), block, cand_topk)
+    g = Hp.gpu_logits(p, plan, d).cpu().numpy().astype(np.float64)
+    assert np.array_equal(O.candidates_rows(g, cl, block, cand_topk, mask.shape[1]), mask)
+
+
+@pytest.mark.parametrize("sampled_high", [True, False])
+def test_sampled_candidate_threshold_fallbacks(sampled_high):
+    """Sampled tiles scoring above every other key put the block threshold too high (the
+    rows go to the exact stream); scoring below, nearly every block passes."""
+    L, rows, cand_topk = 16384, 24, 256
+    p, _ = _sampled_problem(L, rows, 64, sampled_high)
+    p = dataclasses.replace(p, spec=dataclasses.replace(p.spec, cand_block=8,
+                                                        cand_topk=cand_topk))
+    plan = Hp.make_plan(p)
+    d = Hp.device_inputs(p)
+    mask = Hp.gpu_candidates(p, plan, d).cpu().numpy()
+    ref = oracle_rows(p, np.arange(rows))
+    cl = p.compress_len.numpy()
+    for t in range(rows):
+        pooled = Hp.pooled_scores(ref[t], int(cl[t]), 8)
+        want = np.zeros(mask.shape[1], dtype=np.uint8)
+        want[np.argsort(-pooled, kind="stable")[:cand_topk]] = 1
+        assert np.array_equal(mask[t], want), t
+
+
 # ----------------------------------------------------------- full size
 
 def full_size_check(name, per_request, layer_mask=None):
