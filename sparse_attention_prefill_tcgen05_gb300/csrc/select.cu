@@ -532,7 +532,10 @@ __global__ void __launch_bounds__(kSelThreads)
 // row has fewer than rank finite samples.  At least rank samples are at or
 // above it.  Any threshold keeps the selection exact (rows the lists cannot
 // decide are selected again); this one is close to the rank-th sample.
-__global__ void __launch_bounds__(kSelThreads)
+// POOLED: the ranked entries are block maxima (p.pool > 1); the key version keeps
+// its registers low enough for four CTAs per SM.
+template <bool POOLED>
+__global__ void __launch_bounds__(kSelThreads, 2048 / kSelThreads)
     sample_threshold_kernel(const __grid_constant__ SampleParams p)
 {
     __shared__ Scratch sh;
@@ -543,7 +546,7 @@ __global__ void __launch_bounds__(kSelThreads)
     const int req = find_request(p.req_row_begin, p.num_requests, t);
     const int stride = p.req_rank[req];     // sampling stride (0: not sampled)
     const int clen = min(p.compress_len[t], p.req_key_count[req]);
-    const int pool = p.pool > 1 ? p.pool : 1;
+    const int pool = POOLED ? p.pool : 1;
     const int units = (clen + pool - 1) / pool;   // keys, or blocks, the row ranks
     uint32_t* tau_out = p.tau_row + t;
     // rows that keep every entry: unsampled requests and rows with at most k keys
@@ -556,32 +559,41 @@ __global__ void __launch_bounds__(kSelThreads)
     const int64_t ld = p.ld;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float* row = p.samples + (int64_t)blockIdx.x * ld;
-    // the row once into shared memory (ld is a multiple of 128: float4 loads)
-    for (int e = threadIdx.x; e < static_cast<int>(ld) / 4; e += kSelThreads)
-        reinterpret_cast<float4*>(srow)[e] = reinterpret_cast<const float4*>(row)[e];
+    // the row once into shared memory (ld is a multiple of 128: float4 loads), with
+    // the range and the count of its finite samples (keys)
+    uint32_t omin = 0xFFFFFFFFu, omax = 0u, cnt = 0;
+    auto count = [&](float v) {
+        const uint32_t o = f2ord(v);
+        if (o > kOrdNegInf) {
+            omin = min(omin, o);
+            omax = max(omax, o);
+            ++cnt;
+        }
+    };
+    for (int e = threadIdx.x; e < static_cast<int>(ld) / 4; e += kSelThreads) {
+        const float4 v4 = reinterpret_cast<const float4*>(row)[e];
+        reinterpret_cast<float4*>(srow)[e] = v4;
+        if constexpr (!POOLED) {
+            count(v4.x);
+            count(v4.y);
+            count(v4.z);
+            count(v4.w);
+        }
+    }
     // blocks: the maximum of each aligned pool-key group (sampled tiles are whole
-    // 128-key tiles, so every group is a whole block of the row)
+    // 128-key tiles, so every group is a whole block of the row), then their range
+    // and count
     const int n = static_cast<int>(ld) / pool;
     float* vals = srow;
-    __syncthreads();
-    if (pool > 1) {
+    if constexpr (POOLED) {
+        __syncthreads();
         vals = srow + ld;
         for (int b = threadIdx.x; b < n; b += kSelThreads) {
             float m = -INFINITY;
             for (int x = 0; x < pool; ++x)
                 m = fmaxf(m, srow[b * pool + x]);
             vals[b] = m;
-        }
-        __syncthreads();
-    }
-    // the range and the count of the finite samples
-    uint32_t omin = 0xFFFFFFFFu, omax = 0u, cnt = 0;
-    for (int e = threadIdx.x; e < n; e += kSelThreads) {
-        const uint32_t o = f2ord(vals[e]);
-        if (o > kOrdNegInf) {
-            omin = min(omin, o);
-            omax = max(omax, o);
-            ++cnt;
+            count(m);
         }
     }
     for (int i = threadIdx.x; i < kBuckets; i += kSelThreads)
@@ -725,16 +737,16 @@ cudaError_t launch_sample_threshold(const SampleParams& p, cudaStream_t stream)
         return cudaSuccess;
     if (p.ld % 4 != 0 || p.ld > 16384)
         return cudaErrorInvalidValue;
-    const int pool = p.pool > 1 ? p.pool : 1;
-    const size_t dyn = (p.ld + (pool > 1 ? p.ld / pool : 0)) * sizeof(float);
+    const bool pooled = p.pool > 1;
+    const size_t dyn = (p.ld + (pooled ? p.ld / p.pool : 0)) * sizeof(float);
+    auto kern = pooled ? sample_threshold_kernel<true> : sample_threshold_kernel<false>;
     if (dyn > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(sample_threshold_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)dyn);
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
         if (e != cudaSuccess)
             return e;
     }
-    sample_threshold_kernel<<<p.rows, kSelThreads, dyn, stream>>>(p);
+    kern<<<p.rows, kSelThreads, dyn, stream>>>(p);
     return cudaGetLastError();
 }
 
