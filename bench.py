@@ -86,6 +86,52 @@ def fp8_peak_tflops():
     return FALLBACK_BF16_TFLOPS * FP8_PER_BF16, "fallback 1.9 PF bf16 x2, of fallback"
 
 
+def e2e_pipelined(K, plan, pinned, d0, idx0, val0, wsb, out_host, stream, n):
+    """Milliseconds per step of n end-to-end steps run the way a serving loop overlaps
+    them: two sets of device buffers, the host-to-device copy of step i+1 and the
+    device-to-host copy of step i-1's indices on a copy stream while step i computes."""
+    import torch
+    dbuf = [d0, {nm: torch.empty_like(t) for nm, t in d0.items()}]
+    obuf = [(idx0, val0), (torch.empty_like(idx0), torch.empty_like(val0))]
+    cs = torch.cuda.Stream()
+
+    def run(steps):
+        ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+        ev_done = [torch.cuda.Event(), torch.cuda.Event()]
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            for nm, t in pinned.items():
+                dbuf[0][nm].copy_(t, non_blocking=True)
+            ev_in[0].record(cs)
+        for i in range(steps):
+            b = i % 2
+            stream.wait_event(ev_in[b])
+            db, (oi, ov) = dbuf[b], obuf[b]
+            K.indexer_fused_topk(plan, db["q"], db["s_q"], db["w"], db["k"], db["k_scale"],
+                                 db["compress_len"], None, oi, ov, wsb)
+            ev_done[b].record(stream)
+            with torch.cuda.stream(cs):
+                if i + 1 < steps:
+                    nb = 1 - b
+                    if i >= 1:
+                        cs.wait_event(ev_done[nb])   # step i-1 is done with those buffers
+                    for nm, t in pinned.items():
+                        dbuf[nb][nm].copy_(t, non_blocking=True)
+                    ev_in[nb].record(cs)
+                cs.wait_event(ev_done[b])
+                out_host[b].copy_(oi, non_blocking=True)
+        stream.wait_stream(cs)
+        end.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / steps
+
+    run(3)
+    return run(n)
+
+
 def epilogue_ceiling(pairs, H, kernel_ms, clk):
     """The epilogue's own bound: ReLU and one weighted add per (row, head, key), 2*H
     FP32 operations per pair on 128 FP32 lanes per SM (152 SMs) at the sampled SM clock."""
@@ -349,22 +395,25 @@ def main():
     achieved = flops / (kms / 1e3) / 1e12
     traffic = profiled_traffic()
 
-    # end to end through the C ABI with host buffers: H2D inputs, fused call, D2H indices
+    # end to end through the C ABI with host buffers: every step copies its inputs from
+    # pinned host memory, runs the fused call and copies its indices back.
     pinned = {n: t.pin_memory() for n, t in host.items()}
-    out_host = torch.empty((T, p.topk), dtype=torch.int32).pin_memory()
+    out_host = [torch.empty((T, p.topk), dtype=torch.int32).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
-    d2h = out_host.numel() * out_host.element_size()
+    d2h = out_host[0].numel() * out_host[0].element_size()
 
     def e2e_step():
         for n, t in pinned.items():
             d[n].copy_(t, non_blocking=True)
         step()
-        out_host.copy_(idx, non_blocking=True)
+        out_host[0].copy_(idx, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
     etimes = timed(e2e_step, max(10, min(args.steps, 100)))
-    ems = statistics.mean(etimes)
+    ems_serial = statistics.mean(etimes)
+    ems = e2e_pipelined(K, plan, pinned, d, idx, val, wsb, out_host, stream,
+                        max(10, min(args.steps, 100)))
     clk = clocks.stop()
 
     line = {
@@ -391,7 +440,12 @@ def main():
                      "dense_logits_frac": flops / (lms / 1e3) / 1e12 / peak,
                      "cuda_core_co_ceiling": epilogue_ceiling(pairs, spec.H, kms, clk)},
         "e2e": {"value": pairs / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": ems},
+                "d2h_bytes_per_step": d2h, "ms_per_step": ems,
+                "how": "pipelined: step i+1's inputs go up and step i-1's indices come down "
+                       "on a copy stream while step i computes (double-buffered); the timed "
+                       "region spans every step's copies",
+                "serial_ms_per_step": ems_serial,
+                "serial_value": pairs / (ems_serial / 1e3)},
         "gpu_launches": launches,
         "clocks": clk,
         "memory_allocated_bytes": mem0,
