@@ -62,7 +62,7 @@ extern "C" {
 /* Status codes. */
 #define IDX_OK 0
 #define IDX_ERR_INVALID_ARG (-1)   /* bad size, pointer, alignment or layout */
-#define IDX_ERR_UNSUPPORTED (-2)   /* shape/format this build has no kernel for, or not sm_103 */
+#define IDX_ERR_UNSUPPORTED (-2)   /* shape/format the library has no kernel for, or not sm_103 */
 #define IDX_ERR_WORKSPACE (-3)     /* workspace too small, or budget impossible at plan time */
 #define IDX_ERR_CUDA (-4)          /* a CUDA runtime/driver call failed */
 #define IDX_ERR_TIMEOUT (-5)       /* a device-side wait ran out (reported by indexer_status) */
