@@ -267,6 +267,23 @@ long long indexer_launch_count(void);
    the events are owned by the caller. */
 void indexer_profile_main_kernel(void* start_event, void* stop_event);
 
+/* ------------------------------------------------------------ chunk planner
+ * Adaptive prefill chunk ("chunked-prefill-memory.md", section 2.1, for callers
+ * that still materialise [T, L] fp32 logits and must keep T x L under a budget):
+ * for a prefix of prefix_len compressed keys
+ *     chunk(L) = clamp( round_down( budget_token2 / L ), chunk_min, chunk_max )
+ * where round_down goes to a multiple of `page` (pow2 == 0: the section's
+ * formula) or to a power of two (pow2 != 0: this reproduces the schedule the
+ * section prints -- 2048 up to ~98k keys, 1024 to ~195k, 512 to ~390k, 256
+ * beyond).  The section's values: budget_token2 = 2.0e8, chunk_min = 256,
+ * chunk_max = 2048, page = 256.  prefix_len <= 0 gives chunk_max.
+ * Returns the chunk (>= chunk_min > 0), or IDX_ERR_INVALID_ARG when
+ * budget_token2 <= 0 (or not finite), chunk_min < 1, chunk_max < chunk_min or
+ * page < 1.  Host only: no device, no allocation, thread-safe.
+ */
+int indexer_chunk_rows(int64_t prefix_len, double budget_token2, int32_t chunk_min,
+                       int32_t chunk_max, int32_t page, int32_t pow2);
+
 const char* indexer_error_string(int status);
 int indexer_version(void);
 

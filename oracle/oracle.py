@@ -8,7 +8,9 @@ generator as plain arrays.
 
 The arithmetic lives in ``oracle.c`` (see its header for the definition and
 the passages it follows); this file only marshals arguments and walks the
-ragged batch one request at a time.
+ragged batch one request at a time, except for two small definitions written
+out here in plain Python: the adaptive chunk size (:func:`chunk_rows`) and the
+page-index transform (:func:`page_indices_rows`).
 """
 from __future__ import annotations
 
@@ -226,3 +228,23 @@ def problem_candidates(p, rows=None, nthreads=0, logits=None, ld_mask=None):
     if ld_mask is None:
         ld_mask = (vals.shape[1] + b - 1) // b
     return candidates_rows(vals, cl, b, p.spec.cand_topk, ld_mask, nthreads)
+
+
+def chunk_rows(prefix_len, budget_token2=2.0e8, chunk_min=256, chunk_max=2048, page=256,
+               pow2=False):
+    """Adaptive prefill chunk ("chunked-prefill-memory.md", section 2.1):
+    clamp(round_down(BUDGET / L), CHUNK_MIN, CHUNK_MAX), round_down to a multiple of the
+    page (the section's formula) or, with ``pow2``, to a power of two (the rounding its
+    printed schedule follows).  Exact rational arithmetic; prefix_len <= 0 -> chunk_max."""
+    from fractions import Fraction
+    import math
+    if prefix_len <= 0:
+        return chunk_max
+    x = math.floor(Fraction(budget_token2) / prefix_len)
+    if pow2:
+        c = 0
+        while x >= 1 and (c * 2 if c else 1) <= x:
+            c = c * 2 if c else 1
+    else:
+        c = x // page * page
+    return min(chunk_max, max(chunk_min, c))

@@ -34,7 +34,8 @@ EXPORTED = ("indexer_plan", "indexer_plan_destroy", "indexer_plan_info", "indexe
             "indexer_topk", "indexer_fused_topk", "indexer_candidate_blocks",
             "indexer_expand_mask", "indexer_status", "indexer_selftest_timeout",
             "indexer_set_wait_budget", "indexer_launch_count", "indexer_error_string",
-            "indexer_version", "indexer_fused_topk_noalloc", "indexer_profile_main_kernel")
+            "indexer_version", "indexer_fused_topk_noalloc", "indexer_profile_main_kernel",
+            "indexer_chunk_rows")
 IDX_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -91,6 +92,7 @@ def lib():
         L.indexer_profile_main_kernel.argtypes = [P, P]
         L.indexer_profile_main_kernel.restype = None
         L.indexer_fused_topk_noalloc.argtypes = [P, P, P, P, P, P, P, P, i64, P, P, P]
+        L.indexer_chunk_rows.argtypes = [i64, ctypes.c_double, i32, i32, i32, i32]
         L.indexer_error_string.argtypes = [i32]
         L.indexer_error_string.restype = ctypes.c_char_p
         for name in EXPORTED:
@@ -241,3 +243,14 @@ def indexer_profile_main_kernel(start_event=None, stop_event=None):
 
 def indexer_version() -> int:
     return int(lib().indexer_version())
+
+
+def indexer_chunk_rows(prefix_len: int, budget_token2: float = 2.0e8, chunk_min: int = 256,
+                       chunk_max: int = 2048, page: int = 256, pow2: bool = False) -> int:
+    """Prefill chunk size for a prefix of ``prefix_len`` compressed keys under a T x L budget
+    (the library's host-only planner helper; raises on invalid arguments)."""
+    r = int(lib().indexer_chunk_rows(int(prefix_len), float(budget_token2), int(chunk_min),
+                                     int(chunk_max), int(page), 1 if pow2 else 0))
+    if r < 0:
+        raise IndexerError("indexer_chunk_rows", r)
+    return r

@@ -3,6 +3,7 @@
 // allocated here; every call is asynchronous on the caller's stream.
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -570,6 +571,28 @@ int prepare(Ctx& c, const void* q, const float* s_q, const float* w, const void*
 extern "C" {
 
 int indexer_version(void) { return 2; }
+
+int indexer_chunk_rows(int64_t prefix_len, double budget_token2, int32_t chunk_min,
+                       int32_t chunk_max, int32_t page, int32_t pow2)
+{
+    if (!(budget_token2 > 0.0) || !std::isfinite(budget_token2) || chunk_min < 1 ||
+        chunk_max < chunk_min || page < 1)
+        return IDX_ERR_INVALID_ARG;
+    if (prefix_len <= 0)
+        return chunk_max;
+    // budget / L, floored; anything at or above 2^40 rounds the same as 2^40
+    const double x = std::floor(budget_token2 / static_cast<double>(prefix_len));
+    const int64_t xi = x >= 1099511627776.0 ? (int64_t)1099511627776 : static_cast<int64_t>(x);
+    int64_t c = 0;
+    if (pow2) {
+        if (xi >= 1)
+            for (c = 1; c * 2 <= xi; c *= 2) {
+            }
+    } else {
+        c = xi / page * page;
+    }
+    return static_cast<int>(std::min<int64_t>(chunk_max, std::max<int64_t>(chunk_min, c)));
+}
 
 long long indexer_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
