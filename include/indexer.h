@@ -267,6 +267,28 @@ long long indexer_launch_count(void);
    the events are owned by the caller. */
 void indexer_profile_main_kernel(void* start_event, void* stop_event);
 
+/* ------------------------------------------------------ page-index transform
+ * The indexer's selected keys as KV-cache slots ("[SGLang PR 39187]",
+ * Accuracy / equivalence: the indexer's outputs are page_indices and
+ * raw_indices; the pages name the top-k-then-transform step without printing
+ * it, so this is the usual paged addressing):
+ *     page_idx[t, i] = page_table[r, j / page_size] * page_size + j % page_size
+ * for j = raw_idx[t, i] with 0 <= j < L_r, r the request of row t (the plan's
+ * cu_seqlens_q) and L_r its key count (cu_seqlens_k); -1 where j is -1 or out
+ * of [0, L_r), where the table entry is negative (an unmapped page), or where
+ * the slot does not fit an int32.
+ *   raw_idx, page_idx: device int32 [total_rows, topk] (the plan's topk), row-major;
+ *     page_idx may equal raw_idx (in place).
+ *   page_table: device int32 [num_requests, ld_page_table], row r holds request
+ *     r's physical page of each logical page; ld_page_table must be at least
+ *     ceil(max L_r / page_size), else IDX_ERR_INVALID_ARG.
+ *   page_size >= 1 (a power of two takes a shift path).
+ * Async on `stream`, no allocation, no workspace, no device-side errors.
+ */
+int indexer_page_indices(indexer_plan_t plan, const int32_t* raw_idx, const int32_t* page_table,
+                         int64_t ld_page_table, int32_t page_size, int32_t* page_idx,
+                         void* stream);
+
 /* ------------------------------------------------------------ chunk planner
  * Adaptive prefill chunk ("chunked-prefill-memory.md", section 2.1, for callers
  * that still materialise [T, L] fp32 logits and must keep T x L under a budget):

@@ -248,3 +248,27 @@ def chunk_rows(prefix_len, budget_token2=2.0e8, chunk_min=256, chunk_max=2048, p
     else:
         c = x // page * page
     return min(chunk_max, max(chunk_min, c))
+
+
+def page_indices_rows(raw_idx, row_request, key_count, page_table, page_size):
+    """KV-cache slot of each selected key ("[SGLang PR 39187]", Accuracy / equivalence:
+    the indexer emits page_indices beside raw_indices; the usual paged addressing):
+    slot = page_table[r, j // page_size] * page_size + j % page_size for 0 <= j < L_r,
+    -1 for j = -1, keys outside [0, L_r), negative (unmapped) table entries and slots past
+    the int32 range.  Plain loops over numpy arrays."""
+    raw = np.asarray(raw_idx, dtype=np.int64)
+    table = np.asarray(page_table, dtype=np.int64)
+    out = np.full(raw.shape, -1, dtype=np.int64)
+    for t in range(raw.shape[0]):
+        r = int(row_request[t])
+        for i in range(raw.shape[1]):
+            j = int(raw[t, i])
+            if j < 0 or j >= int(key_count[r]):
+                continue
+            page = int(table[r, j // page_size])
+            if page < 0:
+                continue
+            slot = page * page_size + j % page_size
+            if slot <= 2**31 - 1:
+                out[t, i] = slot
+    return out.astype(np.int32)

@@ -35,7 +35,7 @@ EXPORTED = ("indexer_plan", "indexer_plan_destroy", "indexer_plan_info", "indexe
             "indexer_expand_mask", "indexer_status", "indexer_selftest_timeout",
             "indexer_set_wait_budget", "indexer_launch_count", "indexer_error_string",
             "indexer_version", "indexer_fused_topk_noalloc", "indexer_profile_main_kernel",
-            "indexer_chunk_rows")
+            "indexer_chunk_rows", "indexer_page_indices")
 IDX_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -93,6 +93,7 @@ def lib():
         L.indexer_profile_main_kernel.restype = None
         L.indexer_fused_topk_noalloc.argtypes = [P, P, P, P, P, P, P, P, i64, P, P, P]
         L.indexer_chunk_rows.argtypes = [i64, ctypes.c_double, i32, i32, i32, i32]
+        L.indexer_page_indices.argtypes = [P, P, P, i64, i32, P, P]
         L.indexer_error_string.argtypes = [i32]
         L.indexer_error_string.restype = ctypes.c_char_p
         for name in EXPORTED:
@@ -243,6 +244,23 @@ def indexer_profile_main_kernel(start_event=None, stop_event=None):
 
 def indexer_version() -> int:
     return int(lib().indexer_version())
+
+
+def indexer_page_indices(plan: Plan, raw_idx, page_table, page_size: int, page_idx=None,
+                         stream=None):
+    """KV-slot indices of selected raw key indices: page_table[r, j // page_size] *
+    page_size + j % page_size, -1 for -1 / out-of-range keys / unmapped pages.  ``raw_idx``
+    int32 [rows, topk] and ``page_table`` int32 [requests, ld] on the device; writes into
+    ``page_idx`` (default: a new tensor; may be ``raw_idx``) and returns it."""
+    if page_idx is None:
+        page_idx = torch.empty_like(raw_idx)
+    for name, t in (("raw_idx", raw_idx), ("page_table", page_table), ("page_idx", page_idx)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name}: contiguous int32 CUDA tensor expected")
+    _check("indexer_page_indices", lib().indexer_page_indices(
+        plan.handle, _ptr(raw_idx), _ptr(page_table), page_table.stride(0), int(page_size),
+        _ptr(page_idx), _stream(stream)))
+    return page_idx
 
 
 def indexer_chunk_rows(prefix_len: int, budget_token2: float = 2.0e8, chunk_min: int = 256,

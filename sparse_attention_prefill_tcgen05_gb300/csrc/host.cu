@@ -1003,6 +1003,38 @@ int indexer_expand_mask(indexer_plan_t p, const uint8_t* cand_mask, int64_t ld_m
                : IDX_ERR_CUDA;
 }
 
+int indexer_page_indices(indexer_plan_t p, const int32_t* raw_idx, const int32_t* page_table,
+                         int64_t ld_page_table, int32_t page_size, int32_t* page_idx,
+                         void* stream)
+{
+    if (!p || !raw_idx || !page_table || !page_idx || page_size < 1 ||
+        ld_page_table < (p->max_L + page_size - 1) / page_size || p->R > kMaxRequests)
+        return IDX_ERR_INVALID_ARG;
+    if (!device_info().ok)
+        return IDX_ERR_UNSUPPORTED;
+    if (p->T == 0 || p->topk == 0)
+        return IDX_OK;
+    PageIndexParams pp;
+    std::memset(&pp, 0, sizeof(pp));
+    pp.raw = raw_idx;
+    pp.out = page_idx;
+    pp.table = page_table;
+    pp.ld_table = ld_page_table;
+    pp.page = page_size;
+    pp.k = p->topk;
+    pp.rows = p->T;
+    pp.num_requests = p->R;
+    for (int r = 0; r < p->R; ++r) {
+        pp.req_row_begin[r] = p->row_begin[r];
+        pp.req_key_count[r] = p->L[r];
+    }
+    pp.req_row_begin[p->R] = p->row_begin[p->R];
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return launch_page_indices(pp, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? IDX_OK
+               : IDX_ERR_CUDA;
+}
+
 int indexer_selftest_timeout(void* ws, long long cycles, void* stream)
 {
     if (!ws || !aligned(ws, 256) || cycles <= 0)

@@ -167,6 +167,23 @@ cudaError_t launch_expand_mask(const uint8_t* cand_mask, int64_t ld_mask, const 
                                uint8_t* key_mask, int64_t ld, int block, int rows,
                                cudaStream_t st);
 cudaError_t launch_selftest_timeout(uint32_t* status, long long cycles, cudaStream_t st);
+
+// Page (KV slot) indices of selected raw key indices: out[t, i] =
+// table[r, j / page] * page + j % page for 0 <= j < L_r (r the request of row t),
+// else -1; -1 also where the table entry is negative or the slot does not fit int32.
+struct PageIndexParams {
+    const int32_t* raw;          // [rows, k]
+    int32_t* out;                // [rows, k] (may be raw itself)
+    const int32_t* table;        // [num_requests, ld_table]
+    int64_t ld_table;
+    int32_t page;
+    int32_t k;
+    int32_t rows;
+    int32_t num_requests;
+    int32_t req_row_begin[kMaxRequests + 1];
+    int32_t req_key_count[kMaxRequests];
+};
+cudaError_t launch_page_indices(const PageIndexParams& p, cudaStream_t st);
 // e2m1 keys [keys, D/2] (element 2i in the low nibble) with ue8m0 scales
 // [keys, D/32] -> e4m3 keys [keys, D] and fp32 s_k [keys] = 2^(largest block
 // exponent - 127), exactly; a key whose smaller blocks would need more than

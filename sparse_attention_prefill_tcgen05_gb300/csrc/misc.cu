@@ -1,4 +1,4 @@
-// Small kernels: block-mask expansion and the bounded-wait self-test.
+// Small kernels: block-mask expansion, the page-index transform and the bounded-wait self-test.
 #include "internal.h"
 #include "ptx.cuh"
 #include <algorithm>
@@ -125,6 +125,78 @@ __global__ void selftest_timeout_kernel(uint32_t* status, long long cycles)
 }
 
 }  // namespace
+
+// Page-index transform: one thread per four consecutive entries of a row (k a
+// multiple of 4) or per entry; the request of a row by binary search over the
+// batch's row offsets; a power-of-two page divides by shifts.
+__device__ __forceinline__ int32_t page_slot(const PageIndexParams& p, int r, int32_t j,
+                                             int shift)
+{
+    if (j < 0 || j >= p.req_key_count[r])
+        return -1;
+    const int32_t pi = shift >= 0 ? (j >> shift) : j / p.page;
+    const int32_t off = shift >= 0 ? (j & (p.page - 1)) : j - pi * p.page;
+    const int64_t pg = p.table[(int64_t)r * p.ld_table + pi];
+    if (pg < 0)
+        return -1;
+    const int64_t slot = pg * p.page + off;
+    return slot <= 0x7FFFFFFF ? static_cast<int32_t>(slot) : -1;
+}
+
+__device__ __forceinline__ int row_request(const PageIndexParams& p, int t)
+{
+    int lo = 0, hi = p.num_requests - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.req_row_begin[mid] <= t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+__global__ void page_indices_kernel(const __grid_constant__ PageIndexParams p, int shift, int vec)
+{
+    const int64_t total = (int64_t)p.rows * p.k;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    if (vec) {
+        for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < total / 4;
+             v += stride) {
+            const int t = static_cast<int>((v * 4) / p.k);
+            const int r = row_request(p, t);
+            const int4 j = reinterpret_cast<const int4*>(p.raw)[v];
+            reinterpret_cast<int4*>(p.out)[v] =
+                make_int4(page_slot(p, r, j.x, shift), page_slot(p, r, j.y, shift),
+                          page_slot(p, r, j.z, shift), page_slot(p, r, j.w, shift));
+        }
+    } else {
+        for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total; e += stride) {
+            const int t = static_cast<int>(e / p.k);
+            p.out[e] = page_slot(p, row_request(p, t), p.raw[e], shift);
+        }
+    }
+}
+
+cudaError_t launch_page_indices(const PageIndexParams& p, cudaStream_t st)
+{
+    const int64_t total = (int64_t)p.rows * p.k;
+    if (total <= 0)
+        return cudaSuccess;
+    int shift = -1;
+    if ((p.page & (p.page - 1)) == 0)
+        for (shift = 0; (1 << shift) < p.page; ++shift) {
+        }
+    const int vec = (p.k % 4 == 0 && (reinterpret_cast<uintptr_t>(p.raw) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(p.out) & 15) == 0)
+                        ? 1
+                        : 0;
+    const int64_t items = vec ? total / 4 : total;
+    // a grid of whole waves: 152 SMs x 8 blocks of 256 threads at most
+    const int blocks = static_cast<int>(std::min<int64_t>((items + 255) / 256, 152 * 8));
+    page_indices_kernel<<<blocks, 256, 0, st>>>(p, shift, vec);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_expand_mask(const uint8_t* cand_mask, int64_t ld_mask, const int32_t* clen,
                                uint8_t* key_mask, int64_t ld, int block, int rows,
