@@ -267,6 +267,38 @@ long long indexer_launch_count(void);
    the events are owned by the caller. */
 void indexer_profile_main_kernel(void* start_event, void* stop_event);
 
+/* ------------------------------------------- tail-only candidates, row maps
+ * Under a decoder sliding-window bounded replay only each request's tail rows
+ * are consumed by the later layers ("[SGLang PR 39187]", the third change:
+ * publish only each request's tail rows, since the consumer slices every mask
+ * down to them anyway).
+ *
+ * indexer_candidate_blocks_tail: indexer_candidate_blocks for request r's last
+ *   publish_rows[r] rows only (host array [num_requests], 0 <= publish_rows[r]
+ *   <= rows of r), packed: cand_mask is [sum_r publish_rows[r], ld_mask], request
+ *   order, each request's rows in order.  Only those rows are scored.  A row's
+ *   mask is byte-identical to the one indexer_candidate_blocks gives it.
+ *   IDX_ERR_INVALID_ARG for a count out of range or a NULL array.
+ *
+ * indexer_fused_topk_mapped: indexer_fused_topk with a candidate mask whose rows
+ *   are addressed through a row map: row t of the batch uses mask row
+ *   mask_rows[t] (device int32 [total_rows]) of cand_mask [mask_row_count,
+ *   ld_mask].  A map entry outside [0, mask_row_count) is reported by
+ *   indexer_status as IDX_ERR_DEVICE_CHECK (that row then reads mask row 0).
+ *   cand_mask and mask_rows are required (IDX_ERR_INVALID_ARG otherwise).
+ */
+int indexer_candidate_blocks_tail(indexer_plan_t plan, const void* q, const float* s_q,
+                                  const float* w, const void* k, const void* k_scale,
+                                  const int32_t* compress_len, const int32_t* publish_rows,
+                                  uint8_t* cand_mask, int64_t ld_mask, void* ws,
+                                  size_t ws_bytes, void* stream);
+int indexer_fused_topk_mapped(indexer_plan_t plan, const void* q, const float* s_q,
+                              const float* w, const void* k, const void* k_scale,
+                              const int32_t* compress_len, const uint8_t* cand_mask,
+                              int64_t ld_mask, const int32_t* mask_rows, int64_t mask_row_count,
+                              int32_t* out_idx, float* out_val, void* ws, size_t ws_bytes,
+                              void* stream);
+
 /* ------------------------------------------------------ page-index transform
  * The indexer's selected keys as KV-cache slots ("[SGLang PR 39187]",
  * Accuracy / equivalence: the indexer's outputs are page_indices and

@@ -9,6 +9,7 @@ from ._lib import (  # noqa: F401
     IDX_K_FP4_E2M1_UE8M0, IDX_K_FP8_E4M3, IDX_OK, IDX_SELECT_AUTO, IDX_SELECT_STREAM, IndexerError, Plan, indexer_candidate_blocks,
     indexer_expand_mask, indexer_fused_topk, indexer_logits, indexer_plan, indexer_selftest_timeout,
     indexer_launch_count, indexer_profile_main_kernel, indexer_set_wait_budget, indexer_status, indexer_topk, indexer_version,
-    indexer_chunk_rows, indexer_page_indices,
+    indexer_chunk_rows, indexer_page_indices, indexer_candidate_blocks_tail,
+    indexer_fused_topk_mapped,
     lib,
 )

@@ -13,6 +13,7 @@ import os
 from dataclasses import dataclass
 from typing import Optional
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -35,7 +36,8 @@ EXPORTED = ("indexer_plan", "indexer_plan_destroy", "indexer_plan_info", "indexe
             "indexer_expand_mask", "indexer_status", "indexer_selftest_timeout",
             "indexer_set_wait_budget", "indexer_launch_count", "indexer_error_string",
             "indexer_version", "indexer_fused_topk_noalloc", "indexer_profile_main_kernel",
-            "indexer_chunk_rows", "indexer_page_indices")
+            "indexer_chunk_rows", "indexer_page_indices", "indexer_candidate_blocks_tail",
+            "indexer_fused_topk_mapped")
 IDX_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -94,6 +96,9 @@ def lib():
         L.indexer_fused_topk_noalloc.argtypes = [P, P, P, P, P, P, P, P, i64, P, P, P]
         L.indexer_chunk_rows.argtypes = [i64, ctypes.c_double, i32, i32, i32, i32]
         L.indexer_page_indices.argtypes = [P, P, P, i64, i32, P, P]
+        L.indexer_candidate_blocks_tail.argtypes = [P, P, P, P, P, P, P, P, P, i64, P, sz, P]
+        L.indexer_fused_topk_mapped.argtypes = [P, P, P, P, P, P, P, P, i64, P, i64, P, P, P,
+                                                sz, P]
         L.indexer_error_string.argtypes = [i32]
         L.indexer_error_string.restype = ctypes.c_char_p
         for name in EXPORTED:
@@ -199,6 +204,27 @@ def indexer_candidate_blocks(plan: Plan, q, s_q, w, k, k_scale, compress_len, ca
     _check("indexer_candidate_blocks", lib().indexer_candidate_blocks(
         plan.handle, _ptr(q), _ptr(s_q), _ptr(w), _ptr(k), _ptr(k_scale), _ptr(compress_len),
         _ptr(cand_mask), cand_mask.stride(0), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(stream)))
+
+
+def indexer_candidate_blocks_tail(plan: Plan, q, s_q, w, k, k_scale, compress_len,
+                                  publish_rows, cand_mask, ws, stream=None):
+    """Candidate blocks of each request's last ``publish_rows[r]`` rows only, packed into
+    ``cand_mask`` [sum(publish_rows), ld_mask] (``publish_rows``: a host sequence)."""
+    pr = np.ascontiguousarray(np.asarray(publish_rows, dtype=np.int32))
+    _check("indexer_candidate_blocks_tail", lib().indexer_candidate_blocks_tail(
+        plan.handle, _ptr(q), _ptr(s_q), _ptr(w), _ptr(k), _ptr(k_scale), _ptr(compress_len),
+        pr.ctypes.data_as(ctypes.c_void_p), _ptr(cand_mask), cand_mask.stride(0), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def indexer_fused_topk_mapped(plan: Plan, q, s_q, w, k, k_scale, compress_len, cand_mask,
+                              mask_rows, out_idx, out_val, ws, stream=None):
+    """indexer_fused_topk where row t reads candidate-mask row ``mask_rows[t]`` (device int32)."""
+    _check("indexer_fused_topk_mapped", lib().indexer_fused_topk_mapped(
+        plan.handle, _ptr(q), _ptr(s_q), _ptr(w), _ptr(k), _ptr(k_scale), _ptr(compress_len),
+        _ptr(cand_mask), cand_mask.stride(0), _ptr(mask_rows), cand_mask.shape[0],
+        _ptr(out_idx), _ptr(out_val), _ptr(ws), ws.numel() * ws.element_size(),
         _stream(stream)))
 
 

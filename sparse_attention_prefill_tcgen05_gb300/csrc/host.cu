@@ -237,6 +237,10 @@ struct Ctx {
     LogitsParams lp;
     int sms;
     cudaStream_t st;
+    // candidate blocks for each request's last tail[r] rows only (nullptr: every row),
+    // written to mask row t + mask_delta[r] (empty: row t)
+    const int32_t* tail = nullptr;
+    std::vector<int64_t> mask_delta;
 };
 
 int fill_maps(Ctx& c, const void* q, const void* k)
@@ -330,6 +334,7 @@ int pass_launches(Ctx& c, const Pass& ps, const std::vector<int32_t>& cap, int s
         mpc.slots = ns * kListsPerSplit;
         mpc.cap = cap[r];
         mpc.key_count = p->L[r];
+        mpc.mask_delta = c.mask_delta.empty() ? 0 : c.mask_delta[r];
         mpc.list_offset = pc.list_off;
         mpc.count_offset = p->cnt_base[r] + (int64_t)(pc.a - p->row_begin[r]) * ns * kListsPerSplit;
         ctas += pc.b - pc.a;
@@ -397,13 +402,10 @@ int pass_thresholds(Ctx& c, const Pass& ps, float* samples, uint32_t* tau_row, i
         if (rc != IDX_OK)
             return rc;
     }
-    const int rows = ps.pieces.back().b - first;
     SampleParams sp;
     std::memset(&sp, 0, sizeof(sp));
     sp.samples = samples;
     sp.ld = p->sample_cols;
-    sp.row0 = first;
-    sp.rows = rows;
     sp.k = keep;
     sp.pool = pool > 1 ? pool : 1;
     sp.compress_len = c.lp.compress_len;
@@ -415,8 +417,21 @@ int pass_thresholds(Ctx& c, const Pass& ps, float* samples, uint32_t* tau_row, i
         sp.req_key_count[r] = p->L[r];
     }
     sp.req_row_begin[p->R] = p->row_begin[p->R];
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return launch_sample_threshold(sp, c.st) == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+    // one launch per run of adjacent pieces (a pass restricted to some rows of its
+    // requests has gaps, whose sample rows are never written)
+    for (size_t i = 0; i < ps.pieces.size();) {
+        size_t e = i + 1;
+        while (e < ps.pieces.size() && ps.pieces[e].a == ps.pieces[e - 1].b)
+            ++e;
+        sp.row0 = ps.pieces[i].a;
+        sp.rows = ps.pieces[e - 1].b - ps.pieces[i].a;
+        sp.samples = samples + (int64_t)(ps.pieces[i].a - first) * p->sample_cols;
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        if (launch_sample_threshold(sp, c.st) != cudaSuccess)
+            return IDX_ERR_CUDA;
+        i = e;
+    }
+    return IDX_OK;
 }
 
 // Streamed top-k (pool = 0) or candidate blocks (pool > 0), pass by pass.
@@ -431,8 +446,26 @@ int run_streamed(Ctx& c, uint8_t* ws, int pool, int32_t* out_idx, float* out_val
                  uint8_t* mask, int64_t ld_mask)
 {
     const indexer_plan_s* p = c.p;
-    const std::vector<Pass>& passes = pool ? p->passes_b : p->passes_k;
     const std::vector<int32_t>& cap = pool ? p->cap_b : p->cap_k;
+    // the plan's passes, or their pieces cut down to each request's last tail[r] rows
+    // (a piece keeps its list area: its first kept row's lists start per_row entries
+    // further per skipped row)
+    std::vector<Pass> cut;
+    if (c.tail) {
+        for (const Pass& ps : pool ? p->passes_b : p->passes_k) {
+            Pass f;
+            for (const PassPiece& pc : ps.pieces) {
+                const int lo = std::max(pc.a, p->row_begin[pc.r + 1] - c.tail[pc.r]);
+                if (lo >= pc.b)
+                    continue;
+                const int64_t per_row = (int64_t)p->n_splits[pc.r] * kListsPerSplit * cap[pc.r];
+                f.pieces.push_back(PassPiece{pc.r, lo, pc.b, pc.list_off + (lo - pc.a) * per_row});
+            }
+            if (!f.pieces.empty())
+                cut.push_back(f);
+        }
+    }
+    const std::vector<Pass>& passes = c.tail ? cut : (pool ? p->passes_b : p->passes_k);
     const int keep = pool ? p->cand_topk : p->topk;
     const bool sampled = pool == 0 ? p->sample_stride > 0 : p->sample_blocks;
     LogitsParams& lp = c.lp;
@@ -931,10 +964,11 @@ int indexer_topk(indexer_plan_t p, const float* logits, int64_t ld, const int32_
     return launch_topk_dense(tp, c.st) == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 
-int indexer_fused_topk(indexer_plan_t p, const void* q, const float* s_q, const float* w,
+static int fused_topk_impl(indexer_plan_t p, const void* q, const float* s_q, const float* w,
                        const void* k, const void* k_scale, const int32_t* clen,
-                       const uint8_t* cand_mask, int64_t ld_mask, int32_t* out_idx,
-                       float* out_val, void* ws, size_t ws_bytes, void* stream)
+                       const uint8_t* cand_mask, int64_t ld_mask, const int32_t* mask_rows,
+                       int64_t mask_row_count, int32_t* out_idx, float* out_val, void* ws,
+                       size_t ws_bytes, void* stream)
 {
     int rc = check_common(p, ws, ws_bytes);
     if (rc != IDX_OK)
@@ -954,6 +988,8 @@ int indexer_fused_topk(indexer_plan_t p, const void* q, const float* s_q, const 
         return rc;
     c.lp.cand_mask = cand_mask;
     c.lp.ld_mask = ld_mask;
+    c.lp.mask_rows = mask_rows;
+    c.lp.mask_row_count = mask_row_count;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     // shared bounds and row flags
     if (cudaMemsetAsync(wsb + p->off_gtau, 0, (size_t)p->T * 8, c.st) != cudaSuccess)
@@ -961,10 +997,31 @@ int indexer_fused_topk(indexer_plan_t p, const void* q, const float* s_q, const 
     return run_streamed(c, wsb, 0, out_idx, out_val, nullptr, 0);
 }
 
-int indexer_candidate_blocks(indexer_plan_t p, const void* q, const float* s_q, const float* w,
+int indexer_fused_topk(indexer_plan_t p, const void* q, const float* s_q, const float* w,
+                       const void* k, const void* k_scale, const int32_t* clen,
+                       const uint8_t* cand_mask, int64_t ld_mask, int32_t* out_idx,
+                       float* out_val, void* ws, size_t ws_bytes, void* stream)
+{
+    return fused_topk_impl(p, q, s_q, w, k, k_scale, clen, cand_mask, ld_mask, nullptr, 0,
+                           out_idx, out_val, ws, ws_bytes, stream);
+}
+
+int indexer_fused_topk_mapped(indexer_plan_t p, const void* q, const float* s_q, const float* w,
+                              const void* k, const void* k_scale, const int32_t* clen,
+                              const uint8_t* cand_mask, int64_t ld_mask, const int32_t* mask_rows,
+                              int64_t mask_row_count, int32_t* out_idx, float* out_val, void* ws,
+                              size_t ws_bytes, void* stream)
+{
+    if (!cand_mask || !mask_rows || !aligned(mask_rows, 4) || mask_row_count < 1)
+        return IDX_ERR_INVALID_ARG;
+    return fused_topk_impl(p, q, s_q, w, k, k_scale, clen, cand_mask, ld_mask, mask_rows,
+                           mask_row_count, out_idx, out_val, ws, ws_bytes, stream);
+}
+
+static int candidates_impl(indexer_plan_t p, const void* q, const float* s_q, const float* w,
                              const void* k, const void* k_scale, const int32_t* clen,
-                             uint8_t* cand_mask, int64_t ld_mask, void* ws, size_t ws_bytes,
-                             void* stream)
+                             const int32_t* tail, uint8_t* cand_mask, int64_t ld_mask, void* ws,
+                             size_t ws_bytes, void* stream)
 {
     int rc = check_common(p, ws, ws_bytes);
     if (rc != IDX_OK)
@@ -975,6 +1032,19 @@ int indexer_candidate_blocks(indexer_plan_t p, const void* q, const float* s_q, 
         p->cand_topk == 0)
         return IDX_ERR_INVALID_ARG;
     Ctx c;
+    if (tail) {
+        // request r's last tail[r] rows, packed: mask row of row t = t + delta_r
+        int64_t packed = 0;
+        c.mask_delta.resize(p->R);
+        for (int r = 0; r < p->R; ++r) {
+            const int rows = p->row_begin[r + 1] - p->row_begin[r];
+            if (tail[r] < 0 || tail[r] > rows)
+                return IDX_ERR_INVALID_ARG;
+            c.mask_delta[r] = packed - (p->row_begin[r + 1] - tail[r]);
+            packed += tail[r];
+        }
+        c.tail = tail;
+    }
     if ((rc = begin_call(c, p, ws, stream)) != IDX_OK)
         return rc;
     if (p->T == 0)
@@ -986,6 +1056,27 @@ int indexer_candidate_blocks(indexer_plan_t p, const void* q, const float* s_q, 
     if (cudaMemsetAsync(wsb + p->off_gtau, 0, (size_t)p->T * 8, c.st) != cudaSuccess)
         return IDX_ERR_CUDA;
     return run_streamed(c, wsb, p->cand_block, nullptr, nullptr, cand_mask, ld_mask);
+}
+
+int indexer_candidate_blocks(indexer_plan_t p, const void* q, const float* s_q, const float* w,
+                             const void* k, const void* k_scale, const int32_t* clen,
+                             uint8_t* cand_mask, int64_t ld_mask, void* ws, size_t ws_bytes,
+                             void* stream)
+{
+    return candidates_impl(p, q, s_q, w, k, k_scale, clen, nullptr, cand_mask, ld_mask, ws,
+                           ws_bytes, stream);
+}
+
+int indexer_candidate_blocks_tail(indexer_plan_t p, const void* q, const float* s_q,
+                                  const float* w, const void* k, const void* k_scale,
+                                  const int32_t* clen, const int32_t* publish_rows,
+                                  uint8_t* cand_mask, int64_t ld_mask, void* ws, size_t ws_bytes,
+                                  void* stream)
+{
+    if (!publish_rows)
+        return IDX_ERR_INVALID_ARG;
+    return candidates_impl(p, q, s_q, w, k, k_scale, clen, publish_rows, cand_mask, ld_mask, ws,
+                           ws_bytes, stream);
 }
 
 int indexer_expand_mask(indexer_plan_t p, const uint8_t* cand_mask, int64_t ld_mask,

@@ -64,6 +64,8 @@ struct LogitsParams {
     const int32_t* compress_len;  // [rows]
     const uint8_t* cand_mask;     // nullable [rows, ld_mask] 0/1 per key block
     int64_t ld_mask;
+    const int32_t* mask_rows;     // nullable [rows]: row t reads mask row mask_rows[t]
+    int64_t mask_row_count;       // rows of cand_mask when mask_rows is set
     int32_t mask_block;
     int32_t num_segments;
     int32_t total_units;
@@ -99,6 +101,7 @@ struct MergePiece {
     int32_t slots;          // key splits (lists) per row
     int32_t cap;            // entries per list
     int32_t key_count;      // keys (or blocks) of the piece's request: indices are below it
+    int64_t mask_delta;     // mask output: row t of the piece writes mask row t + mask_delta
     int64_t list_offset;    // entry offset of row_begin's first list
     int64_t count_offset;   // counts index of row_begin's first list
 };

@@ -592,9 +592,21 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
             const uint8_t* mrow[RO];
 #pragma unroll
             for (int ro = 0; ro < RO; ++ro) {
-                const int rl = half * RPH + own_rr(ro);
-                mrow[ro] = has_mask ? p.cand_mask + (size_t)(ui.t0 + min(rl, ui.nr - 1)) * p.ld_mask
-                                    : nullptr;
+                mrow[ro] = nullptr;
+                if constexpr (has_mask) {
+                    // the row's mask row: itself, or its entry of the caller's row map
+                    // (an entry outside the mask is reported and read as row 0)
+                    const int t = ui.t0 + min(half * RPH + own_rr(ro), ui.nr - 1);
+                    int64_t mr = t;
+                    if (p.mask_rows != nullptr) {
+                        mr = __ldg(p.mask_rows + t);
+                        if (mr < 0 || mr >= p.mask_row_count) {
+                            atomicOr(p.status, kStatusBadArg);
+                            mr = 0;
+                        }
+                    }
+                    mrow[ro] = p.cand_mask + mr * p.ld_mask;
+                }
             }
             auto mask_at = [&](int m, int jt0) -> uint32_t {
                 const int ro = RPH >= 4 ? (m >> 2) : 0;

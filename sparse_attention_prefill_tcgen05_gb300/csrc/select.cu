@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(kSelThreads)
     }
     __syncthreads();
     if (p.mask) {
-        uint8_t* m = p.mask + (int64_t)t * p.ld_mask;
+        uint8_t* m = p.mask + (t + pc.mask_delta) * p.ld_mask;
         for (int64_t b = threadIdx.x; b < p.ld_mask; b += kSelThreads)
             m[b] = 0;
         __syncthreads();
