@@ -299,6 +299,27 @@ int indexer_fused_topk_mapped(indexer_plan_t plan, const void* q, const float* s
                               int32_t* out_idx, float* out_val, void* ws, size_t ws_bytes,
                               void* stream);
 
+/* ------------------------------------------------------------ fp4 operands
+ * Exact conversion of e2m1 codes with one ue8m0 exponent per 32 elements
+ * (OCP MX fp4: value = e2m1(code) * 2^(e - 127)) into e4m3 codes and one fp32
+ * scale per row, value = e4m3(out) * out_scale[row] exactly, out_scale =
+ * 2^(largest block exponent of the row - 127).  This is how the library runs
+ * e2m1 keys (inside the calls, kdtype IDX_K_FP4_E2M1_UE8M0_32), and how a caller
+ * runs e2m1 queries (fp4 x fp4): convert q as T*H rows of D and pass the e4m3
+ * codes as q and the row scales as s_q.
+ *   codes: device [rows, D/2] bytes, element 2i in the low nibble;
+ *   block_scales: device [rows, D/32]; D a multiple of 32 (64 or 128 here);
+ *   out_e4m3: device [rows, D]; out_scale: device fp32 [rows];
+ *   ws: at least 256 bytes of device memory, 256-byte aligned: its status word is
+ *   cleared, and a row whose smaller blocks fall below e4m3's range sets a bit
+ *   that indexer_status(NULL, ws) reports as IDX_ERR_DEVICE_CHECK (read it before
+ *   the workspace is used by another call, which clears it).
+ * Async on `stream`, no allocation.
+ */
+int indexer_convert_fp4(const uint8_t* codes, const uint8_t* block_scales, int64_t rows,
+                        int32_t D, uint8_t* out_e4m3, float* out_scale, void* ws,
+                        size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------ page-index transform
  * The indexer's selected keys as KV-cache slots ("[SGLang PR 39187]",
  * Accuracy / equivalence: the indexer's outputs are page_indices and

@@ -272,3 +272,57 @@ def page_indices_rows(raw_idx, row_request, key_count, page_table, page_size):
             if slot <= 2**31 - 1:
                 out[t, i] = slot
     return out.astype(np.int32)
+
+
+# ------------------------------------------------------------ fp4 x fp4
+
+def decode_fp4(codes, block_exp):
+    """e2m1 codes [..., D/2] (element 2i in the low nibble) with one ue8m0 exponent per 32
+    elements [..., D/32] -> fp64 values [..., D] = e2m1(code) * 2^(e - 127), exactly (the
+    OCP MX fp4 format the pages' "fp8_fp4" kernel reads for keys)."""
+    tab = np.array([e2m1_value(c) for c in range(16)], dtype=np.float64)
+    c = np.asarray(codes, dtype=np.uint8)
+    v = np.empty(c.shape[:-1] + (2 * c.shape[-1],), dtype=np.float64)
+    v[..., 0::2] = tab[c & 15]
+    v[..., 1::2] = tab[c >> 4]
+    e = np.asarray(block_exp, dtype=np.int64)
+    return v * np.repeat(np.ldexp(1.0, e - 127), 32, axis=-1)
+
+
+def _key_values(p, k0, k1):
+    """fp64 key values [L, D] of keys k0..k1 (scale included)."""
+    if p.spec.kdtype == "fp4":
+        return decode_fp4(_np(p.k, np.uint8)[k0:k1], _np(p.k_scale, np.uint8)[k0:k1])
+    tab = np.array([e4m3_value(b) for b in range(256)], dtype=np.float64)
+    return tab[_np(p.k, np.uint8)[k0:k1]] * _np(p.k_scale, np.float32)[k0:k1, None].astype(
+        np.float64)
+
+
+def problem_logits_fp4q(p, rows=None, ld=None, batch=8):
+    """fp64 logits when the queries too are e2m1 + ue8m0/32 (fp4 x fp4, ``p.q4`` /
+    ``p.q_sf``): the definition's step 3 with decoded values (the scales live in the
+    values, so s_q = 1): x = <q_h, k_j> by an fp64 matmul (every product and partial sum
+    of these short dyadic values is exact), logit = sum over h in order of w * max(x, 0)
+    in fp64, -inf past compress_len.  Same layout as problem_logits."""
+    T = int(p.cu_seqlens_q[-1])
+    rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
+    cu_k = _np(p.cu_seqlens_k, np.int64)
+    ld = int(np.max(np.diff(cu_k))) if ld is None else ld
+    w = _np(p.w, np.float32).astype(np.float64)
+    cl = _np(p.compress_len, np.int64)
+    out = np.full((len(rows), ld), -np.inf, dtype=np.float64)
+    pos_of = {int(g): i for i, g in enumerate(rows)}
+    for r, sel in _request_arrays(p, rows, 1):
+        k0, k1 = int(cu_k[r]), int(cu_k[r + 1])
+        kv = _key_values(p, k0, k1)                                   # [L, D]
+        for a in range(0, len(sel), batch):
+            part = sel[a:a + batch]
+            qv = decode_fp4(_np(p.q4, np.uint8)[part], _np(p.q_sf, np.uint8)[part])
+            s = np.einsum("nhd,ld->nhl", qv, kv)                      # [n, H, L]
+            acc = np.zeros((len(part), k1 - k0), dtype=np.float64)
+            for h in range(p.H):
+                acc += w[part, h][:, None] * np.maximum(s[:, h, :], 0.0)
+            j = np.arange(k1 - k0)[None, :]
+            acc[j >= np.minimum(cl[part], k1 - k0)[:, None]] = -np.inf
+            out[[pos_of[int(g)] for g in part], : k1 - k0] = acc
+    return out

@@ -37,7 +37,7 @@ EXPORTED = ("indexer_plan", "indexer_plan_destroy", "indexer_plan_info", "indexe
             "indexer_set_wait_budget", "indexer_launch_count", "indexer_error_string",
             "indexer_version", "indexer_fused_topk_noalloc", "indexer_profile_main_kernel",
             "indexer_chunk_rows", "indexer_page_indices", "indexer_candidate_blocks_tail",
-            "indexer_fused_topk_mapped")
+            "indexer_fused_topk_mapped", "indexer_convert_fp4")
 IDX_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -96,6 +96,7 @@ def lib():
         L.indexer_fused_topk_noalloc.argtypes = [P, P, P, P, P, P, P, P, i64, P, P, P]
         L.indexer_chunk_rows.argtypes = [i64, ctypes.c_double, i32, i32, i32, i32]
         L.indexer_page_indices.argtypes = [P, P, P, i64, i32, P, P]
+        L.indexer_convert_fp4.argtypes = [P, P, i64, i32, P, P, P, sz, P]
         L.indexer_candidate_blocks_tail.argtypes = [P, P, P, P, P, P, P, P, P, i64, P, sz, P]
         L.indexer_fused_topk_mapped.argtypes = [P, P, P, P, P, P, P, P, i64, P, i64, P, P, P,
                                                 sz, P]
@@ -270,6 +271,15 @@ def indexer_profile_main_kernel(start_event=None, stop_event=None):
 
 def indexer_version() -> int:
     return int(lib().indexer_version())
+
+
+def indexer_convert_fp4(codes, block_scales, out_e4m3, out_scale, ws, stream=None):
+    """e2m1 + ue8m0/32 rows -> e4m3 rows + fp32 row scales, exactly (see the header);
+    ``codes`` [rows, D/2] and ``block_scales`` [rows, D/32] uint8 on the device."""
+    rows, half = codes.shape[0], codes.shape[-1]
+    _check("indexer_convert_fp4", lib().indexer_convert_fp4(
+        _ptr(codes), _ptr(block_scales), rows, 2 * half, _ptr(out_e4m3), _ptr(out_scale),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def indexer_page_indices(plan: Plan, raw_idx, page_table, page_size: int, page_idx=None,

@@ -1094,6 +1094,28 @@ int indexer_expand_mask(indexer_plan_t p, const uint8_t* cand_mask, int64_t ld_m
                : IDX_ERR_CUDA;
 }
 
+int indexer_convert_fp4(const uint8_t* codes, const uint8_t* block_scales, int64_t rows,
+                        int32_t D, uint8_t* out_e4m3, float* out_scale, void* ws,
+                        size_t ws_bytes, void* stream)
+{
+    if (!codes || !block_scales || !out_e4m3 || !out_scale || !ws || ws_bytes < kStatusBytes ||
+        !aligned(ws, 256) || rows < 0 || rows > 0x7FFFFFFF || D < 32 || D % 32 != 0 ||
+        !aligned(codes, 4) || !aligned(out_e4m3, 8))
+        return IDX_ERR_INVALID_ARG;
+    if (!device_info().ok)
+        return IDX_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, kStatusBytes, st) != cudaSuccess)
+        return IDX_ERR_CUDA;
+    if (rows == 0)
+        return IDX_OK;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return launch_fp4_to_fp8(codes, block_scales, static_cast<int>(rows), D, out_e4m3, out_scale,
+                             static_cast<uint32_t*>(ws), st) == cudaSuccess
+               ? IDX_OK
+               : IDX_ERR_CUDA;
+}
+
 int indexer_page_indices(indexer_plan_t p, const int32_t* raw_idx, const int32_t* page_table,
                          int64_t ld_page_table, int32_t page_size, int32_t* page_idx,
                          void* stream)

@@ -69,6 +69,7 @@ class ProblemSpec:
     topk: int
     kdtype: str = "fp8"          # "fp8" or "fp4" (e2m1 + ue8m0 per 32)
     seed: int = 0
+    qdtype: str = "fp8"          # "fp8", or "fp4": e2m1 + ue8m0 per 32 queries (fp4 x fp4)
     heavy_keys_frac: float = 0.0  # fraction of keys multiplied before quantising
     heavy_keys_mult: float = 4.0
     dup_frac: float = 0.0         # fraction of key positions copied from earlier ones
@@ -110,6 +111,11 @@ CONFIGS = {
         "long-context chunk: T=16,384 rows ending a 487,936-token prefix, L=487,936, H=32, "
         "D=128, fp8, 1% of positions duplicated (exact ties), top-512",
         (RequestSpec(16384, 471552, 1),), H=32, D=128, topk=512, seed=4, dup_frac=0.01),
+    "v4fp4qk": ProblemSpec(
+        "low-ratio layer, fp4 x fp4: T=2048 rows at prefix 200,000, ratio 2, L=100,000, "
+        "H=32, D=128, e2m1+ue8m0/32 queries and keys, top-512, key blocks of 32,768",
+        (RequestSpec(2048, 197952, 2),), H=32, D=128, topk=512, kdtype="fp4", seed=6,
+        key_block=32768, qdtype="fp4"),
     "ragged_cand": ProblemSpec(
         "ragged batch + candidates: 4 cold requests of 7,168 rows (ratios 1,2,1,2) and a "
         "2,048-row chunk on a 150,000-token cached prefix; 8-key block pooling, top-2048 "
@@ -139,6 +145,10 @@ class Problem:
     s_q2: Optional[torch.Tensor] = None
     w2: Optional[torch.Tensor] = None
     dup_rows: list = field(default_factory=list)   # rows whose q was copied from an earlier row
+    # qdtype "fp4": the queries as e2m1 codes [T, H, D/2] and ue8m0 exponents [T, H, D/32]
+    # (q and s_q then hold zeros / ones and are not inputs)
+    q4: Optional[torch.Tensor] = None
+    q_sf: Optional[torch.Tensor] = None
 
     @property
     def H(self):
@@ -215,6 +225,7 @@ def make_problem(spec: ProblemSpec) -> Problem:
     H, D = spec.H, spec.D
     qs, sqs, ws, ks, kss, clens, poss = [], [], [], [], [], [], []
     q2s, sq2s, w2s = [], [], []
+    q4s, qsfs = [], []
     dup_rows = []
     row_base = 0
     for req in spec.requests:
@@ -252,7 +263,12 @@ def make_problem(spec: ProblemSpec) -> Problem:
                         qf[a] = qf[b]
                         w[a] = w[b]
                         dup_rows.append(row_base + a)
-            q, s_q = quantize_fp8(qf)
+            if spec.qdtype == "fp4":
+                q4, qsf = quantize_fp4(qf)
+                q4s.append(q4); qsfs.append(qsf)
+                q, s_q = torch.zeros((T_r, H, D), dtype=torch.uint8), torch.ones((T_r, H))
+            else:
+                q, s_q = quantize_fp8(qf)
             qs.append(q); sqs.append(s_q); ws.append(w.float())
             if spec.kdtype == "fp8":
                 k, s_k = quantize_fp8(kf)
@@ -280,6 +296,9 @@ def make_problem(spec: ProblemSpec) -> Problem:
         cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
         compress_len=torch.cat(clens).contiguous(), pos=torch.cat(poss),
         dup_rows=dup_rows)
+    if q4s:
+        p.q4 = torch.cat(q4s).contiguous()
+        p.q_sf = torch.cat(qsfs).contiguous()
     if q2s:
         p.q2 = torch.cat(q2s).contiguous()
         p.s_q2 = torch.cat(sq2s).float().contiguous()
