@@ -358,6 +358,45 @@ int launch_merge(Ctx& c, StreamMergeParams& mp)
     return launch_stream_merge(mp, c.st) == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 
+// Each row's threshold for its top `keep` keys (pool = 1) or pool-key blocks, from
+// the pass's samples [rows, sample_cols] (row t at t - the pass's first row).
+int row_thresholds(Ctx& c, const Pass& ps, float* samples, uint32_t* tau_row, int pool,
+                   int keep)
+{
+    const indexer_plan_s* p = c.p;
+    const int first = ps.pieces.front().a;
+    SampleParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    sp.samples = samples;
+    sp.ld = p->sample_cols;
+    sp.k = keep;
+    sp.pool = pool > 1 ? pool : 1;
+    sp.compress_len = c.lp.compress_len;
+    sp.tau_row = tau_row;
+    sp.num_requests = p->R;
+    for (int r = 0; r < p->R; ++r) {
+        sp.req_row_begin[r] = p->row_begin[r];
+        sp.req_rank[r] = p->sample_rank_r[r] > 0 ? p->sample_stride_r[r] : 0;
+        sp.req_key_count[r] = p->L[r];
+    }
+    sp.req_row_begin[p->R] = p->row_begin[p->R];
+    // one launch per run of adjacent pieces (a pass restricted to some rows of its
+    // requests has gaps, whose sample rows are never written)
+    for (size_t i = 0; i < ps.pieces.size();) {
+        size_t e = i + 1;
+        while (e < ps.pieces.size() && ps.pieces[e].a == ps.pieces[e - 1].b)
+            ++e;
+        sp.row0 = ps.pieces[i].a;
+        sp.rows = ps.pieces[e - 1].b - ps.pieces[i].a;
+        sp.samples = samples + (int64_t)(ps.pieces[i].a - first) * p->sample_cols;
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        if (launch_sample_threshold(sp, c.st) != cudaSuccess)
+            return IDX_ERR_CUDA;
+        i = e;
+    }
+    return IDX_OK;
+}
+
 // Sampled logits of the pass's rows (every sample_stride-th key tile of each
 // request) into `samples` [rows, sample_cols], then each row's threshold for its
 // top `keep` keys (pool = 1) or its top `keep` pool-key blocks.
@@ -402,36 +441,7 @@ int pass_thresholds(Ctx& c, const Pass& ps, float* samples, uint32_t* tau_row, i
         if (rc != IDX_OK)
             return rc;
     }
-    SampleParams sp;
-    std::memset(&sp, 0, sizeof(sp));
-    sp.samples = samples;
-    sp.ld = p->sample_cols;
-    sp.k = keep;
-    sp.pool = pool > 1 ? pool : 1;
-    sp.compress_len = c.lp.compress_len;
-    sp.tau_row = tau_row;
-    sp.num_requests = p->R;
-    for (int r = 0; r < p->R; ++r) {
-        sp.req_row_begin[r] = p->row_begin[r];
-        sp.req_rank[r] = p->sample_rank_r[r] > 0 ? p->sample_stride_r[r] : 0;
-        sp.req_key_count[r] = p->L[r];
-    }
-    sp.req_row_begin[p->R] = p->row_begin[p->R];
-    // one launch per run of adjacent pieces (a pass restricted to some rows of its
-    // requests has gaps, whose sample rows are never written)
-    for (size_t i = 0; i < ps.pieces.size();) {
-        size_t e = i + 1;
-        while (e < ps.pieces.size() && ps.pieces[e].a == ps.pieces[e - 1].b)
-            ++e;
-        sp.row0 = ps.pieces[i].a;
-        sp.rows = ps.pieces[e - 1].b - ps.pieces[i].a;
-        sp.samples = samples + (int64_t)(ps.pieces[i].a - first) * p->sample_cols;
-        g_launches.fetch_add(1, std::memory_order_relaxed);
-        if (launch_sample_threshold(sp, c.st) != cudaSuccess)
-            return IDX_ERR_CUDA;
-        i = e;
-    }
-    return IDX_OK;
+    return row_thresholds(c, ps, samples, tau_row, pool, keep);
 }
 
 // Streamed top-k (pool = 0) or candidate blocks (pool > 0), pass by pass.
@@ -931,6 +941,94 @@ int indexer_logits(indexer_plan_t p, const void* q, const float* s_q, const floa
     return segs.empty() ? IDX_OK : run_logits(c, segs, kSinkLogits);
 }
 
+// Top-k over caller logits by the sampled path, pass by pass: samples gathered from
+// the logits, row thresholds, one read of every row appending the entries at or
+// above its threshold to its list, the verify merge; rows it cannot decide go to the
+// direct kernel afterwards.
+int dense_sampled(Ctx& c, uint8_t* ws, const float* logits, int64_t ld, const int32_t* clen,
+                  TopkParams& tp)
+{
+    const indexer_plan_s* p = c.p;
+    uint32_t* tau_row = reinterpret_cast<uint32_t*>(ws + p->off_tau);
+    uint32_t* row_fail = reinterpret_cast<uint32_t*>(ws + p->off_fail);
+    uint32_t* fail_any = reinterpret_cast<uint32_t*>(ws) + 1;
+    uint2* lists = reinterpret_cast<uint2*>(ws + p->off_lists);
+    uint32_t* counts = reinterpret_cast<uint32_t*>(ws + p->off_counts);
+    if (cudaMemsetAsync(ws + p->off_gtau, 0, (size_t)p->T * 8, c.st) != cudaSuccess ||
+        cudaMemsetAsync(counts, 0, p->off_lists - p->off_counts, c.st) != cudaSuccess)
+        return IDX_ERR_CUDA;
+    c.lp.compress_len = clen;
+    for (const Pass& ps : p->passes_k) {
+        DenseFilterParams dp;
+        std::memset(&dp, 0, sizeof(dp));
+        dp.logits = logits;
+        dp.ld = ld;
+        dp.compress_len = clen;
+        dp.samples = reinterpret_cast<float*>(lists);
+        dp.sample_cols = p->sample_cols;
+        dp.tau_row = tau_row;
+        dp.lists = lists;
+        dp.counts = counts;
+        dp.num_requests = p->R;
+        for (int r = 0; r < p->R; ++r) {
+            dp.req_stride[r] = p->sample_rank_r[r] > 0 ? p->sample_stride_r[r] : 0;
+            dp.req_key_count[r] = p->L[r];
+        }
+        StreamMergeParams mp;
+        std::memset(&mp, 0, sizeof(mp));
+        int ctas = 0, max_slots = 0;
+        for (const PassPiece& pc : ps.pieces) {
+            // the fused path's list layout: slots = splits x 4 lists of cap_k per row,
+            // here one per key chunk of the row (a list that overflows sends its row to
+            // the direct kernel)
+            const int r = pc.r;
+            const int slots = p->n_splits[r] * kListsPerSplit;
+            const int chunk = (int)std::max<int64_t>(256, ceil_div(ceil_div(std::max(p->L[r], 1),
+                                                                            slots), 256) * 256);
+            const int64_t cnt = p->cnt_base[r] + (int64_t)(pc.a - p->row_begin[r]) * slots;
+            dp.piece[dp.num_pieces++] =
+                DensePiece{pc.a, pc.b - pc.a, r, slots, chunk, p->cap_k[r], pc.list_off, cnt};
+            MergePiece& m = mp.piece[mp.num_pieces++];
+            m.row_begin = pc.a;
+            m.nrows = pc.b - pc.a;
+            m.cta_begin = ctas;
+            m.slots = slots;
+            m.cap = p->cap_k[r];
+            m.key_count = p->L[r];
+            m.list_offset = pc.list_off;
+            m.count_offset = cnt;
+            ctas += pc.b - pc.a;
+            max_slots = std::max(max_slots, slots);
+        }
+        const int first = ps.pieces.front().a;
+        const int rows = ps.pieces.back().b - first;
+        g_launches.fetch_add(3, std::memory_order_relaxed);
+        if (launch_dense_gather(dp, rows, c.st) != cudaSuccess)
+            return IDX_ERR_CUDA;
+        int rc = row_thresholds(c, ps, dp.samples, tau_row, 1, p->topk);
+        if (rc != IDX_OK)
+            return rc;
+        if (launch_dense_filter(dp, rows, max_slots, c.st) != cudaSuccess)
+            return IDX_ERR_CUDA;
+        mp.total_ctas = ctas;
+        mp.lists = lists;
+        mp.counts = counts;
+        mp.verify = 1;
+        mp.tau_row = tau_row;
+        mp.row_fail = row_fail;
+        mp.fail_any = fail_any;
+        mp.k = p->topk;
+        mp.bitmap = 1;
+        mp.out_idx = tp.out_idx;
+        mp.out_val = tp.out_val;
+        if (launch_stream_merge(mp, c.st) != cudaSuccess)
+            return IDX_ERR_CUDA;
+    }
+    tp.row_fail = row_fail;
+    tp.fail_any = fail_any;
+    return IDX_OK;
+}
+
 int indexer_topk(indexer_plan_t p, const float* logits, int64_t ld, const int32_t* clen,
                  int32_t* out_idx, float* out_val, void* ws, size_t ws_bytes, void* stream)
 {
@@ -960,6 +1058,12 @@ int indexer_topk(indexer_plan_t p, const float* logits, int64_t ld, const int32_
         tp.req_key_count[r] = p->L[r];
     }
     tp.req_row_begin[p->R] = p->row_begin[p->R];
+    // with the plan's whole workspace, the sampled path decides most rows; the direct
+    // kernel then handles only the rows it could not (or every row, without it)
+    if (ws_bytes >= p->ws_bytes && p->sample_stride > 0 && p->T > 0) {
+        if ((rc = dense_sampled(c, static_cast<uint8_t*>(ws), logits, ld, clen, tp)) != IDX_OK)
+            return rc;
+    }
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return launch_topk_dense(tp, c.st) == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }

@@ -138,10 +138,46 @@ struct TopkParams {
     int32_t pad_;
     int32_t* out_idx;
     float* out_val;
+    const uint32_t* row_fail;    // nullable: only rows with a set flag (none while fail_any is 0)
+    const uint32_t* fail_any;
     int32_t req_row_begin[kMaxRequests + 1];
     int32_t req_key_count[kMaxRequests];
 };
 cudaError_t launch_topk_dense(const TopkParams& p, cudaStream_t stream);
+
+// Sampled path of the top-k over caller logits, one pass of rows [row0, row0 + rows):
+// gather every tile_stride-th 128-key tile of each row into samples [rows, sample_cols]
+// (keys past the row's length read as -inf), then (after the threshold kernel) append
+// every entry at or above the row's threshold to its list.
+struct DensePiece {
+    int32_t row_begin;      // first global row
+    int32_t nrows;
+    int32_t request;
+    int32_t slots;          // lists per row: key chunk c of the row appends to list c
+    int32_t chunk;          // keys per chunk
+    int32_t cap;            // entries per list
+    int64_t list_offset;    // entry offset of row_begin's first list
+    int64_t count_offset;   // counts index of row_begin's first list
+};
+struct DenseFilterParams {
+    const float* logits;
+    int64_t ld;
+    const int32_t* compress_len;
+    float* samples;              // gather: [rows of the pass, sample_cols]
+    int32_t sample_cols;
+    int32_t num_pieces;
+    const uint32_t* tau_row;     // filter: [total rows]
+    uint2* lists;
+    uint32_t* counts;
+    int32_t num_requests;
+    int32_t pad_;
+    int32_t req_stride[kMaxRequests];   // sampled tile stride (0: not sampled)
+    int32_t req_key_count[kMaxRequests];
+    DensePiece piece[kMaxMergePieces];
+};
+cudaError_t launch_dense_gather(const DenseFilterParams& p, int rows, cudaStream_t stream);
+cudaError_t launch_dense_filter(const DenseFilterParams& p, int rows, int max_slots,
+                                cudaStream_t stream);
 
 // Per-row thresholds from sampled logits [rows, ld] (row t at t - row0): about
 // the largest sample of rank mu + 5 sqrt(mu) + 4, mu = k * the row's sampled

@@ -687,6 +687,8 @@ __global__ void __launch_bounds__(kSelThreads) topk_dense_kernel(const __grid_co
 {
     __shared__ Scratch sh;
     const int t = blockIdx.x;
+    if (p.row_fail != nullptr && (*p.fail_any == 0u || p.row_fail[t] == 0u))
+        return;   // decided by the sampled pass
     const int r = find_request(p.req_row_begin, p.num_requests, t);
     const int n = max(0, min(p.compress_len[t], p.req_key_count[r]));
     const float* row = p.logits + (int64_t)t * p.ld;
@@ -710,7 +712,103 @@ __global__ void __launch_bounds__(kSelThreads) topk_dense_kernel(const __grid_co
     }
 }
 
+// ------------------------------------------- sampled top-k over caller logits
+
+__device__ __forceinline__ int dense_piece(const DenseFilterParams& p, int t)
+{
+    int i = 0;
+    while (i + 1 < p.num_pieces && p.piece[i + 1].row_begin <= t)
+        ++i;
+    return i;
+}
+
+// One CTA per row of the pass: sample column e reads key (e / 128) * stride * 128 +
+// e % 128 of the row (scalar loads: caller rows need no alignment), -inf at or past
+// the row's length; rows of unsampled requests are left alone (threshold 0).
+__global__ void __launch_bounds__(256) dense_gather_kernel(const __grid_constant__ DenseFilterParams p)
+{
+    const int t = p.piece[0].row_begin + static_cast<int>(blockIdx.x);
+    const DensePiece& pc = p.piece[dense_piece(p, t)];
+    if (t >= pc.row_begin + pc.nrows)
+        return;                          // a gap between pieces
+    const int stride = p.req_stride[pc.request];
+    if (stride == 0)
+        return;
+    const int clen = min(p.compress_len[t], p.req_key_count[pc.request]);
+    const float* row = p.logits + (int64_t)t * p.ld;
+    float* out = p.samples + (int64_t)blockIdx.x * p.sample_cols;
+    for (int e = threadIdx.x; e < p.sample_cols; e += blockDim.x) {
+        const int j = (e / kTileKeys) * stride * kTileKeys + (e % kTileKeys);
+        out[e] = j < clen ? row[j] : -INFINITY;
+    }
+}
+
+// grid (key chunks, rows of the pass): every entry of the chunk at or above the row's
+// threshold (ord; 0 passes every finite entry) goes to the chunk's own list of the
+// row; its counter is bumped once per warp and load round.  Eight loads per thread
+// are in flight before any is tested.
+__global__ void __launch_bounds__(256) dense_filter_kernel(const __grid_constant__ DenseFilterParams p)
+{
+    constexpr int U = 8;
+    const int t = p.piece[0].row_begin + static_cast<int>(blockIdx.y);
+    const DensePiece& pc = p.piece[dense_piece(p, t)];
+    if (t >= pc.row_begin + pc.nrows || static_cast<int>(blockIdx.x) >= pc.slots)
+        return;
+    const int clen = min(p.compress_len[t], p.req_key_count[pc.request]);
+    const int j0 = static_cast<int>(blockIdx.x) * pc.chunk;
+    const int j1 = min(clen, j0 + pc.chunk);
+    if (j0 >= j1)
+        return;
+    const uint32_t tau = p.tau_row[t];
+    const float* row = p.logits + (int64_t)t * p.ld;
+    const int64_t list0 = pc.list_offset + ((int64_t)(t - pc.row_begin) * pc.slots + blockIdx.x) * pc.cap;
+    uint32_t* cnt = p.counts + pc.count_offset + (int64_t)(t - pc.row_begin) * pc.slots + blockIdx.x;
+    const int lane = threadIdx.x & 31;
+    for (int jb = j0; jb < j1; jb += U * static_cast<int>(blockDim.x)) {
+        float v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = jb + u * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
+            v[u] = row[min(j, j1 - 1)];    // clamped: tested below, so all loads fly together
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = jb + u * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
+            const uint32_t o = f2ord(v[u]);
+            const bool pass = j < j1 && o > kOrdNegInf && o >= tau;
+            const uint32_t m = __ballot_sync(0xffffffffu, pass);
+            if (m == 0)
+                continue;
+            uint32_t base = 0;
+            if (lane == __ffs(m) - 1)
+                base = atomicAdd(cnt, static_cast<uint32_t>(__popc(m)));
+            base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
+            const uint32_t pos = base + __popc(m & ((1u << lane) - 1u));
+            if (pass && pos < static_cast<uint32_t>(pc.cap))
+                p.lists[list0 + pos] = make_uint2(__float_as_uint(v[u]), static_cast<uint32_t>(j));
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_dense_gather(const DenseFilterParams& p, int rows, cudaStream_t stream)
+{
+    if (rows <= 0)
+        return cudaSuccess;
+    dense_gather_kernel<<<rows, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dense_filter(const DenseFilterParams& p, int rows, int max_slots,
+                                cudaStream_t stream)
+{
+    if (rows <= 0 || max_slots <= 0)
+        return cudaSuccess;
+    const dim3 grid(max_slots, rows);
+    dense_filter_kernel<<<grid, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_stream_merge(const StreamMergeParams& p, cudaStream_t stream)
 {

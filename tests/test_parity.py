@@ -441,3 +441,43 @@ def test_workspace_too_small_is_rejected():
         K.indexer_fused_topk(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"],
                              d["compress_len"], None, idx, None, ws)
     assert e.value.code == K.IDX_ERR_WORKSPACE
+
+
+# ------------------------------------------------- top-k over caller logits
+
+@pytest.mark.parametrize("structured", [None, True, False])
+def test_topk_over_logits_sampled_equals_direct(structured):
+    """indexer_topk with the plan's workspace (sampled thresholds, one filtering read,
+    verify merge, direct kernel for undecided rows) equals the direct kernel alone (a
+    status-only workspace), bit for bit, and the oracle's selector; entries past a row's
+    length are ignored even when huge."""
+    L, rows, topk = 16384, 24, 256
+    if structured is None:
+        spec = W.ProblemSpec("long rows", (W.RequestSpec(rows, L - rows, 1),
+                                           W.RequestSpec(10, 3000, 1)), H=32, D=128,
+                             topk=topk, seed=17)
+        p = W.make_problem(spec)
+        plan = Hp.make_plan(p)
+    else:
+        p, plan = _sampled_problem(L, rows, topk, structured)
+    assert plan.info()["sample_stride"] >= 2
+    d = Hp.device_inputs(p)
+    g = Hp.gpu_logits(p, plan, d)
+    cl = p.compress_len.cuda().long()
+    j = torch.arange(g.shape[1], device="cuda")[None, :]
+    g = torch.where(j >= cl[:, None], torch.full_like(g, 1e30), g)    # past the row: ignored
+    T = g.shape[0]
+    n0 = K.indexer_launch_count()
+    ti, tv = Hp.gpu_topk(p, plan, g, d)
+    n1 = K.indexer_launch_count()
+    assert n1 - n0 > 1                                   # the sampled path ran
+    di = torch.empty_like(ti)
+    dv = torch.empty_like(tv)
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    K.indexer_topk(plan, g, d["compress_len"], di, dv, small)
+    assert K.indexer_status(plan, small) == K.IDX_OK
+    assert torch.equal(ti, di) and torch.equal(tv, dv)
+    ref = O.topk_rows(g.cpu().numpy().astype(np.float64), p.compress_len.numpy(), topk)
+    for t in range(T):
+        assert sorted(x for x in ti[t].tolist() if x >= 0) == sorted(
+            x for x in ref[t].tolist() if x >= 0), t
