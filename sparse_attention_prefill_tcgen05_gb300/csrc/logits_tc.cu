@@ -773,21 +773,21 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                     }
                 } else if constexpr (SINK == kSinkFilter) {
                     // fixed threshold: append, no histograms, no refresh (a sub-list
-                    // that overflows is detected by the merge from its count)
+                    // that overflows is detected by the merge from its count).  A
+                    // candidate (about one value in twenty) takes its position from a
+                    // shared-memory counter of the (row, warp) sub-list: no warp-wide
+                    // ballot and prefix count for the other nineteen.
 #pragma unroll
                     for (int m = 0; m < RPH; ++m) {
                         const int ro = RPH >= 4 ? (m >> 2) : 0;
                         const int rl = half * RPH + own_rr(ro);
                         const int j = jt + 8 * slot_bl(RPH >= 4 ? (m & 3) : m) + g;
-                        const bool cand = rl < ui.nr && val[m] >= __uint_as_float(tau_hi[ro]);
-                        const uint32_t mb = __ballot_sync(0xffffffffu, cand) & rowmask;
-                        if (cand) {
-                            const uint32_t pos = wcnt[ro] + __popc(mb & lanes_below);
+                        if (rl < ui.nr && val[m] >= __uint_as_float(tau_hi[ro])) {
+                            const uint32_t pos = atomicAdd(&rows_s[rl].wcnt[quad], 1u);
                             if (pos < static_cast<uint32_t>(sg.cap))
                                 sub_own[ro][pos] =
                                     make_uint2(__float_as_uint(val[m]), static_cast<uint32_t>(j));
                         }
-                        wcnt[ro] += __popc(mb);
                     }
                 } else if constexpr (SINK == kSinkPoolFilter) {
                     // the same over the maxima of cand_block-key blocks: the keys of a
@@ -801,16 +801,12 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                         float bm = val[m];
                         for (int o = 1; o < p.pool; o <<= 1)
                             bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4 * o));
-                        const bool cand = (g % p.pool) == 0 && rl < ui.nr &&
-                                          bm >= __uint_as_float(tau_hi[ro]);
-                        const uint32_t mb = __ballot_sync(0xffffffffu, cand) & rowmask;
-                        if (cand) {
-                            const uint32_t pos = wcnt[ro] + __popc(mb & lanes_below);
+                        if ((g % p.pool) == 0 && rl < ui.nr && bm >= __uint_as_float(tau_hi[ro])) {
+                            const uint32_t pos = atomicAdd(&rows_s[rl].wcnt[quad], 1u);
                             if (pos < static_cast<uint32_t>(sg.cap))
                                 sub_own[ro][pos] = make_uint2(__float_as_uint(bm),
                                                               static_cast<uint32_t>(j / p.pool));
                         }
-                        wcnt[ro] += __popc(mb);
                     }
                 } else {
                     const uint32_t cap = static_cast<uint32_t>(sg.cap);
@@ -982,6 +978,14 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                 // unit end: every warp publishes its own sub-list lengths (also for
                 // units with no tiles; not for units a second pass skips, whose rows
                 // keep the first pass's lists)
+                if constexpr (SINK == kSinkFilter || SINK == kSinkPoolFilter) {
+                    // the fixed-threshold sinks count in shared memory (this warp's own
+                    // counters: its lanes' atomics are done once the warp converges)
+                    __syncwarp();
+#pragma unroll
+                    for (int ro = 0; ro < RO; ++ro)
+                        wcnt[ro] = rows_s[half * RPH + own_rr(ro)].wcnt[quad];
+                }
                 if (row_leader && !ui.skip) {
 #pragma unroll
                     for (int ro = 0; ro < RO; ++ro) {
