@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--config", default="cold64k")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["fused", "logits", "topk"], default=None,
+    ap.add_argument("--only", choices=["fused", "logits", "topk", "candidates"], default=None,
                     help="run just warmup+steps launches of one call (for profiler captures)")
     return ap.parse_args()
 
@@ -307,6 +307,18 @@ def main():
         ld = int(torch.diff(p.cu_seqlens_k).max())
         if args.only == "fused":
             fn = step
+        elif args.only == "candidates":
+            # the candidate layer pair of a workload with candidates: the source call
+            # (block mask) and the consumer (fresh queries, masked fused top-k)
+            b = spec.cand_block
+            mask = torch.empty((T, (ld + b - 1) // b), dtype=torch.uint8, device=dev)
+            d2 = {"q": p.q2.to(dev), "s_q": p.s_q2.to(dev), "w": p.w2.to(dev)}
+
+            def fn():
+                K.indexer_candidate_blocks(plan, d["q"], d["s_q"], d["w"], d["k"],
+                                           d["k_scale"], d["compress_len"], mask, wsb)
+                K.indexer_fused_topk(plan, d2["q"], d2["s_q"], d2["w"], d["k"], d["k_scale"],
+                                     d["compress_len"], mask, idx, val, wsb)
         else:
             logits = torch.empty((T, ld), dtype=torch.float32, device=dev)
 

@@ -255,6 +255,13 @@ int indexer_fused_topk_noalloc(indexer_plan_t plan, const void* q, const float* 
                                const int32_t* compress_len, const uint8_t* cand_mask,
                                int64_t ld_mask, int32_t* out_idx, float* out_val, void* stream);
 
+/* Diagnostic: synchronizes `stream` and returns how many rows the last
+   indexer_fused_topk / indexer_candidate_blocks / indexer_topk call on this
+   workspace sent to the exact path (rows its sampled threshold could not
+   decide), or a negative status.  The result is right only while the
+   workspace has not been used by another call since. */
+long long indexer_fallback_rows(indexer_plan_t plan, const void* ws, void* stream);
+
 /* Number of kernels this library has launched in this process (a
    diagnostic counter for benchmarks; never reset). */
 long long indexer_launch_count(void);

@@ -10,6 +10,6 @@ from ._lib import (  # noqa: F401
     indexer_expand_mask, indexer_fused_topk, indexer_logits, indexer_plan, indexer_selftest_timeout,
     indexer_launch_count, indexer_profile_main_kernel, indexer_set_wait_budget, indexer_status, indexer_topk, indexer_version,
     indexer_chunk_rows, indexer_page_indices, indexer_candidate_blocks_tail,
-    indexer_fused_topk_mapped, indexer_convert_fp4,
+    indexer_fused_topk_mapped, indexer_convert_fp4, indexer_fallback_rows,
     lib,
 )

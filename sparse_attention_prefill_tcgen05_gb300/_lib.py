@@ -37,7 +37,7 @@ EXPORTED = ("indexer_plan", "indexer_plan_destroy", "indexer_plan_info", "indexe
             "indexer_set_wait_budget", "indexer_launch_count", "indexer_error_string",
             "indexer_version", "indexer_fused_topk_noalloc", "indexer_profile_main_kernel",
             "indexer_chunk_rows", "indexer_page_indices", "indexer_candidate_blocks_tail",
-            "indexer_fused_topk_mapped", "indexer_convert_fp4")
+            "indexer_fused_topk_mapped", "indexer_convert_fp4", "indexer_fallback_rows")
 IDX_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -106,6 +106,8 @@ def lib():
             if name not in ("indexer_plan_destroy", "indexer_error_string"):
                 getattr(L, name).restype = ctypes.c_int
         L.indexer_launch_count.restype = ctypes.c_longlong
+        L.indexer_fallback_rows.argtypes = [P, P, P]
+        L.indexer_fallback_rows.restype = ctypes.c_longlong
         _lib = L
     return _lib
 
@@ -267,6 +269,14 @@ def indexer_profile_main_kernel(start_event=None, stop_event=None):
     logits launch of the following top-k calls; no arguments turns it off."""
     h = lambda e: ctypes.c_void_p(e.cuda_event) if e is not None else None
     lib().indexer_profile_main_kernel(h(start_event), h(stop_event))
+
+
+def indexer_fallback_rows(plan: Plan, ws, stream=None) -> int:
+    """Rows the last top-k / candidate call on ``ws`` sent to the exact path (syncs)."""
+    n = int(lib().indexer_fallback_rows(plan.handle, _ptr(ws), _stream(stream)))
+    if n < 0:
+        raise IndexerError("indexer_fallback_rows", n)
+    return n
 
 
 def indexer_version() -> int:

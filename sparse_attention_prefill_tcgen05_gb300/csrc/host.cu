@@ -378,6 +378,11 @@ int row_thresholds(Ctx& c, const Pass& ps, float* samples, uint32_t* tau_row, in
         sp.req_row_begin[r] = p->row_begin[r];
         sp.req_rank[r] = p->sample_rank_r[r] > 0 ? p->sample_stride_r[r] : 0;
         sp.req_key_count[r] = p->L[r];
+        // the sampled pass writes ceil(tiles / stride) tiles of 128 columns per row
+        sp.req_cols[r] = p->sample_rank_r[r] > 0
+                             ? (int)ceil_div(ceil_div(std::max(1, p->L[r]), kTileKeys),
+                                             p->sample_stride_r[r]) * kTileKeys
+                             : 0;
     }
     sp.req_row_begin[p->R] = p->row_begin[p->R];
     // one launch per run of adjacent pieces (a pass restricted to some rows of its
@@ -1321,6 +1326,22 @@ int indexer_fused_topk_noalloc(indexer_plan_t p, const void* q, const float* s_q
         return rc;
     return indexer_fused_topk(p, q, s_q, w, k, k_scale, clen, cand_mask, ld_mask, out_idx,
                               out_val, scratch, kNoAllocScratchBytes, stream);
+}
+
+long long indexer_fallback_rows(indexer_plan_t p, const void* ws, void* stream)
+{
+    if (!p || !ws)
+        return IDX_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return IDX_ERR_CUDA;
+    std::vector<uint32_t> flags(std::max(p->T, 1));
+    if (p->T > 0 && cudaMemcpy(flags.data(), static_cast<const uint8_t*>(ws) + p->off_fail,
+                               (size_t)p->T * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return IDX_ERR_CUDA;
+    long long n = 0;
+    for (int t = 0; t < p->T; ++t)
+        n += flags[t] != 0;
+    return n;
 }
 
 int indexer_status(indexer_plan_t p, const void* ws, void* stream)

@@ -199,6 +199,7 @@ struct SampleParams {
     int32_t req_row_begin[kMaxRequests + 1];
     int32_t req_rank[kMaxRequests];    // sampling stride of the request, 0: not sampled
     int32_t req_key_count[kMaxRequests];
+    int32_t req_cols[kMaxRequests];    // sample columns a row of the request fills (<= ld)
 };
 cudaError_t launch_sample_threshold(const SampleParams& p, cudaStream_t stream);
 

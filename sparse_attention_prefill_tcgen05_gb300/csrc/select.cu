@@ -476,12 +476,47 @@ __global__ void __launch_bounds__(kSelThreads)
     __syncthreads();
     if (p.mask) {
         uint8_t* m = p.mask + (t + pc.mask_delta) * p.ld_mask;
-        for (int64_t b = threadIdx.x; b < p.ld_mask; b += kSelThreads)
-            m[b] = 0;
+        const int64_t n = p.ld_mask;
+        if (n > static_cast<int64_t>(kStageEntries) * 64 - 64) {
+            // (a mask row longer than the staging area holds as a bitmap)
+            for (int64_t b = threadIdx.x; b < n; b += kSelThreads)
+                m[b] = 0;
+            __syncthreads();
+            for (int i = threadIdx.x; i < count; i += kSelThreads)
+                if (skey[i] >= 0 && skey[i] < n)
+                    m[skey[i]] = 1;
+            return;
+        }
+        // the kept blocks as a bitmap in the staging area (free now), then the row in
+        // one pass: bytes up to a 16-byte boundary, 16 bytes per store, the tail
+        uint32_t* bits = reinterpret_cast<uint32_t*>(stage);
+        const int nwords = static_cast<int>((n + 31) / 32) + 1;
+        for (int w = threadIdx.x; w < nwords; w += kSelThreads)
+            bits[w] = 0;
         __syncthreads();
         for (int i = threadIdx.x; i < count; i += kSelThreads)
-            if (skey[i] >= 0 && skey[i] < p.ld_mask)
-                m[skey[i]] = 1;
+            if (skey[i] >= 0 && skey[i] < n)
+                atomicOr(&bits[skey[i] >> 5], 1u << (skey[i] & 31));
+        __syncthreads();
+        auto bit = [&](int64_t b) -> uint32_t { return (bits[b >> 5] >> (b & 31)) & 1u; };
+        const int64_t head = min(n, static_cast<int64_t>((16 - (reinterpret_cast<uintptr_t>(m) & 15)) & 15));
+        for (int64_t b = threadIdx.x; b < head; b += kSelThreads)
+            m[b] = static_cast<uint8_t>(bit(b));
+        const int64_t nvec = (n - head) / 16;
+        uint4* mv = reinterpret_cast<uint4*>(m + head);
+        for (int64_t v = threadIdx.x; v < nvec; v += kSelThreads) {
+            const int64_t b0 = head + v * 16;
+            const int sh = static_cast<int>(b0 & 31);
+            const uint64_t two = static_cast<uint64_t>(bits[b0 >> 5]) |
+                                 (static_cast<uint64_t>(bits[(b0 >> 5) + 1]) << 32);
+            const uint32_t x = static_cast<uint32_t>(two >> sh) & 0xFFFFu;   // 16 block flags
+            // four flags -> four bytes of 0 / 1
+            auto spread = [](uint32_t nib) { return (nib * 0x00204081u) & 0x01010101u; };
+            mv[v] = make_uint4(spread(x & 15u), spread((x >> 4) & 15u), spread((x >> 8) & 15u),
+                               spread(x >> 12));
+        }
+        for (int64_t b = head + nvec * 16 + threadIdx.x; b < n; b += kSelThreads)
+            m[b] = static_cast<uint8_t>(bit(b));
         return;
     }
     int32_t* oi = p.out_idx + (int64_t)t * k;
@@ -570,7 +605,11 @@ __global__ void __launch_bounds__(kSelThreads, 2048 / kSelThreads)
             ++cnt;
         }
     };
-    for (int e = threadIdx.x; e < static_cast<int>(ld) / 4; e += kSelThreads) {
+    // only the columns the request's sampled tiles fill (a row of a request with fewer
+    // sampled tiles than the widest one leaves the rest of its sample row unwritten)
+    const int cols = p.req_cols[req] > 0 ? min(p.req_cols[req], static_cast<int>(ld))
+                                         : static_cast<int>(ld);
+    for (int e = threadIdx.x; e < cols / 4; e += kSelThreads) {
         const float4 v4 = reinterpret_cast<const float4*>(row)[e];
         reinterpret_cast<float4*>(srow)[e] = v4;
         if constexpr (!POOLED) {
@@ -583,7 +622,7 @@ __global__ void __launch_bounds__(kSelThreads, 2048 / kSelThreads)
     // blocks: the maximum of each aligned pool-key group (sampled tiles are whole
     // 128-key tiles, so every group is a whole block of the row), then their range
     // and count
-    const int n = static_cast<int>(ld) / pool;
+    const int n = cols / pool;
     float* vals = srow;
     if constexpr (POOLED) {
         __syncthreads();

@@ -481,3 +481,27 @@ def test_topk_over_logits_sampled_equals_direct(structured):
     for t in range(T):
         assert sorted(x for x in ti[t].tolist() if x >= 0) == sorted(
             x for x in ref[t].tolist() if x >= 0), t
+
+
+def test_repeated_calls_on_one_workspace_decide_the_same_rows():
+    """Requests with different numbers of sampled tiles share a pass (the widest sets the
+    sample row length): a second call on the same workspace must not read the first
+    call's leftovers as samples, so no row needs the exact path on either call."""
+    spec = W.ProblemSpec("mixed sampling", (W.RequestSpec(40, 7128, 1), W.RequestSpec(30, 40000, 1),
+                                            W.RequestSpec(20, 2000, 1)), H=32, D=128, topk=256,
+                         seed=23)
+    p = W.make_problem(spec)
+    plan = Hp.make_plan(p)
+    assert plan.info()["sample_stride"] >= 2
+    d = Hp.device_inputs(p)
+    ws = Hp.workspace(plan)
+    T = int(p.cu_seqlens_q[-1])
+    outs = []
+    for _ in range(3):
+        idx = torch.empty((T, p.topk), dtype=torch.int32, device="cuda")
+        K.indexer_fused_topk(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"],
+                             d["compress_len"], None, idx, None, ws)
+        assert K.indexer_status(plan, ws) == K.IDX_OK
+        assert K.indexer_fallback_rows(plan, ws) == 0
+        outs.append(idx)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
