@@ -31,8 +31,8 @@
 //   * kSinkLogits: fp32 store of the [rows, ld] logits (also used, with a key
 //     tile stride, for the sampled keys of the fused top-k);
 //   * kSinkFilter: append every entry at or above the row's fixed threshold to
-//     the warp's sub-list of its (row, key split); the merge checks that the
-//     lists decide the row;
+//     the warp's sub-list of its (row, key split), its position from a
+//     shared-memory counter; the merge checks that the lists decide the row;
 //   * kSinkStream: streamed exact top-k ("chunked-prefill-memory.md" section
 //     2.3 scores key blocks and keeps per-block top-k; here the block top-k is
 //     kept on the fly).  A key is appended to its row's list only if it is at
@@ -105,7 +105,9 @@ struct Cfg {
 
 // Per-row state of the streamed selection (shared memory, one per row of the group).
 struct RowState {
-    uint32_t wcnt[4];  // entries each epilogue warp of the row's column part appended
+    uint32_t wcnt[4];  // entries each epilogue warp of the row's column part appended (the
+                       // fixed-threshold sinks count here directly; the streams publish
+                       // their register counts here at each refresh)
     uint32_t tau_hi;   // candidate iff (ord(score), ~index) >= (tau_hi, tau_lo)
     uint32_t tau_lo;
     uint32_t b1;       // boundary bin of the top-byte histogram (256 = none yet)
@@ -995,7 +997,7 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                                      (int64_t)(ui.t0 + rl - sg.row_begin) * sg.cnt_ld + quad] =
                                 (SINK == kSinkFilter || SINK == kSinkPoolFilter)
                                     ? wcnt[ro]
-                                                    : min(wcnt[ro], static_cast<uint32_t>(sg.cap));
+                                    : min(wcnt[ro], static_cast<uint32_t>(sg.cap));
                     }
                 }
                 // both halves are done with the row state before the next unit resets it
