@@ -950,8 +950,8 @@ int indexer_logits(indexer_plan_t p, const void* q, const float* s_q, const floa
 // the logits, row thresholds, one read of every row appending the entries at or
 // above its threshold to its list, the verify merge; rows it cannot decide go to the
 // direct kernel afterwards.
-int dense_sampled(Ctx& c, uint8_t* ws, const float* logits, int64_t ld, const int32_t* clen,
-                  TopkParams& tp)
+static int dense_sampled(Ctx& c, uint8_t* ws, const float* logits, int64_t ld,
+                         const int32_t* clen, TopkParams& tp)
 {
     const indexer_plan_s* p = c.p;
     uint32_t* tau_row = reinterpret_cast<uint32_t*>(ws + p->off_tau);
