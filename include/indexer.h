@@ -20,8 +20,9 @@
  *     follow-up format.
  *   - SGLang fork commit log, the ragged-plan commit: per-batch metadata is
  *     built once and reused by every layer; host lengths avoid device syncs.
- * The score formula itself is the problem statement's; the pages name the
- * kernels but never print it.
+ * The score formula is the DeepSeek-V4 / NSA indexer's own (ReLU of the
+ * scaled per-head dot products, weighted by w over the heads); the pages name
+ * its kernels (fp8 / fp8_fp4 MQA logits) but never print it.
  *
  * Conventions shared by every entry point:
  *   - Layout.  Rows of all requests are packed: request r owns global rows

@@ -28,8 +28,9 @@
  *   - SGLang PR #39187 "Bound the dense prefill indexer transient",
  *     Modifications and Accuracy: row chunks change nothing, selected
  *     indices are raw key indices, residual differences are tie order.
- *   - The score formula, the lower-index tie-break and fp64 accumulation
- *     are the problem statement's, the pages never print the formula.
+ *   - The score formula is the DeepSeek-V4 / NSA indexer's own (the pages
+ *     name its fp8 MQA logits kernels but never print it); the lower-index
+ *     tie-break and fp64 accumulation are the readings used throughout.
  *
  * Number formats (decoded from their definitions, no library):
  *   e4m3: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits, subnormals at

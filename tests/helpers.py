@@ -1,6 +1,6 @@
 """Shared test helpers: run the CUDA path through the C ABI and compare with the oracle.
 
-Acceptance rules (the problem statement's tolerances, made precise):
+Acceptance rules (1e-3 relative logits tolerance and exact index sets, made precise):
   * logits: |gpu - oracle| <= 1e-3 * (1 + |oracle|) on eligible keys; -inf on
     exactly the ineligible ones.
   * top-k: with v_k, v_k1 the oracle's k-th and (k+1)-th eligible scores and
