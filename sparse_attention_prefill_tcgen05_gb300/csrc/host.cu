@@ -31,6 +31,7 @@ struct Pass {
 
 constexpr int kUpdateTiles = 4;          // tiles between threshold refreshes
 constexpr int kSampleTiles = 16;         // sampled key tiles per row (at most)
+constexpr int kSampleUnitTiles = 4;      // sampled tiles per work unit of the sampled pass
 constexpr int64_t kPlanSms = 152;        // SMs the planner balances for (GB300)
 constexpr int64_t kUnitsPerSm = 6;       // work units per SM wanted for load balance
 
@@ -425,10 +426,13 @@ int pass_thresholds(Ctx& c, const Pass& ps, float* samples, uint32_t* tau_row, i
         if (p->sample_rank_r[r] == 0)
             continue;                          // its rows keep every entry (threshold 0)
         sg.tile_stride = p->sample_stride_r[r];
-        sg.unit_tiles =
+        // the sampled tiles of a row group in units of a few tiles, so that the pass's
+        // few units per SM spread evenly over the SMs
+        const int sampled =
             (int)ceil_div(ceil_div(std::max(1, p->L[r]), kTileKeys), p->sample_stride_r[r]);
+        sg.unit_tiles = std::min(sampled, kSampleUnitTiles);
         sg.n_row_groups = (int)ceil_div(sg.nrows, p->G);
-        sg.n_chunks = 1;
+        sg.n_chunks = (int)ceil_div(sampled, sg.unit_tiles);
         sg.out_offset = (int64_t)(pc.a - first) * p->sample_cols;
         sg.out_ld = p->sample_cols;
         segs.push_back(sg);

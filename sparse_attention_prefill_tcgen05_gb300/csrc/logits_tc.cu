@@ -542,9 +542,11 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                     // as a float: v >= it <=> ord(v) >= tau for every v but -0.0 against
                     // tau = ord(+0.0), which only lets -0.0 entries through as well (still
                     // every entry at or above a threshold); tau = 0 passes every finite v
+                    // (a row past the group's end gets +inf: nothing of it is appended)
                     const uint32_t tr = rl < ui.nr ? p.tau_row[ui.t0 + rl] : 0u;
-                    tau_hi[ro] = tr > kOrdNegInf ? __float_as_uint(ord2f(tr))
-                                                 : 0xFF7FFFFFu;   // -FLT_MAX
+                    tau_hi[ro] = rl >= ui.nr         ? 0x7F800000u   // +inf
+                                 : tr > kOrdNegInf ? __float_as_uint(ord2f(tr))
+                                                   : 0xFF7FFFFFu;   // -FLT_MAX
                 } else if constexpr (C::STREAM) {
                     tau_hi[ro] = rows_s[rl].tau_hi;
                     tau_lo[ro] = rows_s[rl].tau_lo;
@@ -784,7 +786,7 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                         const int ro = RPH >= 4 ? (m >> 2) : 0;
                         const int rl = half * RPH + own_rr(ro);
                         const int j = jt + 8 * slot_bl(RPH >= 4 ? (m & 3) : m) + g;
-                        if (rl < ui.nr && val[m] >= __uint_as_float(tau_hi[ro])) {
+                        if (val[m] >= __uint_as_float(tau_hi[ro])) {
                             const uint32_t pos = atomicAdd(&rows_s[rl].wcnt[quad], 1u);
                             if (pos < static_cast<uint32_t>(sg.cap))
                                 sub_own[ro][pos] =
@@ -803,7 +805,7 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                         float bm = val[m];
                         for (int o = 1; o < p.pool; o <<= 1)
                             bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4 * o));
-                        if ((g % p.pool) == 0 && rl < ui.nr && bm >= __uint_as_float(tau_hi[ro])) {
+                        if ((g % p.pool) == 0 && bm >= __uint_as_float(tau_hi[ro])) {
                             const uint32_t pos = atomicAdd(&rows_s[rl].wcnt[quad], 1u);
                             if (pos < static_cast<uint32_t>(sg.cap))
                                 sub_own[ro][pos] = make_uint2(__float_as_uint(bm),
