@@ -246,15 +246,24 @@ int indexer_set_wait_budget(indexer_plan_t plan, long long cycles);
  *     contents (the call clears what it needs cleared).  Calls whose work
  *     overlaps on the GPU (different streams, or several threads) race on the
  *     array: serialize them.
- *   - Status: a device-side wait that runs out is recorded in the array's
- *     status word, which no other entry point reads; callers that need that
- *     report use indexer_fused_topk with their own workspace.
+ *   - Status: device-side failures of a call (a wait that ran out, an e2m1 key
+ *     with no exact e4m3 form, a candidate-mask row out of range) are recorded
+ *     in the array's status word, which the call clears when it starts.
+ *     indexer_noalloc_status reads it, as indexer_status reads a workspace.
  */
 #define IDX_NOALLOC_SCRATCH_BYTES (64ull << 20)
 int indexer_fused_topk_noalloc(indexer_plan_t plan, const void* q, const float* s_q,
                                const float* w, const void* k, const void* k_scale,
                                const int32_t* compress_len, const uint8_t* cand_mask,
                                int64_t ld_mask, int32_t* out_idx, float* out_val, void* stream);
+
+/* Status of the last indexer_fused_topk_noalloc call on the current device
+ * (no counterpart in the pages either: it is the allocation-free variant's
+ * indexer_status).  Synchronizes `stream`, then reads the status word of the
+ * library's scratch array: IDX_OK, IDX_ERR_TIMEOUT or IDX_ERR_DEVICE_CHECK
+ * exactly as indexer_status; IDX_ERR_CUDA if a CUDA call fails,
+ * IDX_ERR_UNSUPPORTED on a device other than sm_103.  Allocates nothing. */
+int indexer_noalloc_status(void* stream);
 
 /* Diagnostic: synchronizes `stream` and returns how many rows the last
    indexer_fused_topk / indexer_candidate_blocks / indexer_topk call on this

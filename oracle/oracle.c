@@ -120,7 +120,8 @@ int oracle_logits(int H, int D, int kdtype, int64_t nrows, const uint8_t *q,
 {
     if (H <= 0 || D <= 0 || nrows < 0 || L < 0 || (kdtype != 0 && kdtype != 1))
         return ORACLE_ERR_ARG;
-    if (kdtype == 1 && (D % 32) != 0)
+    /* fp4 keys: one ue8m0 scale per 32 elements, at most 8 blocks (D <= 256) */
+    if (kdtype == 1 && ((D % 32) != 0 || D > 256))
         return ORACLE_ERR_ARG;
     int bad = 0;
 #ifdef _OPENMP
@@ -161,7 +162,7 @@ int oracle_logits(int H, int D, int kdtype, int64_t nrows, const uint8_t *q,
                 }
                 nblk = D / 32;
                 const uint8_t *ue = (const uint8_t *)k_scale + j * (int64_t)nblk;
-                for (int b = 0; b < nblk && b < 8; ++b) {
+                for (int b = 0; b < nblk; ++b) {
                     if (ue[b] == 255)
                         nan = 1;
                     kscale_pow2[b] = ldexp(1.0, (int)ue[b] - 127);

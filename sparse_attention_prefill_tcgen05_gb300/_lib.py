@@ -37,7 +37,8 @@ EXPORTED = ("indexer_plan", "indexer_plan_destroy", "indexer_plan_info", "indexe
             "indexer_set_wait_budget", "indexer_launch_count", "indexer_error_string",
             "indexer_version", "indexer_fused_topk_noalloc", "indexer_profile_main_kernel",
             "indexer_chunk_rows", "indexer_page_indices", "indexer_candidate_blocks_tail",
-            "indexer_fused_topk_mapped", "indexer_convert_fp4", "indexer_fallback_rows")
+            "indexer_fused_topk_mapped", "indexer_convert_fp4", "indexer_fallback_rows",
+            "indexer_noalloc_status")
 IDX_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -94,6 +95,7 @@ def lib():
         L.indexer_profile_main_kernel.argtypes = [P, P]
         L.indexer_profile_main_kernel.restype = None
         L.indexer_fused_topk_noalloc.argtypes = [P, P, P, P, P, P, P, P, i64, P, P, P]
+        L.indexer_noalloc_status.argtypes = [P]
         L.indexer_chunk_rows.argtypes = [i64, ctypes.c_double, i32, i32, i32, i32]
         L.indexer_page_indices.argtypes = [P, P, P, i64, i32, P, P]
         L.indexer_convert_fp4.argtypes = [P, P, i64, i32, P, P, P, sz, P]
@@ -258,6 +260,11 @@ def indexer_fused_topk_noalloc(plan: Plan, q, s_q, w, k, k_scale, compress_len, 
     _check("indexer_fused_topk_noalloc", lib().indexer_fused_topk_noalloc(
         plan.handle, _ptr(q), _ptr(s_q), _ptr(w), _ptr(k), _ptr(k_scale), _ptr(compress_len),
         _ptr(cand_mask), ldm, _ptr(out_idx), _ptr(out_val), _stream(stream)))
+
+
+def indexer_noalloc_status(stream=None) -> int:
+    """Status word of the last indexer_fused_topk_noalloc call on this device (syncs)."""
+    return int(lib().indexer_noalloc_status(_stream(stream)))
 
 
 def indexer_launch_count() -> int:

@@ -1332,6 +1332,17 @@ int indexer_fused_topk_noalloc(indexer_plan_t p, const void* q, const float* s_q
                               out_val, scratch, kNoAllocScratchBytes, stream);
 }
 
+int indexer_noalloc_status(void* stream)
+{
+    if (!device_info().ok)
+        return IDX_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    const int rc = noalloc_scratch(&scratch);
+    if (rc != IDX_OK)
+        return rc;
+    return indexer_status(nullptr, scratch, stream);
+}
+
 long long indexer_fallback_rows(indexer_plan_t p, const void* ws, void* stream)
 {
     if (!p || !ws)

@@ -181,6 +181,25 @@ def test_fp4_block_scales_apply_per_32_elements():
     assert got2[1] == 126.0
 
 
+def test_fp4_keys_with_more_than_eight_scale_blocks_are_refused():
+    """One ue8m0 scale per 32 elements and at most eight of them per key (D <= 256): a
+    wider fp4 key is an argument error, not a key whose last blocks are dropped."""
+    H, D, L = 1, 288, 1
+    q = np.full((1, H, D), 0x38, np.uint8)
+    k = np.full((L, D // 2), 0x22, np.uint8)
+    ue = np.full((L, D // 32), 127, np.uint8)
+    ones = np.ones((1, H), np.float32)
+    with pytest.raises(RuntimeError):
+        O.logits_request(H, D, "fp4", q, ones, ones, k, ue, np.array([L], np.int32))
+    # the widest accepted key uses all eight scales
+    D = 256
+    q = np.full((1, H, D), 0x38, np.uint8)
+    k = np.full((L, D // 2), 0x22, np.uint8)
+    ue = (127 + np.arange(8, dtype=np.uint8))[None, :]
+    got = O.logits_request(H, D, "fp4", q, ones, ones, k, ue, np.array([L], np.int32))[0]
+    assert got[0] == 32 * sum(2.0 ** b for b in range(8))
+
+
 # ---------------------------------------------------------------- invariants
 
 def test_block_merge_identity():

@@ -1,12 +1,18 @@
-"""Tail-only candidate publish and the consumer's mask-row map: the packed masks of
-a subset of rows are byte-identical to the full call's rows, and a consumer reading
-masks through a row map equals one reading the gathered masks (GPU)."""
+"""Tail-only candidate publish and the consumer's mask-row map ("[SGLang PR 39187]",
+Modifications: publish only each request's tail rows).  Against the CPU oracle: the
+packed tail masks by the near-tie rule against the fp64 oracle and bit for bit against
+the oracle's block selector on the GPU's own logits; the row-mapped consumer by the
+near-tie rule under the gathered masks and bit for bit against the oracle's masked
+selector on the GPU's own logits.  Against the GPU's own full-row calls: the packed
+masks are byte-identical to the full call's rows, and the mapped consumer equals one
+given the gathered masks."""
 import dataclasses
 
 import numpy as np
 import pytest
 import torch
 
+from oracle import oracle as O
 from sparse_attention_prefill_tcgen05_gb300 import _lib as K
 from sparse_attention_prefill_tcgen05_gb300 import workloads as W
 from tests import helpers as Hp
@@ -77,3 +83,56 @@ def test_tail_counts_out_of_range_are_rejected():
     with pytest.raises(K.IndexerError) as e:
         _tail_masks(p, plan, d, [91, 0, 0])
     assert e.value.code == K.IDX_ERR_INVALID_ARG
+
+
+def _tail_rows(p, tails):
+    cu = p.cu_seqlens_q.numpy()
+    return np.concatenate([np.arange(cu[r + 1] - n, cu[r + 1]) for r, n in enumerate(tails)]
+                          ).astype(np.int64)
+
+
+@pytest.mark.parametrize("tails", [[7, 0, 50], [90, 60, 1]])
+def test_tail_publish_matches_the_oracle(tails):
+    p, plan = _problem()
+    d = Hp.device_inputs(p)
+    got = _tail_masks(p, plan, d, tails).cpu().numpy()
+    rows = _tail_rows(p, tails)
+    cl = p.compress_len.numpy()[rows]
+    b, ct = p.spec.cand_block, p.spec.cand_topk
+    ref = O.problem_logits(p, rows)
+    for i in range(len(rows)):
+        Hp.check_mask_row(got[i], ref[i], int(cl[i]), b, ct)
+    g = Hp.gpu_logits(p, plan, d).cpu().numpy()[rows].astype(np.float64)
+    assert np.array_equal(O.candidates_rows(g, cl, b, ct, got.shape[1]), got)
+
+
+def test_mapped_consumer_matches_the_oracle():
+    p, plan = _problem()
+    d = Hp.device_inputs(p)
+    tails = [30, 20, 50]
+    packed = _tail_masks(p, plan, d, tails)
+    T = int(p.cu_seqlens_q[-1])
+    rng = np.random.default_rng(9)
+    rows = rng.integers(0, packed.shape[0], size=T).astype(np.int32)
+    d2 = Hp.device_inputs(p, layer=2)
+    idx = torch.empty((T, p.topk), dtype=torch.int32, device="cuda")
+    val = torch.empty((T, p.topk), dtype=torch.float32, device="cuda")
+    ws = Hp.workspace(plan)
+    K.indexer_fused_topk_mapped(plan, d2["q"], d2["s_q"], d2["w"], d2["k"], d2["k_scale"],
+                                d2["compress_len"], packed, torch.from_numpy(rows).cuda(), idx,
+                                val, ws)
+    assert K.indexer_status(plan, ws) == K.IDX_OK
+    fi = idx.cpu().numpy()
+    gathered = packed.cpu().numpy()[rows]
+    cl = p.compress_len.numpy()
+    b = p.spec.cand_block
+    ref2 = O.problem_logits(p, np.arange(T), layer=2)
+    for t in range(T):
+        Hp.check_topk_row(fi[t], ref2[t], int(cl[t]), p.topk, mask_row=gathered[t], block=b)
+    g2 = Hp.gpu_logits(p, plan, d2).cpu().numpy().astype(np.float64)
+    want = O.topk_rows(g2, cl, p.topk, mask=gathered, mask_block=b)
+    for t in range(T):
+        assert np.array_equal(np.sort(fi[t][fi[t] >= 0]), np.sort(want[t][want[t] >= 0])), t
+    m = fi >= 0
+    assert np.array_equal(val.cpu().numpy()[m].astype(np.float64),
+                          g2[np.nonzero(m)[0], fi[m]])

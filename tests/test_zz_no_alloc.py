@@ -5,13 +5,15 @@ owns all device memory through its own pool, or a serving loop where a
 cudaMalloc would stall the device.  For them the library runs the fused
 top-k out of a fixed 64 MiB device array it holds itself.  This checks,
 through the C ABI, that two calls in a row (on different problems, so the
-second one starts from the first one's leftovers) give what the regular
-entry point gives with a caller-allocated workspace, and that a plan too
-big for the array is refused.  Kept in its own file, collected last.
+second one starts from the first one's leftovers) give, bit for bit, what
+the regular entry point gives with a caller-allocated workspace: for fp8
+keys, for e2m1 keys (converted inside the array) and for a consumer reading a
+candidate mask.  A call whose e2m1 keys are refused reports it through
+indexer_noalloc_status, and a plan too big for the array is refused.  Kept in
+its own file, collected last.
 """
 import dataclasses
 
-import numpy as np
 import pytest
 import torch
 
@@ -22,56 +24,76 @@ from . import helpers as Hp
 
 pytestmark = pytest.mark.gpu
 
+BUDGET = K.IDX_NOALLOC_SCRATCH_BYTES
 
-def _problem(name, rows_div, keys_div, topk, seed):
+
+def _problem(name, rows_div, keys_div, topk, seed, **over):
     spec = dataclasses.replace(W.scaled(W.CONFIGS[name], rows_div, keys_div), topk=topk,
-                               seed=seed)
+                               seed=seed, **over)
     return W.make_problem(spec)
 
 
-def _regular(p, plan, d):
-    return Hp.gpu_fused(p, plan, d)
-
-
-def _noalloc(p, plan, d):
+def _noalloc(p, plan, d, mask=None):
     T = int(p.cu_seqlens_q[-1])
     idx = torch.full((T, plan.problem.topk), -7, dtype=torch.int32, device="cuda")
     val = torch.full((T, plan.problem.topk), 7.0, dtype=torch.float32, device="cuda")
     K.indexer_fused_topk_noalloc(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"],
-                                 d["compress_len"], None, idx, val)
-    torch.cuda.synchronize()
+                                 d["compress_len"], mask, idx, val)
+    assert K.indexer_noalloc_status() == K.IDX_OK
     return idx, val
 
 
-def _same(a_idx, a_val, b_idx, b_val):
-    ai, bi = a_idx.cpu().numpy(), b_idx.cpu().numpy()
-    av, bv = a_val.cpu().numpy().astype(np.float64), b_val.cpu().numpy().astype(np.float64)
-    for t in range(ai.shape[0]):
-        assert set(ai[t].tolist()) == set(bi[t].tolist()), t
-        m = ai[t] >= 0
-        order_a = np.argsort(ai[t][m])
-        order_b = np.argsort(bi[t][bi[t] >= 0])
-        va = av[t][m][order_a]
-        vb = bv[t][bi[t] >= 0][order_b]
-        assert np.all(np.abs(va - vb) <= Hp.LOGIT_RTOL * (1 + np.abs(vb))), t
+def _check_pair(p, mask=None, layer=1):
+    plan = Hp.make_plan(p, budget=BUDGET)
+    assert plan.workspace_bytes <= BUDGET
+    d = Hp.device_inputs(p, layer=layer)
+    ri, rv = Hp.gpu_fused(p, plan, d, mask=mask)
+    ni, nv = _noalloc(p, plan, d, mask=mask)
+    # the same kernels on the same plan: identical bits, indices and values
+    assert torch.equal(ni, ri)
+    assert torch.equal(nv, rv)
 
 
 def test_noalloc_matches_the_workspace_entry_point_on_two_calls_in_a_row():
-    budget = K.IDX_NOALLOC_SCRATCH_BYTES
     problems = [_problem("cold64k", 8, 8, 300, seed=21),
                 _problem("long488k", 64, 64, 128, seed=22)]
     for p in problems:
-        plan = Hp.make_plan(p, budget=budget)
-        assert plan.workspace_bytes <= budget
-        d = Hp.device_inputs(p)
-        ri, rv = _regular(p, plan, d)
-        ni, nv = _noalloc(p, plan, d)
-        _same(ni, nv, ri, rv)
+        _check_pair(p)
+
+
+def test_noalloc_fp4_keys_and_masked_consumer():
+    """e2m1 keys are converted to e4m3 inside the array; a consumer reads a block mask."""
+    _check_pair(_problem("v4ratio2", 16, 32, 64, seed=31))
+    spec = dataclasses.replace(W.CONFIGS["ragged_cand"], topk=40, cand_topk=30, seed=32,
+                               requests=(W.RequestSpec(90, 0, 1), W.RequestSpec(50, 2000, 1)))
+    p = W.make_problem(spec)
+    plan = Hp.make_plan(p)
+    mask = Hp.gpu_candidates(p, plan, Hp.device_inputs(p))
+    _check_pair(p, mask=mask, layer=2)
+
+
+def test_noalloc_reports_a_refused_fp4_key():
+    """A key whose block scales span 2^10 with a 0.5 code in the small block has no exact
+    e4m3 form: the status word in the array reports it, and the next good call clears it."""
+    p = _problem("v4ratio2", 64, 256, 16, seed=33)
+    k, ks = p.k.clone(), p.k_scale.clone()
+    ks[0, 0] = 127 + 10
+    ks[0, 1] = 127
+    k[0, 16] = 0x11
+    bad = dataclasses.replace(p, k=k, k_scale=ks)
+    plan = Hp.make_plan(bad, budget=BUDGET)
+    d = Hp.device_inputs(bad)
+    T = int(bad.cu_seqlens_q[-1])
+    idx = torch.empty((T, bad.topk), dtype=torch.int32, device="cuda")
+    K.indexer_fused_topk_noalloc(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"],
+                                 d["compress_len"], None, idx, None)
+    assert K.indexer_noalloc_status() == K.IDX_ERR_DEVICE_CHECK
+    _noalloc(p, Hp.make_plan(p, budget=BUDGET), Hp.device_inputs(p))
 
 
 def test_noalloc_refuses_a_plan_larger_than_its_array():
-    """The full cold chunk planned with the default 2 GiB budget needs ~0.5 GiB: refused on
-    the host before anything is launched."""
+    """The full cold chunk planned with the default 2 GiB budget needs more than the array
+    holds: refused on the host before anything is launched."""
     spec = W.CONFIGS["cold64k"]
     T, L = spec.total_rows, spec.total_keys
     cl = torch.tensor([r + 1 for r in range(L - T, L)], dtype=torch.int32)
