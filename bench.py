@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--config", default="cold64k")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip timing the other full-size workloads")
     ap.add_argument("--only", choices=["fused", "logits", "topk", "candidates"], default=None,
                     help="run just warmup+steps launches of one call (for profiler captures)")
     return ap.parse_args()
@@ -246,6 +248,71 @@ def oracle_sample(p, seconds: float, seed: int = 0):
                       f"{dt:.1f} s"}
 
 
+def other_workloads(K, W, dev, flush, steps, names=("v4ratio2", "long488k", "ragged_cand")):
+    """The other full-size workloads, each timed through its own calls (CUDA events on the
+    launching stream, L2 flushed before every timed call, inputs resident in HBM):
+    latency, dense pairs/s and the fraction of the FP8 tensor peak, and the plan's
+    transient bytes.  The candidate workload times the source layer (block mask) and the
+    masked consumer layer separately and together."""
+    import torch
+    peak, _ = fp8_peak_tflops()
+    out = {}
+    for name in names:
+        spec = W.CONFIGS[name]
+        p = W.make_problem(spec)
+        kd = K.IDX_K_FP8_E4M3 if spec.kdtype == "fp8" else K.IDX_K_FP4_E2M1_UE8M0
+        plan = K.indexer_plan(p.cu_seqlens_q, p.cu_seqlens_k, p.compress_len, p.H, p.D, p.topk,
+                              kdtype=kd, cand_block=spec.cand_block, cand_topk=spec.cand_topk,
+                              key_block=spec.key_block)
+        T = int(p.cu_seqlens_q[-1])
+        ld = int(torch.diff(p.cu_seqlens_k).max())
+        d = {n: getattr(p, n).to(dev) for n in ("q", "s_q", "w", "k", "k_scale", "compress_len")}
+        idx = torch.empty((T, p.topk), dtype=torch.int32, device=dev)
+        val = torch.empty((T, p.topk), dtype=torch.float32, device=dev)
+        wsb = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+        calls = {}
+        if spec.cand_topk:
+            b = spec.cand_block
+            mask = torch.empty((T, (ld + b - 1) // b), dtype=torch.uint8, device=dev)
+            d2 = {"q": p.q2.to(dev), "s_q": p.s_q2.to(dev), "w": p.w2.to(dev)}
+            calls["candidate_source"] = lambda: K.indexer_candidate_blocks(
+                plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"], d["compress_len"], mask, wsb)
+            calls["masked_consumer"] = lambda: K.indexer_fused_topk(
+                plan, d2["q"], d2["s_q"], d2["w"], d["k"], d["k_scale"], d["compress_len"], mask,
+                idx, val, wsb)
+        calls["fused_topk"] = lambda: K.indexer_fused_topk(
+            plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"], d["compress_len"], None, idx,
+            val, wsb)
+        n = max(3, min(steps, 20 if name != "long488k" else 5))
+        res = {"workload": spec.name, "peak_transient_bytes": plan.workspace_bytes,
+               "dense_pairs_per_call": spec.dense_pairs, "timed_calls": n}
+        for cname, fn in calls.items():
+            for _ in range(2):
+                fn()
+            ts = []
+            for _ in range(n):
+                flush.zero_()
+                a = torch.cuda.Event(enable_timing=True)
+                e = torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                e.record()
+                ts.append((a, e))
+            torch.cuda.synchronize()
+            ms = statistics.median(x.elapsed_time(y) for x, y in ts)
+            flops = 2.0 * spec.dense_pairs * spec.H * spec.D
+            res[cname] = {"latency_ms": ms, "pairs_per_s": spec.dense_pairs / (ms / 1e3),
+                          "frac_fp8_peak": flops / (ms / 1e3) / 1e12 / peak}
+        if spec.cand_topk:
+            both = res["candidate_source"]["latency_ms"] + res["masked_consumer"]["latency_ms"]
+            res["source_plus_consumer_ms"] = both
+        assert K.indexer_status(plan, wsb) == K.IDX_OK
+        out[name] = res
+        del d, idx, val, wsb
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_reference(args, p, spec):
     """The reference arm: the CPU oracle as it stands, on the host cores.  Each step is a
     bounded row sample of the workload; ``ms_per_step`` is the measured wall time of a
@@ -435,6 +502,7 @@ def main():
     ems_serial = statistics.mean(etimes)
     ems = e2e_pipelined(K, plan, pinned, d, idx, val, wsb, out_host, stream,
                         max(10, min(args.steps, 100)))
+    others = None if args.no_other_configs else other_workloads(K, W, dev, flush, args.steps)
     clk = clocks.stop()
 
     line = {
@@ -471,6 +539,8 @@ def main():
         "clocks": clk,
         "memory_allocated_bytes": mem0,
     }
+    if others is not None:
+        line["other_workloads"] = others
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(p, args.cpu_seconds)
     if rank == 0:

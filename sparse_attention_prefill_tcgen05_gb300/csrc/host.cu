@@ -764,9 +764,28 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
     p->cnt_base.resize(R);
     // Each of a split's four sub-lists receives 32 of every 128 keys (its warp's
     // TMEM lanes), or 32 / cand_block blocks.  A sub-list holds a whole split when
-    // that is small; else room for the kept set plus two refresh intervals of
-    // appends, and at least 4 x keep so that compactions stay rare.
+    // that is small, and for requests too short to be sampled (their rows keep every
+    // entry).  Otherwise it needs room for two things:
+    //   * the exact stream: a compaction leaves a quarter of the kept set in each of
+    //     the four sub-lists, plus two refresh intervals of appends;
+    //   * the fixed-threshold pass: twice the entries a sub-list receives on average
+    //     when the row's sampled threshold sits at the sample of rank
+    //     mu + 5 sqrt(mu) + 4 (about keep * rank / mu entries per row, spread over the
+    //     row's splits x 4 sub-lists), plus 64.  A sub-list that still overflows
+    //     sends its row to the exact stream, so this only sizes the common case.
     const int slack = 2 * kUpdateTiles * 32;
+    auto sub_cap = [&](int keep, int split_units, int ns, int st) {
+        if (st == 0)
+            return split_units;   // not sampled: every entry is kept
+        int need = (keep + 3) / 4 + slack;
+        {
+            const double mu = (double)keep / st;
+            const double rank = std::ceil(mu + 5.0 * std::sqrt(mu) + 4.0);
+            need = std::max(need, (int)std::ceil(2.0 * keep * (rank / mu) /
+                                                 (kListsPerSplit * ns)) + 64);
+        }
+        return std::min(split_units, need);
+    };
     int64_t counts = 0;
     for (int r = 0; r < R; ++r) {
         const int ns = (int)std::max<int64_t>(1, ceil_div(p->L[r], p->split_r[r]));
@@ -777,9 +796,13 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
         p->n_splits[r] = ns;
         const int split_tiles =
             (int)ceil_div(std::max(1, std::min(p->split_r[r], p->L[r])), kTileKeys);
-        p->cap_k[r] = std::min(split_tiles * 32, std::max(4 * p->topk, p->topk + slack));
-        p->cap_b[r] =
-            ct ? std::min(split_tiles * (32 / cb), std::max(4 * ct, ct + slack)) : 1;
+        // the sampling stride this request gets below (0: not sampled)
+        const int tiles_r = (int)ceil_div(std::max(1, p->L[r]), kTileKeys);
+        const int st = (pr->select_mode == IDX_SELECT_AUTO && tiles_r >= 2 * kSampleTiles)
+                           ? (int)ceil_div(tiles_r, kSampleTiles)
+                           : 0;
+        p->cap_k[r] = sub_cap(p->topk, split_tiles * 32, ns, st);
+        p->cap_b[r] = ct ? sub_cap(ct, split_tiles * (32 / cb), ns, st) : 1;
         p->cnt_base[r] = counts;
         counts += (int64_t)(p->row_begin[r + 1] - p->row_begin[r]) * ns * kListsPerSplit;
     }

@@ -936,16 +936,50 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                             };
                             const CompositeThr thr = group_threshold<kHalfThreads>(
                                 *sel_s, htid, n, static_cast<uint32_t>(p.keep), load, half_sync);
-                            // kept entry number pos goes to sub-list 0, index pos <= e
+                            // kept entry number pos goes to list[pos] (the four sub-lists
+                            // are contiguous), at or before the entry's own place: pos <= e
+                            // and entry e lies at or after list[e]
                             auto emit = [&](int pos, int e, uint32_t hi, uint32_t lo) {
                                 (void)e;
                                 list[pos] = make_uint2(__float_as_uint(ord2f(hi)), ~lo);
                             };
                             const int kept = group_emit<kHalfThreads>(*sel_s, htid, n, thr, load,
                                                                       emit, half_sync);
+                            half_sync();
+                            // spread the kept entries so that sub-list w holds
+                            // c_w = (kept + 3 - w) / 4 (at most cap - slack): the entries
+                            // past c_w of a sub-list the linear fill left above c_w move, in
+                            // order, to the free slots [n_d, c_d) of the sub-lists below; the
+                            // two sets of slots are disjoint, so the copies need no order
+                            int fill[4], goal[4], surplus[4], room[4], moves = 0;
+#pragma unroll
+                            for (int w4 = 0; w4 < 4; ++w4) {
+                                fill[w4] = min(max(kept - w4 * static_cast<int>(cap), 0),
+                                               static_cast<int>(cap));
+                                goal[w4] = (kept + 3 - w4) / 4;
+                                surplus[w4] = max(fill[w4] - goal[w4], 0);
+                                room[w4] = max(goal[w4] - fill[w4], 0);
+                                moves += surplus[w4];
+                            }
+                            for (int x = htid; x < moves; x += kHalfThreads) {
+                                int ws = 0, rs_ = x;
+                                while (rs_ >= surplus[ws]) {
+                                    rs_ -= surplus[ws];
+                                    ++ws;
+                                }
+                                int wd = 0, rd = x;
+                                while (rd >= room[wd]) {
+                                    rd -= room[wd];
+                                    ++wd;
+                                }
+                                list[(int64_t)wd * sg.cap + fill[wd] + rd] =
+                                    list[(int64_t)ws * sg.cap + goal[ws] + rs_];
+                            }
+                            half_sync();
                             if (htid == 0) {
-                                rs.wcnt[0] = static_cast<uint32_t>(kept);
-                                rs.wcnt[1] = rs.wcnt[2] = rs.wcnt[3] = 0;
+#pragma unroll
+                                for (int w4 = 0; w4 < 4; ++w4)
+                                    rs.wcnt[w4] = static_cast<uint32_t>(goal[w4]);
                                 rs.compact = 0;
                                 // later entries must reach the kept set's threshold
                                 if (thr.phi > rs.tau_hi ||

@@ -159,7 +159,7 @@ struct BucketThr {
     }
 };
 
-constexpr int kStageEntries = 6400;   // candidates staged in shared memory per row (50 KB)
+constexpr int kStageEntries = 4608;   // candidates staged in shared memory per row (36 KB)
 static_assert(kStageEntries * 8 >= kBitmapWords * 8, "the bitmap reuses the staging area");
 
 __global__ void __launch_bounds__(kSelThreads)
@@ -762,8 +762,10 @@ __device__ __forceinline__ int dense_piece(const DenseFilterParams& p, int t)
 }
 
 // One CTA per row of the pass: sample column e reads key (e / 128) * stride * 128 +
-// e % 128 of the row (scalar loads: caller rows need no alignment), -inf at or past
-// the row's length; rows of unsampled requests are left alone (threshold 0).
+// e % 128 of the row, -inf at or past the row's length; rows of unsampled requests
+// are left alone (threshold 0).  VEC: 16-byte aligned rows, four columns per load (a
+// group of four never straddles a 128-key tile).
+template <bool VEC>
 __global__ void __launch_bounds__(256) dense_gather_kernel(const __grid_constant__ DenseFilterParams p)
 {
     const int t = p.piece[0].row_begin + static_cast<int>(blockIdx.x);
@@ -776,57 +778,122 @@ __global__ void __launch_bounds__(256) dense_gather_kernel(const __grid_constant
     const int clen = min(p.compress_len[t], p.req_key_count[pc.request]);
     const float* row = p.logits + (int64_t)t * p.ld;
     float* out = p.samples + (int64_t)blockIdx.x * p.sample_cols;
-    for (int e = threadIdx.x; e < p.sample_cols; e += blockDim.x) {
-        const int j = (e / kTileKeys) * stride * kTileKeys + (e % kTileKeys);
-        out[e] = j < clen ? row[j] : -INFINITY;
+    if constexpr (VEC) {
+        for (int e = 4 * static_cast<int>(threadIdx.x); e < p.sample_cols; e += 4 * blockDim.x) {
+            const int j = (e / kTileKeys) * stride * kTileKeys + (e % kTileKeys);
+            float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (j + 3 < clen) {
+                x = *reinterpret_cast<const float4*>(row + j);
+            } else {
+                if (j < clen) x.x = row[j];
+                if (j + 1 < clen) x.y = row[j + 1];
+                if (j + 2 < clen) x.z = row[j + 2];
+            }
+            *reinterpret_cast<float4*>(out + e) = x;
+        }
+    } else {
+        for (int e = threadIdx.x; e < p.sample_cols; e += blockDim.x) {
+            const int j = (e / kTileKeys) * stride * kTileKeys + (e % kTileKeys);
+            out[e] = j < clen ? row[j] : -INFINITY;
+        }
     }
 }
 
 // grid (key chunks, rows of the pass): every entry of the chunk at or above the row's
 // threshold (ord; 0 passes every finite entry) goes to the chunk's own list of the
-// row; its counter is bumped once per warp and load round.  Eight loads per thread
-// are in flight before any is tested.
-__global__ void __launch_bounds__(256) dense_filter_kernel(const __grid_constant__ DenseFilterParams p)
+// row, which no other CTA writes.  The chunk's keys are read before the row's causal
+// length arrives (bounded by the request's key count, a launch parameter), so the
+// loads do not wait on it.  VEC: rows are 16-byte aligned (aligned base, ld a multiple
+// of 4), a thread reads four entries per load with U loads (128 bytes) in flight;
+// otherwise one entry per load.  Positions come from a block-wide scan of the
+// threads' pass counts, and the list length is written once at the end.
+constexpr int kFilterThreads = 128;
+
+template <bool VEC>
+__global__ void __launch_bounds__(kFilterThreads) dense_filter_kernel(const __grid_constant__ DenseFilterParams p)
 {
-    constexpr int U = 8;
+    constexpr int U = 8;                      // loads in flight per thread
+    constexpr int W = VEC ? 4 : 1;            // entries per load
+    constexpr int PER = U * W;                // entries per thread per round
+    constexpr int NW = kFilterThreads / 32;
+    __shared__ uint32_t s_warp[NW];
     const int t = p.piece[0].row_begin + static_cast<int>(blockIdx.y);
     const DensePiece& pc = p.piece[dense_piece(p, t)];
     if (t >= pc.row_begin + pc.nrows || static_cast<int>(blockIdx.x) >= pc.slots)
         return;
-    const int clen = min(p.compress_len[t], p.req_key_count[pc.request]);
+    const int L = p.req_key_count[pc.request];
     const int j0 = static_cast<int>(blockIdx.x) * pc.chunk;
-    const int j1 = min(clen, j0 + pc.chunk);
-    if (j0 >= j1)
+    const int jmax = min(L, j0 + pc.chunk);
+    if (j0 >= jmax)
         return;
-    const uint32_t tau = p.tau_row[t];
     const float* row = p.logits + (int64_t)t * p.ld;
+    const int clen_raw = p.compress_len[t];
+    const uint32_t tau = p.tau_row[t];
     const int64_t list0 = pc.list_offset + ((int64_t)(t - pc.row_begin) * pc.slots + blockIdx.x) * pc.cap;
-    uint32_t* cnt = p.counts + pc.count_offset + (int64_t)(t - pc.row_begin) * pc.slots + blockIdx.x;
-    const int lane = threadIdx.x & 31;
-    for (int jb = j0; jb < j1; jb += U * static_cast<int>(blockDim.x)) {
-        float v[U];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t cap = static_cast<uint32_t>(pc.cap);
+    uint32_t total = 0;   // entries of the chunk appended so far (same in every thread)
+    for (int jb = j0; jb < jmax; jb += kFilterThreads * PER) {
+        float v[PER];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int j = jb + u * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
-            v[u] = row[min(j, j1 - 1)];    // clamped: tested below, so all loads fly together
+            const int j = jb + (u * kFilterThreads + static_cast<int>(threadIdx.x)) * W;
+            if constexpr (VEC) {
+                // j is a multiple of 4 and j < jmax <= ld keeps the whole load inside
+                // the row; a load at or past jmax is replaced by -inf
+                float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                if (j < jmax)
+                    x = __ldcs(reinterpret_cast<const float4*>(row + j));
+                v[4 * u] = x.x;
+                v[4 * u + 1] = x.y;
+                v[4 * u + 2] = x.z;
+                v[4 * u + 3] = x.w;
+            } else {
+                v[u] = j < jmax ? __ldcs(row + j) : -INFINITY;
+            }
         }
+        const int j1 = min(jmax, clen_raw);
+        uint32_t pass = 0;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int j = jb + u * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
-            const uint32_t o = f2ord(v[u]);
-            const bool pass = j < j1 && o > kOrdNegInf && o >= tau;
-            const uint32_t m = __ballot_sync(0xffffffffu, pass);
-            if (m == 0)
-                continue;
-            uint32_t base = 0;
-            if (lane == __ffs(m) - 1)
-                base = atomicAdd(cnt, static_cast<uint32_t>(__popc(m)));
-            base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
-            const uint32_t pos = base + __popc(m & ((1u << lane) - 1u));
-            if (pass && pos < static_cast<uint32_t>(pc.cap))
-                p.lists[list0 + pos] = make_uint2(__float_as_uint(v[u]), static_cast<uint32_t>(j));
+        for (int e = 0; e < PER; ++e) {
+            const int j = jb + ((e / W) * kFilterThreads + static_cast<int>(threadIdx.x)) * W + e % W;
+            const uint32_t o = f2ord(v[e]);
+            if (j < j1 && o > kOrdNegInf && o >= tau)
+                pass |= 1u << e;
         }
+        const uint32_t c = __popc(pass);
+        uint32_t incl = c;   // inclusive scan of the counts over the warp, then the CTA
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        if (lane == 31)
+            s_warp[warp] = incl;
+        __syncthreads();
+        uint32_t before = 0, round = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const uint32_t x = s_warp[w];
+            before += w < warp ? x : 0u;
+            round += x;
+        }
+        __syncthreads();
+        uint32_t pos = total + before + incl - c;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            if (pass & (1u << e)) {
+                const int j = jb + ((e / W) * kFilterThreads + static_cast<int>(threadIdx.x)) * W + e % W;
+                if (pos < cap)
+                    p.lists[list0 + pos] = make_uint2(__float_as_uint(v[e]), static_cast<uint32_t>(j));
+                ++pos;
+            }
+        }
+        total += round;
     }
+    if (threadIdx.x == 0)
+        p.counts[pc.count_offset + (int64_t)(t - pc.row_begin) * pc.slots + blockIdx.x] = total;
 }
 
 }  // namespace
@@ -835,7 +902,13 @@ cudaError_t launch_dense_gather(const DenseFilterParams& p, int rows, cudaStream
 {
     if (rows <= 0)
         return cudaSuccess;
-    dense_gather_kernel<<<rows, 256, 0, stream>>>(p);
+    // samples rows are sample_cols (a multiple of 128) floats apart in the workspace
+    const bool vec = (reinterpret_cast<uintptr_t>(p.logits) % 16) == 0 && p.ld % 4 == 0 &&
+                     (reinterpret_cast<uintptr_t>(p.samples) % 16) == 0;
+    if (vec)
+        dense_gather_kernel<true><<<rows, 256, 0, stream>>>(p);
+    else
+        dense_gather_kernel<false><<<rows, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -845,7 +918,11 @@ cudaError_t launch_dense_filter(const DenseFilterParams& p, int rows, int max_sl
     if (rows <= 0 || max_slots <= 0)
         return cudaSuccess;
     const dim3 grid(max_slots, rows);
-    dense_filter_kernel<<<grid, 256, 0, stream>>>(p);
+    const bool vec = (reinterpret_cast<uintptr_t>(p.logits) % 16) == 0 && p.ld % 4 == 0;
+    if (vec)
+        dense_filter_kernel<true><<<grid, kFilterThreads, 0, stream>>>(p);
+    else
+        dense_filter_kernel<false><<<grid, kFilterThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

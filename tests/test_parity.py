@@ -528,6 +528,35 @@ def test_topk_over_logits_sampled_equals_direct(structured):
             x for x in ref[t].tolist() if x >= 0), t
 
 
+def test_topk_over_unaligned_logits_rows():
+    """Rows that do not start on a 16-byte boundary (a view one column into a wider
+    buffer, odd row stride) take the one-entry-per-load path of the filtering read and
+    the sample gather: same result, bit for bit, as the aligned rows, and the oracle's
+    selector."""
+    L, rows, topk = 16384, 24, 256
+    spec = W.ProblemSpec("long rows", (W.RequestSpec(rows, L - rows, 1),
+                                       W.RequestSpec(10, 3000, 1)), H=32, D=128, topk=topk,
+                         seed=19)
+    p = W.make_problem(spec)
+    plan = Hp.make_plan(p)
+    assert plan.info()["sample_stride"] >= 2
+    d = Hp.device_inputs(p)
+    g = Hp.gpu_logits(p, plan, d)
+    T = g.shape[0]
+    wide = torch.full((T, L + 3), 5.0e30, dtype=torch.float32, device="cuda")
+    wide[:, 1:L + 1] = g
+    view = wide[:, 1:L + 1]                     # 4-byte offset, row stride L + 3
+    assert view.data_ptr() % 16 != 0 and view.stride(0) % 4 != 0
+    ai, av = Hp.gpu_topk(p, plan, g, d)
+    ui, uv = Hp.gpu_topk(p, plan, view, d)
+    assert torch.equal(ai, ui) and torch.equal(av, uv)
+    ref = O.topk_rows(g.cpu().numpy().astype(np.float64), p.compress_len.numpy(), topk)
+    ui = ui.cpu().numpy()
+    for t in range(T):
+        assert sorted(x for x in ui[t].tolist() if x >= 0) == sorted(
+            x for x in ref[t].tolist() if x >= 0), t
+
+
 def test_repeated_calls_on_one_workspace_decide_the_same_rows():
     """Requests with different numbers of sampled tiles share a pass (the widest sets the
     sample row length): a second call on the same workspace must not read the first
