@@ -771,8 +771,12 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
     //   * the fixed-threshold pass: twice the entries a sub-list receives on average
     //     when the row's sampled threshold sits at the sample of rank
     //     mu + 5 sqrt(mu) + 4 (about keep * rank / mu entries per row, spread over the
-    //     row's splits x 4 sub-lists), plus 64.  A sub-list that still overflows
-    //     sends its row to the exact stream, so this only sizes the common case.
+    //     row's splits x 4 sub-lists), plus 64.  A plan with a candidate path may serve
+    //     masked consumers, whose passing entries come in candidate blocks of up to
+    //     cand_block keys that all land in one sub-list, so they spread unevenly over
+    //     the splits: those plans size for all of a row's entries in one split.  A
+    //     sub-list that still overflows sends its row to the exact stream, so this only
+    //     sizes the common case.
     const int slack = 2 * kUpdateTiles * 32;
     auto sub_cap = [&](int keep, int split_units, int ns, int st) {
         if (st == 0)
@@ -781,8 +785,9 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
         {
             const double mu = (double)keep / st;
             const double rank = std::ceil(mu + 5.0 * std::sqrt(mu) + 4.0);
+            const int spread = ct > 0 ? 1 : ns;
             need = std::max(need, (int)std::ceil(2.0 * keep * (rank / mu) /
-                                                 (kListsPerSplit * ns)) + 64);
+                                                 (kListsPerSplit * spread)) + 64);
         }
         return std::min(split_units, need);
     };

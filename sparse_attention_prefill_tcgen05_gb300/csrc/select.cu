@@ -162,7 +162,8 @@ struct BucketThr {
 constexpr int kStageEntries = 4608;   // candidates staged in shared memory per row (36 KB)
 static_assert(kStageEntries * 8 >= kBitmapWords * 8, "the bitmap reuses the staging area");
 
-__global__ void __launch_bounds__(kSelThreads)
+// (three CTAs per SM: the staging area allows no more)
+__global__ void __launch_bounds__(kSelThreads, 3)
     stream_merge_kernel(const __grid_constant__ StreamMergeParams p)
 {
     __shared__ Scratch sh;
@@ -183,10 +184,13 @@ __global__ void __launch_bounds__(kSelThreads)
     __shared__ int s_total;
     __shared__ int s_bnd, s_need, s_bsize, s_bcount;
     __shared__ uint64_t s_cut;
+    __shared__ uint32_t s_omin, s_omax;   // range of the staged entries' order keys
     if (threadIdx.x == 0) {
         s_overflow = 0;
         s_staged = 0;
         s_nall = 0;
+        s_omin = 0xFFFFFFFFu;
+        s_omax = 0u;
     }
     __syncthreads();
     const int cta = blockIdx.x;
@@ -209,6 +213,7 @@ __global__ void __launch_bounds__(kSelThreads)
     // are in flight together.
     {
         const int lane = threadIdx.x & 31;
+        uint32_t omin = 0xFFFFFFFFu, omax = 0u;
         for (int s = threadIdx.x >> 5; s < nslots; s += kSelThreads / 32) {
             const uint32_t raw = p.counts[cbase + s];
             const int c = static_cast<int>(min(raw, static_cast<uint32_t>(pc.cap)));
@@ -226,22 +231,46 @@ __global__ void __launch_bounds__(kSelThreads)
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
                     ent[u] = src[min(i0 + u * 32 + lane, c - 1)];
+                // the round's passing entries: one shared atomic reserves the warp's room
+                uint32_t passm = 0;
+                int round = 0, mine = 0;
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int i = i0 + u * 32 + lane;
-                    const bool pass = i < c && f2ord(__uint_as_float(ent[u].x)) >= floor_ord;
+                    const uint32_t o = f2ord(__uint_as_float(ent[u].x));
+                    const bool pass = i < c && o >= floor_ord;
                     const uint32_t m = __ballot_sync(0xffffffffu, pass);
-                    if (m == 0)
-                        continue;
-                    int base = 0;
-                    if (lane == 0)
-                        base = atomicAdd(&s_staged, __popc(m));
-                    base = __shfl_sync(0xffffffffu, base, 0);
-                    const int pos = base + __popc(m & ((1u << lane) - 1u));
-                    if (pass && pos < kStageEntries)
-                        stage[pos] = ent[u];
+                    if (pass) {
+                        passm |= 1u << u;
+                        omin = min(omin, o);
+                        omax = max(omax, o);
+                    }
+                    round += __popc(m);
+                    mine += __popc(m & ((1u << lane) - 1u));
+                }
+                if (round == 0)
+                    continue;
+                int base = 0;
+                if (lane == 0)
+                    base = atomicAdd(&s_staged, round);
+                base = __shfl_sync(0xffffffffu, base, 0);
+                // lane's entries go after the lower lanes' entries of the round
+                int pos = base + mine;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (passm & (1u << u)) {
+                        if (pos < kStageEntries)
+                            stage[pos] = ent[u];
+                        ++pos;
+                    }
                 }
             }
+        }
+        omin = __reduce_min_sync(0xffffffffu, omin);
+        omax = __reduce_max_sync(0xffffffffu, omax);
+        if (lane == 0 && omin <= omax) {
+            atomicMin(&s_omin, omin);
+            atomicMax(&s_omax, omax);
         }
     }
     __syncthreads();
@@ -302,18 +331,6 @@ __global__ void __launch_bounds__(kSelThreads)
         uint32_t* bhist = reinterpret_cast<uint32_t*>(skey);
         uint64_t* bcand = reinterpret_cast<uint64_t*>(bhist + kBuckets);
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        uint32_t omin = 0xFFFFFFFFu, omax = 0u;
-        for (int e = threadIdx.x; e < n; e += kSelThreads) {
-            const uint32_t o = f2ord(__uint_as_float(stage[e].x));
-            omin = min(omin, o);
-            omax = max(omax, o);
-        }
-        omin = __reduce_min_sync(0xffffffffu, omin);
-        omax = __reduce_max_sync(0xffffffffu, omax);
-        if (lane == 0) {
-            sh.hist[0][warp] = omin;
-            sh.hist[1][warp] = omax;
-        }
         for (int i = threadIdx.x; i < kBuckets; i += kSelThreads)
             bhist[i] = 0;
         if (threadIdx.x == 0)
@@ -321,11 +338,8 @@ __global__ void __launch_bounds__(kSelThreads)
         __syncthreads();
         BucketThr bt;
         {
-            uint32_t a = 0xFFFFFFFFu, b = 0u;
-            for (int w = 0; w < kSelThreads / 32; ++w) {
-                a = min(a, sh.hist[0][w]);
-                b = max(b, sh.hist[1][w]);
-            }
+            // the staged entries' range, gathered while staging
+            const uint32_t a = s_omin, b = s_omax;
             bt.vmin = ord2f(a);
             const float range = __fsub_rn(ord2f(b), bt.vmin);
             bt.scale = range > 0.0f ? __fdiv_rn(static_cast<float>(kBuckets), range) : 0.0f;
@@ -418,16 +432,18 @@ __global__ void __launch_bounds__(kSelThreads)
         const int total = bitmap_prefix(bits, wpre, nw, sh, s_total);
         int32_t* oi = p.out_idx + (int64_t)t * k;
         float* ov = p.out_val ? p.out_val + (int64_t)t * k : nullptr;
+        // a row's list entries have distinct keys, so an entry is kept iff its key's
+        // bit is set
         for (int e = threadIdx.x; e < n; e += kSelThreads) {
-            uint32_t hi, lo;
-            load(e, hi, lo);
-            if (hi > kOrdNegInf && keep_entry(hi, lo)) {
-                const uint32_t j = ~lo;
+            const uint2 ent = stage[e];
+            const uint32_t j = ent.y;
+            const uint32_t word = bits[j >> 5];
+            if ((word >> (j & 31)) & 1u) {
                 const int pos = static_cast<int>(wpre[j >> 5] +
-                                                 __popc(bits[j >> 5] & ((1u << (j & 31)) - 1u)));
+                                                 __popc(word & ((1u << (j & 31)) - 1u)));
                 oi[pos] = static_cast<int32_t>(j);
                 if (ov)
-                    ov[pos] = ord2f(hi);
+                    ov[pos] = __uint_as_float(ent.x);
             }
         }
         for (int i = total + threadIdx.x; i < k; i += kSelThreads) {
