@@ -41,7 +41,9 @@ struct indexer_plan_s {
     int R = 0, T = 0, Lk = 0, H = 0, D = 0, topk = 0, kdtype = 0;
     int kH = 0;                       // heads the kernels run with (H, or H padded with zero heads)
     size_t off_pad = 0;               // padded q / s_q / w when kH != H
+    bool fp4_native = false;          // e2m1 keys scored by the block-scaled MMA
     size_t off_k8 = 0;                // e4m3 keys [Lk, D] + s_k [Lk] converted from e2m1
+                                      // (shapes without a block-scaled kernel)
     size_t pad_end = 0;               // end of the per-call input preparation area
     int cand_block = 8, cand_topk = 0;
     int G = 8;                        // query rows per MMA tile
@@ -189,6 +191,26 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t row_byte
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over packed e2m1 keys [rows, D/2 bytes] that unpacks each group of 16 codes
+// into a 16-byte shared-memory slot (8 data bytes, 8 bytes of padding): the 8-bit
+// container layout the f8f6f4 MMA kinds read 4-bit operands in.  A box of D = 128 codes
+// x box_rows lands as box_rows rows of 128 bytes, 128-byte swizzled like the e4m3 tiles.
+bool make_map_fp4(CUtensorMap* m, const void* base, uint64_t rows, uint32_t D,
+                  uint32_t box_rows)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {D, rows};
+    const cuuint64_t strides[1] = {D / 2};
+    const cuuint32_t box[2] = {D, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 struct DeviceInfo {
     int sms = 0;
     bool ok = false;
@@ -226,9 +248,10 @@ int check_inputs(const indexer_plan_s* p, const void* q, const float* s_q, const
 {
     if (!q || !s_q || !w || !k || !k_scale || !clen)
         return IDX_ERR_INVALID_ARG;
+    // e2m1 keys scored natively read their block scales as one 32-bit word per key
     if (!aligned(q, 16) || !aligned(k, p->kdtype == IDX_K_FP8_E4M3 ? 16 : 32) ||
-        !aligned(s_q, 4) || !aligned(w, 4) ||
-        !aligned(clen, 4) || (p->kdtype == IDX_K_FP8_E4M3 && !aligned(k_scale, 4)))
+        !aligned(s_q, 4) || !aligned(w, 4) || !aligned(clen, 4) ||
+        ((p->kdtype == IDX_K_FP8_E4M3 || p->fp4_native) && !aligned(k_scale, 4)))
         return IDX_ERR_INVALID_ARG;
     return IDX_OK;
 }
@@ -251,7 +274,8 @@ int fill_maps(Ctx& c, const void* q, const void* k)
     if (!make_map(&c.lp.tmap_q, q, (uint64_t)p->T * p->kH, p->D, p->G * p->kH))
         return IDX_ERR_CUDA;
     const uint64_t krows = (uint64_t)std::max(p->Lk, 1);
-    if (!make_map(&c.lp.tmap_k, k, krows, p->D, kTileKeys))
+    if (!(p->fp4_native ? make_map_fp4(&c.lp.tmap_k, k, krows, p->D, kTileKeys)
+                        : make_map(&c.lp.tmap_k, k, krows, p->D, kTileKeys)))
         return IDX_ERR_CUDA;
     return IDX_OK;
 }
@@ -574,8 +598,15 @@ void set_inputs(Ctx& c, const float* s_q, const float* w, const void* k_scale,
 {
     c.lp.s_q = s_q;
     c.lp.w = w;
-    // (e2m1 keys arrive here already converted to e4m3 + s_k)
-    c.lp.s_k = static_cast<const float*>(k_scale);
+    // e2m1 keys scored natively keep their block scales (the MMA applies them); others
+    // arrive here as e4m3 keys with s_k (converted from e2m1 where they were e2m1)
+    if (c.p->fp4_native) {
+        c.lp.k_sf = static_cast<const uint32_t*>(k_scale);
+        c.lp.s_k = nullptr;
+    } else {
+        c.lp.k_sf = nullptr;
+        c.lp.s_k = static_cast<const float*>(k_scale);
+    }
     c.lp.compress_len = clen;
     c.lp.status = static_cast<uint32_t*>(ws);
     c.lp.mask_block = c.p->cand_block;
@@ -600,7 +631,7 @@ int prepare(Ctx& c, const void* q, const float* s_q, const float* w, const void*
         s_q = s_q_pad;
         w = w_pad;
     }
-    if (p->kdtype == IDX_K_FP4_E2M1_UE8M0) {
+    if (p->kdtype == IDX_K_FP4_E2M1_UE8M0 && !p->fp4_native) {
         uint8_t* k8 = static_cast<uint8_t*>(ws) + p->off_k8;
         float* s_k = reinterpret_cast<float*>(k8 + (size_t)std::max(p->Lk, 1) * p->D);
         g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -729,7 +760,8 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
     }
     // 4 heads run as 8 (zero heads 4..7 add exactly 0 to every logit)
     p->kH = p->H == 4 ? 8 : p->H;
-    p->G = logits_rows_per_group(p->kH);
+    p->fp4_native = p->kdtype == IDX_K_FP4_E2M1_UE8M0 && logits_fp4_native(p->kH, p->D);
+    p->G = logits_rows_per_group(p->kH, p->fp4_native);
     const int G = p->G;
 
     // Key splits: the caller's size, else per request the fewest splits that keep
@@ -841,7 +873,7 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
     if (p->kH != p->H)
         off = align_up(off + (size_t)p->T * p->kH * (p->D + 8), 256);
     p->off_k8 = off;
-    if (p->kdtype == IDX_K_FP4_E2M1_UE8M0)
+    if (p->kdtype == IDX_K_FP4_E2M1_UE8M0 && !p->fp4_native)
         off = align_up(off + (size_t)std::max(p->Lk, 1) * (p->D + 4), 256);
     p->pad_end = off;
     p->off_gtau = off;                       // [T] shared bound, then [T] row flags

@@ -57,10 +57,13 @@ struct Segment {
 
 struct LogitsParams {
     CUtensorMap tmap_q;  // [rows*H, D] bytes, box [256 rows, D]
-    CUtensorMap tmap_k;  // [keys, D or D/2] bytes, box [128 rows, ...]
+    CUtensorMap tmap_k;  // [keys, D] bytes, box [128 rows, D]; e2m1 keys: [keys, D/2]
+                         // packed, unpacked by the map into 16-byte groups of 16 codes
     const float* s_q;    // [rows, H]
     const float* w;      // [rows, H]
     const float* s_k;    // fp8 keys: [keys]
+    const uint32_t* k_sf; // e2m1 keys scored natively: [keys] four ue8m0 block scales
+                          // (byte b: elements 32b..32b+31); nullptr for e4m3 keys
     const int32_t* compress_len;  // [rows]
     const uint8_t* cand_mask;     // nullable [rows, ld_mask] 0/1 per key block
     int64_t ld_mask;
@@ -89,7 +92,8 @@ struct LogitsParams {
 // Host-side launchers (defined in the .cu files).
 cudaError_t launch_logits(const LogitsParams& p, int H, int D, int sink, int grid,
                           cudaStream_t stream);
-int logits_rows_per_group(int H);   // query rows per MMA tile
+int logits_rows_per_group(int H, bool fp4_keys);   // query rows per MMA tile
+bool logits_fp4_native(int H, int D);   // e2m1 keys scored by the block-scaled MMA
 
 // Exact selection over the lists appended by the streaming sinks.  A piece is
 // a row range of one request whose lists were filled by the same launch; one

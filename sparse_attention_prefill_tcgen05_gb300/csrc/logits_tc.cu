@@ -59,19 +59,26 @@ namespace {
 
 constexpr int kHalfThreads = 128;
 
-template <int H, int D, int SINK>
+// FP4K: e2m1 keys with one ue8m0 scale per 32 elements, scored by the block-scaled MMA.
+// Its tiles are 192 columns (6 rows of 32 heads): two accumulators of 192 columns and
+// the scale factors fit the 512 TMEM columns (24 columns of key scales, one 4-column
+// group per K stage, then 8 columns of query scales).
+template <int H, int D, int SINK, bool FP4K = false>
 struct Cfg {
-    // tiles are 256 columns (16 rows for small H)
-    static constexpr int NMAX = H >= 16 ? kTileN : 16 * H;
+    // tiles are 256 columns (16 rows for small H; 192 for e2m1 keys)
+    static constexpr int NMAX = FP4K ? 192 : (H >= 16 ? kTileN : 16 * H);
     static constexpr int G = NMAX / H;                 // query rows per tile
     static constexpr int N = G * H;                    // MMA N
     static constexpr int QBYTES = N * D;               // Q tile: N rows of D bytes
-    static constexpr int KBYTES = kTileKeys * D;       // K tile
+    static constexpr int KBYTES = kTileKeys * D;       // K tile in shared memory
+    // bytes a K tile's TMA load counts on its barrier: the packed bytes it reads (e2m1
+    // codes are unpacked into 16-byte groups of 16 on the way into shared memory)
+    static constexpr int KTX = FP4K ? KBYTES / 2 : KBYTES;
     static constexpr int STAGES = (D >= 128) ? 6 : 8;
     static constexpr int KSTEPS = D / 32;              // MMA K = 32 elements
     // epilogue warps: 16 for the list sinks (their per-tile selection work needs the
     // latency hiding), 8 for plain logits (fewer instructions per tile, 168 registers)
-    static constexpr int EPI = SINK == kSinkLogits ? 8 : 16;
+    static constexpr int EPI = FP4K ? 12 : (SINK == kSinkLogits ? 8 : 16);
     static constexpr int THREADS = 128 + 32 * EPI;
     static constexpr int NPART = EPI / 4;              // column parts (4 warps each)
     static constexpr int RPH = G / NPART;              // rows of one column part
@@ -86,10 +93,19 @@ struct Cfg {
     static_assert(H >= 8 && (RPH == 1 || RPH == 2 || RPH == 4 || RPH == 8),
                   "the epilogue's head split needs 8..64 heads");
     static_assert(!STREAM || G <= 16, "streamed selection keeps at most 16 rows per CTA");
+    static_assert(!FP4K || (H == 32 && D == 128), "e2m1 keys: 32 heads of 128");
+    // TMEM columns of the scale factors (after the two accumulators)
+    static constexpr int SFA_COL = 2 * ACC_COLS;            // + 4 per K stage
+    static constexpr int SFB_COL = SFA_COL + 4 * STAGES;    // 8 columns
+    static_assert(!FP4K || SFB_COL + 8 <= 512, "scale factors must fit the allocation");
     // shared memory carve-up (offsets from a 1024-byte aligned base)
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + ((2 * QBYTES + 1023) / 1024) * 1024;
-    static constexpr int OFF_C = OFF_K + STAGES * KBYTES;           // float c[2][kTileN]
+    // e2m1 keys: per K stage the tile's key scale words, 16 bytes per key (the layout
+    // tcgen05.cp 128x128b reads)
+    static constexpr int OFF_SF = OFF_K + STAGES * KBYTES;
+    static constexpr int SF_BYTES = FP4K ? kTileKeys * 16 : 0;
+    static constexpr int OFF_C = OFF_SF + STAGES * SF_BYTES;        // float c[2][kTileN]
     static constexpr int OFF_HIST = OFF_C + 2 * kTileN * 4;          // u32 [G][2][256]
     static constexpr int HIST_BYTES = STREAM ? G * 2 * 256 * 4 : 0;
     static constexpr int OFF_ROWS = OFF_HIST + HIST_BYTES;           // row state [G]
@@ -278,16 +294,17 @@ __device__ __forceinline__ uint32_t warp_sum_bins(const uint32_t* hist, int lane
 
 // MASK: the launch applies a candidate-block mask (a separate instantiation, so that
 // the unmasked kernels carry none of its registers).
-template <int H, int D, int SINK, bool MASK>
-__global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
+template <int H, int D, int SINK, bool MASK, bool FP4K>
+__global__ void __launch_bounds__(Cfg<H, D, SINK, FP4K>::THREADS, 1)
     logits_tc_kernel(const __grid_constant__ LogitsParams p)
 {
-    using C = Cfg<H, D, SINK>;
+    using C = Cfg<H, D, SINK, FP4K>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* q_s = smem + C::OFF_Q;
     uint8_t* k_s = smem + C::OFF_K;
+    uint8_t* sf_s = smem + C::OFF_SF;
     float* c_s = reinterpret_cast<float*>(smem + C::OFF_C);
     uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);
     RowState* rows_s = reinterpret_cast<RowState*>(smem + C::OFF_ROWS);
@@ -317,7 +334,8 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
             mbar_init(&a_empty[i], C::EPI);
         }
         for (int i = 0; i < C::STAGES; ++i) {
-            mbar_init(&k_full[i], 1);
+            // e2m1 keys: one arrival with the TMA bytes, one when the scales are staged
+            mbar_init(&k_full[i], FP4K ? 2 : 1);
             mbar_init(&k_empty[i], 1);
         }
         mbar_init(drain, 1);
@@ -337,6 +355,19 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const long long budget = p.timeout_cycles;
+    if constexpr (FP4K) {
+        // the queries carry no block scale: every query scale cell holds 2^0 (ue8m0 127)
+        // in all four bytes, in every lane quadrant (each quadrant reads its own copy)
+        if (warp >= 4 && warp < 8) {
+            tmem_st_32x32b_x8_fill(tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) +
+                                       C::SFB_COL,
+                                   0x7F7F7F7Fu);
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         int issued[C::STAGES];
@@ -368,7 +399,7 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                         report(p, abort_flag, kStatusTimeout);
                         ok = false;
                     } else {
-                        mbar_arrive_expect_tx(&k_full[ks], C::KBYTES);
+                        mbar_arrive_expect_tx(&k_full[ks], C::KTX);
                         tma_load_2d(k_s + ks * C::KBYTES, &p.tmap_k, &k_full[ks], 0, key0);
                         ++issued[ks];
                     }
@@ -376,6 +407,28 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok)
                     break;
+                if constexpr (FP4K) {
+                    // the tile's key scale words (four ue8m0 bytes, one per 32-element
+                    // block) into the stage's scale area: key r at byte 16 r + 4 (r / 32),
+                    // so that the 128x128b copy puts it in TMEM lane r, column r / 32 of
+                    // the stage's four columns, the cell the block-scaled MMA reads for
+                    // row r; keys past the request read as 2^0 (they are masked anyway).
+                    // The previous MMAs of this stage finished (k_empty), and with them
+                    // the copy that read the area.
+                    uint8_t* sf = sf_s + ks * C::SF_BYTES;
+#pragma unroll
+                    for (int r0 = 0; r0 < kTileKeys; r0 += 32) {
+                        const int r = r0 + lane;
+                        const int local = ui.j0 + i * ui.step + r;
+                        const uint32_t word =
+                            local < sg.key_count ? __ldg(p.k_sf + key0 + r) : 0x7F7F7F7Fu;
+                        *reinterpret_cast<uint32_t*>(sf + 16 * r + 4 * (r0 / 32)) = word;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&k_full[ks]);
+                }
                 if (++ks == C::STAGES) {
                     ks = 0;
                     kph ^= 1;
@@ -422,11 +475,27 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                     tc_fence_after();
                     const uint32_t k_addr = smem_u32(k_s + ks * C::KBYTES);
                     const uint32_t d_tmem = tmem_base + ab * C::ACC_COLS;
+                    if constexpr (FP4K) {
+                        // the stage's key scales into TMEM, then one block-scaled MMA per
+                        // 32-element block (A = e2m1 keys, B = e4m3 queries); the scale
+                        // byte of block kk is byte kk of each cell
+                        const uint32_t sfa = tmem_base + C::SFA_COL + 4 * ks;
+                        tmem_cp_128x128b(sfa, smem_desc_noswizzle(smem_u32(sf_s + ks * C::SF_BYTES), 128));
 #pragma unroll
-                    for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                        const uint64_t adesc = smem_desc_kmajor(k_addr + kk * 32, D);
-                        const uint64_t bdesc = smem_desc_kmajor(q_addr + kk * 32, D);
-                        mma_f8f6f4(d_tmem, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                            const uint64_t adesc = smem_desc_kmajor(k_addr + kk * 32, D);
+                            const uint64_t bdesc = smem_desc_kmajor(q_addr + kk * 32, D);
+                            mma_mxf8f6f4(d_tmem, adesc, bdesc,
+                                         idesc_mxf8f6f4(kTileKeys, C::N, 5, 0, kk, kk), sfa,
+                                         tmem_base + C::SFB_COL, kk > 0 ? 1u : 0u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                            const uint64_t adesc = smem_desc_kmajor(k_addr + kk * 32, D);
+                            const uint64_t bdesc = smem_desc_kmajor(q_addr + kk * 32, D);
+                            mma_f8f6f4(d_tmem, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+                        }
                     }
                     mma_commit(&k_empty[ks]);
                     mma_commit(&a_full[ab]);
@@ -585,8 +654,8 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
             // or past key_count are masked to -inf whatever scale they get.
             const float* sk_row = p.s_k + sg.key_base;
             const int sk_last = max(sg.key_count - 1, 0);
-            float sk_next = 0.0f;
-            if (ui.ntiles_mma > 0)
+            float sk_next = 1.0f;   // e2m1 keys: the scales are inside the MMA
+            if (!FP4K && ui.ntiles_mma > 0)
                 sk_next = __ldg(sk_row + min(ui.j0 + quad * 32 + lane, sk_last));
             // candidate-mask bytes of this thread's keys, one tile ahead like the key
             // scales (row and key indices clamped: a byte read for a key that the
@@ -638,7 +707,7 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
                 }
                 if (i < ui.ntiles_mma) {
                     const float sk_lane = sk_next;
-                    if (i + 1 < ui.ntiles_mma)
+                    if (!FP4K && i + 1 < ui.ntiles_mma)
                         sk_next = __ldg(sk_row + min(jt + ui.step + lane, sk_last));
                     if constexpr (has_mask) {
 #pragma unroll
@@ -1049,11 +1118,11 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK>::THREADS, 1)
         tmem_dealloc(tmem_base, 512);
 }
 
-template <int H, int D, int SINK, bool MASK>
+template <int H, int D, int SINK, bool MASK, bool FP4K>
 cudaError_t launch_one(const LogitsParams& p, int grid, cudaStream_t stream)
 {
-    using C = Cfg<H, D, SINK>;
-    auto kern = logits_tc_kernel<H, D, SINK, MASK>;
+    using C = Cfg<H, D, SINK, FP4K>;
+    auto kern = logits_tc_kernel<H, D, SINK, MASK, FP4K>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);
     if (e != cudaSuccess)
@@ -1062,37 +1131,47 @@ cudaError_t launch_one(const LogitsParams& p, int grid, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-template <int H, int D>
+template <int H, int D, bool FP4K = false>
 cudaError_t launch_sink(const LogitsParams& p, int sink, int grid, cudaStream_t stream)
 {
     // masked launches: the consumer's key paths (samples, fixed threshold, stream);
     // the candidate producer itself is never masked
     const bool m = p.cand_mask != nullptr;
     if (sink == kSinkLogits)
-        return m ? launch_one<H, D, kSinkLogits, true>(p, grid, stream)
-                 : launch_one<H, D, kSinkLogits, false>(p, grid, stream);
+        return m ? launch_one<H, D, kSinkLogits, true, FP4K>(p, grid, stream)
+                 : launch_one<H, D, kSinkLogits, false, FP4K>(p, grid, stream);
     if (sink == kSinkStream)
-        return m ? launch_one<H, D, kSinkStream, true>(p, grid, stream)
-                 : launch_one<H, D, kSinkStream, false>(p, grid, stream);
+        return m ? launch_one<H, D, kSinkStream, true, FP4K>(p, grid, stream)
+                 : launch_one<H, D, kSinkStream, false, FP4K>(p, grid, stream);
     if (sink == kSinkFilter)
-        return m ? launch_one<H, D, kSinkFilter, true>(p, grid, stream)
-                 : launch_one<H, D, kSinkFilter, false>(p, grid, stream);
+        return m ? launch_one<H, D, kSinkFilter, true, FP4K>(p, grid, stream)
+                 : launch_one<H, D, kSinkFilter, false, FP4K>(p, grid, stream);
     if (m)
         return cudaErrorInvalidValue;
     if (sink == kSinkPool)
-        return launch_one<H, D, kSinkPool, false>(p, grid, stream);
+        return launch_one<H, D, kSinkPool, false, FP4K>(p, grid, stream);
     if (sink == kSinkPoolFilter)
-        return launch_one<H, D, kSinkPoolFilter, false>(p, grid, stream);
+        return launch_one<H, D, kSinkPoolFilter, false, FP4K>(p, grid, stream);
     return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-int logits_rows_per_group(int H) { return H >= 16 ? kTileN / H : 16; }
+bool logits_fp4_native(int H, int D) { return H == 32 && D == 128; }
+
+int logits_rows_per_group(int H, bool fp4_keys)
+{
+    if (fp4_keys && logits_fp4_native(H, 128))
+        return Cfg<32, 128, kSinkFilter, true>::G;
+    return H >= 16 ? kTileN / H : 16;
+}
 
 cudaError_t launch_logits(const LogitsParams& p, int H, int D, int sink, int grid,
                           cudaStream_t stream)
 {
+    if (p.k_sf != nullptr)
+        return (H == 32 && D == 128) ? launch_sink<32, 128, true>(p, sink, grid, stream)
+                                     : cudaErrorInvalidValue;
     if (H == 32 && D == 128)
         return launch_sink<32, 128>(p, sink, grid, stream);
     if (H == 16 && D == 128)

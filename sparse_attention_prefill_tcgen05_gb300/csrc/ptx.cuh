@@ -164,6 +164,54 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint
         : "memory");
 }
 
+// Block-scaled variant, kind::mxf8f6f4: D (+)= (A x 2^sfa) * (B x 2^sfb)^T with one
+// ue8m0 scale per row and 32-element K block for A (keys) and for B (query columns).
+// The scales live in TMEM: sfa_tmem / sfb_tmem address 32-bit cells holding four scale
+// bytes, the instruction descriptor's scale IDs select the byte of this K block.
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t sfa_tmem,
+                                             uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+        "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Copy 128 rows x 128 bits from shared memory (no-swizzle canonical layout, row r at
+// byte 16 r) into TMEM: row r lands in lane r, four 32-bit columns.  Asynchronous,
+// ordered with the tcgen05.mma this thread issues after it.
+__device__ __forceinline__ void tmem_cp_128x128b(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
+// 32 lanes x 8 columns of 32-bit from registers into TMEM (the warp's lane quadrant),
+// the same value in every cell.
+__device__ __forceinline__ void tmem_st_32x32b_x8_fill(uint32_t taddr, uint32_t v)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1};" ::"r"(
+            taddr),
+        "r"(v)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Make this thread's shared-memory writes visible to the async proxy (tcgen05.cp, TMA).
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so
 // far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar)
@@ -229,6 +277,31 @@ __host__ __device__ constexpr uint32_t idesc_f8f6f4(int M, int N, int a_fmt, int
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+
+// Shared-memory descriptor of a no-swizzle K-major matrix of 16-byte rows whose 8-row
+// core matrices are `sbo` bytes apart (the layout tcgen05.cp 128x128b reads).
+__device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t saddr, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= 1ull << 16;
+    d |= static_cast<uint64_t>(sbo >> 4) << 32;
+    d |= 1ull << 46;
+    return d;
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with ue8m0 scales (fp32 accumulator, both
+// operands K-major): B scale byte ID (bits 4-5), A format (7-9), B format (10-12),
+// N >> 3 (17-22), scale type ue8m0 (bit 23), M >> 4 (24-28), A scale byte ID (29-30).
+// Formats: 0 = e4m3, 5 = e2m1.
+__host__ __device__ constexpr uint32_t idesc_mxf8f6f4(int M, int N, int a_fmt, int b_fmt,
+                                                      int a_sf_id, int b_sf_id)
+{
+    return (static_cast<uint32_t>(b_sf_id & 3) << 4) | (static_cast<uint32_t>(a_fmt) << 7) |
+           (static_cast<uint32_t>(b_fmt) << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) |
+           (static_cast<uint32_t>(a_sf_id & 3) << 29);
+}
 
 // ReLU on the FMA pipe, scaled by 2^-25: sat(x * 2^-25) clamps to [0, 1],
 // which equals max(x, 0) * 2^-25 exactly whenever |x| < 2^25 (scaling by a

@@ -49,7 +49,8 @@ def gpu_logits(p, plan, d, ld=None):
     ws = workspace(plan)
     K.indexer_logits(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"], d["compress_len"],
                      out, ws)
-    assert K.indexer_status(plan, ws) == K.IDX_OK
+    st = K.indexer_status(plan, ws)
+    assert st == K.IDX_OK, K.error_string(st)
     return out
 
 
@@ -61,7 +62,8 @@ def gpu_fused(p, plan, d, mask=None, with_values=True):
     ws = workspace(plan)
     K.indexer_fused_topk(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"],
                          d["compress_len"], mask, idx, val, ws)
-    assert K.indexer_status(plan, ws) == K.IDX_OK
+    st = K.indexer_status(plan, ws)
+    assert st == K.IDX_OK, K.error_string(st)
     return idx, val
 
 
@@ -72,7 +74,8 @@ def gpu_topk(p, plan, logits, d):
     val = torch.empty((T, k), dtype=torch.float32, device="cuda")
     ws = workspace(plan)
     K.indexer_topk(plan, logits, d["compress_len"], idx, val, ws)
-    assert K.indexer_status(plan, ws) == K.IDX_OK
+    st = K.indexer_status(plan, ws)
+    assert st == K.IDX_OK, K.error_string(st)
     return idx, val
 
 
@@ -84,7 +87,8 @@ def gpu_candidates(p, plan, d, ld_mask=None):
     ws = workspace(plan)
     K.indexer_candidate_blocks(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"],
                                d["compress_len"], mask, ws)
-    assert K.indexer_status(plan, ws) == K.IDX_OK
+    st = K.indexer_status(plan, ws)
+    assert st == K.IDX_OK, K.error_string(st)
     return mask
 
 

@@ -125,15 +125,41 @@ def test_fp4_exact_arithmetic_inputs_are_bit_exact():
     assert np.array_equal(g, ref)
 
 
-def test_fp4_key_outside_the_e4m3_range_is_reported():
-    """A key whose block scales span 2^10 with a 0.5 code in the small block has no exact
-    e4m3 form: the call reports IDX_ERR_DEVICE_CHECK through indexer_status."""
-    p = small("v4ratio2", 64, 256, topk=16)
+def _wide_scale_key(p):
+    """Key 0 gets block scales 2^10 apart with a 0.5 code in the small block: an e2m1 key
+    with no exact e4m3 form under one per-key scale."""
     k, ks = p.k.clone(), p.k_scale.clone()
     ks[0, 0] = 127 + 10
     ks[0, 1] = 127
     k[0, 16] = 0x11                       # elements 32, 33 (block 1): code 1 = 0.5
-    p = dataclasses.replace(p, k=k, k_scale=ks)
+    return dataclasses.replace(p, k=k, k_scale=ks)
+
+
+def test_fp4_keys_with_widely_spread_block_scales_match_the_oracle():
+    """The block-scaled MMA applies each 32-element block's scale itself, so a key whose
+    block scales are far apart is scored like any other: logits within tolerance of the
+    oracle, the key's own row entries included, and the top-k sets."""
+    p = _wide_scale_key(small("v4ratio2", 64, 256, topk=16))
+    plan = Hp.make_plan(p)
+    d = Hp.device_inputs(p)
+    T = int(p.cu_seqlens_q[-1])
+    ref = oracle_rows(p, np.arange(T))
+    g = Hp.gpu_logits(p, plan, d).cpu().numpy()
+    Hp.check_logits(g, ref)
+    fi, _ = Hp.gpu_fused(p, plan, d)
+    fi = fi.cpu().numpy()
+    cl = p.compress_len.numpy()
+    for t in range(T):
+        Hp.check_topk_row(fi[t], ref[t], int(cl[t]), p.topk)
+
+
+def test_fp4_key_outside_the_e4m3_range_is_reported_by_the_conversion():
+    """Head counts without a block-scaled kernel (16 heads here) score e2m1 keys through
+    their exact e4m3 form; a key that has none is reported as IDX_ERR_DEVICE_CHECK
+    through indexer_status instead of being scored wrongly."""
+    spec = W.ProblemSpec("H=16 fp4", (W.RequestSpec(24, 400, 1),), H=16, D=128, topk=16,
+                         kdtype="fp4", seed=51)
+    p = _wide_scale_key(W.make_problem(spec))
     plan = Hp.make_plan(p)
     d = Hp.device_inputs(p)
     out = torch.empty((int(p.cu_seqlens_q[-1]), Hp.max_keys(p)), dtype=torch.float32,
@@ -142,6 +168,13 @@ def test_fp4_key_outside_the_e4m3_range_is_reported():
     K.indexer_logits(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"], d["compress_len"],
                      out, ws)
     assert K.indexer_status(plan, ws) == K.IDX_ERR_DEVICE_CHECK
+
+
+def test_fp4_keys_other_head_counts_parity():
+    """e2m1 keys with 16 heads (the exact conversion) against the oracle."""
+    spec = W.ProblemSpec("H=16 fp4", (W.RequestSpec(40, 3000, 2),), H=16, D=128, topk=48,
+                         kdtype="fp4", seed=52)
+    check_all(W.make_problem(spec), key_block=1024)
 
 
 def test_exact_arithmetic_inputs_are_bit_exact():

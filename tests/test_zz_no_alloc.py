@@ -7,8 +7,8 @@ top-k out of a fixed 64 MiB device array it holds itself.  This checks,
 through the C ABI, that two calls in a row (on different problems, so the
 second one starts from the first one's leftovers) give, bit for bit, what
 the regular entry point gives with a caller-allocated workspace: for fp8
-keys, for e2m1 keys (converted inside the array) and for a consumer reading a
-candidate mask.  A call whose e2m1 keys are refused reports it through
+keys, for e2m1 keys (block-scaled MMA) and for a consumer reading a
+candidate mask.  A call whose e2m1 keys the conversion refuses reports it through
 indexer_noalloc_status, and a plan too big for the array is refused.  Kept in
 its own file, collected last.
 """
@@ -62,7 +62,7 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls_in_a_row():
 
 
 def test_noalloc_fp4_keys_and_masked_consumer():
-    """e2m1 keys are converted to e4m3 inside the array; a consumer reads a block mask."""
+    """e2m1 keys scored by the block-scaled MMA; a consumer reads a block mask."""
     _check_pair(_problem("v4ratio2", 16, 32, 64, seed=31))
     spec = dataclasses.replace(W.CONFIGS["ragged_cand"], topk=40, cand_topk=30, seed=32,
                                requests=(W.RequestSpec(90, 0, 1), W.RequestSpec(50, 2000, 1)))
@@ -73,9 +73,12 @@ def test_noalloc_fp4_keys_and_masked_consumer():
 
 
 def test_noalloc_reports_a_refused_fp4_key():
-    """A key whose block scales span 2^10 with a 0.5 code in the small block has no exact
-    e4m3 form: the status word in the array reports it, and the next good call clears it."""
-    p = _problem("v4ratio2", 64, 256, 16, seed=33)
+    """With 16 heads e2m1 keys are converted to e4m3 inside the array; a key whose block
+    scales span 2^10 with a 0.5 code in the small block has no exact e4m3 form.  The
+    status word in the array reports it, and the next good call clears it."""
+    spec = W.ProblemSpec("H=16 fp4", (W.RequestSpec(24, 400, 1),), H=16, D=128, topk=16,
+                         kdtype="fp4", seed=33)
+    p = W.make_problem(spec)
     k, ks = p.k.clone(), p.k_scale.clone()
     ks[0, 0] = 127 + 10
     ks[0, 1] = 127
