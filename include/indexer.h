@@ -72,7 +72,11 @@ extern "C" {
 /* Key formats. */
 #define IDX_K_FP8_E4M3 0           /* k: e4m3 [keys, D]; k_scale: float s_k[keys] */
 #define IDX_K_FP4_E2M1_UE8M0 1     /* k: e2m1 [keys, D/2], element 2i in the low nibble;
-                                      k_scale: uint8 ue8m0 [keys, D/32]; s_k is 1 */
+                                      k_scale: uint8 ue8m0 [keys, D/32]; s_k is 1.  With 32
+                                      heads of 128 the block-scaled MMA applies the block
+                                      scales (any block-scale span; k_scale 4-byte
+                                      aligned); other head counts score the keys through
+                                      their exact e4m3 form (see indexer_convert_fp4) */
 
 /* Row selection strategies of indexer_fused_topk (both exact). */
 #define IDX_SELECT_AUTO 0          /* sampled row thresholds where rows are long enough,
@@ -247,7 +251,7 @@ int indexer_set_wait_budget(indexer_plan_t plan, long long cycles);
  *     overlaps on the GPU (different streams, or several threads) race on the
  *     array: serialize them.
  *   - Status: device-side failures of a call (a wait that ran out, an e2m1 key
- *     with no exact e4m3 form, a candidate-mask row out of range) are recorded
+ *     the e4m3 conversion cannot represent, a candidate-mask row out of range) are recorded
  *     in the array's status word, which the call clears when it starts.
  *     indexer_noalloc_status reads it, as indexer_status reads a workspace.
  */
@@ -321,8 +325,9 @@ int indexer_fused_topk_mapped(indexer_plan_t plan, const void* q, const float* s
  * (OCP MX fp4: value = e2m1(code) * 2^(e - 127)) into e4m3 codes and one fp32
  * scale per row, value = e4m3(out) * out_scale[row] exactly, out_scale =
  * 2^(largest block exponent of the row - 127).  This is how the library runs
- * e2m1 keys (inside the calls, kdtype IDX_K_FP4_E2M1_UE8M0_32), and how a caller
- * runs e2m1 queries (fp4 x fp4): convert q as T*H rows of D and pass the e4m3
+ * e2m1 keys for head counts without a block-scaled kernel (inside the calls, kdtype
+ * IDX_K_FP4_E2M1_UE8M0; 32 heads of 128 use the block-scaled MMA instead), and how a
+ * caller runs e2m1 queries (fp4 x fp4): convert q as T*H rows of D and pass the e4m3
  * codes as q and the row scales as s_q.
  *   codes: device [rows, D/2] bytes, element 2i in the low nibble;
  *   block_scales: device [rows, D/32]; D a multiple of 32 (64 or 128 here);
