@@ -62,8 +62,6 @@ struct LogitsParams {
     const float* s_q;    // [rows, H]
     const float* w;      // [rows, H]
     const float* s_k;    // fp8 keys: [keys]
-    const uint32_t* k_sf; // e2m1 keys scored natively: [keys] four ue8m0 block scales
-                          // (byte b: elements 32b..32b+31); nullptr for e4m3 keys
     const int32_t* compress_len;  // [rows]
     const uint8_t* cand_mask;     // nullable [rows, ld_mask] 0/1 per key block
     int64_t ld_mask;
@@ -87,6 +85,8 @@ struct LogitsParams {
     const uint32_t* row_fail;  // nullable [rows]: only row groups with a set row run
     const uint32_t* fail_any;  // nullable: the whole launch has no work while it reads 0
     Segment seg[kMaxSegments];
+    const uint32_t* k_sf; // e2m1 keys scored natively: [keys] four ue8m0 block scales
+                          // (byte b: elements 32b..32b+31); nullptr for e4m3 keys
 };
 
 // Host-side launchers (defined in the .cu files).

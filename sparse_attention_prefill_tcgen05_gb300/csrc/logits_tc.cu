@@ -733,14 +733,20 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK, FP4K>::THREADS, 1)
                         // multiply with 2^-25 (FMA pipe) for column 2q + 1, whose weight
                         // carries 2^25; every product and sum is bit-identical to
                         // fmaf(c, max(S, 0), part).
+                        // (the list sinks start every accumulator with the first product of
+                        // its chunk, equal to fmaf(c, max(S, 0), 0) up to the sign of a zero;
+                        // the dense-logits sink, with registers to spare, starts from zero)
+                        constexpr bool kMulFirst = SINK != kSinkLogits;
                         float2 acc2[RPH][2][2];
+                        if constexpr (!kMulFirst) {
 #pragma unroll
-                        for (int r = 0; r < RPH; ++r)
+                            for (int r = 0; r < RPH; ++r)
 #pragma unroll
-                            for (int b2 = 0; b2 < 2; ++b2) {
-                                acc2[r][b2][0] = make_float2(0.0f, 0.0f);
-                                acc2[r][b2][1] = make_float2(0.0f, 0.0f);
-                            }
+                                for (int b2 = 0; b2 < 2; ++b2) {
+                                    acc2[r][b2][0] = make_float2(0.0f, 0.0f);
+                                    acc2[r][b2][1] = make_float2(0.0f, 0.0f);
+                                }
+                        }
                         const uint32_t tbase = tmem_base +
                                                (static_cast<uint32_t>(quad * 32) << 16) +
                                                ab * C::ACC_COLS + half * C::HALF_COLS;
@@ -767,8 +773,13 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK, FP4K>::THREADS, 1)
                                                               relu_scaled(cur[4 * k + 1]));
                                 const float2 hi = make_float2(fmaxf(cur[4 * k + 2], 0.0f),
                                                               relu_scaled(cur[4 * k + 3]));
-                                acc2[r][blk][0] = __ffma2_rn(c2, lo, acc2[r][blk][0]);
-                                acc2[r][blk][1] = __ffma2_rn(c2, hi, acc2[r][blk][1]);
+                                if (kMulFirst && (ch * 32 + 8 * k) % H == 0) {   // a row's first group
+                                    acc2[r][blk][0] = __fmul2_rn(c2, lo);
+                                    acc2[r][blk][1] = __fmul2_rn(c2, hi);
+                                } else {
+                                    acc2[r][blk][0] = __ffma2_rn(c2, lo, acc2[r][blk][0]);
+                                    acc2[r][blk][1] = __ffma2_rn(c2, hi, acc2[r][blk][1]);
+                                }
                             }
                             if (ld + 1 < NLD)
                                 tmem_wait_ld();
@@ -820,8 +831,11 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK, FP4K>::THREADS, 1)
                     }
                 }
                 // causal and candidate masks (most tiles lie below every row's causal
-                // length: one warp-uniform test skips the per-value work there)
-                if (has_mask || ui.j0 + i * ui.step + kTileKeys > clen_min) {
+                // length: one warp-uniform test skips the per-value work there); the
+                // fixed-threshold sink tests a key's eligibility only for the few values
+                // at or above the threshold, in its append branch below
+                if (SINK != kSinkFilter &&
+                    (has_mask || ui.j0 + i * ui.step + kTileKeys > clen_min)) {
 #pragma unroll
                     for (int m = 0; m < RPH; ++m) {
                         const int ro = RPH >= 4 ? (m >> 2) : 0;
@@ -855,7 +869,8 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK, FP4K>::THREADS, 1)
                         const int ro = RPH >= 4 ? (m >> 2) : 0;
                         const int rl = half * RPH + own_rr(ro);
                         const int j = jt + 8 * slot_bl(RPH >= 4 ? (m & 3) : m) + g;
-                        if (val[m] >= __uint_as_float(tau_hi[ro])) {
+                        if (val[m] >= __uint_as_float(tau_hi[ro]) && j < clen[ro] &&
+                            (!has_mask || mk_cur[m] != 0u)) {
                             const uint32_t pos = atomicAdd(&rows_s[rl].wcnt[quad], 1u);
                             if (pos < static_cast<uint32_t>(sg.cap))
                                 sub_own[ro][pos] =
