@@ -30,7 +30,29 @@ struct Pass {
 };
 
 constexpr int kUpdateTiles = 4;          // tiles between threshold refreshes
-constexpr int kSampleTiles = 16;         // sampled key tiles per row (at most)
+constexpr int kSampleTiles = 16;         // sampled key tiles per row (at least, once sampled)
+constexpr int kSampleTilesMax = 128;     // ... and at most (16,384 sampled keys per row)
+constexpr double kMinSampledMu = 8.0;    // expected samples among a row's top keep, at least
+
+// Sampling stride of a request of `tiles` key tiles whose rows keep `keep` entries: every
+// st-th tile, at least kSampleTiles of them, and enough that a row's top `keep` keys hold
+// kMinSampledMu samples on average (a small expected count makes the rank of the sampled
+// threshold small and the number of keys above it spread widely); 0 = not sampled (short
+// requests keep every entry).
+int sample_stride_for(int tiles, int keep)
+{
+    if (tiles < 2 * kSampleTiles)
+        return 0;
+    const int want = (int)std::ceil(kMinSampledMu * tiles / std::max(keep, 1));
+    const int n = std::min(kSampleTilesMax, std::max(kSampleTiles, want));
+    return (int)((tiles + n - 1) / n);
+}
+
+// Upper-tail factor of the number of keys above a row's sampled threshold, relative to its
+// mean keep * rank / mu: that number is about the mean times Gamma(rank) / rank, and
+// 1 + 5 / sqrt(rank) + 10 / rank is above its 1 - 1e-7 quantile for the ranks used here
+// (3.05 at rank 14, 1.57 at rank 108).
+double rank_tail_factor(double rank) { return 1.0 + 5.0 / std::sqrt(rank) + 10.0 / rank; }
 constexpr int kSampleUnitTiles = 4;      // sampled tiles per work unit of the sampled pass
 constexpr int64_t kPlanSms = 152;        // SMs the planner balances for (GB300)
 constexpr int64_t kUnitsPerSm = 6;       // work units per SM wanted for load balance
@@ -800,10 +822,10 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
     // entry).  Otherwise it needs room for two things:
     //   * the exact stream: a compaction leaves a quarter of the kept set in each of
     //     the four sub-lists, plus two refresh intervals of appends;
-    //   * the fixed-threshold pass: twice the entries a sub-list receives on average
-    //     when the row's sampled threshold sits at the sample of rank
-    //     mu + 5 sqrt(mu) + 4 (about keep * rank / mu entries per row, spread over the
-    //     row's splits x 4 sub-lists), plus 64.  A plan with a candidate path may serve
+    //   * the fixed-threshold pass: the upper tail (rank_tail_factor) of the entries a
+    //     sub-list receives when the row's sampled threshold sits at the sample of rank
+    //     mu + 5 sqrt(mu) + 4 (on average keep * rank / mu entries per row, spread over
+    //     the row's splits x 4 sub-lists), plus 64.  A plan with a candidate path may serve
     //     masked consumers, whose passing entries come in candidate blocks of up to
     //     cand_block keys that all land in one sub-list, so they spread unevenly over
     //     the splits: those plans size for all of a row's entries in one split.  A
@@ -818,7 +840,7 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
             const double mu = (double)keep / st;
             const double rank = std::ceil(mu + 5.0 * std::sqrt(mu) + 4.0);
             const int spread = ct > 0 ? 1 : ns;
-            need = std::max(need, (int)std::ceil(2.0 * keep * (rank / mu) /
+            need = std::max(need, (int)std::ceil(rank_tail_factor(rank) * keep * (rank / mu) /
                                                  (kListsPerSplit * spread)) + 64);
         }
         return std::min(split_units, need);
@@ -835,16 +857,16 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
             (int)ceil_div(std::max(1, std::min(p->split_r[r], p->L[r])), kTileKeys);
         // the sampling stride this request gets below (0: not sampled)
         const int tiles_r = (int)ceil_div(std::max(1, p->L[r]), kTileKeys);
-        const int st = (pr->select_mode == IDX_SELECT_AUTO && tiles_r >= 2 * kSampleTiles)
-                           ? (int)ceil_div(tiles_r, kSampleTiles)
-                           : 0;
+        const int st = pr->select_mode == IDX_SELECT_AUTO ? sample_stride_for(tiles_r, p->topk)
+                                                           : 0;
         p->cap_k[r] = sub_cap(p->topk, split_tiles * 32, ns, st);
         p->cap_b[r] = ct ? sub_cap(ct, split_tiles * (32 / cb), ns, st) : 1;
         p->cnt_base[r] = counts;
         counts += (int64_t)(p->row_begin[r + 1] - p->row_begin[r]) * ns * kListsPerSplit;
     }
     // Sampled thresholds, per request with at least 2 x kSampleTiles key tiles:
-    // tiles 0, s, 2s, ... (at most kSampleTiles per row).  With mu = k / s samples
+    // tiles 0, s, 2s, ... (sample_stride_for: at least kSampleTiles per row, more where a
+    // row's top k would hold fewer than kMinSampledMu samples).  With mu = k / s samples
     // expected among a row's top k (keys in random order), the threshold is the
     // sample of rank mu + 5 sqrt(mu) + 4, so that a row whose lists end up with
     // fewer than k entries (decided again by the exact path) is rare.  Shorter
@@ -854,9 +876,9 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
     if (pr->select_mode == IDX_SELECT_AUTO) {
         for (int r = 0; r < R; ++r) {
             const int tiles = (int)ceil_div(std::max(1, p->L[r]), kTileKeys);
-            if (tiles < 2 * kSampleTiles)
+            const int st = sample_stride_for(tiles, p->topk);
+            if (st == 0)
                 continue;
-            const int st = (int)ceil_div(tiles, kSampleTiles);
             const double mu = (double)p->topk / st;
             const int cols = (int)ceil_div(tiles, st) * kTileKeys;
             p->sample_stride_r[r] = st;
