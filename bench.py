@@ -248,12 +248,14 @@ def oracle_sample(p, seconds: float, seed: int = 0):
                       f"{dt:.1f} s"}
 
 
-def other_workloads(K, W, dev, flush, steps, names=("v4ratio2", "long488k", "ragged_cand")):
+def other_workloads(K, W, dev, flush, steps,
+                    names=("v4ratio2", "v4fp4qk", "long488k", "ragged_cand")):
     """The other full-size workloads, each timed through its own calls (CUDA events on the
     launching stream, L2 flushed before every timed call, inputs resident in HBM):
     latency, dense pairs/s and the fraction of the FP8 tensor peak, and the plan's
     transient bytes.  The candidate workload times the source layer (block mask) and the
-    masked consumer layer separately and together."""
+    masked consumer layer separately and together; the fp4-query workload times the
+    exact query conversion and the fused call together."""
     import torch
     peak, _ = fp8_peak_tflops()
     out = {}
@@ -280,9 +282,24 @@ def other_workloads(K, W, dev, flush, steps, names=("v4ratio2", "long488k", "rag
             calls["masked_consumer"] = lambda: K.indexer_fused_topk(
                 plan, d2["q"], d2["s_q"], d2["w"], d["k"], d["k_scale"], d["compress_len"], mask,
                 idx, val, wsb)
-        calls["fused_topk"] = lambda: K.indexer_fused_topk(
-            plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"], d["compress_len"], None, idx,
-            val, wsb)
+        if spec.qdtype == "fp4":
+            # e2m1 queries: converted exactly to e4m3 + a scale per head vector, then the
+            # fused call on the converted queries
+            Tq, Hq, Dq = p.q.shape
+            q4 = p.q4.reshape(Tq * Hq, Dq // 2).to(dev)
+            qsf = p.q_sf.reshape(Tq * Hq, Dq // 32).to(dev)
+            q8 = torch.empty((Tq * Hq, Dq), dtype=torch.uint8, device=dev)
+            sq8 = torch.empty(Tq * Hq, dtype=torch.float32, device=dev)
+
+            def fp4q_call():
+                K.indexer_convert_fp4(q4, qsf, q8, sq8, wsb)
+                K.indexer_fused_topk(plan, q8.view(Tq, Hq, Dq), sq8.view(Tq, Hq), d["w"], d["k"],
+                                     d["k_scale"], d["compress_len"], None, idx, val, wsb)
+            calls["convert_q_and_fused_topk"] = fp4q_call
+        else:
+            calls["fused_topk"] = lambda: K.indexer_fused_topk(
+                plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"], d["compress_len"], None,
+                idx, val, wsb)
         n = max(3, min(steps, 20 if name != "long488k" else 5))
         res = {"workload": spec.name, "peak_transient_bytes": plan.workspace_bytes,
                "dense_pairs_per_call": spec.dense_pairs, "timed_calls": n}
