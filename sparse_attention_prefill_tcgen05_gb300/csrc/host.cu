@@ -420,6 +420,7 @@ int row_thresholds(Ctx& c, const Pass& ps, float* samples, uint32_t* tau_row, in
     sp.pool = pool > 1 ? pool : 1;
     sp.compress_len = c.lp.compress_len;
     sp.tau_row = tau_row;
+    sp.smax_row = tau_row + p->T;
     sp.num_requests = p->R;
     for (int r = 0; r < p->R; ++r) {
         sp.req_row_begin[r] = p->row_begin[r];
@@ -571,6 +572,7 @@ int run_streamed(Ctx& c, uint8_t* ws, int pool, int32_t* out_idx, float* out_val
             mp.gtau = nullptr;
             mp.verify = 1;
             mp.tau_row = tau_row;
+            mp.smax_row = tau_row + p->T;
             mp.row_fail = row_fail;
             mp.fail_any = fail_any;
             if ((rc = launch_merge(c, mp)) != IDX_OK)
@@ -901,8 +903,8 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
     p->off_gtau = off;                       // [T] shared bound, then [T] row flags
     p->off_fail = off + (size_t)std::max(p->T, 1) * 4;
     off = align_up(p->off_fail + (size_t)std::max(p->T, 1) * 4, 256);
-    p->off_tau = off;
-    off = align_up(off + (size_t)std::max(p->T, 1) * 4, 256);
+    p->off_tau = off;                        // [T] sampled thresholds, then [T] sample maxima
+    off = align_up(off + (size_t)std::max(p->T, 1) * 8, 256);
     p->off_counts = off;
     off = align_up(off + (size_t)std::max<int64_t>(counts, 1) * 4, 256);
     p->off_lists = off;
@@ -1106,6 +1108,7 @@ static int dense_sampled(Ctx& c, uint8_t* ws, const float* logits, int64_t ld,
         mp.counts = counts;
         mp.verify = 1;
         mp.tau_row = tau_row;
+        mp.smax_row = tau_row + p->T;
         mp.row_fail = row_fail;
         mp.fail_any = fail_any;
         mp.k = p->topk;

@@ -8,6 +8,26 @@
 
 namespace idx {
 
+// Launch with programmatic stream serialization: the kernel may begin before the
+// previous kernel in the stream has finished; it calls pdl_wait_then_release() before
+// any global memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 constexpr int kTileKeys = 128;   // MMA M: keys per tile (one TMEM lane each)
 constexpr int kTileN = 256;      // MMA N: (row, head) columns per tile
 constexpr int kMaxSegments = 48;
@@ -116,6 +136,7 @@ struct StreamMergeParams {
     uint32_t* row_fail;     // [rows] verify: set for rows the lists cannot decide;
                             // only_failed: rows with a clear entry are skipped
     const uint32_t* tau_row;  // verify: the threshold the lists were filled with
+    const uint32_t* smax_row; // nullable, verify: the largest sample of each row (ord)
     uint32_t* fail_any;       // verify: set when any row is flagged; only_failed: 0 = no work
     int32_t verify;
     int32_t only_failed;
@@ -200,6 +221,8 @@ struct SampleParams {
     int32_t pad_;
     const int32_t* compress_len;
     uint32_t* tau_row;           // [total rows], written at row0 .. row0 + rows - 1
+    uint32_t* smax_row;          // [total rows]: ord of the row's largest ranked sample where
+                                 // tau is nonzero, else 0
     int32_t req_row_begin[kMaxRequests + 1];
     int32_t req_rank[kMaxRequests];    // sampling stride of the request, 0: not sampled
     int32_t req_key_count[kMaxRequests];

@@ -298,6 +298,7 @@ template <int H, int D, int SINK, bool MASK, bool FP4K>
 __global__ void __launch_bounds__(Cfg<H, D, SINK, FP4K>::THREADS, 1)
     logits_tc_kernel(const __grid_constant__ LogitsParams p)
 {
+    pdl_wait_then_release();
     using C = Cfg<H, D, SINK, FP4K>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -1142,8 +1143,7 @@ cudaError_t launch_one(const LogitsParams& p, int grid, cudaStream_t stream)
                                          C::SMEM);
     if (e != cudaSuccess)
         return e;
-    kern<<<grid, C::THREADS, C::SMEM, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM, stream, p);
 }
 
 template <int H, int D, bool FP4K = false>

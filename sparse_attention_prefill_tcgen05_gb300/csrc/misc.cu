@@ -11,6 +11,7 @@ __global__ void expand_mask_kernel(const uint8_t* __restrict__ cand_mask, int64_
                                    const int32_t* __restrict__ clen, uint8_t* __restrict__ key_mask,
                                    int64_t ld, int block, int rows)
 {
+    pdl_wait_then_release();
     const int t = blockIdx.y;
     if (t >= rows)
         return;
@@ -33,6 +34,7 @@ __global__ void pad_heads_kernel(const uint4* __restrict__ q, const float* __res
                                  float* __restrict__ s_q_out, float* __restrict__ w_out, int rows,
                                  int h_in, int h_out, int d16)
 {
+    pdl_wait_then_release();
     const int64_t nq = (int64_t)rows * h_out * d16;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nq;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -61,6 +63,7 @@ __global__ void fp4_to_fp8_kernel(const uint8_t* __restrict__ k4, const uint8_t*
                                   int keys, int D, uint8_t* __restrict__ k8,
                                   float* __restrict__ s_k, uint32_t* status)
 {
+    pdl_wait_then_release();
     const int per_key = D / 8;
     const int64_t n = (int64_t)keys * per_key;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -158,6 +161,7 @@ __device__ __forceinline__ int row_request(const PageIndexParams& p, int t)
 
 __global__ void page_indices_kernel(const __grid_constant__ PageIndexParams p, int shift, int vec)
 {
+    pdl_wait_then_release();
     const int64_t total = (int64_t)p.rows * p.k;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     if (vec) {
@@ -194,8 +198,7 @@ cudaError_t launch_page_indices(const PageIndexParams& p, cudaStream_t st)
     const int64_t items = vec ? total / 4 : total;
     // a grid of whole waves: 152 SMs x 8 blocks of 256 threads at most
     const int blocks = static_cast<int>(std::min<int64_t>((items + 255) / 256, 152 * 8));
-    page_indices_kernel<<<blocks, 256, 0, st>>>(p, shift, vec);
-    return cudaGetLastError();
+    return launch_pdl(page_indices_kernel, dim3(blocks), dim3(256), 0, st, p, shift, vec);
 }
 
 cudaError_t launch_expand_mask(const uint8_t* cand_mask, int64_t ld_mask, const int32_t* clen,
@@ -206,8 +209,8 @@ cudaError_t launch_expand_mask(const uint8_t* cand_mask, int64_t ld_mask, const 
         return cudaSuccess;
     const int64_t per_row = (ld + 255) / 256;
     dim3 grid((unsigned)std::min<int64_t>(per_row, 64), (unsigned)rows);
-    expand_mask_kernel<<<grid, 256, 0, st>>>(cand_mask, ld_mask, clen, key_mask, ld, block, rows);
-    return cudaGetLastError();
+    return launch_pdl(expand_mask_kernel, grid, dim3(256), 0, st, cand_mask, ld_mask, clen,
+                      key_mask, ld, block, rows);
 }
 
 cudaError_t launch_fp4_to_fp8(const uint8_t* k4, const uint8_t* sf, int keys, int D, uint8_t* k8,
@@ -217,8 +220,8 @@ cudaError_t launch_fp4_to_fp8(const uint8_t* k4, const uint8_t* sf, int keys, in
         return cudaSuccess;
     const int64_t n = (int64_t)keys * (D / 8);
     const int blocks = (int)std::min<int64_t>((n + 255) / 256, 8192);
-    fp4_to_fp8_kernel<<<blocks, 256, 0, st>>>(k4, sf, keys, D, k8, s_k, status);
-    return cudaGetLastError();
+    return launch_pdl(fp4_to_fp8_kernel, dim3(blocks), dim3(256), 0, st, k4, sf, keys, D, k8, s_k,
+                      status);
 }
 
 cudaError_t launch_pad_heads(const void* q, const float* s_q, const float* w, void* q_out,
@@ -229,10 +232,9 @@ cudaError_t launch_pad_heads(const void* q, const float* s_q, const float* w, vo
         return cudaSuccess;
     const int64_t nq = (int64_t)rows * h_out * (D / 16);
     const int blocks = (int)std::min<int64_t>((nq + 255) / 256, 4096);
-    pad_heads_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(q), s_q, w,
-                                             static_cast<uint4*>(q_out), s_q_out, w_out, rows,
-                                             h_in, h_out, D / 16);
-    return cudaGetLastError();
+    return launch_pdl(pad_heads_kernel, dim3(blocks), dim3(256), 0, st,
+                      static_cast<const uint4*>(q), s_q, w, static_cast<uint4*>(q_out), s_q_out,
+                      w_out, rows, h_in, h_out, D / 16);
 }
 
 cudaError_t launch_selftest_timeout(uint32_t* status, long long cycles, cudaStream_t st)

@@ -329,4 +329,15 @@ __device__ __forceinline__ float ord2f(uint32_t u)
 // ord(-inf): anything at or below it is "not eligible" for selection.
 constexpr uint32_t kOrdNegInf = 0x007FFFFFu;
 
+// Programmatic dependent launch.  Every kernel of the library is launched so that it
+// may start while the previous kernel of its stream is still running: it first waits
+// for that kernel to complete (its writes visible), then lets the next kernel's blocks
+// be placed as resources free up (they in turn wait before touching anything).  Both
+// are no-ops for a kernel launched the ordinary way.
+__device__ __forceinline__ void pdl_wait_then_release()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace idx

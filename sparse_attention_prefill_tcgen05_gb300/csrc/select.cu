@@ -11,6 +11,8 @@
 //     is the top-k of the row (same section, "holds exactly");
 //   * candidate blocks: the same over 8-key block maxima, written as a mask.
 // The threshold search and ordered emission are in groupsel.cuh.
+#include <algorithm>
+
 #include "groupsel.cuh"
 #include "internal.h"
 
@@ -161,16 +163,219 @@ struct BucketThr {
 
 constexpr int kStageEntries = 4608;   // candidates staged in shared memory per row (36 KB)
 static_assert(kStageEntries * 8 >= kBitmapWords * 8, "the bitmap reuses the staging area");
+// dynamic shared memory of the merge: [stage: kStageEntries x 8 B][scratch: keys and
+// values n2 x 4 B each, or the bitmap and its prefix][output row: n2 indices, n2 values
+// (index outputs only)]
+__host__ __device__ constexpr size_t merge_obuf_offset(int n2)
+{
+    return 8 * (size_t)kStageEntries + (8 * (size_t)n2 > 8 * (size_t)kBitmapWords
+                                            ? 8 * (size_t)n2
+                                            : 8 * (size_t)kBitmapWords);
+}
 
-// (three CTAs per SM: the staging area allows no more)
-__global__ void __launch_bounds__(kSelThreads, 3)
-    stream_merge_kernel(const __grid_constant__ StreamMergeParams p)
+// The verify merge of a row whose lists were filled at a sampled threshold tau (every
+// listed entry is at or above it) and whose keys fit the bitmap (at most 65,536): the
+// entries go to shared memory at the prefix of the sub-list lengths, bucketed on the way
+// (2048 equal-width buckets from tau to the row's largest sample; larger values share
+// the top bucket) with the bucket kept in the upper 16 bits of the entry's key field;
+// then the boundary bucket, the bitmap of kept keys and the ordered output as in the
+// general path.  Returns false, having written nothing to global memory, when the row
+// needs the general path (no sampled range, more entries than the staging area holds,
+// a boundary bucket too large to rank directly); true when the row is done (flagged or
+// written).  Every thread calls it; the result is the same in all of them.
+__device__ __forceinline__ bool merge_row_verified(const StreamMergeParams& p, const MergePiece& pc,
+                                                   const int t, const int64_t lbase,
+                                                   const int64_t cbase, const int n2,
+                                                   uint8_t* dyn, Scratch& sh)
+{
+    __shared__ uint32_t v_cnt[kMaxStreamSlots];
+    __shared__ int v_bcount, v_total;
+    __shared__ uint64_t v_cut;
+    const uint32_t tau = p.tau_row[t];
+    const uint32_t smax = p.smax_row[t];
+    const int nslots = pc.slots, cap = pc.cap;
+    const int row_words = (pc.key_count + 31) / 32;
+    if (tau <= kOrdNegInf || smax <= tau || !p.bitmap || row_words > kBitmapWords || cap <= 0)
+        return false;
+    BucketThr bt;
+    bt.vmin = ord2f(tau);
+    {
+        const float range = __fsub_rn(ord2f(smax), bt.vmin);
+        bt.scale = range > 0.0f ? __fdiv_rn(static_cast<float>(kBuckets), range) : 0.0f;
+        if (!(bt.scale > 0.0f && bt.scale < INFINITY))
+            return false;
+    }
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kWarps = kSelThreads / 32;
+    uint2* stage = reinterpret_cast<uint2*>(dyn);
+    uint32_t* bhist = reinterpret_cast<uint32_t*>(dyn + 8 * (size_t)kStageEntries);
+    uint64_t* bcand = reinterpret_cast<uint64_t*>(bhist + kBuckets);
+    for (int i = tid; i < kBuckets; i += kSelThreads)
+        bhist[i] = 0;
+    if (tid == 0)
+        v_bcount = 0;
+    // the first 256 entries of the warp's first sub-list load together with the counts
+    // (indices clamped to the capacity: the loads do not wait for the count)
+    uint2 ent[8];
+    if (warp < nslots) {
+        const uint2* src = p.lists + lbase + (int64_t)warp * cap;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            ent[u] = src[min(u * 32 + lane, cap - 1)];
+    }
+    int over = 0;
+    for (int s = tid; s < nslots; s += kSelThreads) {
+        const uint32_t raw = p.counts[cbase + s];
+        v_cnt[s] = min(raw, static_cast<uint32_t>(cap));
+        over |= raw > static_cast<uint32_t>(cap);
+    }
+    const int overflow = __syncthreads_or(over);
+    uint32_t tot = 0;
+    for (int s = lane; s < nslots; s += 32)
+        tot += v_cnt[s];
+    const int n = static_cast<int>(__reduce_add_sync(0xffffffffu, tot));
+    if (overflow || n < p.k) {
+        // the lists hold every entry at or above tau unless a sub-list overflowed; with
+        // fewer than k of them they cannot decide the row
+        if (tid == 0) {
+            p.row_fail[t] = 1u;
+            atomicOr(p.fail_any, 1u);
+        }
+        return true;
+    }
+    if (n > kStageEntries)
+        return false;
+    for (int s = warp; s < nslots; s += kWarps) {
+        uint32_t o = 0;
+        for (int x = lane; x < s; x += 32)
+            o += v_cnt[x];
+        const int off = static_cast<int>(__reduce_add_sync(0xffffffffu, o));
+        const int c = static_cast<int>(v_cnt[s]);
+        const uint2* src = p.lists + lbase + (int64_t)s * cap;
+        for (int i0 = 0; i0 < c; i0 += 256) {
+            if (s != warp || i0 > 0) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    ent[u] = src[min(i0 + u * 32 + lane, c - 1)];
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * 32 + lane;
+                if (i < c) {
+                    const uint32_t b = static_cast<uint32_t>(bt.bucket(__uint_as_float(ent[u].x)));
+                    atomicAdd(&bhist[b], 1u);
+                    stage[off + i] = make_uint2(ent[u].x, (ent[u].y & 0xFFFFu) | (b << 16));
+                }
+            }
+        }
+    }
+    __syncthreads();
+    // the bucket holding the k-th largest entry, from the top: thread i owns buckets
+    // [2048 - 4 (i + 1), 2048 - 4 i)
+    const uint32_t k = static_cast<uint32_t>(p.k);
+    {
+        constexpr int kPer = kBuckets / kSelThreads;
+        const int top = kBuckets - kPer * tid;
+        uint32_t c4[kPer], local = 0;
+#pragma unroll
+        for (int x = 0; x < kPer; ++x) {
+            c4[x] = bhist[top - 1 - x];
+            local += c4[x];
+        }
+        const uint32_t above_me = block_exclusive_sum(local, sh);
+        if (above_me < k && above_me + local >= k) {
+            uint32_t cum = above_me;
+#pragma unroll
+            for (int x = 0; x < kPer; ++x) {
+                if (cum + c4[x] >= k) {
+                    sh.bcast[0] = static_cast<uint32_t>(top - 1 - x);
+                    sh.bcast[1] = k - cum;
+                    sh.bcast[2] = c4[x];
+                    break;
+                }
+                cum += c4[x];
+            }
+        }
+        __syncthreads();
+    }
+    const uint32_t bnd = sh.bcast[0], need = sh.bcast[1], bsize = sh.bcast[2];
+    // composite key (ord(score), ~index) of a staged entry
+    auto comp = [](const uint2 en) {
+        return (static_cast<uint64_t>(f2ord(__uint_as_float(en.x))) << 32) |
+               static_cast<uint32_t>(~(en.y & 0xFFFFu));
+    };
+    uint64_t cut = 0;   // the whole boundary bucket is kept when it gives all of its entries
+    if (bsize != need) {
+        if (bsize > static_cast<uint32_t>(kBucketCands))
+            return false;
+        for (int e = tid; e < n; e += kSelThreads) {
+            const uint2 en = stage[e];
+            if ((en.y >> 16) == bnd)
+                bcand[atomicAdd(&v_bcount, 1)] = comp(en);
+        }
+        __syncthreads();
+        // the need-th largest candidate: the one with exactly need - 1 above it
+        for (int i = tid; i < static_cast<int>(bsize); i += kSelThreads) {
+            const uint64_t mine = bcand[i];
+            uint32_t rank = 0;
+            for (int x = 0; x < static_cast<int>(bsize); ++x)
+                rank += bcand[x] > mine;
+            if (rank == need - 1)
+                v_cut = mine;
+        }
+        __syncthreads();
+        cut = v_cut;
+    }
+    __syncthreads();   // the bucket scratch becomes the bitmap
+    uint32_t* bits = bhist;
+    uint32_t* wpre = bits + kBitmapWords;
+    const int nw = max(row_words, 1);
+    for (int w = tid; w < nw; w += kSelThreads)
+        bits[w] = 0;
+    __syncthreads();
+    for (int e = tid; e < n; e += kSelThreads) {
+        const uint2 en = stage[e];
+        const uint32_t b = en.y >> 16, j = en.y & 0xFFFFu;
+        if (b > bnd || (b == bnd && comp(en) >= cut))
+            atomicOr(&bits[j >> 5], 1u << (j & 31));
+    }
+    __syncthreads();
+    const int total = bitmap_prefix(bits, wpre, nw, sh, v_total);
+    int32_t* obi = reinterpret_cast<int32_t*>(dyn + merge_obuf_offset(n2));
+    float* obv = reinterpret_cast<float*>(obi + n2);
+    for (int e = tid; e < n; e += kSelThreads) {
+        const uint2 en = stage[e];
+        const uint32_t j = en.y & 0xFFFFu;
+        const uint32_t word = bits[j >> 5];
+        if ((word >> (j & 31)) & 1u) {
+            const int pos = static_cast<int>(wpre[j >> 5] + __popc(word & ((1u << (j & 31)) - 1u)));
+            obi[pos] = static_cast<int32_t>(j);
+            obv[pos] = __uint_as_float(en.x);
+        }
+    }
+    __syncthreads();
+    int32_t* oi = p.out_idx + (int64_t)t * p.k;
+    float* ov = p.out_val ? p.out_val + (int64_t)t * p.k : nullptr;
+    for (int i = tid; i < p.k; i += kSelThreads) {
+        const bool have = i < total;
+        oi[i] = have ? obi[i] : -1;
+        if (ov)
+            ov[i] = have ? obv[i] : -INFINITY;
+    }
+    return true;
+}
+
+// Row `cta` of a merge launch (its rows are numbered across the pieces).  Every thread
+// of the CTA calls it; every return is taken by the whole CTA.  FAST: verify merges try
+// merge_row_verified first.
+template <bool FAST>
+__device__ __forceinline__ void merge_row(const StreamMergeParams& p, const int cta)
 {
     __shared__ Scratch sh;
     __shared__ int32_t s_off[kMaxStreamSlots + 1];
     extern __shared__ __align__(16) uint8_t dyn[];
-    // [stage: kStageEntries x 8 B][keys: n2 x 4 B][values: n2 x 4 B], n2 = k rounded up
-    // to a power of two
+    // [stage: kStageEntries x 8 B][keys: n2 x 4 B][values: n2 x 4 B][output row], n2 = k
+    // rounded up to a power of two (merge_obuf_offset)
     int n2 = 1;
     while (n2 < p.k)
         n2 <<= 1;
@@ -193,7 +398,6 @@ __global__ void __launch_bounds__(kSelThreads, 3)
         s_omax = 0u;
     }
     __syncthreads();
-    const int cta = blockIdx.x;
     int pi = 0;
     while (pi + 1 < p.num_pieces && p.piece[pi + 1].cta_begin <= cta)
         ++pi;
@@ -205,6 +409,11 @@ __global__ void __launch_bounds__(kSelThreads, 3)
     const int64_t cbase = pc.count_offset + (int64_t)tr * nslots;
     if (p.only_failed && (*p.fail_any == 0u || p.row_fail[t] == 0))
         return;   // decided by the first pass
+    if constexpr (FAST) {
+        if (p.verify && p.smax_row != nullptr && !p.mask &&
+            merge_row_verified(p, pc, t, lbase, cbase, n2, dyn, sh))
+            return;
+    }
     // entries below the row's final threshold bound cannot be among its top k
     const uint32_t floor_ord = p.gtau ? p.gtau[t] : 0u;
     // copy the entries that pass the floor into shared memory (order is irrelevant:
@@ -215,6 +424,14 @@ __global__ void __launch_bounds__(kSelThreads, 3)
         const int lane = threadIdx.x & 31;
         uint32_t omin = 0xFFFFFFFFu, omax = 0u;
         for (int s = threadIdx.x >> 5; s < nslots; s += kSelThreads / 32) {
+            const uint2* src = p.lists + lbase + (int64_t)s * pc.cap;
+            // the first round's entries are loaded together with the count (indices
+            // clamped to the sub-list's capacity, not to its count: the loads do not
+            // wait for it; entries past the count are dropped below)
+            uint2 ent[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                ent[u] = pc.cap > 0 ? src[min(u * 32 + lane, pc.cap - 1)] : make_uint2(0u, 0u);
             const uint32_t raw = p.counts[cbase + s];
             const int c = static_cast<int>(min(raw, static_cast<uint32_t>(pc.cap)));
             if (lane == 0) {
@@ -222,15 +439,15 @@ __global__ void __launch_bounds__(kSelThreads, 3)
                     s_overflow = 1;   // benign race: every writer stores 1
                 atomicAdd(&s_nall, c);
             }
-            const uint2* src = p.lists + lbase + (int64_t)s * pc.cap;
             for (int i0 = 0; i0 < c; i0 += 32 * 8) {
                 // eight loads in flight per lane before any of them is used
                 // (clamped indices: no load result is selected on, so all eight
                 // are in flight at once; entries past c are dropped below)
-                uint2 ent[8];
+                if (i0 > 0) {
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    ent[u] = src[min(i0 + u * 32 + lane, c - 1)];
+                    for (int u = 0; u < 8; ++u)
+                        ent[u] = src[min(i0 + u * 32 + lane, c - 1)];
+                }
                 // the round's passing entries: one shared atomic reserves the warp's room
                 uint32_t passm = 0;
                 int round = 0, mine = 0;
@@ -330,7 +547,6 @@ __global__ void __launch_bounds__(kSelThreads, 3)
         // --- value buckets (the scratch below is the bitmap's, free until then)
         uint32_t* bhist = reinterpret_cast<uint32_t*>(skey);
         uint64_t* bcand = reinterpret_cast<uint64_t*>(bhist + kBuckets);
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         for (int i = threadIdx.x; i < kBuckets; i += kSelThreads)
             bhist[i] = 0;
         if (threadIdx.x == 0)
@@ -433,7 +649,10 @@ __global__ void __launch_bounds__(kSelThreads, 3)
         int32_t* oi = p.out_idx + (int64_t)t * k;
         float* ov = p.out_val ? p.out_val + (int64_t)t * k : nullptr;
         // a row's list entries have distinct keys, so an entry is kept iff its key's
-        // bit is set
+        // bit is set; it goes to its position in the shared output row, which is then
+        // written out with consecutive threads on consecutive positions
+        int32_t* obi = reinterpret_cast<int32_t*>(dyn + merge_obuf_offset(n2));
+        float* obv = reinterpret_cast<float*>(obi + n2);
         for (int e = threadIdx.x; e < n; e += kSelThreads) {
             const uint2 ent = stage[e];
             const uint32_t j = ent.y;
@@ -441,15 +660,16 @@ __global__ void __launch_bounds__(kSelThreads, 3)
             if ((word >> (j & 31)) & 1u) {
                 const int pos = static_cast<int>(wpre[j >> 5] +
                                                  __popc(word & ((1u << (j & 31)) - 1u)));
-                oi[pos] = static_cast<int32_t>(j);
-                if (ov)
-                    ov[pos] = __uint_as_float(ent.x);
+                obi[pos] = static_cast<int32_t>(j);
+                obv[pos] = __uint_as_float(ent.x);
             }
         }
-        for (int i = total + threadIdx.x; i < k; i += kSelThreads) {
-            oi[i] = -1;
+        __syncthreads();
+        for (int i = threadIdx.x; i < k; i += kSelThreads) {
+            const bool have = i < total;
+            oi[i] = have ? obi[i] : -1;
             if (ov)
-                ov[i] = -INFINITY;
+                ov[i] = have ? obv[i] : -INFINITY;
         }
         return;
     }
@@ -575,6 +795,28 @@ __global__ void __launch_bounds__(kSelThreads, 3)
     }
 }
 
+// WALK = false: one row per CTA.  WALK = true (the merge of undecided rows, usually
+// none): a grid of one wave walking the rows.  Three CTAs per SM: the staging area
+// allows no more.
+template <bool WALK>
+__global__ void __launch_bounds__(kSelThreads, 3)
+    stream_merge_kernel(const __grid_constant__ StreamMergeParams p)
+{
+    pdl_wait_then_release();
+    // a merge of undecided rows with none flagged anywhere has nothing to do (the flag
+    // was written by an earlier launch, so every thread reads the same value)
+    if (p.only_failed && *p.fail_any == 0u)
+        return;
+    if constexpr (!WALK) {
+        merge_row<true>(p, blockIdx.x);
+    } else {
+        for (int r = blockIdx.x; r < p.total_ctas; r += gridDim.x) {
+            merge_row<false>(p, r);
+            __syncthreads();   // the next row resets the shared state
+        }
+    }
+}
+
 // ------------------------------------------------- sampled row thresholds
 
 // tau[t] = the smallest ord among the samples of row t that lie in or above
@@ -583,90 +825,102 @@ __global__ void __launch_bounds__(kSelThreads, 3)
 // row has fewer than rank finite samples.  At least rank samples are at or
 // above it.  Any threshold keeps the selection exact (rows the lists cannot
 // decide are selected again); this one is close to the rank-th sample.
-// POOLED: the ranked entries are block maxima (p.pool > 1); the key version keeps
-// its registers low enough for four CTAs per SM.
-template <bool POOLED>
-__global__ void __launch_bounds__(kSelThreads, 2048 / kSelThreads)
+// One CTA of 128 threads per row, its bucket counts in shared memory; the row is read
+// three times (range, counts, threshold): from L2, where the sampled pass just wrote it,
+// then from L1.  POOL > 1: the ranked entries are the maxima of aligned POOL-sample
+// blocks.
+constexpr int kThrThreads = 128;
+
+template <int POOL>
+__global__ void __launch_bounds__(kThrThreads, 12)
     sample_threshold_kernel(const __grid_constant__ SampleParams p)
 {
-    __shared__ Scratch sh;
-    __shared__ uint32_t bhist[kBuckets];
-    __shared__ int s_bnd;
-    extern __shared__ __align__(16) float srow[];
-    const int t = p.row0 + blockIdx.x;
+    pdl_wait_then_release();
+    __shared__ __align__(16) uint32_t hist[kBuckets];
+    __shared__ uint32_t s_red[3][kThrThreads / 32];
+    __shared__ uint32_t s_bcast[2];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kWarps = kThrThreads / 32;
+    const int tl = blockIdx.x;   // row of the launch
+    const int t = p.row0 + tl;
     const int req = find_request(p.req_row_begin, p.num_requests, t);
     const int stride = p.req_rank[req];     // sampling stride (0: not sampled)
     const int clen = min(p.compress_len[t], p.req_key_count[req]);
-    const int pool = POOLED ? p.pool : 1;
-    const int units = (clen + pool - 1) / pool;   // keys, or blocks, the row ranks
+    const int units = (clen + POOL - 1) / POOL;   // keys, or blocks, the row ranks
     uint32_t* tau_out = p.tau_row + t;
     // rows that keep every entry: unsampled requests and rows with at most k keys
     // (blocks)
     if (stride == 0 || units <= p.k) {
-        if (threadIdx.x == 0)
+        if (tid == 0) {
             *tau_out = 0u;
+            p.smax_row[t] = 0u;
+        }
         return;
     }
-    const int64_t ld = p.ld;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const float* row = p.samples + (int64_t)blockIdx.x * ld;
-    // the row once into shared memory (ld is a multiple of 128: float4 loads), with
-    // the range and the count of its finite samples (keys)
+    const float* row = p.samples + (int64_t)tl * p.ld;
+    // only the columns the request's sampled tiles fill (a row of a request with fewer
+    // sampled tiles than the widest one leaves the rest of its sample row unwritten);
+    // a multiple of 128, so every thread's group of 8 samples is whole
+    const int cols = p.req_cols[req] > 0 ? min(p.req_cols[req], static_cast<int>(p.ld))
+                                         : static_cast<int>(p.ld);
+    // f(v) for every ranked value of the row: thread i takes samples [8 i, 8 i + 8) of
+    // every 1024, two such groups in flight per round
+    auto visit = [&](auto&& f) {
+        constexpr int kGroups = 2;
+        for (int b0 = 0; b0 < cols; b0 += kGroups * 8 * kThrThreads) {
+            float x[kGroups][8];
+#pragma unroll
+            for (int u = 0; u < kGroups; ++u) {
+                const int b = b0 + (u * kThrThreads + tid) * 8;
+                float4 lo = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), hi = lo;
+                if (b < cols) {
+                    lo = __ldg(reinterpret_cast<const float4*>(row + b));
+                    hi = __ldg(reinterpret_cast<const float4*>(row + b + 4));
+                }
+                x[u][0] = lo.x; x[u][1] = lo.y; x[u][2] = lo.z; x[u][3] = lo.w;
+                x[u][4] = hi.x; x[u][5] = hi.y; x[u][6] = hi.z; x[u][7] = hi.w;
+            }
+#pragma unroll
+            for (int u = 0; u < kGroups; ++u)
+#pragma unroll
+                for (int g = 0; g < 8 / POOL; ++g) {
+                    float m = x[u][g * POOL];
+#pragma unroll
+                    for (int i = 1; i < POOL; ++i)
+                        m = fmaxf(m, x[u][g * POOL + i]);
+                    f(m);
+                }
+        }
+    };
+    for (int i = tid; i < kBuckets / 4; i += kThrThreads)
+        reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
+    // range and count of the finite ranked values
     uint32_t omin = 0xFFFFFFFFu, omax = 0u, cnt = 0;
-    auto count = [&](float v) {
+    visit([&](float v) {
         const uint32_t o = f2ord(v);
         if (o > kOrdNegInf) {
             omin = min(omin, o);
             omax = max(omax, o);
             ++cnt;
         }
-    };
-    // only the columns the request's sampled tiles fill (a row of a request with fewer
-    // sampled tiles than the widest one leaves the rest of its sample row unwritten)
-    const int cols = p.req_cols[req] > 0 ? min(p.req_cols[req], static_cast<int>(ld))
-                                         : static_cast<int>(ld);
-    for (int e = threadIdx.x; e < cols / 4; e += kSelThreads) {
-        const float4 v4 = reinterpret_cast<const float4*>(row)[e];
-        reinterpret_cast<float4*>(srow)[e] = v4;
-        if constexpr (!POOLED) {
-            count(v4.x);
-            count(v4.y);
-            count(v4.z);
-            count(v4.w);
-        }
-    }
-    // blocks: the maximum of each aligned pool-key group (sampled tiles are whole
-    // 128-key tiles, so every group is a whole block of the row), then their range
-    // and count
-    const int n = cols / pool;
-    float* vals = srow;
-    if constexpr (POOLED) {
-        __syncthreads();
-        vals = srow + ld;
-        for (int b = threadIdx.x; b < n; b += kSelThreads) {
-            float m = -INFINITY;
-            for (int x = 0; x < pool; ++x)
-                m = fmaxf(m, srow[b * pool + x]);
-            vals[b] = m;
-            count(m);
-        }
-    }
-    for (int i = threadIdx.x; i < kBuckets; i += kSelThreads)
-        bhist[i] = 0;
+    });
     omin = __reduce_min_sync(0xffffffffu, omin);
     omax = __reduce_max_sync(0xffffffffu, omax);
     cnt = __reduce_add_sync(0xffffffffu, cnt);
     if (lane == 0) {
-        sh.hist[0][warp] = omin;
-        sh.hist[1][warp] = omax;
-        sh.warp_sum[warp] = cnt;
+        s_red[0][warp] = omin;
+        s_red[1][warp] = omax;
+        s_red[2][warp] = cnt;
     }
     __syncthreads();
-    uint32_t a = 0xFFFFFFFFu, b = 0u, m = 0;
-    for (int w = 0; w < kSelThreads / 32; ++w) {
-        a = min(a, sh.hist[0][w]);
-        b = max(b, sh.hist[1][w]);
-        m += sh.warp_sum[w];
+    uint32_t m = 0;
+    omin = 0xFFFFFFFFu;
+    omax = 0u;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        omin = min(omin, s_red[0][w]);
+        omax = max(omax, s_red[1][w]);
+        m += s_red[2][w];
     }
     // mu = samples expected among the row's top k: k times the sampled fraction,
     // which is m / units for a short row (its first tile is always sampled) and
@@ -675,75 +929,90 @@ __global__ void __launch_bounds__(kSelThreads, 2048 / kSelThreads)
     const float frac = fmaxf(static_cast<float>(m) / static_cast<float>(units),
                              1.0f / static_cast<float>(stride));
     const float mu = static_cast<float>(p.k) * frac;
-    const int rank = static_cast<int>(ceilf(mu + 5.0f * sqrtf(mu) + 4.0f));
-    if (m < static_cast<uint32_t>(rank)) {
-        if (threadIdx.x == 0)
+    const uint32_t r = static_cast<uint32_t>(ceilf(mu + 5.0f * sqrtf(mu) + 4.0f));
+    if (m < r) {
+        if (tid == 0) {
             *tau_out = 0u;
+            p.smax_row[t] = 0u;
+        }
         return;
     }
     BucketThr bt;
-    bt.vmin = ord2f(a);
-    const float range = __fsub_rn(ord2f(b), bt.vmin);
+    bt.vmin = ord2f(omin);
+    const float range = __fsub_rn(ord2f(omax), bt.vmin);
     bt.scale = range > 0.0f ? __fdiv_rn(static_cast<float>(kBuckets), range) : 0.0f;
     if (!(bt.scale < INFINITY))
         bt.scale = 0.0f;                      // degenerate range: one bucket
-    __syncthreads();                          // (sh is reused by the scan below)
-    for (int e = threadIdx.x; e < n; e += kSelThreads) {
-        const float v = vals[e];
+    visit([&](float v) {
         if (f2ord(v) > kOrdNegInf)
-            atomicAdd(&bhist[bt.bucket(v)], 1u);
-    }
+            atomicAdd(&hist[bt.bucket(v)], 1u);
+    });
     __syncthreads();
-    constexpr int kPer = kBuckets / kSelThreads;
-    const int top = kBuckets - kPer * threadIdx.x;
-    uint32_t c[kPer], local = 0;
+    // the bucket holding the r-th largest value, from the top: thread i owns buckets
+    // [2048 - 16 (i + 1), 2048 - 16 i)
+    constexpr int kPer = kBuckets / kThrThreads;
+    const int top = kBuckets - kPer * tid;
+    uint32_t local = 0;
+    {
+        const uint4* h4 = reinterpret_cast<const uint4*>(hist + top - kPer);
 #pragma unroll
-    for (int x = 0; x < kPer; ++x) {
-        c[x] = bhist[top - 1 - x];
-        local += c[x];
+        for (int x = 0; x < kPer / 4; ++x) {
+            const uint4 c = h4[x];
+            local += c.x + c.y + c.z + c.w;
+        }
     }
-    const uint32_t above_me = block_exclusive_sum(local, sh);
-    const uint32_t r = static_cast<uint32_t>(rank);
-    if (above_me < r && above_me + local >= r) {
-        uint32_t cum = above_me;
+    uint32_t incl = local;
 #pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    if (lane == 31)
+        s_red[0][warp] = incl;
+    __syncthreads();
+    uint32_t above = incl - local;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+        above += w < warp ? s_red[0][w] : 0u;
+    if (above < r && above + local >= r) {
+        uint32_t cum = above;
         for (int x = 0; x < kPer; ++x) {
-            if (cum + c[x] >= r) {
-                s_bnd = top - 1 - x;
+            const uint32_t c = hist[top - 1 - x];
+            if (cum + c >= r) {
+                s_bcast[0] = static_cast<uint32_t>(top - 1 - x);
                 break;
             }
-            cum += c[x];
+            cum += c;
         }
     }
     __syncthreads();
-    const int bnd = s_bnd;
+    const int bnd = static_cast<int>(s_bcast[0]);
     uint32_t tmin = 0xFFFFFFFFu;
-    for (int e = threadIdx.x; e < n; e += kSelThreads) {
-        const float v = vals[e];
+    visit([&](float v) {
         const uint32_t o = f2ord(v);
         if (o > kOrdNegInf && bt.bucket(v) >= bnd)
             tmin = min(tmin, o);
-    }
+    });
     tmin = __reduce_min_sync(0xffffffffu, tmin);
     if (lane == 0)
-        sh.hist[0][warp] = tmin;
+        s_red[1][warp] = tmin;
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         uint32_t x = 0xFFFFFFFFu;
-        for (int w = 0; w < kSelThreads / 32; ++w)
-            x = min(x, sh.hist[0][w]);
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+            x = min(x, s_red[1][w]);
         *tau_out = x;
+        p.smax_row[t] = omax;
     }
 }
 
 // ------------------------------------------------------- standalone top-k
 
-__global__ void __launch_bounds__(kSelThreads) topk_dense_kernel(const __grid_constant__ TopkParams p)
+// Exact top-k of one row of caller logits (all threads of the CTA call it).
+__device__ __forceinline__ void topk_dense_row(const TopkParams& p, Scratch& sh, const int t)
 {
-    __shared__ Scratch sh;
-    const int t = blockIdx.x;
-    if (p.row_fail != nullptr && (*p.fail_any == 0u || p.row_fail[t] == 0u))
-        return;   // decided by the sampled pass
     const int r = find_request(p.req_row_begin, p.num_requests, t);
     const int n = max(0, min(p.compress_len[t], p.req_key_count[r]));
     const float* row = p.logits + (int64_t)t * p.ld;
@@ -767,6 +1036,22 @@ __global__ void __launch_bounds__(kSelThreads) topk_dense_kernel(const __grid_co
     }
 }
 
+// One row per CTA, or (rows the sampled pass left undecided, usually none) a small grid
+// walking the flagged rows.
+__global__ void __launch_bounds__(kSelThreads) topk_dense_kernel(const __grid_constant__ TopkParams p)
+{
+    pdl_wait_then_release();
+    __shared__ Scratch sh;
+    if (p.row_fail != nullptr && *p.fail_any == 0u)
+        return;   // every row decided by the sampled pass
+    for (int t = blockIdx.x; t < p.total_rows; t += gridDim.x) {
+        if (p.row_fail == nullptr || p.row_fail[t] != 0u) {
+            topk_dense_row(p, sh, t);
+            __syncthreads();   // the next row reuses the scratch
+        }
+    }
+}
+
 // ------------------------------------------- sampled top-k over caller logits
 
 __device__ __forceinline__ int dense_piece(const DenseFilterParams& p, int t)
@@ -784,6 +1069,7 @@ __device__ __forceinline__ int dense_piece(const DenseFilterParams& p, int t)
 template <bool VEC>
 __global__ void __launch_bounds__(256) dense_gather_kernel(const __grid_constant__ DenseFilterParams p)
 {
+    pdl_wait_then_release();
     const int t = p.piece[0].row_begin + static_cast<int>(blockIdx.x);
     const DensePiece& pc = p.piece[dense_piece(p, t)];
     if (t >= pc.row_begin + pc.nrows)
@@ -828,6 +1114,7 @@ constexpr int kFilterThreads = 128;
 template <bool VEC>
 __global__ void __launch_bounds__(kFilterThreads) dense_filter_kernel(const __grid_constant__ DenseFilterParams p)
 {
+    pdl_wait_then_release();
     constexpr int U = 8;                      // loads in flight per thread
     constexpr int W = VEC ? 4 : 1;            // entries per load
     constexpr int PER = U * W;                // entries per thread per round
@@ -921,11 +1208,8 @@ cudaError_t launch_dense_gather(const DenseFilterParams& p, int rows, cudaStream
     // samples rows are sample_cols (a multiple of 128) floats apart in the workspace
     const bool vec = (reinterpret_cast<uintptr_t>(p.logits) % 16) == 0 && p.ld % 4 == 0 &&
                      (reinterpret_cast<uintptr_t>(p.samples) % 16) == 0;
-    if (vec)
-        dense_gather_kernel<true><<<rows, 256, 0, stream>>>(p);
-    else
-        dense_gather_kernel<false><<<rows, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(vec ? dense_gather_kernel<true> : dense_gather_kernel<false>, dim3(rows),
+                      dim3(256), 0, stream, p);
 }
 
 cudaError_t launch_dense_filter(const DenseFilterParams& p, int rows, int max_slots,
@@ -935,11 +1219,25 @@ cudaError_t launch_dense_filter(const DenseFilterParams& p, int rows, int max_sl
         return cudaSuccess;
     const dim3 grid(max_slots, rows);
     const bool vec = (reinterpret_cast<uintptr_t>(p.logits) % 16) == 0 && p.ld % 4 == 0;
-    if (vec)
-        dense_filter_kernel<true><<<grid, kFilterThreads, 0, stream>>>(p);
-    else
-        dense_filter_kernel<false><<<grid, kFilterThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(vec ? dense_filter_kernel<true> : dense_filter_kernel<false>, dim3(grid),
+                      dim3(kFilterThreads), 0, stream, p);
+}
+
+// SMs of the current device (read once per device)
+int sm_count()
+{
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 152;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            n <= 0)
+            n = 152;
+        cached[dev] = n;
+    }
+    return cached[dev];
 }
 
 cudaError_t launch_stream_merge(const StreamMergeParams& p, cudaStream_t stream)
@@ -951,41 +1249,48 @@ cudaError_t launch_stream_merge(const StreamMergeParams& p, cudaStream_t stream)
     int n2 = 1;
     while (n2 < p.k)
         n2 <<= 1;
-    const size_t dyn = sizeof(uint2) * kStageEntries +
-                       std::max<size_t>((sizeof(int32_t) + sizeof(float)) * n2, 8 * kBitmapWords);
-    cudaError_t e = cudaFuncSetAttribute(stream_merge_kernel,
+    const size_t dyn = merge_obuf_offset(n2) + (p.mask ? 0 : 8 * (size_t)n2);
+    cudaError_t e = cudaFuncSetAttribute(p.only_failed ? stream_merge_kernel<true>
+                                                       : stream_merge_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
     if (e != cudaSuccess)
         return e;
-    stream_merge_kernel<<<p.total_ctas, kSelThreads, dyn, stream>>>(p);
-    return cudaGetLastError();
+    // the merge of undecided rows: a grid of one wave (it walks the flagged rows, and
+    // exits at once when there are none)
+    if (p.only_failed)
+        return launch_pdl(stream_merge_kernel<true>, dim3(std::min(p.total_ctas, 3 * sm_count())),
+                          dim3(kSelThreads), dyn, stream, p);
+    return launch_pdl(stream_merge_kernel<false>, dim3(p.total_ctas), dim3(kSelThreads), dyn,
+                      stream, p);
 }
 
 cudaError_t launch_sample_threshold(const SampleParams& p, cudaStream_t stream)
 {
     if (p.rows <= 0)
         return cudaSuccess;
-    if (p.ld % 4 != 0 || p.ld > 16384)
+    if (p.ld % 8 != 0 || p.ld > 16384)
         return cudaErrorInvalidValue;
-    const bool pooled = p.pool > 1;
-    const size_t dyn = (p.ld + (pooled ? p.ld / p.pool : 0)) * sizeof(float);
-    auto kern = pooled ? sample_threshold_kernel<true> : sample_threshold_kernel<false>;
-    if (dyn > 48 * 1024) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
-        if (e != cudaSuccess)
-            return e;
+    for (int r = 0; r < p.num_requests; ++r)
+        if (p.req_cols[r] % 8 != 0)
+            return cudaErrorInvalidValue;
+    const int grid = p.rows;
+    void (*kern)(SampleParams) = nullptr;
+    switch (p.pool) {
+    case 1: kern = sample_threshold_kernel<1>; break;
+    case 2: kern = sample_threshold_kernel<2>; break;
+    case 4: kern = sample_threshold_kernel<4>; break;
+    case 8: kern = sample_threshold_kernel<8>; break;
+    default: return cudaErrorInvalidValue;
     }
-    kern<<<p.rows, kSelThreads, dyn, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThrThreads), 0, stream, p);
 }
 
 cudaError_t launch_topk_dense(const TopkParams& p, cudaStream_t stream)
 {
     if (p.total_rows <= 0)
         return cudaSuccess;
-    topk_dense_kernel<<<p.total_rows, kSelThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    const int grid = p.row_fail != nullptr ? std::min(p.total_rows, 4 * sm_count()) : p.total_rows;
+    return launch_pdl(topk_dense_kernel, dim3(grid), dim3(kSelThreads), 0, stream, p);
 }
 
 }  // namespace idx
