@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libindexer.so")
-SOURCES = ["logits_tc.cu", "select.cu", "misc.cu", "host.cu"]
+SOURCES = ["logits_tc.cu", "select.cu", "rowtopk.cu", "misc.cu", "host.cu"]
 HEADERS = ["internal.h", "ptx.cuh", "groupsel.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -1123,6 +1123,75 @@ static int dense_sampled(Ctx& c, uint8_t* ws, const float* logits, int64_t ld,
     return IDX_OK;
 }
 
+// Top-k over caller logits in one read of every row: each row's sampled threshold
+// straight from the logits, then the single-read kernel (candidates and the exact
+// selection in shared memory); rows it cannot decide go to the direct kernel afterwards.
+// For plans whose requests have at most 65,536 keys and 16-byte aligned logits rows.
+static int dense_single_read(Ctx& c, uint8_t* ws, const float* logits, int64_t ld,
+                             const int32_t* clen, TopkParams& tp)
+{
+    const indexer_plan_s* p = c.p;
+    uint32_t* tau_row = reinterpret_cast<uint32_t*>(ws + p->off_tau);
+    uint32_t* row_fail = reinterpret_cast<uint32_t*>(ws + p->off_fail);
+    uint32_t* fail_any = reinterpret_cast<uint32_t*>(ws) + 1;
+    uint32_t* row_counter = reinterpret_cast<uint32_t*>(ws) + 2;   // zeroed with the status
+    if (cudaMemsetAsync(ws + p->off_gtau, 0, (size_t)p->T * 8, c.st) != cudaSuccess)
+        return IDX_ERR_CUDA;
+    SampleParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    sp.samples = nullptr;
+    sp.logits = logits;
+    sp.ld_logits = ld;
+    sp.ld = p->sample_cols;
+    sp.row0 = 0;
+    sp.rows = p->T;
+    sp.k = p->topk;
+    sp.pool = 1;
+    sp.compress_len = clen;
+    sp.tau_row = tau_row;
+    sp.smax_row = tau_row + p->T;
+    sp.num_requests = p->R;
+    for (int r = 0; r < p->R; ++r) {
+        sp.req_row_begin[r] = p->row_begin[r];
+        sp.req_rank[r] = p->sample_rank_r[r] > 0 ? p->sample_stride_r[r] : 0;
+        sp.req_key_count[r] = p->L[r];
+        sp.req_cols[r] = p->sample_rank_r[r] > 0
+                             ? (int)ceil_div(ceil_div(std::max(1, p->L[r]), kTileKeys),
+                                             p->sample_stride_r[r]) * kTileKeys
+                             : 0;
+    }
+    sp.req_row_begin[p->R] = p->row_begin[p->R];
+    RowTopkParams rp;
+    std::memset(&rp, 0, sizeof(rp));
+    rp.logits = logits;
+    rp.ld = ld;
+    rp.compress_len = clen;
+    rp.tau_row = tau_row;
+    rp.smax_row = tau_row + p->T;
+    rp.row_fail = row_fail;
+    rp.fail_any = fail_any;
+    rp.row_counter = row_counter;
+    rp.status = reinterpret_cast<uint32_t*>(ws);
+    rp.timeout_cycles = p->wait_budget;
+    rp.out_idx = tp.out_idx;
+    rp.out_val = tp.out_val;
+    rp.k = p->topk;
+    rp.total_rows = p->T;
+    rp.num_requests = p->R;
+    for (int r = 0; r < p->R; ++r) {
+        rp.req_row_begin[r] = p->row_begin[r];
+        rp.req_key_count[r] = p->L[r];
+    }
+    rp.req_row_begin[p->R] = p->row_begin[p->R];
+    g_launches.fetch_add(2, std::memory_order_relaxed);
+    if (launch_sample_threshold(sp, c.st) != cudaSuccess ||
+        launch_row_topk(rp, c.st) != cudaSuccess)
+        return IDX_ERR_CUDA;
+    tp.row_fail = row_fail;
+    tp.fail_any = fail_any;
+    return IDX_OK;
+}
+
 int indexer_topk(indexer_plan_t p, const float* logits, int64_t ld, const int32_t* clen,
                  int32_t* out_idx, float* out_val, void* ws, size_t ws_bytes, void* stream)
 {
@@ -1155,7 +1224,11 @@ int indexer_topk(indexer_plan_t p, const float* logits, int64_t ld, const int32_
     // with the plan's whole workspace, the sampled path decides most rows; the direct
     // kernel then handles only the rows it could not (or every row, without it)
     if (ws_bytes >= p->ws_bytes && p->sample_stride > 0 && p->T > 0) {
-        if ((rc = dense_sampled(c, static_cast<uint8_t*>(ws), logits, ld, clen, tp)) != IDX_OK)
+        const bool single = p->max_L <= row_topk_max_keys() && ld % 4 == 0 &&
+                            aligned(logits, 16);
+        if ((rc = single ? dense_single_read(c, static_cast<uint8_t*>(ws), logits, ld, clen, tp)
+                         : dense_sampled(c, static_cast<uint8_t*>(ws), logits, ld, clen, tp)) !=
+            IDX_OK)
             return rc;
     }
     g_launches.fetch_add(1, std::memory_order_relaxed);

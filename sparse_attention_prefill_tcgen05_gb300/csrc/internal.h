@@ -220,6 +220,10 @@ struct SampleParams {
     int32_t pool;                // keys per ranked entry (1: keys; 2, 4, 8: block maxima)
     int32_t pad_;
     const int32_t* compress_len;
+    const float* logits;         // nullable: read the samples from caller logits [rows, ld]
+                                 // (row t at t, sample e at key (e / 128) stride 128 + e % 128)
+                                 // instead of `samples`
+    int64_t ld_logits;
     uint32_t* tau_row;           // [total rows], written at row0 .. row0 + rows - 1
     uint32_t* smax_row;          // [total rows]: ord of the row's largest ranked sample where
                                  // tau is nonzero, else 0
@@ -229,6 +233,33 @@ struct SampleParams {
     int32_t req_cols[kMaxRequests];    // sample columns a row of the request fills (<= ld)
 };
 cudaError_t launch_sample_threshold(const SampleParams& p, cudaStream_t stream);
+
+// Top-k over caller logits in one read per row (rows of at most 65,536 keys, k <= 2048):
+// every entry at or above the row's sampled threshold is kept in shared memory and the
+// exact selection runs there.  Rows it cannot decide (fewer than k entries at or above
+// the threshold, more candidates than it holds) are flagged for the direct kernel.
+struct RowTopkParams {
+    const float* logits;         // [rows, ld], 16-byte aligned rows
+    int64_t ld;
+    const int32_t* compress_len;
+    const uint32_t* tau_row;     // [rows] ord threshold, 0: every finite entry
+    const uint32_t* smax_row;    // [rows] ord of the largest sample (bucket range)
+    uint32_t* row_fail;
+    uint32_t* fail_any;
+    uint32_t* row_counter;       // zero at launch: rows are taken in order by the CTAs
+    uint32_t* status;
+    long long timeout_cycles;
+    int32_t* out_idx;
+    float* out_val;              // nullable
+    int32_t k;
+    int32_t total_rows;
+    int32_t num_requests;
+    int32_t pad_;
+    int32_t req_row_begin[kMaxRequests + 1];
+    int32_t req_key_count[kMaxRequests];
+};
+cudaError_t launch_row_topk(const RowTopkParams& p, cudaStream_t st);
+int row_topk_max_keys();   // longest row (keys) the kernel takes
 
 cudaError_t launch_expand_mask(const uint8_t* cand_mask, int64_t ld_mask, const int32_t* clen,
                                uint8_t* key_mask, int64_t ld, int block, int rows,

@@ -97,6 +97,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
     }
 }
 
+// The same wait for roles that spend most of their time waiting: between polls the
+// thread sleeps (32 ns, doubling up to 512 ns), so waiting warps take almost no issue
+// slots from the warps doing work.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity,
+                                                  long long budget, volatile int* abort)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const long long t0 = clock64();
+    uint32_t ns = 32;
+    while (true) {
+        __nanosleep(ns);
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (*abort)
+            return false;
+        if (clock64() - t0 > budget)
+            return false;
+        ns = ns < 512u ? 2u * ns : 512u;
+    }
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
@@ -115,6 +137,34 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
         : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
+// to shared memory, counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Named barrier `id` over `count` threads that also returns whether `v` holds in all
+// of them.
+__device__ __forceinline__ bool bar_all(bool v, int id, int count)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
 }
 
 // ---------------------------------------------------------------- tcgen05

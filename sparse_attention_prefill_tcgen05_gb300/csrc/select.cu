@@ -863,6 +863,11 @@ __global__ void __launch_bounds__(kThrThreads, 12)
     // a multiple of 128, so every thread's group of 8 samples is whole
     const int cols = p.req_cols[req] > 0 ? min(p.req_cols[req], static_cast<int>(p.ld))
                                          : static_cast<int>(p.ld);
+    // samples read from the caller's logits: group b of 8 is keys key0 .. key0 + 7 of
+    // the row, key0 = (b / 128) stride 128 + b % 128 (one 128-key tile), keys at or past
+    // the row's length read as -inf (a float4 is loaded only when its first key is below
+    // it, which keeps it inside the row: ld and key0 are multiples of 4)
+    const float* lrow = p.logits ? p.logits + (int64_t)t * p.ld_logits : nullptr;
     // f(v) for every ranked value of the row: thread i takes samples [8 i, 8 i + 8) of
     // every 1024, two such groups in flight per round
     auto visit = [&](auto&& f) {
@@ -874,8 +879,22 @@ __global__ void __launch_bounds__(kThrThreads, 12)
                 const int b = b0 + (u * kThrThreads + tid) * 8;
                 float4 lo = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), hi = lo;
                 if (b < cols) {
-                    lo = __ldg(reinterpret_cast<const float4*>(row + b));
-                    hi = __ldg(reinterpret_cast<const float4*>(row + b + 4));
+                    if (lrow == nullptr) {
+                        lo = __ldg(reinterpret_cast<const float4*>(row + b));
+                        hi = __ldg(reinterpret_cast<const float4*>(row + b + 4));
+                    } else {
+                        const int key0 = (b / kTileKeys) * stride * kTileKeys + b % kTileKeys;
+                        if (key0 < clen)
+                            lo = __ldg(reinterpret_cast<const float4*>(lrow + key0));
+                        if (key0 + 4 < clen)
+                            hi = __ldg(reinterpret_cast<const float4*>(lrow + key0 + 4));
+                        if (key0 + 1 >= clen) lo.y = -INFINITY;
+                        if (key0 + 2 >= clen) lo.z = -INFINITY;
+                        if (key0 + 3 >= clen) lo.w = -INFINITY;
+                        if (key0 + 5 >= clen) hi.y = -INFINITY;
+                        if (key0 + 6 >= clen) hi.z = -INFINITY;
+                        if (key0 + 7 >= clen) hi.w = -INFINITY;
+                    }
                 }
                 x[u][0] = lo.x; x[u][1] = lo.y; x[u][2] = lo.z; x[u][3] = lo.w;
                 x[u][4] = hi.x; x[u][5] = hi.y; x[u][6] = hi.z; x[u][7] = hi.w;

@@ -561,6 +561,50 @@ def test_topk_over_logits_sampled_equals_direct(structured):
             x for x in ref[t].tolist() if x >= 0), t
 
 
+def test_topk_single_read_edge_rows():
+    """The single-read top-k (rows of at most 65,536 keys, aligned rows) on rows built to
+    reach each of its exits: a row of equal logits (every entry passes the threshold, the
+    candidate buffer overflows, the direct kernel decides it; ties go to the lower index),
+    a row of -inf but a few entries (the threshold lets everything through and fewer than
+    k are finite), a row whose tail is -inf, a row with a few huge values, a short request
+    that is not sampled; against the oracle's selector and, bit for bit, the direct kernel
+    alone."""
+    L, rows, topk = 32768, 12, 512
+    spec = W.ProblemSpec("edge rows", (W.RequestSpec(rows, L - rows, 1),
+                                       W.RequestSpec(6, 1500, 1)), H=32, D=128, topk=topk,
+                         seed=29)
+    p = W.make_problem(spec)
+    plan = Hp.make_plan(p)
+    assert plan.info()["sample_stride"] >= 2
+    d = Hp.device_inputs(p)
+    g = Hp.gpu_logits(p, plan, d).clone()
+    cl = p.compress_len.numpy()
+    g[0, :] = 1.0                                        # ties everywhere
+    g[1, :] = -float("inf")
+    g[1, 100:100 + topk // 3] = torch.linspace(-5.0, 5.0, topk // 3)
+    g[2, int(cl[2]) // 2:] = -float("inf")               # the second half of the row
+    g[3, 7::997] = 1.0e30                                # a few huge values
+    T = g.shape[0]
+    ti, tv = Hp.gpu_topk(p, plan, g, d)
+    di = torch.empty_like(ti)
+    dv = torch.empty_like(tv)
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    K.indexer_topk(plan, g, d["compress_len"], di, dv, small)
+    assert K.indexer_status(plan, small) == K.IDX_OK
+    assert torch.equal(ti, di) and torch.equal(tv, dv)
+    # -inf entries are not eligible (the entry point's contract): the oracle's selector
+    # gets that rule as its eligibility mask, one byte per key
+    gh = g.cpu().numpy().astype(np.float64)
+    finite = np.isfinite(gh).astype(np.uint8)
+    ref = O.topk_rows(gh, cl, topk, mask=finite, mask_block=1)
+    ti = ti.cpu().numpy()
+    for t in range(T):                                   # (the oracle lists by score)
+        assert sorted(x for x in ti[t].tolist() if x >= 0) == sorted(
+            x for x in ref[t].tolist() if x >= 0), t
+        assert (ti[t] < 0).sum() == (ref[t] < 0).sum(), t
+    assert ti[0].tolist() == list(range(topk))           # equal logits: the lowest indices
+
+
 def test_topk_over_unaligned_logits_rows():
     """Rows that do not start on a 16-byte boundary (a view one column into a wider
     buffer, odd row stride) take the one-entry-per-load path of the filtering read and
