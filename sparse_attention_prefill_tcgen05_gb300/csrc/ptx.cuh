@@ -98,10 +98,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
 }
 
 // The same wait for roles that spend most of their time waiting: between polls the
-// thread sleeps (32 ns, doubling up to 512 ns), so waiting warps take almost no issue
+// thread sleeps (32 ns, doubling up to max_ns), so waiting warps take almost no issue
 // slots from the warps doing work.
 __device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity,
-                                                  long long budget, volatile int* abort)
+                                                  long long budget, volatile int* abort,
+                                                  uint32_t max_ns = 512u)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -115,7 +116,7 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity
             return false;
         if (clock64() - t0 > budget)
             return false;
-        ns = ns < 512u ? 2u * ns : 512u;
+        ns = ns < max_ns ? 2u * ns : max_ns;
     }
 }
 

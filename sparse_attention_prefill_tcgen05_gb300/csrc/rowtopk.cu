@@ -7,13 +7,13 @@
 // row needs no global lists and no second kernel.  One persistent CTA per SM, three
 // roles:
 //   warp 0        producer: takes rows in order from a global counter and streams each
-//                 row through a ring of 16 KB stages with bulk copies;
-//   warps 1..8    filter: each warp takes its 1/8 of every stage; a lane tests its 16
+//                 row through a ring of three 32 KB stages with bulk copies;
+//   warps 1..16   filter: each warp takes its 1/16 of every stage; a lane tests its 16
 //                 values against tau, and the warp appends the passing ones (positions
 //                 from a warp prefix sum of the lanes' counts, values read again from
 //                 the stage) to its own region of the row's candidate buffer (two
 //                 buffers, rows alternate); the warps never wait for one another;
-//   warps 9..16   select: the exact top-k of a full buffer (2048 equal-width value
+//   warps 17..24  select: the exact top-k of a full buffer (2048 equal-width value
 //                 buckets from tau to the row's largest sample, larger values in the top
 //                 one; the bucket holding the k-th entry, its entries ranked directly, a
 //                 bitmap of the kept keys, their positions by a prefix sum) written in
@@ -29,21 +29,23 @@
 namespace idx {
 namespace {
 
-constexpr int kFiltWarps = 8;
+constexpr int kFiltWarps = 16;
 constexpr int kSelWarps = 8;
-constexpr int kFiltThreads = 32 * kFiltWarps;              // 256
+constexpr int kFiltThreads = 32 * kFiltWarps;              // 512
 constexpr int kSelThr = 32 * kSelWarps;                    // 256
-constexpr int kRtThreads = 32 + kFiltThreads + kSelThr;    // 544
-constexpr int kChunk = 4096;                               // floats per ring stage
-constexpr int kStages = 6;
-constexpr int kRegion = 640;                               // candidates per filter warp
+constexpr int kRtThreads = 32 + kFiltThreads + kSelThr;    // 800
+constexpr int kChunk = 8192;                               // floats per ring stage (32 KB)
+constexpr int kStages = 3;                                 // (a larger stage count does not fit)
+constexpr int kF4 = kChunk / (4 * kFiltThreads);           // float4 per filter lane per stage
+constexpr int kRegion = 320;                               // candidates per filter warp
 constexpr int kCand = kFiltWarps * kRegion;                // per buffer
 constexpr int kRtBuckets = 2048;
 constexpr int kRtMaxK = 2048;
 constexpr int kRtWords = 2048;                             // bitmap words: keys < 65536
 constexpr int kRtBucketCands = 256;
 constexpr int kBarSel = 2;                                 // named barrier of the select warps
-static_assert(kChunk == 16 * kFiltThreads, "a filter thread takes four float4 of a stage");
+static_assert(kChunk == 4 * kF4 * kFiltThreads && kF4 <= 8, "a filter thread takes kF4 float4 of a stage");
+static_assert(kFiltWarps % kSelWarps == 0, "a select warp takes whole filter regions");
 
 // What the producer publishes with each stage.
 struct StageMeta {
@@ -231,8 +233,8 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
 
     if (warp <= kFiltWarps) {
         // -------------------------------------------------------------- filter
-        // thread ft takes float4 ft + 256 u (u = 0..3) of every stage, so warp fw covers
-        // floats [128 fw, 128 fw + 128) of every 1024; decisions are per warp
+        // thread ft takes float4 ft + 512 u (u < kF4) of every stage, so warp fw covers
+        // floats [128 fw, 128 fw + 128) of every 2048; decisions are per warp
         const int fw = warp - 1;
         const int ft = threadIdx.x - 32;
         int s = 0, ph = 0, b = 0, bph = 0;
@@ -276,9 +278,9 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
             }
             const float* stage = ring + (size_t)s * kChunk;
             const float4* src = reinterpret_cast<const float4*>(stage);
-            uint32_t pm = 0;   // which of the lane's 16 values pass
+            uint32_t pm = 0;   // which of the lane's values pass
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kF4; ++u) {
                 const float4 x = src[ft + kFiltThreads * u];
                 pm |= (x.x >= tauf ? 1u : 0u) << (4 * u);
                 pm |= (x.y >= tauf ? 1u : 0u) << (4 * u + 1);
@@ -288,7 +290,7 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
             if (m.nfl < kChunk) {
                 // the row's last, partial stage: only its first nfl floats are keys
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
+                for (int e = 0; e < 4 * kF4; ++e)
                     if (4 * (ft + kFiltThreads * (e >> 2)) + (e & 3) >= m.nfl)
                         pm &= ~(1u << e);
             }
@@ -370,6 +372,17 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
             const int w = e / kRegion;
             return static_cast<uint32_t>(e - w * kRegion) < rc[w];
         };
+        // f(e) for every candidate: select warp sw walks the regions sw, sw + 8, ... with
+        // all of its lanes
+        auto each_cand = [&](auto&& f) {
+            const int sw = st >> 5, sln = st & 31;
+#pragma unroll 1
+            for (int w = sw; w < kFiltWarps; w += kSelWarps) {
+                const int n = static_cast<int>(min(rc[w], static_cast<uint32_t>(kRegion)));
+                for (int i = sln; i < n; i += 32)
+                    f(w * kRegion + i);
+            }
+        };
         if (overflow || (sl.tau > kOrdNegInf && total_c < k)) {
             // the candidates cannot decide the row: the direct kernel will
             if (st == 0) {
@@ -406,15 +419,13 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                     for (int i = st; i < kRtBuckets / 4; i += kSelThr)
                         reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
                     bar_all(true, kBarSel, kSelThr);
-                    for (int e = st; e < kCand; e += kSelThr) {
-                        if (!valid(e))
-                            continue;
+                    each_cand([&](const int e) {
                         const uint2 en = cb[e];
                         const uint32_t bk = static_cast<uint32_t>(min(kRtBuckets - 1, static_cast<int>(
                             __fmul_rn(__fsub_rn(__uint_as_float(en.x), bvmin), bscale))));
                         atomicAdd(&hist[bk], 1u);
                         cb[e].y = (en.y & 0xFFFFu) | (bk << 16);
-                    }
+                    });
                     bar_all(true, kBarSel, kSelThr);
                     // the bucket holding the k-th largest, from the top: thread i owns
                     // buckets [2048 - 8 (i + 1), 2048 - 8 i)
@@ -450,13 +461,11 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                         if (st == 0)
                             bcast[3] = 0;
                         bar_all(true, kBarSel, kSelThr);
-                        for (int e = st; e < kCand; e += kSelThr) {
-                            if (!valid(e))
-                                continue;
+                        each_cand([&](const int e) {
                             const uint2 en = cb[e];
                             if ((en.y >> 16) == bnd)
                                 bc[atomicAdd(&bcast[3], 1u)] = comp(en);
-                        }
+                        });
                         bar_all(true, kBarSel, kSelThr);
                         // the need-th largest: the one with exactly need - 1 above it
                         for (int i = st; i < static_cast<int>(bsize); i += kSelThr) {
@@ -497,15 +506,13 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
             for (int w = st; w < nw; w += kSelThr)
                 bits[w] = 0;
             bar_all(true, kBarSel, kSelThr);
-            for (int e = st; e < kCand; e += kSelThr) {
-                if (!valid(e))
-                    continue;
+            each_cand([&](const int e) {
                 const uint2 en = cb[e];
                 if (kept(en)) {
                     const uint32_t j = en.y & 0xFFFFu;
                     atomicOr(&bits[j >> 5], 1u << (j & 31));
                 }
-            }
+            });
             bar_all(true, kBarSel, kSelThr);
             constexpr int kPerW = kRtWords / kSelThr;   // consecutive words per thread
             const int w0 = st * kPerW;
@@ -525,9 +532,7 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                 bcast[0] = run;   // kept entries
             bar_all(true, kBarSel, kSelThr);
             const int total = static_cast<int>(bcast[0]);
-            for (int e = st; e < kCand; e += kSelThr) {
-                if (!valid(e))
-                    continue;
+            each_cand([&](const int e) {
                 const uint2 en = cb[e];
                 const uint32_t j = en.y & 0xFFFFu;
                 const uint32_t word = bits[j >> 5];
@@ -537,7 +542,7 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                     obi[pos] = static_cast<int32_t>(j);
                     obv[pos] = __uint_as_float(en.x);
                 }
-            }
+            });
             bar_all(true, kBarSel, kSelThr);
             int32_t* oi = p.out_idx + (int64_t)t * p.k;
             float* ov = p.out_val ? p.out_val + (int64_t)t * p.k : nullptr;
