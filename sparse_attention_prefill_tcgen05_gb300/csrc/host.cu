@@ -516,12 +516,35 @@ int run_streamed(Ctx& c, uint8_t* ws, int pool, int32_t* out_idx, float* out_val
     // the plan's passes, or their pieces cut down to each request's last tail[r] rows
     // (a piece keeps its list area: its first kept row's lists start per_row entries
     // further per skipped row)
+    // candidate blocks: a request whose rows have at most cand_topk blocks keeps every
+    // valid block of every row, whatever its logits; its mask rows are written directly
+    // and its rows are left out of the passes
+    std::vector<char> whole(p->R, 0);
+    bool any_whole = false;
+    if (pool) {
+        for (int r = 0; r < p->R; ++r) {
+            whole[r] = ceil_div(std::max(p->L[r], 0), p->cand_block) <= p->cand_topk;
+            any_whole = any_whole || whole[r];
+            if (!whole[r])
+                continue;
+            const int b = p->row_begin[r + 1];
+            const int a = c.tail ? b - c.tail[r] : p->row_begin[r];
+            g_launches.fetch_add(1, std::memory_order_relaxed);
+            if (launch_fill_mask_rows(mask, ld_mask, c.lp.compress_len, a, b - a, p->L[r],
+                                      p->cand_block, c.mask_delta.empty() ? 0 : c.mask_delta[r],
+                                      c.st) != cudaSuccess)
+                return IDX_ERR_CUDA;
+        }
+    }
     std::vector<Pass> cut;
-    if (c.tail) {
+    if (c.tail || any_whole) {
         for (const Pass& ps : pool ? p->passes_b : p->passes_k) {
             Pass f;
             for (const PassPiece& pc : ps.pieces) {
-                const int lo = std::max(pc.a, p->row_begin[pc.r + 1] - c.tail[pc.r]);
+                if (whole[pc.r])
+                    continue;
+                const int lo = c.tail ? std::max(pc.a, p->row_begin[pc.r + 1] - c.tail[pc.r])
+                                      : pc.a;
                 if (lo >= pc.b)
                     continue;
                 const int64_t per_row = (int64_t)p->n_splits[pc.r] * kListsPerSplit * cap[pc.r];
@@ -531,7 +554,8 @@ int run_streamed(Ctx& c, uint8_t* ws, int pool, int32_t* out_idx, float* out_val
                 cut.push_back(f);
         }
     }
-    const std::vector<Pass>& passes = c.tail ? cut : (pool ? p->passes_b : p->passes_k);
+    const std::vector<Pass>& passes =
+        c.tail || any_whole ? cut : (pool ? p->passes_b : p->passes_k);
     const int keep = pool ? p->cand_topk : p->topk;
     const bool sampled = pool == 0 ? p->sample_stride > 0 : p->sample_blocks;
     LogitsParams& lp = c.lp;

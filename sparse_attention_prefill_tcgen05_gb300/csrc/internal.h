@@ -261,6 +261,11 @@ struct RowTopkParams {
 cudaError_t launch_row_topk(const RowTopkParams& p, cudaStream_t st);
 int row_topk_max_keys();   // longest row (keys) the kernel takes
 
+// Mask rows of rows with at most cand_topk candidate blocks: row t (of row0 .. row0 +
+// rows - 1) writes mask row t + delta, 1 for its blocks below ceil(min(clen[t], keys) /
+// block), 0 for the rest of the ld bytes.
+cudaError_t launch_fill_mask_rows(uint8_t* mask, int64_t ld, const int32_t* clen, int row0,
+                                  int rows, int keys, int block, int64_t delta, cudaStream_t st);
 cudaError_t launch_expand_mask(const uint8_t* cand_mask, int64_t ld_mask, const int32_t* clen,
                                uint8_t* key_mask, int64_t ld, int block, int rows,
                                cudaStream_t st);

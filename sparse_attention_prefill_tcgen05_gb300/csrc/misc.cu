@@ -127,6 +127,42 @@ __global__ void selftest_timeout_kernel(uint32_t* status, long long cycles)
     }
 }
 
+// Candidate mask rows of rows with at most cand_topk blocks (every one of their valid
+// blocks is a candidate, whatever the logits): row t of rows [row0, row0 + rows) writes
+// mask row t + delta, 1 for the blocks below ceil(min(clen[t], keys) / block), 0 for the
+// rest of its ld bytes.  One CTA per row; 16-byte stores between the row's unaligned head
+// and tail.
+__global__ void fill_mask_rows_kernel(uint8_t* __restrict__ mask, int64_t ld,
+                                      const int32_t* __restrict__ clen, int row0, int keys,
+                                      int block, int64_t delta)
+{
+    pdl_wait_then_release();
+    const int t = row0 + static_cast<int>(blockIdx.x);
+    const int n = max(0, min(clen[t], keys));
+    const int64_t nb = (n + block - 1) / block;   // candidate blocks of the row
+    uint8_t* m = mask + (t + delta) * ld;
+    const int64_t head = min(ld, static_cast<int64_t>((16 - (reinterpret_cast<uintptr_t>(m) & 15)) & 15));
+    for (int64_t b = threadIdx.x; b < head; b += blockDim.x)
+        m[b] = b < nb ? 1 : 0;
+    const int64_t nvec = (ld - head) / 16;
+    uint4* mv = reinterpret_cast<uint4*>(m + head);
+    for (int64_t v = threadIdx.x; v < nvec; v += blockDim.x) {
+        const int64_t b0 = head + 16 * v;
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t x = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                x |= (b0 + 4 * i + j < nb ? 1u : 0u) << (8 * j);
+            w[i] = x;
+        }
+        mv[v] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    for (int64_t b = head + 16 * nvec + threadIdx.x; b < ld; b += blockDim.x)
+        m[b] = b < nb ? 1 : 0;
+}
+
 }  // namespace
 
 // Page-index transform: one thread per four consecutive entries of a row (k a
@@ -199,6 +235,15 @@ cudaError_t launch_page_indices(const PageIndexParams& p, cudaStream_t st)
     // a grid of whole waves: 152 SMs x 8 blocks of 256 threads at most
     const int blocks = static_cast<int>(std::min<int64_t>((items + 255) / 256, 152 * 8));
     return launch_pdl(page_indices_kernel, dim3(blocks), dim3(256), 0, st, p, shift, vec);
+}
+
+cudaError_t launch_fill_mask_rows(uint8_t* mask, int64_t ld, const int32_t* clen, int row0,
+                                  int rows, int keys, int block, int64_t delta, cudaStream_t st)
+{
+    if (rows <= 0)
+        return cudaSuccess;
+    return launch_pdl(fill_mask_rows_kernel, dim3(rows), dim3(256), 0, st, mask, ld, clen, row0,
+                      keys, block, delta);
 }
 
 cudaError_t launch_expand_mask(const uint8_t* cand_mask, int64_t ld_mask, const int32_t* clen,
