@@ -832,7 +832,7 @@ __global__ void __launch_bounds__(kSelThreads, 3)
 constexpr int kThrThreads = 128;
 
 template <int POOL>
-__global__ void __launch_bounds__(kThrThreads, 12)
+__global__ void __launch_bounds__(kThrThreads, 16)
     sample_threshold_kernel(const __grid_constant__ SampleParams p)
 {
     pdl_wait_then_release();

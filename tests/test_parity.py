@@ -605,6 +605,32 @@ def test_topk_single_read_edge_rows():
     assert ti[0].tolist() == list(range(topk))           # equal logits: the lowest indices
 
 
+def test_topk_over_rows_longer_than_the_single_read_takes():
+    """Rows of more than 65,536 keys (the single-read kernel's key field is 16 bits) take
+    the gather / filtering read / verify merge path: against the oracle's selector on the
+    same logits and, bit for bit, the direct kernel alone."""
+    L, rows, topk = 70000, 6, 300
+    spec = W.ProblemSpec("rows past 65,536 keys", (W.RequestSpec(rows, L - rows, 1),), H=32,
+                         D=128, topk=topk, seed=37)
+    p = W.make_problem(spec)
+    plan = Hp.make_plan(p)
+    assert plan.info()["sample_stride"] >= 2
+    d = Hp.device_inputs(p)
+    g = Hp.gpu_logits(p, plan, d)
+    ti, tv = Hp.gpu_topk(p, plan, g, d)
+    di = torch.empty_like(ti)
+    dv = torch.empty_like(tv)
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    K.indexer_topk(plan, g, d["compress_len"], di, dv, small)
+    assert K.indexer_status(plan, small) == K.IDX_OK
+    assert torch.equal(ti, di) and torch.equal(tv, dv)
+    ref = O.topk_rows(g.cpu().numpy().astype(np.float64), p.compress_len.numpy(), topk)
+    ti = ti.cpu().numpy()
+    for t in range(rows):
+        assert sorted(x for x in ti[t].tolist() if x >= 0) == sorted(
+            x for x in ref[t].tolist() if x >= 0), t
+
+
 def test_topk_over_unaligned_logits_rows():
     """Rows that do not start on a 16-byte boundary (a view one column into a wider
     buffer, odd row stride) take the one-entry-per-load path of the filtering read and
