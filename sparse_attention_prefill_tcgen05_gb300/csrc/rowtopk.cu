@@ -18,8 +18,8 @@
 //                 one; the bucket holding the k-th entry, its entries ranked directly, a
 //                 bitmap of the kept keys, their positions by a prefix sum) written in
 //                 ascending key order, while the filter warps fill the other buffer.
-// A row whose candidates cannot decide it (fewer than k at or above tau, or more than a
-// warp's region holds) is flagged for the direct kernel.  Every wait is bounded: a
+// A row whose candidates cannot decide it (fewer than k at or above tau, or more than the
+// warps' regions and the shared spill area hold) is flagged for the direct kernel.  Every wait is bounded: a
 // timeout sets the status word and every role leaves its loop.
 #include "groupsel.cuh"
 #include "internal.h"
@@ -37,8 +37,9 @@ constexpr int kRtThreads = 32 + kFiltThreads + kSelThr;    // 800
 constexpr int kChunk = 8192;                               // floats per ring stage (32 KB)
 constexpr int kStages = 3;                                 // (a larger stage count does not fit)
 constexpr int kF4 = kChunk / (4 * kFiltThreads);           // float4 per filter lane per stage
-constexpr int kRegion = 320;                               // candidates per filter warp
-constexpr int kCand = kFiltWarps * kRegion;                // per buffer
+constexpr int kRegion = 256;                               // candidates per filter warp
+constexpr int kSpill = 1024;                               // shared by the warps, after their own
+constexpr int kCand = kFiltWarps * kRegion + kSpill;       // per buffer
 constexpr int kRtBuckets = 2048;
 constexpr int kRtMaxK = 2048;
 constexpr int kRtWords = 2048;                             // bitmap words: keys < 65536
@@ -75,7 +76,8 @@ constexpr size_t kOffObuf = kOffWpre + (size_t)kRtWords * 4;              // + 8
 constexpr size_t kOffMeta = kOffObuf + 2 * (size_t)kRtMaxK * 4;           // + 16 KB
 constexpr size_t kOffSlot = kOffMeta + kStages * sizeof(StageMeta);
 constexpr size_t kOffRcnt = kOffSlot + 2 * sizeof(RowSlot);               // [2][kFiltWarps]
-constexpr size_t kOffBar = (kOffRcnt + 2 * kFiltWarps * 4 + 7) / 8 * 8;
+constexpr size_t kOffSpill = kOffRcnt + 2 * kFiltWarps * 4;               // [2] spill counts
+constexpr size_t kOffBar = (kOffSpill + 2 * 4 + 7) / 8 * 8;
 constexpr int kNumBars = 2 * kStages + 4;
 constexpr size_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr size_t kRtSmem = kOffMisc + 64 + 128;                          // + alignment slack
@@ -133,6 +135,7 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
     StageMeta* meta = reinterpret_cast<StageMeta*>(smem + kOffMeta);
     RowSlot* slot = reinterpret_cast<RowSlot*>(smem + kOffSlot);
     uint32_t* rcnt = reinterpret_cast<uint32_t*>(smem + kOffRcnt);   // [2][kFiltWarps]
+    uint32_t* spill_n = reinterpret_cast<uint32_t*>(smem + kOffSpill);   // [2]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
     uint64_t* full = bars;                 // ring stage filled (producer, bytes)
     uint64_t* empty = bars + kStages;      // ring stage read (one arrival per filter warp)
@@ -154,6 +157,8 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
             mbar_init(&cempty[b], 1);
         }
         *abort_flag = 0;
+        spill_n[0] = 0;
+        spill_n[1] = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -306,14 +311,23 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
             const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
             uint32_t pos = count + incl - c;
             uint2* region = cand + (size_t)b * kCand + (size_t)fw * kRegion;
+            uint2* spill = cand + (size_t)b * kCand + (size_t)kFiltWarps * kRegion;
             const uint32_t jbase = static_cast<uint32_t>(m.chunk * kChunk);
             while (pm != 0) {
                 const int e = __ffs(pm) - 1;
                 pm &= pm - 1;
                 const int jl = 4 * (ft + kFiltThreads * (e >> 2)) + (e & 3);
-                if (pos < static_cast<uint32_t>(kRegion))
-                    region[pos] = make_uint2(__float_as_uint(stage[jl]),
+                const uint2 ent = make_uint2(__float_as_uint(stage[jl]),
                                              jbase + static_cast<uint32_t>(jl));
+                if (pos < static_cast<uint32_t>(kRegion)) {
+                    region[pos] = ent;
+                } else {
+                    // the warp's region is full: the shared spill area (its count past
+                    // kSpill marks the row as overflowed)
+                    const uint32_t sp = atomicAdd(&spill_n[b], 1u);
+                    if (sp < static_cast<uint32_t>(kSpill))
+                        spill[sp] = ent;
+                }
                 ++pos;
             }
             count += wtot;
@@ -322,8 +336,8 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
             if (lane == 0)
                 mbar_arrive(&empty[s]);
             if (m.last) {
-                // the warp's part of the row is done: its count (more than its region
-                // holds: overflow), then its arrival on the buffer
+                // the warp's part of the row is done: its count (past its region: the
+                // rest went to the spill area), then its arrival on the buffer
                 if (lane == 0) {
                     rcnt[b * kFiltWarps + fw] = count;
                     mbar_arrive(&cfull[b]);
@@ -359,21 +373,24 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
         const int t = sl.t;
         uint2* cb = cand + (size_t)b * kCand;
         const uint32_t* rc = rcnt + b * kFiltWarps;
-        uint32_t total_c = 0;
-        bool overflow = false;
+        // the warps' regions, then the spill area (overflowed when its count passed it)
+        const uint32_t nspill = spill_n[b];
+        const bool overflow = nspill > static_cast<uint32_t>(kSpill);
+        const int spilled = static_cast<int>(min(nspill, static_cast<uint32_t>(kSpill)));
+        uint32_t total_c = static_cast<uint32_t>(spilled);
 #pragma unroll
-        for (int w = 0; w < kFiltWarps; ++w) {
-            overflow |= rc[w] > static_cast<uint32_t>(kRegion);
+        for (int w = 0; w < kFiltWarps; ++w)
             total_c += min(rc[w], static_cast<uint32_t>(kRegion));
-        }
         // candidate e (of the kCand places) holds an entry iff it is below its warp
-        // region's count
+        // region's count, or below the spill count in the spill area
         auto valid = [&](int e) {
+            if (e >= kFiltWarps * kRegion)
+                return e - kFiltWarps * kRegion < spilled;
             const int w = e / kRegion;
             return static_cast<uint32_t>(e - w * kRegion) < rc[w];
         };
         // f(e) for every candidate: select warp sw walks the regions sw, sw + 8, ... with
-        // all of its lanes
+        // all of its lanes, then all select threads share the spill area
         auto each_cand = [&](auto&& f) {
             const int sw = st >> 5, sln = st & 31;
 #pragma unroll 1
@@ -382,6 +399,8 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                 for (int i = sln; i < n; i += 32)
                     f(w * kRegion + i);
             }
+            for (int i = st; i < spilled; i += kSelThr)
+                f(kFiltWarps * kRegion + i);
         };
         if (overflow || (sl.tau > kOrdNegInf && total_c < k)) {
             // the candidates cannot decide the row: the direct kernel will
@@ -553,10 +572,13 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                     ov[i] = have ? obv[i] : -INFINITY;
             }
         }
-        // everything of the buffer (and the output row) has been read: release it
+        // everything of the buffer (and the output row) has been read: release it, its
+        // spill count zeroed for its next row
         bar_all(true, kBarSel, kSelThr);
-        if (st == 0)
+        if (st == 0) {
+            spill_n[b] = 0;
             mbar_arrive(&cempty[b]);
+        }
         if (++b == 2) {
             b = 0;
             bph ^= 1;

@@ -605,6 +605,43 @@ def test_topk_single_read_edge_rows():
     assert ti[0].tolist() == list(range(topk))           # equal logits: the lowest indices
 
 
+def test_topk_single_read_uneven_candidates_use_the_spill_area():
+    """Every large logit of a row in one filter warp's key slice (the 512 keys j with
+    128 <= j % 2048 < 160, none of them in a sampled tile): that warp's region fills and the
+    rest of its candidates go to the shared spill area; the row is still decided by the
+    single read (no fallback row), and matches the oracle's selector and the direct kernel
+    bit for bit."""
+    L, rows, topk = 32768, 8, 512
+    spec = W.ProblemSpec("clustered", (W.RequestSpec(rows, L - rows, 1),), H=32, D=128,
+                         topk=topk, seed=41)
+    p = W.make_problem(spec)
+    plan = Hp.make_plan(p)
+    assert plan.info()["sample_stride"] >= 2
+    d = Hp.device_inputs(p)
+    gen = torch.Generator().manual_seed(41)
+    g = torch.randn((rows, L), generator=gen, dtype=torch.float32)
+    j = torch.arange(L)
+    g[:, ((j % 2048) >= 128) & ((j % 2048) < 160)] += 20.0
+    g = g.cuda()
+    T = rows
+    idx = torch.empty((T, topk), dtype=torch.int32, device="cuda")
+    val = torch.empty((T, topk), dtype=torch.float32, device="cuda")
+    ws = Hp.workspace(plan)
+    K.indexer_topk(plan, g, d["compress_len"], idx, val, ws)
+    assert K.indexer_status(plan, ws) == K.IDX_OK
+    assert K.indexer_fallback_rows(plan, ws) == 0
+    di = torch.empty_like(idx)
+    dv = torch.empty_like(val)
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    K.indexer_topk(plan, g, d["compress_len"], di, dv, small)
+    assert torch.equal(idx, di) and torch.equal(val, dv)
+    ref = O.topk_rows(g.cpu().numpy().astype(np.float64), p.compress_len.numpy(), topk)
+    ti = idx.cpu().numpy()
+    for t in range(T):
+        assert sorted(x for x in ti[t].tolist() if x >= 0) == sorted(
+            x for x in ref[t].tolist() if x >= 0), t
+
+
 def test_topk_over_rows_longer_than_the_single_read_takes():
     """Rows of more than 65,536 keys (the single-read kernel's key field is 16 bits) take
     the gather / filtering read / verify merge path: against the oracle's selector on the
