@@ -195,8 +195,12 @@ __device__ __forceinline__ bool merge_row_verified(const StreamMergeParams& p, c
     const uint32_t smax = p.smax_row[t];
     const int nslots = pc.slots, cap = pc.cap;
     const int row_words = (pc.key_count + 31) / 32;
-    if (tau <= kOrdNegInf || smax <= tau || !p.bitmap || row_words > kBitmapWords || cap <= 0)
+    if (tau <= kOrdNegInf || smax <= tau || !p.bitmap || cap <= 0)
         return false;
+    // rows of at most 65,536 keys keep the bucket in the upper 16 bits of the key field and
+    // write the kept keys in order from a bitmap; longer rows recompute the bucket and sort
+    // the kept keys
+    const bool packed = row_words <= kBitmapWords;
     BucketThr bt;
     bt.vmin = ord2f(tau);
     {
@@ -264,7 +268,8 @@ __device__ __forceinline__ bool merge_row_verified(const StreamMergeParams& p, c
                 if (i < c) {
                     const uint32_t b = static_cast<uint32_t>(bt.bucket(__uint_as_float(ent[u].x)));
                     atomicAdd(&bhist[b], 1u);
-                    stage[off + i] = make_uint2(ent[u].x, (ent[u].y & 0xFFFFu) | (b << 16));
+                    stage[off + i] =
+                        packed ? make_uint2(ent[u].x, (ent[u].y & 0xFFFFu) | (b << 16)) : ent[u];
                 }
             }
         }
@@ -299,10 +304,15 @@ __device__ __forceinline__ bool merge_row_verified(const StreamMergeParams& p, c
         __syncthreads();
     }
     const uint32_t bnd = sh.bcast[0], need = sh.bcast[1], bsize = sh.bcast[2];
-    // composite key (ord(score), ~index) of a staged entry
-    auto comp = [](const uint2 en) {
+    // a staged entry's key, bucket and composite key (ord(score), ~index)
+    auto key_of = [&](const uint2 en) { return packed ? (en.y & 0xFFFFu) : en.y; };
+    auto bucket_of = [&](const uint2 en) {
+        return packed ? (en.y >> 16)
+                      : static_cast<uint32_t>(bt.bucket(__uint_as_float(en.x)));
+    };
+    auto comp = [&](const uint2 en) {
         return (static_cast<uint64_t>(f2ord(__uint_as_float(en.x))) << 32) |
-               static_cast<uint32_t>(~(en.y & 0xFFFFu));
+               static_cast<uint32_t>(~key_of(en));
     };
     uint64_t cut = 0;   // the whole boundary bucket is kept when it gives all of its entries
     if (bsize != need) {
@@ -310,7 +320,7 @@ __device__ __forceinline__ bool merge_row_verified(const StreamMergeParams& p, c
             return false;
         for (int e = tid; e < n; e += kSelThreads) {
             const uint2 en = stage[e];
-            if ((en.y >> 16) == bnd)
+            if (bucket_of(en) == bnd)
                 bcand[atomicAdd(&v_bcount, 1)] = comp(en);
         }
         __syncthreads();
@@ -326,7 +336,42 @@ __device__ __forceinline__ bool merge_row_verified(const StreamMergeParams& p, c
         __syncthreads();
         cut = v_cut;
     }
-    __syncthreads();   // the bucket scratch becomes the bitmap
+    __syncthreads();   // the bucket scratch becomes the bitmap (or the sort area)
+    int32_t* oi = p.out_idx + (int64_t)t * p.k;
+    float* ov = p.out_val ? p.out_val + (int64_t)t * p.k : nullptr;
+    if (!packed) {
+        // the k kept entries (any order), then sorted by key
+        int32_t* skey = reinterpret_cast<int32_t*>(bhist);
+        float* sval = reinterpret_cast<float*>(skey + n2);
+        if (tid == 0)
+            v_total = 0;
+        for (int i = tid; i < n2; i += kSelThreads) {
+            skey[i] = INT32_MAX;
+            sval[i] = -INFINITY;
+        }
+        __syncthreads();
+        for (int e = tid; e < n; e += kSelThreads) {
+            const uint2 en = stage[e];
+            const uint32_t b = bucket_of(en);
+            if (b > bnd || (b == bnd && comp(en) >= cut)) {
+                const int pos = atomicAdd(&v_total, 1);
+                if (pos < n2) {
+                    skey[pos] = static_cast<int32_t>(en.y);
+                    sval[pos] = __uint_as_float(en.x);
+                }
+            }
+        }
+        bitonic_sort(skey, sval, n2);
+        __syncthreads();
+        const int total = min(v_total, static_cast<int>(k));
+        for (int i = tid; i < p.k; i += kSelThreads) {
+            const bool have = i < total;
+            oi[i] = have ? skey[i] : -1;
+            if (ov)
+                ov[i] = have ? sval[i] : -INFINITY;
+        }
+        return true;
+    }
     uint32_t* bits = bhist;
     uint32_t* wpre = bits + kBitmapWords;
     const int nw = max(row_words, 1);
@@ -354,8 +399,6 @@ __device__ __forceinline__ bool merge_row_verified(const StreamMergeParams& p, c
         }
     }
     __syncthreads();
-    int32_t* oi = p.out_idx + (int64_t)t * p.k;
-    float* ov = p.out_val ? p.out_val + (int64_t)t * p.k : nullptr;
     for (int i = tid; i < p.k; i += kSelThreads) {
         const bool have = i < total;
         oi[i] = have ? obi[i] : -1;
