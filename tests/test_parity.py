@@ -719,3 +719,39 @@ def test_repeated_calls_on_one_workspace_decide_the_same_rows():
         assert K.indexer_fallback_rows(plan, ws) == 0
         outs.append(idx)
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+def test_calls_between_torch_kernels_on_one_stream():
+    """Every kernel of the library may start while the previous kernel of its stream is
+    still running, and waits for it before touching memory.  A call right after a PyTorch
+    kernel that rewrites an input (the head weights doubled in place: every logit doubles
+    exactly) sees the new values, and a PyTorch kernel right after the call reads its
+    outputs; the same for indexer_topk after a kernel that writes its logits."""
+    spec = dataclasses.replace(W.scaled(W.CONFIGS["cold64k"], 8, 4), topk=256, seed=43)
+    p = W.make_problem(spec)
+    plan = Hp.make_plan(p)
+    assert plan.info()["sample_stride"] >= 2
+    d = Hp.device_inputs(p)
+    ri, rv = Hp.gpu_fused(p, plan, d, with_values=True)
+    T = int(p.cu_seqlens_q[-1])
+    idx = torch.empty((T, p.topk), dtype=torch.int32, device="cuda")
+    val = torch.empty((T, p.topk), dtype=torch.float32, device="cuda")
+    ws = Hp.workspace(plan)
+    d["w"].mul_(2.0)                                     # a kernel, just before the call
+    K.indexer_fused_topk(plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"],
+                         d["compress_len"], None, idx, val, ws)
+    half = val.mul(0.5)                                  # a kernel, just after it
+    i2 = idx.clone()
+    assert K.indexer_status(plan, ws) == K.IDX_OK
+    assert torch.equal(i2, ri)
+    assert torch.equal(half, rv)
+    d["w"].mul_(0.5)
+    # indexer_topk over logits a kernel has just written
+    g = Hp.gpu_logits(p, plan, d)
+    ti, tv = Hp.gpu_topk(p, plan, g, d)
+    g2 = torch.empty_like(g)
+    torch.mul(g, 2.0, out=g2)
+    K.indexer_topk(plan, g2, d["compress_len"], idx, val, ws)
+    half = val.mul(0.5)
+    assert K.indexer_status(plan, ws) == K.IDX_OK
+    assert torch.equal(idx, ti) and torch.equal(half, tv)
