@@ -555,7 +555,7 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK, FP4K>::THREADS, 1)
                                  : RPH == 2 ? (0x33333333u << (q & 2))
                                             : 0xFFFFFFFFu;
         const bool row_leader = g == 0 && (RPH >= 4 || (q & (4 / RPH - 1)) == 0);
-        const uint32_t lanes_below = (1u << lane) - 1u;
+        [[maybe_unused]] const uint32_t lanes_below = (1u << lane) - 1u;
         const NamedSync half_sync{2 + half, kHalfThreads};
         const NamedSync epi_sync{1, C::EPI * 32};
         SelScratch<kHalfThreads>* sel_s =
