@@ -170,7 +170,13 @@ int indexer_logits(indexer_plan_t plan, const void* q, const float* s_q, const f
  * Ragged per-row top-k over given logits [T, ld] (the ragged top-k of
  * "chunked-prefill-memory.md" section 2.3).  Entries j >= compress_len[t] and
  * -inf entries are not eligible.  out_idx int32 [T, topk]; out_val float
- * [T, topk] or NULL.
+ * [T, topk] or NULL.  A row's kept keys are written in ascending key order,
+ * then -1 (value -inf) padding.
+ * With at least the plan's workspace, rows are sampled for a threshold and read
+ * once (for 16-byte aligned rows of at most 65,536 keys the candidates and the
+ * exact selection stay in shared memory); rows the sample cannot decide, and
+ * every row when ws holds only the status area (256 bytes), get a direct exact
+ * selection.  All of these give identical outputs.
  */
 int indexer_topk(indexer_plan_t plan, const float* logits, int64_t ld,
                  const int32_t* compress_len, int32_t* out_idx, float* out_val, void* ws,
