@@ -254,8 +254,9 @@ def other_workloads(K, W, dev, flush, steps,
     launching stream, L2 flushed before every timed call, inputs resident in HBM):
     latency, dense pairs/s and the fraction of the FP8 tensor peak, and the plan's
     transient bytes.  The candidate workload times the source layer (block mask) and the
-    masked consumer layer separately and together; the fp4-query workload times the
-    exact query conversion and the fused call together."""
+    masked consumer layer separately and together; the fp4-query workload passes its e2m1
+    queries and block scales straight to the fused call (the block-scaled fp4 MMA) and is
+    also reported against the FP4 tensor peak."""
     import torch
     peak, _ = fp8_peak_tflops()
     out = {}
@@ -263,9 +264,10 @@ def other_workloads(K, W, dev, flush, steps,
         spec = W.CONFIGS[name]
         p = W.make_problem(spec)
         kd = K.IDX_K_FP8_E4M3 if spec.kdtype == "fp8" else K.IDX_K_FP4_E2M1_UE8M0
+        qd = K.IDX_Q_FP4_E2M1_UE8M0 if spec.qdtype == "fp4" else K.IDX_Q_FP8_E4M3
         plan = K.indexer_plan(p.cu_seqlens_q, p.cu_seqlens_k, p.compress_len, p.H, p.D, p.topk,
                               kdtype=kd, cand_block=spec.cand_block, cand_topk=spec.cand_topk,
-                              key_block=spec.key_block)
+                              key_block=spec.key_block, qdtype=qd)
         T = int(p.cu_seqlens_q[-1])
         ld = int(torch.diff(p.cu_seqlens_k).max())
         d = {n: getattr(p, n).to(dev) for n in ("q", "s_q", "w", "k", "k_scale", "compress_len")}
@@ -283,23 +285,11 @@ def other_workloads(K, W, dev, flush, steps,
                 plan, d2["q"], d2["s_q"], d2["w"], d["k"], d["k_scale"], d["compress_len"], mask,
                 idx, val, wsb)
         if spec.qdtype == "fp4":
-            # e2m1 queries: converted exactly to e4m3 + a scale per head vector, then the
-            # fused call on the converted queries
-            Tq, Hq, Dq = p.q.shape
-            q4 = p.q4.reshape(Tq * Hq, Dq // 2).to(dev)
-            qsf = p.q_sf.reshape(Tq * Hq, Dq // 32).to(dev)
-            q8 = torch.empty((Tq * Hq, Dq), dtype=torch.uint8, device=dev)
-            sq8 = torch.empty(Tq * Hq, dtype=torch.float32, device=dev)
-
-            def fp4q_call():
-                K.indexer_convert_fp4(q4, qsf, q8, sq8, wsb)
-                K.indexer_fused_topk(plan, q8.view(Tq, Hq, Dq), sq8.view(Tq, Hq), d["w"], d["k"],
-                                     d["k_scale"], d["compress_len"], None, idx, val, wsb)
-            calls["convert_q_and_fused_topk"] = fp4q_call
-        else:
-            calls["fused_topk"] = lambda: K.indexer_fused_topk(
-                plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"], d["compress_len"], None,
-                idx, val, wsb)
+            # e2m1 queries: the packed codes, and their ue8m0 block scales in the s_q slot
+            d["q"], d["s_q"] = p.q4.to(dev), p.q_sf.to(dev)
+        calls["fused_topk"] = lambda: K.indexer_fused_topk(
+            plan, d["q"], d["s_q"], d["w"], d["k"], d["k_scale"], d["compress_len"], None,
+            idx, val, wsb)
         n = max(3, min(steps, 20 if name != "long488k" else 5))
         res = {"workload": spec.name, "peak_transient_bytes": plan.workspace_bytes,
                "dense_pairs_per_call": spec.dense_pairs, "timed_calls": n}
@@ -320,6 +310,9 @@ def other_workloads(K, W, dev, flush, steps,
             flops = 2.0 * spec.dense_pairs * spec.H * spec.D
             res[cname] = {"latency_ms": ms, "pairs_per_s": spec.dense_pairs / (ms / 1e3),
                           "frac_fp8_peak": flops / (ms / 1e3) / 1e12 / peak}
+            if spec.qdtype == "fp4":
+                # FP4 peak: the FP8 figure x the nominal FP4 / FP8 dense ratio (13.5 / 4.5)
+                res[cname]["frac_fp4_peak"] = flops / (ms / 1e3) / 1e12 / (3.0 * peak)
         if spec.cand_topk:
             both = res["candidate_source"]["latency_ms"] + res["masked_consumer"]["latency_ms"]
             res["source_plus_consumer_ms"] = both

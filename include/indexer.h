@@ -78,6 +78,18 @@ extern "C" {
                                       aligned); other head counts score the keys through
                                       their exact e4m3 form (see indexer_convert_fp4) */
 
+/* Query formats. */
+#define IDX_Q_FP8_E4M3 0           /* q: e4m3 [T, H, D]; s_q: float [T, H] */
+#define IDX_Q_FP4_E2M1_UE8M0 1     /* q: e2m1 [T, H, D/2], element 2i in the low nibble;
+                                      the s_q argument carries its block scales instead of
+                                      float scales: uint8 ue8m0 [T, H, D/32] (4-byte
+                                      aligned, passed as (const float*)); value =
+                                      e2m1(code) * 2^(e - 127).  Needs kdtype
+                                      IDX_K_FP4_E2M1_UE8M0 and 32 heads of 128: both operands
+                                      then stay e2m1 in the block-scaled fp4 MMA
+                                      (tcgen05 kind::mxf4, ue8m0 per 32 elements), any
+                                      block-scale span on either side */
+
 /* Row selection strategies of indexer_fused_topk (both exact). */
 #define IDX_SELECT_AUTO 0          /* sampled row thresholds where rows are long enough,
                                       the running-threshold stream for undecided rows */
@@ -96,6 +108,8 @@ extern "C" {
  *   compress_len  [T] causal length of every row, 0 <= compress_len[t] <= the
  *                 keys of its request (e.g. floor((pos+1)/ratio))
  *   kdtype        IDX_K_FP8_E4M3 or IDX_K_FP4_E2M1_UE8M0
+ *   qdtype        IDX_Q_FP8_E4M3 (0) or IDX_Q_FP4_E2M1_UE8M0; other values
+ *                 IDX_ERR_INVALID_ARG, an unsupported pairing IDX_ERR_UNSUPPORTED
  *   cand_block    keys per candidate block: 1, 2, 4 or 8 (0 means 8)
  *   cand_topk     candidate blocks kept per row by indexer_candidate_blocks,
  *                 1..4096 (e.g. 2048); 0 = the plan makes no candidate-block
@@ -129,7 +143,7 @@ typedef struct indexer_problem {
     int32_t key_block;
     uint64_t transient_budget_bytes;
     int32_t select_mode;
-    int32_t reserved_;
+    int32_t qdtype;
 } indexer_problem;
 
 typedef struct indexer_plan_s* indexer_plan_t;

@@ -28,6 +28,8 @@ IDX_ERR_TIMEOUT = -5
 IDX_ERR_DEVICE_CHECK = -6
 IDX_K_FP8_E4M3 = 0
 IDX_K_FP4_E2M1_UE8M0 = 1
+IDX_Q_FP8_E4M3 = 0
+IDX_Q_FP4_E2M1_UE8M0 = 1
 IDX_SELECT_AUTO = 0
 IDX_SELECT_STREAM = 1
 
@@ -59,7 +61,7 @@ class _Problem(ctypes.Structure):
         ("kdtype", ctypes.c_int32), ("cand_block", ctypes.c_int32),
         ("cand_topk", ctypes.c_int32), ("key_block", ctypes.c_int32),
         ("transient_budget_bytes", ctypes.c_uint64),
-        ("select_mode", ctypes.c_int32), ("reserved_", ctypes.c_int32),
+        ("select_mode", ctypes.c_int32), ("qdtype", ctypes.c_int32),
     ]
 
 
@@ -161,8 +163,10 @@ class Plan:
 def indexer_plan(cu_seqlens_q, cu_seqlens_k, compress_len, H: int, D: int, topk: int,
                  kdtype: int = IDX_K_FP8_E4M3, cand_block: int = 0, cand_topk: int = 0,
                  key_block: int = 0, transient_budget_bytes: int = 0,
-                 select_mode: int = 0) -> Plan:
-    """Host-only planning: lengths are host (CPU) int32 arrays/tensors."""
+                 select_mode: int = 0, qdtype: int = IDX_Q_FP8_E4M3) -> Plan:
+    """Host-only planning: lengths are host (CPU) int32 arrays/tensors.  With
+    ``qdtype=IDX_Q_FP4_E2M1_UE8M0`` the calls take q as packed e2m1 [T, H, D/2] and its
+    ue8m0 block scales [T, H, D/32] (uint8) in the ``s_q`` argument."""
     def host_i32(x):
         t = torch.as_tensor(x).to(device="cpu", dtype=torch.int32).contiguous()
         return t, t.numpy().ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
@@ -174,7 +178,7 @@ def indexer_plan(cu_seqlens_q, cu_seqlens_k, compress_len, H: int, D: int, topk:
                     H=H, D=D, topk=topk, cu_seqlens_q=pq, cu_seqlens_k=pk, compress_len=pl,
                     kdtype=kdtype, cand_block=cand_block, cand_topk=cand_topk,
                     key_block=key_block, transient_budget_bytes=transient_budget_bytes,
-                    select_mode=select_mode)
+                    select_mode=select_mode, qdtype=qdtype)
     handle = ctypes.c_void_p()
     ws = ctypes.c_size_t()
     _check("indexer_plan", lib().indexer_plan(ctypes.byref(prob), ctypes.byref(handle),

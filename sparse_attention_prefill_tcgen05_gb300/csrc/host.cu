@@ -64,6 +64,7 @@ struct indexer_plan_s {
     int kH = 0;                       // heads the kernels run with (H, or H padded with zero heads)
     size_t off_pad = 0;               // padded q / s_q / w when kH != H
     bool fp4_native = false;          // e2m1 keys scored by the block-scaled MMA
+    bool fp4_queries = false;         // e2m1 queries as well (the fp4 MMA kind)
     size_t off_k8 = 0;                // e4m3 keys [Lk, D] + s_k [Lk] converted from e2m1
                                       // (shapes without a block-scaled kernel)
     size_t pad_end = 0;               // end of the per-call input preparation area
@@ -270,7 +271,8 @@ int check_inputs(const indexer_plan_s* p, const void* q, const float* s_q, const
 {
     if (!q || !s_q || !w || !k || !k_scale || !clen)
         return IDX_ERR_INVALID_ARG;
-    // e2m1 keys scored natively read their block scales as one 32-bit word per key
+    // e2m1 keys scored natively read their block scales as one 32-bit word per key, and
+    // e2m1 queries theirs (passed as s_q) as one word per query vector
     if (!aligned(q, 16) || !aligned(k, p->kdtype == IDX_K_FP8_E4M3 ? 16 : 32) ||
         !aligned(s_q, 4) || !aligned(w, 4) || !aligned(clen, 4) ||
         ((p->kdtype == IDX_K_FP8_E4M3 || p->fp4_native) && !aligned(k_scale, 4)))
@@ -293,11 +295,16 @@ int fill_maps(Ctx& c, const void* q, const void* k)
 {
     const indexer_plan_s* p = c.p;
     std::memset(&c.lp, 0, sizeof(c.lp));
-    if (!make_map(&c.lp.tmap_q, q, (uint64_t)p->T * p->kH, p->D, p->G * p->kH))
+    if (!make_map(&c.lp.tmap_q, q, (uint64_t)p->T * p->kH, p->fp4_queries ? p->D / 2 : p->D,
+                  p->G * p->kH))
         return IDX_ERR_CUDA;
     const uint64_t krows = (uint64_t)std::max(p->Lk, 1);
-    if (!(p->fp4_native ? make_map_fp4(&c.lp.tmap_k, k, krows, p->D, kTileKeys)
-                        : make_map(&c.lp.tmap_k, k, krows, p->D, kTileKeys)))
+    // e2m1 keys: unpacked to the 8-bit container layout for the mxf8f6f4 kind, kept packed
+    // (64-byte rows) for the fp4 kind that e2m1 queries take
+    const bool unpack = p->fp4_native && !p->fp4_queries;
+    if (!(unpack ? make_map_fp4(&c.lp.tmap_k, k, krows, p->D, kTileKeys)
+                 : make_map(&c.lp.tmap_k, k, krows, p->fp4_queries ? p->D / 2 : p->D,
+                            kTileKeys)))
         return IDX_ERR_CUDA;
     return IDX_OK;
 }
@@ -644,7 +651,9 @@ int begin_call(Ctx& c, const indexer_plan_s* p, void* ws, void* stream)
 void set_inputs(Ctx& c, const float* s_q, const float* w, const void* k_scale,
                 const int32_t* clen, void* ws)
 {
-    c.lp.s_q = s_q;
+    // e2m1 queries: s_q carries their ue8m0 block scales, four bytes per query vector
+    c.lp.s_q = c.p->fp4_queries ? nullptr : s_q;
+    c.lp.q_sf = c.p->fp4_queries ? reinterpret_cast<const uint32_t*>(s_q) : nullptr;
     c.lp.w = w;
     // e2m1 keys scored natively keep their block scales (the MMA applies them); others
     // arrive here as e4m3 keys with s_k (converted from e2m1 where they were e2m1)
@@ -760,6 +769,8 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
         return IDX_ERR_INVALID_ARG;
     if (pr->kdtype != IDX_K_FP8_E4M3 && pr->kdtype != IDX_K_FP4_E2M1_UE8M0)
         return IDX_ERR_INVALID_ARG;
+    if (pr->qdtype != IDX_Q_FP8_E4M3 && pr->qdtype != IDX_Q_FP4_E2M1_UE8M0)
+        return IDX_ERR_INVALID_ARG;
     const int cb = pr->cand_block ? pr->cand_block : 8;
     const int ct = pr->cand_topk;
     if (cb < 1 || cb > 8 || (cb & (cb - 1)) != 0 || ct < 0 || ct > 4096)
@@ -809,6 +820,12 @@ int indexer_plan(const indexer_problem* pr, indexer_plan_t* out, size_t* ws_byte
     // 4 heads run as 8 (zero heads 4..7 add exactly 0 to every logit)
     p->kH = p->H == 4 ? 8 : p->H;
     p->fp4_native = p->kdtype == IDX_K_FP4_E2M1_UE8M0 && logits_fp4_native(p->kH, p->D);
+    // e2m1 queries run with e2m1 keys on the block-scaled fp4 MMA (32 heads of 128)
+    p->fp4_queries = pr->qdtype == IDX_Q_FP4_E2M1_UE8M0;
+    if (p->fp4_queries && !p->fp4_native) {
+        delete p;
+        return IDX_ERR_UNSUPPORTED;
+    }
     p->G = logits_rows_per_group(p->kH, p->fp4_native);
     const int G = p->G;
 

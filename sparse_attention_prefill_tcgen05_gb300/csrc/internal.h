@@ -76,10 +76,11 @@ struct Segment {
 };
 
 struct LogitsParams {
-    CUtensorMap tmap_q;  // [rows*H, D] bytes, box [256 rows, D]
+    CUtensorMap tmap_q;  // [rows*H, D] bytes, box [256 rows, D]; e2m1 queries: [rows*H, D/2]
+                         // packed, 64-byte swizzled
     CUtensorMap tmap_k;  // [keys, D] bytes, box [128 rows, D]; e2m1 keys: [keys, D/2]
                          // packed, unpacked by the map into 16-byte groups of 16 codes
-    const float* s_q;    // [rows, H]
+    const float* s_q;    // [rows, H]; nullptr for e2m1 queries
     const float* w;      // [rows, H]
     const float* s_k;    // fp8 keys: [keys]
     const int32_t* compress_len;  // [rows]
@@ -107,6 +108,8 @@ struct LogitsParams {
     Segment seg[kMaxSegments];
     const uint32_t* k_sf; // e2m1 keys scored natively: [keys] four ue8m0 block scales
                           // (byte b: elements 32b..32b+31); nullptr for e4m3 keys
+    const uint32_t* q_sf; // e2m1 queries (with e2m1 keys): [rows * H] four ue8m0 block
+                          // scales per query vector; nullptr for e4m3 queries
 };
 
 // Host-side launchers (defined in the .cu files).

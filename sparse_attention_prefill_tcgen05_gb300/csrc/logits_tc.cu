@@ -59,23 +59,35 @@ namespace {
 
 constexpr int kHalfThreads = 128;
 
-// FP4K: e2m1 keys with one ue8m0 scale per 32 elements, scored by the block-scaled MMA.
-// Its tiles are 192 columns (6 rows of 32 heads): two accumulators of 192 columns and
-// the scale factors fit the 512 TMEM columns (24 columns of key scales, one 4-column
-// group per K stage, then 8 columns of query scales).
-template <int H, int D, int SINK, bool FP4K = false>
+// Operand kinds of the contraction.
+constexpr int kOpsE4M3 = 0;   // e4m3 keys x e4m3 queries, kind::f8f6f4
+constexpr int kOpsE2M1K = 1;  // e2m1 keys x e4m3 queries, kind::mxf8f6f4 (ue8m0 key scales)
+constexpr int kOpsE2M1 = 2;   // e2m1 keys x e2m1 queries, kind::mxf4 (ue8m0 scales on both)
+
+// e2m1 keys (one ue8m0 scale per 32 elements) are scored by the block-scaled MMA.  Their
+// tiles are 192 columns (6 rows of 32 heads): two accumulators of 192 columns and the
+// scale factors fit the 512 TMEM columns (24 columns of key scales, one 4-column group
+// per K stage, then the query scales: 8 columns of 2^0 for e4m3 queries, two buffers of 8
+// for e2m1 queries, one per Q tile buffer).  e2m1 queries take the fp4 kind: both
+// operands stay packed in shared memory (64-byte rows for D = 128), K = 64 per MMA.
+template <int H, int D, int SINK, int OPS = kOpsE4M3>
 struct Cfg {
+    static constexpr bool FP4K = OPS != kOpsE4M3;   // e2m1 keys
+    static constexpr bool FP4Q = OPS == kOpsE2M1;   // e2m1 queries too
     // tiles are 256 columns (16 rows for small H; 192 for e2m1 keys)
     static constexpr int NMAX = FP4K ? 192 : (H >= 16 ? kTileN : 16 * H);
     static constexpr int G = NMAX / H;                 // query rows per tile
     static constexpr int N = G * H;                    // MMA N
-    static constexpr int QBYTES = N * D;               // Q tile: N rows of D bytes
-    static constexpr int KBYTES = kTileKeys * D;       // K tile in shared memory
-    // bytes a K tile's TMA load counts on its barrier: the packed bytes it reads (e2m1
-    // codes are unpacked into 16-byte groups of 16 on the way into shared memory)
-    static constexpr int KTX = FP4K ? KBYTES / 2 : KBYTES;
+    static constexpr int QROW = FP4Q ? D / 2 : D;      // bytes of a Q row in shared memory
+    // bytes of a K row in shared memory: e2m1 keys of the f8f6f4 kinds are unpacked into
+    // 16-byte groups of 16 codes on the way in; the fp4 kind reads them packed
+    static constexpr int KROW = FP4Q ? D / 2 : D;
+    static constexpr int QBYTES = N * QROW;            // Q tile: N rows
+    static constexpr int KBYTES = kTileKeys * KROW;    // K tile in shared memory
+    // bytes a K tile's TMA load counts on its barrier: the packed bytes it reads
+    static constexpr int KTX = (FP4K && !FP4Q) ? KBYTES / 2 : KBYTES;
     static constexpr int STAGES = (D >= 128) ? 6 : 8;
-    static constexpr int KSTEPS = D / 32;              // MMA K = 32 elements
+    static constexpr int KSTEPS = D / (FP4Q ? 64 : 32);   // MMA K = 32 elements (64 for fp4)
     // epilogue warps: 16 for the list sinks (their per-tile selection work needs the
     // latency hiding), 8 for plain logits (fewer instructions per tile, 168 registers)
     static constexpr int EPI = FP4K ? 12 : (SINK == kSinkLogits ? 8 : 16);
@@ -97,7 +109,8 @@ struct Cfg {
     // TMEM columns of the scale factors (after the two accumulators)
     static constexpr int SFA_COL = 2 * ACC_COLS;            // + 4 per K stage
     static constexpr int SFB_COL = SFA_COL + 4 * STAGES;    // 8 columns
-    static_assert(!FP4K || SFB_COL + 8 <= 512, "scale factors must fit the allocation");
+    static constexpr int SFB_COLS = FP4Q ? 16 : 8;
+    static_assert(!FP4K || SFB_COL + SFB_COLS <= 512, "scale factors must fit the allocation");
     // shared memory carve-up (offsets from a 1024-byte aligned base)
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + ((2 * QBYTES + 1023) / 1024) * 1024;
@@ -105,7 +118,13 @@ struct Cfg {
     // tcgen05.cp 128x128b reads)
     static constexpr int OFF_SF = OFF_K + STAGES * KBYTES;
     static constexpr int SF_BYTES = FP4K ? kTileKeys * 16 : 0;
-    static constexpr int OFF_C = OFF_SF + STAGES * SF_BYTES;        // float c[2][kTileN]
+    // e2m1 queries: per Q buffer the tile's query scale words as two 128-row x 16-byte
+    // sources of tcgen05.cp 128x128b (row 32 quadrant + m, word i of copy j: query column
+    // 32 (4 j + i) + m, the same in every quadrant)
+    static constexpr int OFF_QSF = OFF_SF + STAGES * SF_BYTES;
+    static constexpr int QSF_ONE = 2 * kTileKeys * 16;
+    static constexpr int QSF_BYTES = FP4Q ? 2 * QSF_ONE : 0;
+    static constexpr int OFF_C = OFF_QSF + QSF_BYTES;               // float c[2][kTileN]
     static constexpr int OFF_HIST = OFF_C + 2 * kTileN * 4;          // u32 [G][2][256]
     static constexpr int HIST_BYTES = STREAM ? G * 2 * 256 * 4 : 0;
     static constexpr int OFF_ROWS = OFF_HIST + HIST_BYTES;           // row state [G]
@@ -294,18 +313,21 @@ __device__ __forceinline__ uint32_t warp_sum_bins(const uint32_t* hist, int lane
 
 // MASK: the launch applies a candidate-block mask (a separate instantiation, so that
 // the unmasked kernels carry none of its registers).
-template <int H, int D, int SINK, bool MASK, bool FP4K>
-__global__ void __launch_bounds__(Cfg<H, D, SINK, FP4K>::THREADS, 1)
+template <int H, int D, int SINK, bool MASK, int OPS>
+__global__ void __launch_bounds__(Cfg<H, D, SINK, OPS>::THREADS, 1)
     logits_tc_kernel(const __grid_constant__ LogitsParams p)
 {
     pdl_wait_then_release();
-    using C = Cfg<H, D, SINK, FP4K>;
+    using C = Cfg<H, D, SINK, OPS>;
+    constexpr bool FP4K = C::FP4K;
+    constexpr bool FP4Q = C::FP4Q;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* q_s = smem + C::OFF_Q;
     uint8_t* k_s = smem + C::OFF_K;
     uint8_t* sf_s = smem + C::OFF_SF;
+    uint8_t* qsf_s = smem + C::OFF_QSF;
     float* c_s = reinterpret_cast<float*>(smem + C::OFF_C);
     uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);
     RowState* rows_s = reinterpret_cast<RowState*>(smem + C::OFF_ROWS);
@@ -329,7 +351,8 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK, FP4K>::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&q_full[i], 1);
+            // e2m1 queries: one arrival with the TMA bytes, one when the scales are staged
+            mbar_init(&q_full[i], FP4Q ? 2 : 1);
             mbar_init(&q_empty[i], 1);
             mbar_init(&a_full[i], 1);
             mbar_init(&a_empty[i], C::EPI);
@@ -356,8 +379,8 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK, FP4K>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const long long budget = p.timeout_cycles;
-    if constexpr (FP4K) {
-        // the queries carry no block scale: every query scale cell holds 2^0 (ue8m0 127)
+    if constexpr (FP4K && !FP4Q) {
+        // e4m3 queries carry no block scale: every query scale cell holds 2^0 (ue8m0 127)
         // in all four bytes, in every lane quadrant (each quadrant reads its own copy)
         if (warp >= 4 && warp < 8) {
             tmem_st_32x32b_x8_fill(tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) +
@@ -393,6 +416,34 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK, FP4K>::THREADS, 1)
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if constexpr (FP4Q) {
+                if (ok) {
+                    // the tile's query scale words (four ue8m0 bytes of query column n = row
+                    // x H + head) into the buffer's two copy sources; columns of rows past
+                    // the group and past N read as 2^0.  The previous unit on this buffer
+                    // finished its MMAs (q_empty), and with them the copies that read it.
+                    uint32_t wv[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int n = 32 * c + lane;
+                        wv[c] = (n < C::N && n / H < ui.nr)
+                                    ? __ldg(p.q_sf + (size_t)ui.t0 * H + n)
+                                    : 0x7F7F7F7Fu;
+                    }
+                    uint8_t* dst = qsf_s + qb * C::QSF_ONE;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+#pragma unroll
+                        for (int quad4 = 0; quad4 < 4; ++quad4)
+                            *reinterpret_cast<uint4*>(dst + j * (C::QSF_ONE / 2) +
+                                                      16 * (32 * quad4 + lane)) =
+                                make_uint4(wv[4 * j], wv[4 * j + 1], wv[4 * j + 2], wv[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&q_full[qb]);
+                }
+            }
             for (int i = 0; i < ui.ntiles_mma && ok; ++i) {
                 const int key0 = sg.key_base + ui.j0 + i * ui.step;
                 if (lane == 0) {
@@ -465,6 +516,16 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK, FP4K>::THREADS, 1)
                     report(p, abort_flag, kStatusTimeout);
                     ok = false;
                 }
+                [[maybe_unused]] const uint32_t sfb = tmem_base + C::SFB_COL + (FP4Q ? 8 * qb : 0);
+                if constexpr (FP4Q) {
+                    // the unit's query scales into this Q buffer's 8 scale columns
+                    if (ok) {
+                        tc_fence_after();
+                        const uint32_t src = smem_u32(qsf_s + qb * C::QSF_ONE);
+                        tmem_cp_128x128b(sfb, smem_desc_noswizzle(src, 128));
+                        tmem_cp_128x128b(sfb + 4, smem_desc_noswizzle(src + C::QSF_ONE / 2, 128));
+                    }
+                }
                 const uint32_t q_addr = smem_u32(q_s + qb * C::QBYTES);
                 for (int i = 0; i < ui.ntiles_mma && ok; ++i) {
                     if (!mbar_wait(&a_empty[ab], aph ^ 1, budget, abort_flag) ||
@@ -476,7 +537,21 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK, FP4K>::THREADS, 1)
                     tc_fence_after();
                     const uint32_t k_addr = smem_u32(k_s + ks * C::KBYTES);
                     const uint32_t d_tmem = tmem_base + ab * C::ACC_COLS;
-                    if constexpr (FP4K) {
+                    if constexpr (FP4Q) {
+                        // the stage's key scales into TMEM, then one fp4 MMA per two
+                        // 32-element blocks (64 packed codes, 32 bytes of each row): scale
+                        // bytes 2 kk and 2 kk + 1 of each cell
+                        const uint32_t sfa = tmem_base + C::SFA_COL + 4 * ks;
+                        tmem_cp_128x128b(sfa, smem_desc_noswizzle(smem_u32(sf_s + ks * C::SF_BYTES), 128));
+#pragma unroll
+                        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                            const uint64_t adesc = smem_desc_kmajor(k_addr + kk * 32, C::KROW);
+                            const uint64_t bdesc = smem_desc_kmajor(q_addr + kk * 32, C::QROW);
+                            mma_mxf4(d_tmem, adesc, bdesc,
+                                     idesc_mxf4(kTileKeys, C::N, 2 * kk, 2 * kk), sfa, sfb,
+                                     kk > 0 ? 1u : 0u);
+                        }
+                    } else if constexpr (FP4K) {
                         // the stage's key scales into TMEM, then one block-scaled MMA per
                         // 32-element block (A = e2m1 keys, B = e4m3 queries); the scale
                         // byte of block kk is byte kk of each cell
@@ -488,7 +563,7 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK, FP4K>::THREADS, 1)
                             const uint64_t bdesc = smem_desc_kmajor(q_addr + kk * 32, D);
                             mma_mxf8f6f4(d_tmem, adesc, bdesc,
                                          idesc_mxf8f6f4(kTileKeys, C::N, 5, 0, kk, kk), sfa,
-                                         tmem_base + C::SFB_COL, kk > 0 ? 1u : 0u);
+                                         sfb, kk > 0 ? 1u : 0u);
                         }
                     } else {
 #pragma unroll
@@ -575,7 +650,8 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK, FP4K>::THREADS, 1)
             if (etid < C::N) {
                 const int rl = etid / H;
                 const size_t o = (size_t)(ui.t0 + rl) * H + (etid % H);
-                const float cv = rl < ui.nr ? p.w[o] * p.s_q[o] : 0.0f;
+                // (e2m1 queries: their scales are inside the MMA)
+                const float cv = rl < ui.nr ? (FP4Q ? p.w[o] : p.w[o] * p.s_q[o]) : 0.0f;
                 cbuf[etid] = (etid & 1) ? cv * 33554432.0f : cv;
             }
             if constexpr (C::STREAM) {
@@ -1134,11 +1210,11 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK, FP4K>::THREADS, 1)
         tmem_dealloc(tmem_base, 512);
 }
 
-template <int H, int D, int SINK, bool MASK, bool FP4K>
+template <int H, int D, int SINK, bool MASK, int OPS>
 cudaError_t launch_one(const LogitsParams& p, int grid, cudaStream_t stream)
 {
-    using C = Cfg<H, D, SINK, FP4K>;
-    auto kern = logits_tc_kernel<H, D, SINK, MASK, FP4K>;
+    using C = Cfg<H, D, SINK, OPS>;
+    auto kern = logits_tc_kernel<H, D, SINK, MASK, OPS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);
     if (e != cudaSuccess)
@@ -1146,27 +1222,27 @@ cudaError_t launch_one(const LogitsParams& p, int grid, cudaStream_t stream)
     return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM, stream, p);
 }
 
-template <int H, int D, bool FP4K = false>
+template <int H, int D, int OPS = kOpsE4M3>
 cudaError_t launch_sink(const LogitsParams& p, int sink, int grid, cudaStream_t stream)
 {
     // masked launches: the consumer's key paths (samples, fixed threshold, stream);
     // the candidate producer itself is never masked
     const bool m = p.cand_mask != nullptr;
     if (sink == kSinkLogits)
-        return m ? launch_one<H, D, kSinkLogits, true, FP4K>(p, grid, stream)
-                 : launch_one<H, D, kSinkLogits, false, FP4K>(p, grid, stream);
+        return m ? launch_one<H, D, kSinkLogits, true, OPS>(p, grid, stream)
+                 : launch_one<H, D, kSinkLogits, false, OPS>(p, grid, stream);
     if (sink == kSinkStream)
-        return m ? launch_one<H, D, kSinkStream, true, FP4K>(p, grid, stream)
-                 : launch_one<H, D, kSinkStream, false, FP4K>(p, grid, stream);
+        return m ? launch_one<H, D, kSinkStream, true, OPS>(p, grid, stream)
+                 : launch_one<H, D, kSinkStream, false, OPS>(p, grid, stream);
     if (sink == kSinkFilter)
-        return m ? launch_one<H, D, kSinkFilter, true, FP4K>(p, grid, stream)
-                 : launch_one<H, D, kSinkFilter, false, FP4K>(p, grid, stream);
+        return m ? launch_one<H, D, kSinkFilter, true, OPS>(p, grid, stream)
+                 : launch_one<H, D, kSinkFilter, false, OPS>(p, grid, stream);
     if (m)
         return cudaErrorInvalidValue;
     if (sink == kSinkPool)
-        return launch_one<H, D, kSinkPool, false, FP4K>(p, grid, stream);
+        return launch_one<H, D, kSinkPool, false, OPS>(p, grid, stream);
     if (sink == kSinkPoolFilter)
-        return launch_one<H, D, kSinkPoolFilter, false, FP4K>(p, grid, stream);
+        return launch_one<H, D, kSinkPoolFilter, false, OPS>(p, grid, stream);
     return cudaErrorInvalidValue;
 }
 
@@ -1177,16 +1253,21 @@ bool logits_fp4_native(int H, int D) { return H == 32 && D == 128; }
 int logits_rows_per_group(int H, bool fp4_keys)
 {
     if (fp4_keys && logits_fp4_native(H, 128))
-        return Cfg<32, 128, kSinkFilter, true>::G;
+        return Cfg<32, 128, kSinkFilter, kOpsE2M1K>::G;
     return H >= 16 ? kTileN / H : 16;
 }
 
 cudaError_t launch_logits(const LogitsParams& p, int H, int D, int sink, int grid,
                           cudaStream_t stream)
 {
-    if (p.k_sf != nullptr)
-        return (H == 32 && D == 128) ? launch_sink<32, 128, true>(p, sink, grid, stream)
+    if (p.k_sf != nullptr && p.q_sf != nullptr)
+        return (H == 32 && D == 128) ? launch_sink<32, 128, kOpsE2M1>(p, sink, grid, stream)
                                      : cudaErrorInvalidValue;
+    if (p.k_sf != nullptr)
+        return (H == 32 && D == 128) ? launch_sink<32, 128, kOpsE2M1K>(p, sink, grid, stream)
+                                     : cudaErrorInvalidValue;
+    if (p.q_sf != nullptr)
+        return cudaErrorInvalidValue;
     if (H == 32 && D == 128)
         return launch_sink<32, 128>(p, sink, grid, stream);
     if (H == 16 && D == 128)

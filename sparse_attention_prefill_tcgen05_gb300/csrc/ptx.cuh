@@ -232,6 +232,22 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, ui
         : "memory");
 }
 
+// Block-scaled fp4 x fp4, kind::mxf4: both operands packed e2m1 (two codes a byte,
+// K = 64 per MMA), one ue8m0 scale per row and 32-element K block, two blocks per MMA
+// (scale_vec::2X): the scale IDs select bytes {0,1} or {2,3} of each 32-bit cell.
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, "
+        "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Copy 128 rows x 128 bits from shared memory (no-swizzle canonical layout, row r at
 // byte 16 r) into TMEM: row r lands in lane r, four 32-bit columns.  Asynchronous,
 // ordered with the tcgen05.mma this thread issues after it.
@@ -352,6 +368,14 @@ __host__ __device__ constexpr uint32_t idesc_mxf8f6f4(int M, int N, int a_fmt, i
            (static_cast<uint32_t>(b_fmt) << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
            (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) |
            (static_cast<uint32_t>(a_sf_id & 3) << 29);
+}
+
+// Instruction descriptor, kind::mxf4 with ue8m0 scales: the same fields, e2m1 coded 1
+// for both operands (the only format of this kind), dense K = 64 (bit 31 clear).  The
+// scale IDs of scale_vec::2X are 0 or 2.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, int a_sf_id, int b_sf_id)
+{
+    return idesc_mxf8f6f4(M, N, 1, 1, a_sf_id, b_sf_id);
 }
 
 // ReLU on the FMA pipe, scaled by 2^-25: sat(x * 2^-25) clamps to [0, 1],

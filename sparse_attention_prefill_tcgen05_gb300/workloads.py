@@ -242,6 +242,16 @@ def make_problem(spec: ProblemSpec) -> Problem:
             else:
                 k = torch.randint(0, 256, (L_r, D // 2), generator=gen).to(torch.uint8)
                 s_k = torch.randint(124, 131, (L_r, D // 32), generator=gen).to(torch.uint8)
+            if spec.qdtype == "fp4":
+                # e2m1 codes of magnitude <= 1.5 (codes 0-3 and 8-11) and block exponents
+                # 126..128: with the keys above, every product, block sum and head sum is
+                # a short dyadic number, exact in fp32 in any order
+                codes = (torch.randint(0, 4, (T_r, H, D), generator=gen) |
+                         (torch.randint(0, 2, (T_r, H, D), generator=gen) << 3))
+                q4s.append((codes[..., 0::2] | (codes[..., 1::2] << 4)).to(torch.uint8))
+                qsfs.append(torch.randint(126, 129, (T_r, H, D // 32),
+                                          generator=gen).to(torch.uint8))
+                q, s_q = torch.zeros((T_r, H, D), dtype=torch.uint8), torch.ones((T_r, H))
             qs.append(q); sqs.append(s_q); ws.append(w); ks.append(k); kss.append(s_k)
         else:
             qf = torch.randn((T_r, H, D), generator=gen)

@@ -21,17 +21,25 @@ LOGIT_RTOL = 1e-3
 
 
 def device_inputs(p, layer=1, dev="cuda"):
+    """The call's inputs on the device.  e2m1 queries (qdtype "fp4", first layer) go in as
+    their packed codes, with their ue8m0 block scales in the s_q slot."""
     q, s_q, w = (p.q, p.s_q, p.w) if layer == 1 else (p.q2, p.s_q2, p.w2)
+    if layer == 1 and p.spec.qdtype == "fp4":
+        q, s_q = p.q4, p.q_sf
     return dict(q=q.to(dev), s_q=s_q.to(dev), w=w.to(dev), k=p.k.to(dev),
                 k_scale=p.k_scale.to(dev), compress_len=p.compress_len.to(dev))
 
 
-def make_plan(p, key_block=0, budget=0, topk=None, select_mode=K.IDX_SELECT_AUTO):
+def make_plan(p, key_block=0, budget=0, topk=None, select_mode=K.IDX_SELECT_AUTO,
+              qdtype=None):
     kd = K.IDX_K_FP8_E4M3 if p.spec.kdtype == "fp8" else K.IDX_K_FP4_E2M1_UE8M0
+    if qdtype is None:
+        qdtype = K.IDX_Q_FP4_E2M1_UE8M0 if p.spec.qdtype == "fp4" else K.IDX_Q_FP8_E4M3
     return K.indexer_plan(p.cu_seqlens_q, p.cu_seqlens_k, p.compress_len, p.H, p.D,
                           topk or p.topk, kdtype=kd, cand_block=p.spec.cand_block,
                           cand_topk=p.spec.cand_topk, key_block=key_block,
-                          transient_budget_bytes=budget, select_mode=select_mode)
+                          transient_budget_bytes=budget, select_mode=select_mode,
+                          qdtype=qdtype)
 
 
 def workspace(plan, dev="cuda"):

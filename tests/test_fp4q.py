@@ -1,6 +1,8 @@
 """fp4 x fp4 (e2m1 + ue8m0/32 queries and keys): the oracle's fp4-query mode pinned
-against the fp8 oracle on equal values and against exact rationals (CPU); the exact
-conversion kernel and the full path against the oracle (GPU)."""
+against the fp8 oracle on equal values and against exact rationals (CPU); plans for e2m1
+queries (CPU); the exact conversion kernel and the conversion route against the oracle
+(GPU).  The native route (the block-scaled fp4 MMA) is checked with the other parity
+cases."""
 import dataclasses
 from fractions import Fraction
 
@@ -90,7 +92,8 @@ def test_convert_fp4_is_exact():
 
 @pytest.mark.gpu
 def test_fp4_queries_and_keys_end_to_end():
-    """Convert q on the GPU, then the fp4-key logits and fused top-k, against the oracle."""
+    """The conversion route (for head counts without the fp4 MMA kind): convert q on the
+    GPU, then the fp4-key logits and fused top-k, against the oracle."""
     p = _fp4q_problem()
     T, H, D = p.q.shape
     d = Hp.device_inputs(p)
@@ -101,7 +104,7 @@ def test_fp4_queries_and_keys_end_to_end():
                           q8, s_q, ws)
     assert K.indexer_status(None, ws) == K.IDX_OK
     d["q"], d["s_q"] = q8.reshape(T, H, D), s_q.reshape(T, H)
-    plan = Hp.make_plan(p)
+    plan = Hp.make_plan(p, qdtype=K.IDX_Q_FP8_E4M3)
     ref = O.problem_logits_fp4q(p)
     g = Hp.gpu_logits(p, plan, d).cpu().numpy()
     Hp.check_logits(g, ref)
@@ -110,3 +113,22 @@ def test_fp4_queries_and_keys_end_to_end():
     cl = p.compress_len.numpy()
     for t in range(T):
         Hp.check_topk_row(fi[t], ref[t], int(cl[t]), p.topk)
+
+
+def _tiny_plan(qdtype, kdtype=K.IDX_K_FP4_E2M1_UE8M0, H=32, D=128):
+    cu_q = torch.tensor([0, 4], dtype=torch.int32)
+    cu_k = torch.tensor([0, 300], dtype=torch.int32)
+    clen = torch.tensor([100, 200, 300, 300], dtype=torch.int32)
+    return K.indexer_plan(cu_q, cu_k, clen, H, D, 8, kdtype=kdtype, qdtype=qdtype)
+
+
+def test_plans_for_fp4_queries():
+    """e2m1 queries plan with e2m1 keys and 32 heads of 128; other pairings are refused."""
+    assert _tiny_plan(K.IDX_Q_FP4_E2M1_UE8M0).workspace_bytes > 0
+    for bad in ({"kdtype": K.IDX_K_FP8_E4M3}, {"H": 16}, {"H": 8, "D": 64}):
+        with pytest.raises(K.IndexerError) as e:
+            _tiny_plan(K.IDX_Q_FP4_E2M1_UE8M0, **bad)
+        assert e.value.code == K.IDX_ERR_UNSUPPORTED, bad
+    with pytest.raises(K.IndexerError) as e:
+        _tiny_plan(7)
+    assert e.value.code == K.IDX_ERR_INVALID_ARG

@@ -30,6 +30,8 @@ def small(name, rows_div, keys_div, topk=None, **over):
 
 
 def oracle_rows(p, rows, layer=1):
+    if layer == 1 and p.spec.qdtype == "fp4":
+        return O.problem_logits_fp4q(p, rows)
     return O.problem_logits(p, rows, layer=layer)
 
 
@@ -175,6 +177,61 @@ def test_fp4_keys_other_head_counts_parity():
     spec = W.ProblemSpec("H=16 fp4", (W.RequestSpec(40, 3000, 2),), H=16, D=128, topk=48,
                          kdtype="fp4", seed=52)
     check_all(W.make_problem(spec), key_block=1024)
+
+
+def test_fp4_queries_and_keys_scaled_parity():
+    """e2m1 queries x e2m1 keys, one ue8m0 scale per 32 elements on both sides, through the
+    block-scaled fp4 MMA (neither operand converted) against the oracle's fp4-query mode:
+    logits element by element, top-k against the oracle and against the oracle's selector on
+    the GPU's own logits, both selection strategies bit-identical."""
+    p = small("v4fp4qk", 16, 32, topk=64)
+    check_all(p, key_block=1024)
+
+
+def test_fp4_queries_exact_arithmetic_inputs_are_bit_exact():
+    spec = dataclasses.replace(W.scaled(W.CONFIGS["v4fp4qk"], 32, 64), topk=50, exact=True)
+    p = W.make_problem(spec)
+    T = int(p.cu_seqlens_q[-1])
+    # the premise: per (row, key) the sum over heads of w * sum_d |q k| stays below
+    # 2^15 while every term is a multiple of 2^-9, so fp32 holds every partial sum exactly
+    qv = O.decode_fp4(p.q4.numpy(), p.q_sf.numpy())
+    kv = O.decode_fp4(p.k.numpy(), p.k_scale.numpy())
+    bound = np.einsum("th,thl->tl", p.w.numpy().astype(np.float64),
+                      np.einsum("thd,ld->thl", np.abs(qv), np.abs(kv)))
+    assert bound.max() < 2.0 ** 15
+    plan = Hp.make_plan(p, key_block=512)
+    d = Hp.device_inputs(p)
+    ref = oracle_rows(p, np.arange(T))
+    g = Hp.gpu_logits(p, plan, d).cpu().numpy().astype(np.float64)
+    assert np.array_equal(g, ref)
+    fi, _ = Hp.gpu_fused(p, plan, d)
+    want = O.topk_rows(ref, p.compress_len.numpy(), p.topk)
+    fi = fi.cpu().numpy()
+    for t in range(T):
+        assert sorted(fi[t][fi[t] >= 0].tolist()) == sorted(want[t][want[t] >= 0].tolist())
+
+
+def test_fp4_queries_and_keys_with_widely_spread_block_scales_match_the_oracle():
+    """A query vector and a key whose block scales are 2^20 and 2^10 apart, with small codes
+    in the small blocks (neither has an exact e4m3 form under one scale per vector): the
+    fp4 MMA applies every block's scale itself, so both are scored like any other."""
+    p = _wide_scale_key(small("v4fp4qk", 64, 256, topk=16))
+    q4, qsf = p.q4.clone(), p.q_sf.clone()
+    qsf[0, 0, 0] = 127 + 10
+    qsf[0, 0, 1] = 127 - 10
+    q4[0, 0, 16] = 0x11                   # elements 32, 33 (block 1): code 1 = 0.5
+    p = dataclasses.replace(p, q4=q4, q_sf=qsf)
+    plan = Hp.make_plan(p)
+    d = Hp.device_inputs(p)
+    T = int(p.cu_seqlens_q[-1])
+    ref = oracle_rows(p, np.arange(T))
+    g = Hp.gpu_logits(p, plan, d).cpu().numpy()
+    Hp.check_logits(g, ref)
+    fi, _ = Hp.gpu_fused(p, plan, d)
+    fi = fi.cpu().numpy()
+    cl = p.compress_len.numpy()
+    for t in range(T):
+        Hp.check_topk_row(fi[t], ref[t], int(cl[t]), p.topk)
 
 
 def test_exact_arithmetic_inputs_are_bit_exact():
@@ -456,6 +513,10 @@ def test_full_cold_chunk_t2048_l65536_top2048():
 
 def test_full_v4_low_ratio_fp4_t2048_l100000_top512():
     full_size_check("v4ratio2")
+
+
+def test_full_v4_fp4_queries_and_keys_t2048_l100000_top512():
+    full_size_check("v4fp4qk")
 
 
 def test_full_long_context_t16384_l487936_top512():
