@@ -373,11 +373,15 @@ def main():
     dev = torch.device("cuda", torch.cuda.current_device())
     p = W.make_problem(spec)
     kd = K.IDX_K_FP8_E4M3 if spec.kdtype == "fp8" else K.IDX_K_FP4_E2M1_UE8M0
+    qd = K.IDX_Q_FP4_E2M1_UE8M0 if spec.qdtype == "fp4" else K.IDX_Q_FP8_E4M3
     plan = K.indexer_plan(p.cu_seqlens_q, p.cu_seqlens_k, p.compress_len, p.H, p.D, p.topk,
                           kdtype=kd, cand_block=spec.cand_block, cand_topk=spec.cand_topk,
-                          key_block=spec.key_block)
+                          key_block=spec.key_block, qdtype=qd)
     T = int(p.cu_seqlens_q[-1])
-    host = dict(q=p.q, s_q=p.s_q, w=p.w, k=p.k, k_scale=p.k_scale, compress_len=p.compress_len)
+    # e2m1 queries: the packed codes, and their ue8m0 block scales in the s_q slot
+    q_in, s_q_in = (p.q4, p.q_sf) if spec.qdtype == "fp4" else (p.q, p.s_q)
+    host = dict(q=q_in, s_q=s_q_in, w=p.w, k=p.k, k_scale=p.k_scale,
+                compress_len=p.compress_len)
     d = {n: t.to(dev) for n, t in host.items()}
     idx = torch.empty((T, p.topk), dtype=torch.int32, device=dev)
     val = torch.empty((T, p.topk), dtype=torch.float32, device=dev)
