@@ -175,6 +175,9 @@ int indexer_plan_info(indexer_plan_t plan, int32_t* key_block, int32_t* row_chun
  *   logits   float [T, ld], ld >= the largest key count of the batch;
  *            logits[t, j] for j < compress_len[t], -inf for the rest of the row
  * ws/ws_bytes: the plan's workspace (256-byte aligned).
+ * Range: every head's score (its fp32 dot product, block scales included) is applied
+ * exactly for 2^-62 <= |S| < 2^64 (smaller ones keep an absolute error below 2^-150
+ * times the head weight), with |w * s_q| < 2^64.
  */
 int indexer_logits(indexer_plan_t plan, const void* q, const float* s_q, const float* w,
                    const void* k, const void* k_scale, const int32_t* compress_len,

@@ -644,7 +644,7 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK, OPS>::THREADS, 1)
             const UnitInfo ui = decode_unit<C::G>(p, u, lane);
             const Segment sg = p.seg[ui.seg];   // by value: loop-invariant registers
             // head weights c[n] = w * s_q of column n = row * H + head; odd columns
-            // carry 2^25 (their relu is a saturating multiply by 2^-25).  Double
+            // carry 2^64 (their relu is a saturating multiply by 2^-64).  Double
             // buffered by unit: the other half may still read the previous one.
             float* cbuf = c_s + (it & 1) * kTileN;
             if (etid < C::N) {
@@ -652,7 +652,7 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK, OPS>::THREADS, 1)
                 const size_t o = (size_t)(ui.t0 + rl) * H + (etid % H);
                 // (e2m1 queries: their scales are inside the MMA)
                 const float cv = rl < ui.nr ? (FP4Q ? p.w[o] : p.w[o] * p.s_q[o]) : 0.0f;
-                cbuf[etid] = (etid & 1) ? cv * 33554432.0f : cv;
+                cbuf[etid] = (etid & 1) ? cv * 18446744073709551616.0f : cv;
             }
             if constexpr (C::STREAM) {
                 for (int i = etid; i < C::G * 512; i += C::EPI * 32)
@@ -807,8 +807,8 @@ __global__ void __launch_bounds__(Cfg<H, D, SINK, OPS>::THREADS, 1)
                         tc_fence_after();
                         // partial sums [row][block][lane g or g+8], two heads per packed
                         // FMA: relu by max (ALU pipe) for column 2q, by a saturating
-                        // multiply with 2^-25 (FMA pipe) for column 2q + 1, whose weight
-                        // carries 2^25; every product and sum is bit-identical to
+                        // multiply with 2^-64 (FMA pipe) for column 2q + 1, whose weight
+                        // carries 2^64; every product and sum is bit-identical to
                         // fmaf(c, max(S, 0), part).
                         // (the list sinks start every accumulator with the first product of
                         // its chunk, equal to fmaf(c, max(S, 0), 0) up to the sign of a zero;

@@ -378,14 +378,16 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, int a_sf_id, int
     return idesc_mxf8f6f4(M, N, 1, 1, a_sf_id, b_sf_id);
 }
 
-// ReLU on the FMA pipe, scaled by 2^-25: sat(x * 2^-25) clamps to [0, 1],
-// which equals max(x, 0) * 2^-25 exactly whenever |x| < 2^25 (scaling by a
-// power of two is exact at these magnitudes).  FMNMX runs on the ALU pipe at
-// half the FMA rate, so the epilogue spreads its ReLUs over both pipes.
+// ReLU on the FMA pipe, scaled by 2^-64: sat(x * 2^-64) clamps to [0, 1], which equals
+// max(x, 0) * 2^-64 exactly whenever 2^-62 <= |x| < 2^64 (scaling by a power of two is
+// exact there; below, the scaled value is subnormal and keeps an absolute error under
+// 2^-150).  e4m3 x e4m3 scores lie in [2^-18, D * 448^2] when not zero; block-scaled e2m1
+// scores carry their block scales and can be far larger, hence the wide margin.  FMNMX
+// runs on the ALU pipe at half the FMA rate, so the epilogue spreads its ReLUs over both.
 __device__ __forceinline__ float relu_scaled(float x)
 {
     float r;
-    asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(r) : "f"(x), "f"(2.98023223876953125e-08f));
+    asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(r) : "f"(x), "f"(5.42101086242752217e-20f));
     return r;
 }
 

@@ -155,6 +155,36 @@ def test_fp4_keys_with_widely_spread_block_scales_match_the_oracle():
         Hp.check_topk_row(fi[t], ref[t], int(cl[t]), p.topk)
 
 
+@pytest.mark.parametrize("name", ["v4ratio2", "v4fp4qk"])
+def test_fp4_scores_far_above_the_fp8_range_match_the_oracle(name):
+    """Block scales put a few keys' scores above 2^29, far beyond anything e4m3 x e4m3 can
+    reach (D * 448^2 < 2^25); the epilogue's ReLU must still be exact on every head
+    column (logits element by element, and those keys at the top of every row)."""
+    p = small(name, 64, 256, topk=16)
+    ks = p.k_scale.clone()
+    ks[:48] = (ks[:48].to(torch.int32) + 24).clamp(max=254).to(torch.uint8)
+    p = dataclasses.replace(p, k_scale=ks)
+    T = int(p.cu_seqlens_q[-1])
+    ref = oracle_rows(p, np.arange(T))
+    # the raw scores the MMA accumulates: query codes (e4m3 values, or e2m1 with their
+    # block scales) against the keys' block-scaled values
+    if p.spec.qdtype == "fp4":
+        qv = O.decode_fp4(p.q4.numpy(), p.q_sf.numpy())
+    else:
+        qv = np.array([O.e4m3_value(b) for b in range(256)])[p.q.numpy()]
+    kv = O.decode_fp4(p.k.numpy(), ks.numpy())
+    assert np.abs(np.einsum("thd,ld->thl", qv[:4], kv[:48])).max() > 2.0 ** 25
+    plan = Hp.make_plan(p)
+    d = Hp.device_inputs(p)
+    g = Hp.gpu_logits(p, plan, d).cpu().numpy()
+    Hp.check_logits(g, ref)
+    fi, _ = Hp.gpu_fused(p, plan, d)
+    fi = fi.cpu().numpy()
+    cl = p.compress_len.numpy()
+    for t in range(T):
+        Hp.check_topk_row(fi[t], ref[t], int(cl[t]), p.topk)
+
+
 def test_fp4_key_outside_the_e4m3_range_is_reported_by_the_conversion():
     """Head counts without a block-scaled kernel (16 heads here) score e2m1 keys through
     their exact e4m3 form; a key that has none is reported as IDX_ERR_DEVICE_CHECK
