@@ -6,14 +6,15 @@
 // about 1.7 k of its entries; those fit in shared memory, so the exact selection of a
 // row needs no global lists and no second kernel.  One persistent CTA per SM, three
 // roles:
-//   warp 0        producer: takes rows in order from a global counter and streams each
-//                 row through a ring of three 32 KB stages with bulk copies;
-//   warps 1..16   filter: each warp takes its 1/16 of every stage; a lane tests its 16
+//   warp 0        producer: takes rows in order from a global counter (the next row's
+//                 number, length and thresholds read while the current row streams) and
+//                 streams each row through a ring of three 32 KB stages with bulk copies;
+//   warps 1..8    filter: each warp takes its 1/8 of every stage; a lane tests its 32
 //                 values against tau, and the warp appends the passing ones (positions
 //                 from a warp prefix sum of the lanes' counts, values read again from
 //                 the stage) to its own region of the row's candidate buffer (two
 //                 buffers, rows alternate); the warps never wait for one another;
-//   warps 17..24  select: the exact top-k of a full buffer (2048 equal-width value
+//   warps 9..16   select: the exact top-k of a full buffer (2048 equal-width value
 //                 buckets from tau to the row's largest sample, larger values in the top
 //                 one; the bucket holding the k-th entry, its entries ranked directly, a
 //                 bitmap of the kept keys, their positions by a prefix sum) written in
@@ -29,15 +30,17 @@
 namespace idx {
 namespace {
 
-constexpr int kFiltWarps = 16;
+// (more filter or select warps measured slower: the selection is bound by the latency
+// of its shared-memory passes, and extra warps only take issue slots from it)
+constexpr int kFiltWarps = 8;
 constexpr int kSelWarps = 8;
-constexpr int kFiltThreads = 32 * kFiltWarps;              // 512
+constexpr int kFiltThreads = 32 * kFiltWarps;              // 256
 constexpr int kSelThr = 32 * kSelWarps;                    // 256
-constexpr int kRtThreads = 32 + kFiltThreads + kSelThr;    // 800
+constexpr int kRtThreads = 32 + kFiltThreads + kSelThr;    // 544
 constexpr int kChunk = 8192;                               // floats per ring stage (32 KB)
 constexpr int kStages = 3;                                 // (a larger stage count does not fit)
 constexpr int kF4 = kChunk / (4 * kFiltThreads);           // float4 per filter lane per stage
-constexpr int kRegion = 256;                               // candidates per filter warp
+constexpr int kRegion = 512;                               // candidates per filter warp
 constexpr int kSpill = 1024;                               // shared by the warps, after their own
 constexpr int kCand = kFiltWarps * kRegion + kSpill;       // per buffer
 constexpr int kRtBuckets = 2048;
@@ -55,7 +58,17 @@ struct StageMeta {
     int32_t nfl;     // valid floats in the stage
     int32_t last;    // the row's last chunk
     int32_t keys;    // keys of the row's request
-    int32_t pad_[3];
+    uint32_t tau;    // the row's sampled threshold (ord of a score)
+    uint32_t smax;   // the row's largest sample (ord of a score)
+    int32_t pad_;
+};
+
+// What the producer knows of a row before streaming it.
+struct RowInfo {
+    int t;           // global row (>= total_rows: no more rows)
+    int keys;        // keys of its request
+    int n;           // keys streamed (its causal length, clamped)
+    uint32_t tau, smax;
 };
 
 // A full candidate buffer, as the select warps find it (written by filter warp 0).
@@ -63,7 +76,7 @@ struct RowSlot {
     int32_t t;
     int32_t keys;
     uint32_t tau;
-    int32_t pad_;
+    uint32_t smax;
 };
 
 // shared memory carve-up (bytes from a 128-byte aligned base)
@@ -144,7 +157,6 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
     uint32_t* wsum = reinterpret_cast<uint32_t*>(smem + kOffMisc);        // [kSelWarps]
     uint32_t* bcast = wsum + kSelWarps;                                   // [4]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bcast + 4);
-    uint64_t* cut_s = reinterpret_cast<uint64_t*>(smem + kOffMisc + 56);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -190,13 +202,34 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                 ph ^= 1;
             }
         };
-        while (ok) {
-            const int t = static_cast<int>(atomicAdd(p.row_counter, 1u));
-            if (t >= p.total_rows)
-                break;
-            const int r = rt_request(p, t);
-            const int keys = p.req_key_count[r];
-            const int n = max(0, min(p.compress_len[t], keys));
+        // A row's number, length and threshold come from a chain of dependent global
+        // reads; the next row's chain runs while the current row's first stages stream,
+        // so the ring does not drain at row boundaries.
+        auto row_info = [&](int t) {
+            RowInfo ri;
+            ri.t = t;
+            ri.keys = 0;
+            ri.n = 0;
+            ri.tau = 0;
+            ri.smax = 0;
+            if (t < p.total_rows) {
+                const int r = rt_request(p, t);
+                ri.keys = p.req_key_count[r];
+                ri.n = max(0, min(p.compress_len[t], ri.keys));
+                ri.tau = p.tau_row[t];
+                ri.smax = p.smax_row[t];
+            }
+            return ri;
+        };
+        RowInfo cur = row_info(static_cast<int>(atomicAdd(p.row_counter, 1u)));
+        while (ok && cur.t < p.total_rows) {
+            const int t = cur.t;
+            const int keys = cur.keys;
+            const int n = cur.n;
+            // the next row's number, taken now; its reads are issued after this row's
+            // first stage
+            const int t_next = static_cast<int>(atomicAdd(p.row_counter, 1u));
+            RowInfo nxt = {p.total_rows, 0, 0, 0u, 0u};
             const float* row = p.logits + (int64_t)t * p.ld;
             const int nchunks = max(1, (n + kChunk - 1) / kChunk);
             for (int c = 0; c < nchunks && ok; ++c) {
@@ -209,6 +242,8 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                 m.nfl = max(nfl, 0);
                 m.last = c == nchunks - 1;
                 m.keys = keys;
+                m.tau = cur.tau;
+                m.smax = cur.smax;
                 if (nfl > 0) {
                     // whole 16-byte groups: ld is a multiple of 4, so the group holding
                     // the row's last key is inside the row
@@ -220,7 +255,12 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                 }
                 ++uses[s];
                 advance();
+                if (c == 0)
+                    nxt = row_info(t_next);
             }
+            if (!ok)
+                break;
+            cur = nxt;
         }
         if (ok && next_stage()) {
             meta[s].t = -1;   // no more rows
@@ -238,8 +278,8 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
 
     if (warp <= kFiltWarps) {
         // -------------------------------------------------------------- filter
-        // thread ft takes float4 ft + 512 u (u < kF4) of every stage, so warp fw covers
-        // floats [128 fw, 128 fw + 128) of every 2048; decisions are per warp
+        // thread ft takes float4 ft + 256 u (u < kF4) of every stage, so warp fw covers
+        // floats [128 fw, 128 fw + 128) of every 1024; decisions are per warp
         const int fw = warp - 1;
         const int ft = threadIdx.x - 32;
         int s = 0, ph = 0, b = 0, bph = 0;
@@ -270,7 +310,7 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                     }
                     break;
                 }
-                const uint32_t tau = p.tau_row[m.t];
+                const uint32_t tau = m.tau;
                 // at or above tau as a float: every v whose ord is at least tau (and
                 // -0.0 against +0.0, harmless); tau = 0 keeps every finite entry
                 tauf = tau > kOrdNegInf ? ord2f(tau) : -3.402823466e38f;
@@ -279,6 +319,7 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                     slot[b].t = m.t;
                     slot[b].keys = m.keys;
                     slot[b].tau = tau;
+                    slot[b].smax = m.smax;
                 }
             }
             const float* stage = ring + (size_t)s * kChunk;
@@ -391,16 +432,28 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
         };
         // f(e) for every candidate: select warp sw walks the regions sw, sw + 8, ... with
         // all of its lanes, then all select threads share the spill area
+        // f(e, entry e) for every candidate: select warp sw walks the regions sw, sw + 8,
+        // ... with all of its lanes, then all select threads share the spill area; each
+        // thread loads four entries before it works on any of them
         auto each_cand = [&](auto&& f) {
+            auto walk = [&](const int base, const int n, int i0, const int step) {
+                for (; i0 < n; i0 += 4 * step) {
+                    uint2 en[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        en[u] = cb[base + min(i0 + u * step, n - 1)];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (i0 + u * step < n)
+                            f(base + i0 + u * step, en[u]);
+                }
+            };
             const int sw = st >> 5, sln = st & 31;
 #pragma unroll 1
-            for (int w = sw; w < kFiltWarps; w += kSelWarps) {
-                const int n = static_cast<int>(min(rc[w], static_cast<uint32_t>(kRegion)));
-                for (int i = sln; i < n; i += 32)
-                    f(w * kRegion + i);
-            }
-            for (int i = st; i < spilled; i += kSelThr)
-                f(kFiltWarps * kRegion + i);
+            for (int w = sw; w < kFiltWarps; w += kSelWarps)
+                walk(w * kRegion, static_cast<int>(min(rc[w], static_cast<uint32_t>(kRegion))),
+                     sln, 32);
+            walk(kFiltWarps * kRegion, spilled, st, kSelThr);
         };
         if (overflow || (sl.tau > kOrdNegInf && total_c < k)) {
             // the candidates cannot decide the row: the direct kernel will
@@ -414,17 +467,23 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                 return (static_cast<uint64_t>(f2ord(__uint_as_float(en.x))) << 32) |
                        static_cast<uint32_t>(~(en.y & 0xFFFFu));
             };
-            // which candidates are kept: all of them (at most k), those above the
-            // boundary bucket plus the best of it, or (no bucket range, or a boundary
-            // bucket too large to rank directly) the radix threshold over the candidates
-            int mode = 0;   // 0 all, 1 buckets, 2 radix
-            uint32_t bnd = 0;
-            uint64_t cut = 0;
+            // which candidates are kept: all of them (at most k); those above the
+            // boundary bucket, with the whole boundary bucket or the best of it; or (no
+            // bucket range, or a boundary bucket too large to rank directly) the radix
+            // threshold over the candidates
+            int mode = 0;   // 0 all, 1 buckets down to the boundary one, 2 radix,
+                            // 3 buckets above the boundary one plus its best `need`
+            uint32_t bnd = 0, need = 0, bsize = 0;
             CompositeThr thr{0u, 0u, 0u, 0u};
+            float bvmin = 0.0f, bscale = 0.0f;
+            // a candidate's value bucket (the same arithmetic in every pass)
+            auto bucket_of = [&](const uint32_t vbits) {
+                return static_cast<uint32_t>(min(kRtBuckets - 1, static_cast<int>(
+                    __fmul_rn(__fsub_rn(__uint_as_float(vbits), bvmin), bscale))));
+            };
             if (total_c > k) {
                 mode = 2;
-                const uint32_t smax = p.smax_row[t];
-                float bvmin = 0.0f, bscale = 0.0f;
+                const uint32_t smax = sl.smax;
                 bool bucketed = false;
                 if (sl.tau > kOrdNegInf && smax > sl.tau) {
                     bvmin = ord2f(sl.tau);
@@ -434,16 +493,12 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                     bucketed = bscale > 0.0f && bscale < INFINITY;
                 }
                 if (bucketed) {
-                    // value buckets: counted, and kept in the upper 16 bits of the key
+                    // value buckets, counted
                     for (int i = st; i < kRtBuckets / 4; i += kSelThr)
                         reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
                     bar_all(true, kBarSel, kSelThr);
-                    each_cand([&](const int e) {
-                        const uint2 en = cb[e];
-                        const uint32_t bk = static_cast<uint32_t>(min(kRtBuckets - 1, static_cast<int>(
-                            __fmul_rn(__fsub_rn(__uint_as_float(en.x), bvmin), bscale))));
-                        atomicAdd(&hist[bk], 1u);
-                        cb[e].y = (en.y & 0xFFFFu) | (bk << 16);
+                    each_cand([&](const int, const uint2 en) {
+                        atomicAdd(&hist[bucket_of(en.x)], 1u);
                     });
                     bar_all(true, kBarSel, kSelThr);
                     // the bucket holding the k-th largest, from the top: thread i owns
@@ -472,33 +527,12 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                     }
                     bar_all(true, kBarSel, kSelThr);
                     bnd = bcast[0];
-                    const uint32_t need = bcast[1], bsize = bcast[2];
-                    if (bsize == need) {
+                    need = bcast[1];
+                    bsize = bcast[2];
+                    if (bsize == need)
                         mode = 1;   // the whole boundary bucket is kept
-                    } else if (bsize <= static_cast<uint32_t>(kRtBucketCands)) {
-                        uint64_t* bc = reinterpret_cast<uint64_t*>(wpre);   // free until the bitmap
-                        if (st == 0)
-                            bcast[3] = 0;
-                        bar_all(true, kBarSel, kSelThr);
-                        each_cand([&](const int e) {
-                            const uint2 en = cb[e];
-                            if ((en.y >> 16) == bnd)
-                                bc[atomicAdd(&bcast[3], 1u)] = comp(en);
-                        });
-                        bar_all(true, kBarSel, kSelThr);
-                        // the need-th largest: the one with exactly need - 1 above it
-                        for (int i = st; i < static_cast<int>(bsize); i += kSelThr) {
-                            const uint64_t mine = bc[i];
-                            uint32_t rank = 0;
-                            for (int x = 0; x < static_cast<int>(bsize); ++x)
-                                rank += bc[x] > mine;
-                            if (rank == need - 1)
-                                *cut_s = mine;
-                        }
-                        bar_all(true, kBarSel, kSelThr);
-                        cut = *cut_s;
-                        mode = 1;
-                    }
+                    else if (bsize <= static_cast<uint32_t>(kRtBucketCands))
+                        mode = 3;   // its entries are collected with the bitmap and ranked
                 }
                 if (mode == 2) {
                     auto load = [&](int e, uint32_t& hi, uint32_t& lo) {
@@ -511,28 +545,50 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                     bar_all(true, kBarSel, kSelThr);   // (the radix scratch becomes the bitmap)
                 }
             }
-            auto kept = [&](const uint2 en) {
-                if (mode == 0)
-                    return true;
-                if (mode == 1) {
-                    const uint32_t bk = en.y >> 16;
-                    return bk > bnd || (bk == bnd && comp(en) >= cut);
-                }
-                return thr.kept(f2ord(__uint_as_float(en.x)), ~(en.y & 0xFFFFu));
-            };
-            // the kept keys as a bitmap, then their output positions in key order
+            // the kept keys as a bitmap (mode 3: the boundary bucket's entries are
+            // collected on the way, its best `need` added after), then their output
+            // positions in key order
+            uint64_t* bc = reinterpret_cast<uint64_t*>(wpre);   // free until the prefix sums
             const int nw = max((sl.keys + 31) / 32, 1);
             for (int w = st; w < nw; w += kSelThr)
                 bits[w] = 0;
+            if (st == 0)
+                bcast[3] = 0;
             bar_all(true, kBarSel, kSelThr);
-            each_cand([&](const int e) {
-                const uint2 en = cb[e];
-                if (kept(en)) {
+            each_cand([&](const int, const uint2 en) {
+                bool keep = true;
+                if (mode == 2) {
+                    keep = thr.kept(f2ord(__uint_as_float(en.x)), ~(en.y & 0xFFFFu));
+                } else if (mode != 0) {
+                    const uint32_t bk = bucket_of(en.x);
+                    keep = bk > bnd || (mode == 1 && bk == bnd);
+                    if (mode == 3 && bk == bnd) {
+                        const uint32_t x = atomicAdd(&bcast[3], 1u);
+                        if (x < static_cast<uint32_t>(kRtBucketCands))
+                            bc[x] = comp(en);
+                    }
+                }
+                if (keep) {
                     const uint32_t j = en.y & 0xFFFFu;
                     atomicOr(&bits[j >> 5], 1u << (j & 31));
                 }
             });
             bar_all(true, kBarSel, kSelThr);
+            if (mode == 3) {
+                // the boundary bucket's best `need`: the entries with fewer than `need`
+                // above them (composite keys are distinct)
+                for (int i = st; i < static_cast<int>(bsize); i += kSelThr) {
+                    const uint64_t mine = bc[i];
+                    uint32_t rank = 0;
+                    for (int x = 0; x < static_cast<int>(bsize); ++x)
+                        rank += bc[x] > mine;
+                    if (rank < need) {
+                        const uint32_t j = ~static_cast<uint32_t>(mine) & 0xFFFFu;
+                        atomicOr(&bits[j >> 5], 1u << (j & 31));
+                    }
+                }
+                bar_all(true, kBarSel, kSelThr);
+            }
             constexpr int kPerW = kRtWords / kSelThr;   // consecutive words per thread
             const int w0 = st * kPerW;
             uint32_t local = 0;
@@ -551,8 +607,7 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                 bcast[0] = run;   // kept entries
             bar_all(true, kBarSel, kSelThr);
             const int total = static_cast<int>(bcast[0]);
-            each_cand([&](const int e) {
-                const uint2 en = cb[e];
+            each_cand([&](const int, const uint2 en) {
                 const uint32_t j = en.y & 0xFFFFu;
                 const uint32_t word = bits[j >> 5];
                 if ((word >> (j & 31)) & 1u) {
