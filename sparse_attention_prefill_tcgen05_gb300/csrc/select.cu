@@ -315,9 +315,13 @@ __device__ __forceinline__ bool merge_row_verified(const StreamMergeParams& p, c
                static_cast<uint32_t>(~key_of(en));
     };
     uint64_t cut = 0;   // the whole boundary bucket is kept when it gives all of its entries
+    // rows of the bitmap path collect the boundary bucket's entries during the bitmap pass
+    const bool collect = packed && bsize != need;
     if (bsize != need) {
         if (bsize > static_cast<uint32_t>(kBucketCands))
             return false;
+    }
+    if (bsize != need && !packed) {
         for (int e = tid; e < n; e += kSelThreads) {
             const uint2 en = stage[e];
             if (bucket_of(en) == bnd)
@@ -378,18 +382,51 @@ __device__ __forceinline__ bool merge_row_verified(const StreamMergeParams& p, c
     for (int w = tid; w < nw; w += kSelThreads)
         bits[w] = 0;
     __syncthreads();
-    for (int e = tid; e < n; e += kSelThreads) {
-        const uint2 en = stage[e];
+    // f(staged entry) for every staged entry, four loaded before any is used
+    auto each_staged = [&](auto&& f) {
+        for (int e0 = tid; e0 < n; e0 += 4 * kSelThreads) {
+            uint2 en[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                en[u] = stage[min(e0 + u * kSelThreads, n - 1)];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (e0 + u * kSelThreads < n)
+                    f(en[u]);
+        }
+    };
+    // the kept keys: buckets above the boundary one, the whole boundary bucket when it
+    // gives all of its entries, else its entries collected (bcand lies past the bitmap,
+    // in the prefix area, which is written only after the ranking) and their best `need`
+    each_staged([&](const uint2 en) {
         const uint32_t b = en.y >> 16, j = en.y & 0xFFFFu;
-        if (b > bnd || (b == bnd && comp(en) >= cut))
+        if (b > bnd || (b == bnd && !collect))
             atomicOr(&bits[j >> 5], 1u << (j & 31));
-    }
+        else if (b == bnd) {
+            const int x = atomicAdd(&v_bcount, 1);
+            if (x < kBucketCands)
+                bcand[x] = comp(en);
+        }
+    });
     __syncthreads();
+    if (collect) {
+        // the entries with fewer than `need` above them (composite keys are distinct)
+        for (int i = tid; i < static_cast<int>(bsize); i += kSelThreads) {
+            const uint64_t mine = bcand[i];
+            uint32_t rank = 0;
+            for (int x = 0; x < static_cast<int>(bsize); ++x)
+                rank += bcand[x] > mine;
+            if (rank < need) {
+                const uint32_t j = ~static_cast<uint32_t>(mine) & 0xFFFFu;
+                atomicOr(&bits[j >> 5], 1u << (j & 31));
+            }
+        }
+        __syncthreads();
+    }
     const int total = bitmap_prefix(bits, wpre, nw, sh, v_total);
     int32_t* obi = reinterpret_cast<int32_t*>(dyn + merge_obuf_offset(n2));
     float* obv = reinterpret_cast<float*>(obi + n2);
-    for (int e = tid; e < n; e += kSelThreads) {
-        const uint2 en = stage[e];
+    each_staged([&](const uint2 en) {
         const uint32_t j = en.y & 0xFFFFu;
         const uint32_t word = bits[j >> 5];
         if ((word >> (j & 31)) & 1u) {
@@ -397,7 +434,7 @@ __device__ __forceinline__ bool merge_row_verified(const StreamMergeParams& p, c
             obi[pos] = static_cast<int32_t>(j);
             obv[pos] = __uint_as_float(en.x);
         }
-    }
+    });
     __syncthreads();
     for (int i = tid; i < p.k; i += kSelThreads) {
         const bool have = i < total;
