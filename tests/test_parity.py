@@ -438,6 +438,34 @@ def test_candidate_blocks_and_masked_consumer_scaled():
         assert np.array_equal(km[t], ((j < cl[t]) & (mask[t][j // 8] != 0)).astype(np.uint8))
 
 
+def test_fp4_queries_candidate_blocks_and_masked_call():
+    """e2m1 queries and keys on the fp4 MMA kind through the candidate path: the block
+    masks against the oracle (fp4-query mode) and against the oracle's block selector on
+    the GPU's own logits, then a masked fused call on the same queries against the oracle's
+    top-k within those blocks (short requests, and one long enough to be sampled)."""
+    spec = W.ProblemSpec("fp4 x fp4 candidates", (W.RequestSpec(90, 0, 1),
+                         W.RequestSpec(90, 0, 2), W.RequestSpec(50, 12000, 1)),
+                         H=32, D=128, topk=40, kdtype="fp4", qdtype="fp4", seed=61,
+                         cand_block=8, cand_topk=30)
+    p = W.make_problem(spec)
+    plan = Hp.make_plan(p, key_block=1024)
+    assert plan.info()["sample_stride"] >= 2
+    d = Hp.device_inputs(p)
+    T = int(p.cu_seqlens_q[-1])
+    rows = np.arange(T)
+    ref = oracle_rows(p, rows)
+    mask = Hp.gpu_candidates(p, plan, d).cpu().numpy()
+    cl = p.compress_len.numpy()
+    for t in rows:
+        Hp.check_mask_row(mask[t], ref[t], int(cl[t]), 8, 30)
+    g = Hp.gpu_logits(p, plan, d).cpu().numpy().astype(np.float64)
+    assert np.array_equal(O.candidates_rows(g, cl, 8, 30, mask.shape[1]), mask)
+    fi, _ = Hp.gpu_fused(p, plan, d, mask=torch.from_numpy(mask).cuda())
+    fi = fi.cpu().numpy()
+    for t in rows:
+        Hp.check_topk_row(fi[t], ref[t], int(cl[t]), p.topk, mask_row=mask[t])
+
+
 @pytest.mark.parametrize("block,cand_topk", [(8, 64), (4, 200)])
 def test_sampled_candidate_blocks_match_the_stream(block, cand_topk):
     """Requests long enough to be sampled: the block threshold from pooled samples, the
