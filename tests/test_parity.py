@@ -264,6 +264,20 @@ def test_fp4_queries_and_keys_with_widely_spread_block_scales_match_the_oracle()
         Hp.check_topk_row(fi[t], ref[t], int(cl[t]), p.topk)
 
 
+@pytest.mark.parametrize("name", ["cold64k", "v4fp4qk"])
+def test_mixed_sign_head_weights(name):
+    """Head weights of both signs (a learned projection has no sign constraint): negative
+    weighted ReLU terms, rows whose logits are mostly negative, negative sampled
+    thresholds; logits, top-k and both selection strategies against the oracle."""
+    p = small(name, 32, 8, topk=100)     # long enough rows to be sampled
+    gen = torch.Generator().manual_seed(77)
+    w = torch.randn(tuple(p.w.shape), generator=gen) / float(np.sqrt(p.H))
+    w[: w.shape[0] // 4] -= 0.5          # the first rows mostly negative
+    p = dataclasses.replace(p, w=w.float().contiguous())
+    assert Hp.make_plan(p, key_block=1024).info()["sample_stride"] >= 2
+    check_all(p, key_block=1024)
+
+
 def test_exact_arithmetic_inputs_are_bit_exact():
     """Small integer codes and power-of-two scales: every fp32 step is exact, so GPU logits
     equal the oracle's bitwise and selections match including ties."""
