@@ -350,8 +350,9 @@ int indexer_fused_topk_mapped(indexer_plan_t plan, const void* q, const float* s
  * 2^(largest block exponent of the row - 127).  This is how the library runs
  * e2m1 keys for head counts without a block-scaled kernel (inside the calls, kdtype
  * IDX_K_FP4_E2M1_UE8M0; 32 heads of 128 use the block-scaled MMA instead), and how a
- * caller runs e2m1 queries (fp4 x fp4): convert q as T*H rows of D and pass the e4m3
- * codes as q and the row scales as s_q.
+ * caller runs e2m1 queries with those head counts: convert q as T*H rows of D and pass
+ * the e4m3 codes as q and the row scales as s_q (qdtype IDX_Q_FP8_E4M3).  With 32 heads
+ * of 128, qdtype IDX_Q_FP4_E2M1_UE8M0 scores e2m1 queries natively instead.
  *   codes: device [rows, D/2] bytes, element 2i in the low nibble;
  *   block_scales: device [rows, D/32]; D a multiple of 32 (64 or 128 here);
  *   out_e4m3: device [rows, D]; out_scale: device fp32 [rows];
