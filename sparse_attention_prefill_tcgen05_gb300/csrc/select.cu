@@ -194,13 +194,17 @@ __device__ __forceinline__ bool merge_row_verified(const StreamMergeParams& p, c
     const uint32_t tau = p.tau_row[t];
     const uint32_t smax = p.smax_row[t];
     const int nslots = pc.slots, cap = pc.cap;
-    const int row_words = (pc.key_count + 31) / 32;
-    if (tau <= kOrdNegInf || smax <= tau || !p.bitmap || cap <= 0)
+    // (a candidate-mask merge ranks blocks: its bitmap spans the mask row)
+    const int row_words = p.mask ? static_cast<int>((p.ld_mask + 31) / 32) : (pc.key_count + 31) / 32;
+    if (tau <= kOrdNegInf || smax <= tau || !(p.bitmap || p.mask) || cap <= 0)
         return false;
     // rows of at most 65,536 keys keep the bucket in the upper 16 bits of the key field and
     // write the kept keys in order from a bitmap; longer rows recompute the bucket and sort
-    // the kept keys
+    // the kept keys.  A mask row is written from the bitmap (one word past the row's last
+    // is read, so it must fit too)
     const bool packed = row_words <= kBitmapWords;
+    if (p.mask && row_words + 1 > kBitmapWords)
+        return false;
     BucketThr bt;
     bt.vmin = ord2f(tau);
     {
@@ -379,7 +383,7 @@ __device__ __forceinline__ bool merge_row_verified(const StreamMergeParams& p, c
     uint32_t* bits = bhist;
     uint32_t* wpre = bits + kBitmapWords;
     const int nw = max(row_words, 1);
-    for (int w = tid; w < nw; w += kSelThreads)
+    for (int w = tid; w < nw + (p.mask ? 1 : 0); w += kSelThreads)
         bits[w] = 0;
     __syncthreads();
     // f(staged entry) for every staged entry, four loaded before any is used
@@ -422,6 +426,33 @@ __device__ __forceinline__ bool merge_row_verified(const StreamMergeParams& p, c
             }
         }
         __syncthreads();
+    }
+    if (p.mask) {
+        // the candidate-mask row from the bitmap of kept blocks: bytes up to a 16-byte
+        // boundary, 16 bytes per store, the tail; every byte of the row is written
+        uint8_t* m = p.mask + (t + pc.mask_delta) * p.ld_mask;
+        const int64_t nb = p.ld_mask;
+        auto bit = [&](int64_t b) -> uint32_t { return (bits[b >> 5] >> (b & 31)) & 1u; };
+        const int64_t head =
+            min(nb, static_cast<int64_t>((16 - (reinterpret_cast<uintptr_t>(m) & 15)) & 15));
+        for (int64_t b = tid; b < head; b += kSelThreads)
+            m[b] = static_cast<uint8_t>(bit(b));
+        const int64_t nvec = (nb - head) / 16;
+        uint4* mv = reinterpret_cast<uint4*>(m + head);
+        for (int64_t v = tid; v < nvec; v += kSelThreads) {
+            const int64_t b0 = head + v * 16;
+            const int shf = static_cast<int>(b0 & 31);
+            const uint64_t two = static_cast<uint64_t>(bits[b0 >> 5]) |
+                                 (static_cast<uint64_t>(bits[(b0 >> 5) + 1]) << 32);
+            const uint32_t x = static_cast<uint32_t>(two >> shf) & 0xFFFFu;   // 16 block flags
+            // four flags -> four bytes of 0 / 1
+            auto spread = [](uint32_t nib) { return (nib * 0x00204081u) & 0x01010101u; };
+            mv[v] = make_uint4(spread(x & 15u), spread((x >> 4) & 15u), spread((x >> 8) & 15u),
+                               spread(x >> 12));
+        }
+        for (int64_t b = head + nvec * 16 + tid; b < nb; b += kSelThreads)
+            m[b] = static_cast<uint8_t>(bit(b));
+        return true;
     }
     const int total = bitmap_prefix(bits, wpre, nw, sh, v_total);
     int32_t* obi = reinterpret_cast<int32_t*>(dyn + merge_obuf_offset(n2));
@@ -490,7 +521,7 @@ __device__ __forceinline__ void merge_row(const StreamMergeParams& p, const int 
     if (p.only_failed && (*p.fail_any == 0u || p.row_fail[t] == 0))
         return;   // decided by the first pass
     if constexpr (FAST) {
-        if (p.verify && p.smax_row != nullptr && !p.mask &&
+        if (p.verify && p.smax_row != nullptr &&
             merge_row_verified(p, pc, t, lbase, cbase, n2, dyn, sh))
             return;
     }
