@@ -18,7 +18,8 @@
 //                 buckets from tau to the row's largest sample, larger values in the top
 //                 one; the bucket holding the k-th entry, its entries ranked directly, a
 //                 bitmap of the kept keys, their positions by a prefix sum) written in
-//                 ascending key order, while the filter warps fill the other buffer.
+//                 ascending key order, each kept entry straight to its place, while the
+//                 filter warps fill the other buffer.
 // A row whose candidates cannot decide it (fewer than k at or above tau, or more than the
 // warps' regions and the shared spill area hold) is flagged for the direct kernel.  Every wait is bounded: a
 // timeout sets the status word and every role leaves its loop.
@@ -85,8 +86,7 @@ constexpr size_t kOffCand = kOffRing + (size_t)kStages * kChunk * 4;      // 96 
 constexpr size_t kOffHist = kOffCand + 2 * (size_t)kCand * 8;             // + 80 KB
 constexpr size_t kOffBits = kOffHist + (size_t)kRtBuckets * 4;            // + 8 KB
 constexpr size_t kOffWpre = kOffBits + (size_t)kRtWords * 4;              // + 8 KB
-constexpr size_t kOffObuf = kOffWpre + (size_t)kRtWords * 4;              // + 8 KB
-constexpr size_t kOffMeta = kOffObuf + 2 * (size_t)kRtMaxK * 4;           // + 16 KB
+constexpr size_t kOffMeta = kOffWpre + (size_t)kRtWords * 4;              // + 8 KB
 constexpr size_t kOffSlot = kOffMeta + kStages * sizeof(StageMeta);
 constexpr size_t kOffRcnt = kOffSlot + 2 * sizeof(RowSlot);               // [2][kFiltWarps]
 constexpr size_t kOffSpill = kOffRcnt + 2 * kFiltWarps * 4;               // [2] spill counts
@@ -143,8 +143,6 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
     uint32_t* bits = reinterpret_cast<uint32_t*>(smem + kOffBits);
     uint32_t* wpre = reinterpret_cast<uint32_t*>(smem + kOffWpre);
-    int32_t* obi = reinterpret_cast<int32_t*>(smem + kOffObuf);
-    float* obv = reinterpret_cast<float*>(obi + kRtMaxK);
     StageMeta* meta = reinterpret_cast<StageMeta*>(smem + kOffMeta);
     RowSlot* slot = reinterpret_cast<RowSlot*>(smem + kOffSlot);
     uint32_t* rcnt = reinterpret_cast<uint32_t*>(smem + kOffRcnt);   // [2][kFiltWarps]
@@ -607,27 +605,28 @@ __global__ void __launch_bounds__(kRtThreads, 1) row_topk_kernel(const __grid_co
                 bcast[0] = run;   // kept entries
             bar_all(true, kBarSel, kSelThr);
             const int total = static_cast<int>(bcast[0]);
+            // each kept entry straight to its place in the output row (a shared-memory
+            // copy of the row and a coalesced pass measured no faster), then the padding
+            int32_t* oi = p.out_idx + (int64_t)t * p.k;
+            float* ov = p.out_val ? p.out_val + (int64_t)t * p.k : nullptr;
             each_cand([&](const int, const uint2 en) {
                 const uint32_t j = en.y & 0xFFFFu;
                 const uint32_t word = bits[j >> 5];
                 if ((word >> (j & 31)) & 1u) {
                     const int pos =
                         static_cast<int>(wpre[j >> 5] + __popc(word & ((1u << (j & 31)) - 1u)));
-                    obi[pos] = static_cast<int32_t>(j);
-                    obv[pos] = __uint_as_float(en.x);
+                    oi[pos] = static_cast<int32_t>(j);
+                    if (ov)
+                        ov[pos] = __uint_as_float(en.x);
                 }
             });
-            bar_all(true, kBarSel, kSelThr);
-            int32_t* oi = p.out_idx + (int64_t)t * p.k;
-            float* ov = p.out_val ? p.out_val + (int64_t)t * p.k : nullptr;
-            for (int i = st; i < p.k; i += kSelThr) {
-                const bool have = i < total;
-                oi[i] = have ? obi[i] : -1;
+            for (int i = total + st; i < p.k; i += kSelThr) {
+                oi[i] = -1;
                 if (ov)
-                    ov[i] = have ? obv[i] : -INFINITY;
+                    ov[i] = -INFINITY;
             }
         }
-        // everything of the buffer (and the output row) has been read: release it, its
+        // everything of the buffer has been read: release it, its
         // spill count zeroed for its next row
         bar_all(true, kBarSel, kSelThr);
         if (st == 0) {
