@@ -164,9 +164,9 @@ struct BucketThr {
 constexpr int kStageEntries = 4608;   // candidates staged in shared memory per row (36 KB)
 static_assert(kStageEntries * 8 >= kBitmapWords * 8, "the bitmap reuses the staging area");
 // dynamic shared memory of the merge: [stage: kStageEntries x 8 B][scratch: keys and
-// values n2 x 4 B each, or the bitmap and its prefix][output row: n2 indices, n2 values
-// (index outputs only)]
-__host__ __device__ constexpr size_t merge_obuf_offset(int n2)
+// values n2 x 4 B each, or the bitmap and its prefix] (output rows go straight to global
+// memory)
+__host__ __device__ constexpr size_t merge_smem_bytes(int n2)
 {
     return 8 * (size_t)kStageEntries + (8 * (size_t)n2 > 8 * (size_t)kBitmapWords
                                             ? 8 * (size_t)n2
@@ -455,23 +455,21 @@ __device__ __forceinline__ bool merge_row_verified(const StreamMergeParams& p, c
         return true;
     }
     const int total = bitmap_prefix(bits, wpre, nw, sh, v_total);
-    int32_t* obi = reinterpret_cast<int32_t*>(dyn + merge_obuf_offset(n2));
-    float* obv = reinterpret_cast<float*>(obi + n2);
+    // each kept entry straight to its place in the output row, then the padding
     each_staged([&](const uint2 en) {
         const uint32_t j = en.y & 0xFFFFu;
         const uint32_t word = bits[j >> 5];
         if ((word >> (j & 31)) & 1u) {
             const int pos = static_cast<int>(wpre[j >> 5] + __popc(word & ((1u << (j & 31)) - 1u)));
-            obi[pos] = static_cast<int32_t>(j);
-            obv[pos] = __uint_as_float(en.x);
+            oi[pos] = static_cast<int32_t>(j);
+            if (ov)
+                ov[pos] = __uint_as_float(en.x);
         }
     });
-    __syncthreads();
-    for (int i = tid; i < p.k; i += kSelThreads) {
-        const bool have = i < total;
-        oi[i] = have ? obi[i] : -1;
+    for (int i = total + tid; i < p.k; i += kSelThreads) {
+        oi[i] = -1;
         if (ov)
-            ov[i] = have ? obv[i] : -INFINITY;
+            ov[i] = -INFINITY;
     }
     return true;
 }
@@ -485,8 +483,8 @@ __device__ __forceinline__ void merge_row(const StreamMergeParams& p, const int 
     __shared__ Scratch sh;
     __shared__ int32_t s_off[kMaxStreamSlots + 1];
     extern __shared__ __align__(16) uint8_t dyn[];
-    // [stage: kStageEntries x 8 B][keys: n2 x 4 B][values: n2 x 4 B][output row], n2 = k
-    // rounded up to a power of two (merge_obuf_offset)
+    // [stage: kStageEntries x 8 B][keys: n2 x 4 B][values: n2 x 4 B], n2 = k rounded up
+    // to a power of two (merge_smem_bytes)
     int n2 = 1;
     while (n2 < p.k)
         n2 <<= 1;
@@ -760,10 +758,8 @@ __device__ __forceinline__ void merge_row(const StreamMergeParams& p, const int 
         int32_t* oi = p.out_idx + (int64_t)t * k;
         float* ov = p.out_val ? p.out_val + (int64_t)t * k : nullptr;
         // a row's list entries have distinct keys, so an entry is kept iff its key's
-        // bit is set; it goes to its position in the shared output row, which is then
-        // written out with consecutive threads on consecutive positions
-        int32_t* obi = reinterpret_cast<int32_t*>(dyn + merge_obuf_offset(n2));
-        float* obv = reinterpret_cast<float*>(obi + n2);
+        // bit is set; it goes straight to its position in the output row, then the
+        // padding
         for (int e = threadIdx.x; e < n; e += kSelThreads) {
             const uint2 ent = stage[e];
             const uint32_t j = ent.y;
@@ -771,16 +767,15 @@ __device__ __forceinline__ void merge_row(const StreamMergeParams& p, const int 
             if ((word >> (j & 31)) & 1u) {
                 const int pos = static_cast<int>(wpre[j >> 5] +
                                                  __popc(word & ((1u << (j & 31)) - 1u)));
-                obi[pos] = static_cast<int32_t>(j);
-                obv[pos] = __uint_as_float(ent.x);
+                oi[pos] = static_cast<int32_t>(j);
+                if (ov)
+                    ov[pos] = __uint_as_float(ent.x);
             }
         }
-        __syncthreads();
-        for (int i = threadIdx.x; i < k; i += kSelThreads) {
-            const bool have = i < total;
-            oi[i] = have ? obi[i] : -1;
+        for (int i = total + threadIdx.x; i < k; i += kSelThreads) {
+            oi[i] = -1;
             if (ov)
-                ov[i] = have ? obv[i] : -INFINITY;
+                ov[i] = -INFINITY;
         }
         return;
     }
@@ -1379,7 +1374,7 @@ cudaError_t launch_stream_merge(const StreamMergeParams& p, cudaStream_t stream)
     int n2 = 1;
     while (n2 < p.k)
         n2 <<= 1;
-    const size_t dyn = merge_obuf_offset(n2) + (p.mask ? 0 : 8 * (size_t)n2);
+    const size_t dyn = merge_smem_bytes(n2);
     cudaError_t e = cudaFuncSetAttribute(p.only_failed ? stream_merge_kernel<true>
                                                        : stream_merge_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
