@@ -52,6 +52,23 @@ def test_tail_publish_equals_the_full_rows(tails):
     assert np.array_equal(got, want)
 
 
+def test_tail_publish_with_fp4_queries_equals_the_full_rows():
+    """The same for e2m1 queries and keys on the fp4 MMA kind (the full call's masks are
+    checked against the oracle with the other fp4-query parity cases)."""
+    spec = dataclasses.replace(W.CONFIGS["ragged_cand"], topk=48, cand_topk=30, requests=(
+        W.RequestSpec(90, 0, 1), W.RequestSpec(60, 3000, 2), W.RequestSpec(50, 16000, 1)),
+        seed=23, kdtype="fp4", qdtype="fp4")
+    p = W.make_problem(spec)
+    plan = Hp.make_plan(p)
+    d = Hp.device_inputs(p)
+    tails = [7, 60, 30]
+    full = Hp.gpu_candidates(p, plan, d).cpu().numpy()
+    got = _tail_masks(p, plan, d, tails).cpu().numpy()
+    cu = p.cu_seqlens_q.numpy()
+    want = np.concatenate([full[cu[r + 1] - n:cu[r + 1]] for r, n in enumerate(tails)])
+    assert np.array_equal(got, want)
+
+
 def test_mapped_consumer_equals_gathered_masks():
     p, plan = _problem()
     d = Hp.device_inputs(p)

@@ -7,8 +7,8 @@ top-k out of a fixed 64 MiB device array it holds itself.  This checks,
 through the C ABI, that two calls in a row (on different problems, so the
 second one starts from the first one's leftovers) give, bit for bit, what
 the regular entry point gives with a caller-allocated workspace: for fp8
-keys, for e2m1 keys (block-scaled MMA) and for a consumer reading a
-candidate mask.  A call whose e2m1 keys the conversion refuses reports it through
+keys, for e2m1 keys (block-scaled MMA), for e2m1 queries and keys (fp4 MMA kind)
+and for a consumer reading a candidate mask.  A call whose e2m1 keys the conversion refuses reports it through
 indexer_noalloc_status, and a plan too big for the array is refused.  Kept in
 its own file, collected last.
 """
@@ -70,6 +70,11 @@ def test_noalloc_fp4_keys_and_masked_consumer():
     plan = Hp.make_plan(p)
     mask = Hp.gpu_candidates(p, plan, Hp.device_inputs(p))
     _check_pair(p, mask=mask, layer=2)
+
+
+def test_noalloc_fp4_queries_and_keys():
+    """e2m1 queries and keys on the fp4 MMA kind through the allocation-free entry point."""
+    _check_pair(_problem("v4fp4qk", 16, 32, 64, seed=34))
 
 
 def test_noalloc_reports_a_refused_fp4_key():
