@@ -58,3 +58,11 @@ def test_single_process_needs_no_process_group(monkeypatch):
     assert bench.replica_env()[0] == 1
     assert bench.max_over_ranks(3.5, "cpu") == 3.5
     assert bench.whole_job_rate(10.0, 1, 1.0) == pytest.approx(1e4)
+
+
+def test_bench_reads_the_dominant_kernels_traffic_from_its_profile():
+    """The bench line's roofline traffic comes from the committed ncu summary of the
+    dominant kernel (DRAM bytes read + written per launch)."""
+    import bench
+    t = bench.profiled_traffic()
+    assert isinstance(t, int) and t > 0
