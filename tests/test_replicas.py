@@ -63,6 +63,7 @@ def test_single_process_needs_no_process_group(monkeypatch):
 def test_bench_reads_the_dominant_kernels_traffic_from_its_profile():
     """The bench line's roofline traffic comes from the committed ncu summary of the
     dominant kernel (DRAM bytes read + written per launch)."""
+    sys.path.insert(0, ROOT)
     import bench
     t = bench.profiled_traffic()
     assert isinstance(t, int) and t > 0
